@@ -1,0 +1,343 @@
+// Host side of the C ABI declared in include/la.h: argument validation,
+// sequence segmentation, workspace layout and kernel dispatch. Nothing here
+// allocates device memory or synchronises the stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "la_internal.cuh"
+
+namespace la {
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+std::atomic<int> g_path{LA_PATH_AUTO};
+
+la_status fail(la_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+la_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(LA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e),
+              cudaGetErrorString(e));
+}
+
+bool head_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Common size checks. Returns LA_OK and sets *empty when there is nothing to do.
+la_status check_sizes(int B, int H, int N, int dk, int dv, la_dtype dtype,
+                      float eps, bool* empty) {
+  if (B < 0 || H < 0 || N < 0) return fail(LA_ERR_INVALID_ARG, "negative size B=%d H=%d N=%d", B, H, N);
+  if (dtype != LA_F32 && dtype != LA_BF16) return fail(LA_ERR_UNSUPPORTED, "dtype %d not supported", (int)dtype);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(LA_ERR_UNSUPPORTED, "head sizes dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+  if (!(eps >= 0.f) || isinf(eps)) return fail(LA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL) return fail(LA_ERR_INVALID_ARG, "B*H too large");
+  const long long elems = BH * (long long)N * (dk > dv ? dk : dv);
+  if (elems > (1LL << 40)) return fail(LA_ERR_INVALID_ARG, "problem too large");
+  *empty = (BH == 0 || N == 0);
+  return LA_OK;
+}
+
+// Workspace layout for a plan: [state records][reverse records][token scalars],
+// each region 256-byte aligned.
+struct WsLayout {
+  size_t state_off, rev_off, tok_off, total;
+};
+
+WsLayout layout(long long BH, int N, int dk, int dv, const SegPlan& plan, bool backward) {
+  WsLayout w{};
+  const size_t rec = sizeof(float) * (size_t)state_words(dk, dv) * (size_t)plan.P * (size_t)BH;
+  w.state_off = 0;
+  size_t off = align_up(rec, 256);
+  if (backward) {
+    w.rev_off = off;
+    off += align_up(rec, 256);
+    w.tok_off = off;
+    off += align_up(sizeof(float) * 2 * (size_t)BH * (size_t)N, 256);
+  }
+  w.total = off;
+  return w;
+}
+
+struct Span {
+  int label;
+  cudaEvent_t start, stop;
+  bool closed;
+};
+
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::vector<Span> g_spans;
+std::vector<cudaEvent_t> g_free_events;
+std::atomic<long long> g_launches{0};
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void recycle_spans_locked() {
+  for (Span& s : g_spans) {
+    if (s.start) g_free_events.push_back(s.start);
+    if (s.stop) g_free_events.push_back(s.stop);
+  }
+  g_spans.clear();
+}
+
+}  // namespace
+
+void prof_begin(int label, cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  Span s{label, take_event(), take_event(), false};
+  if (s.start) cudaEventRecord(s.start, stream);
+  g_spans.push_back(s);
+}
+
+void prof_end(int label, cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto it = g_spans.rbegin(); it != g_spans.rend(); ++it) {
+    if (it->label == label && !it->closed) {
+      if (it->stop) cudaEventRecord(it->stop, stream);
+      it->closed = true;
+      return;
+    }
+  }
+}
+
+void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Pick the number of segments per sequence. Cost model in units of one
+// kSegGranule-token chunk: every CTA pays its chunks plus about one chunk of
+// prologue (loading its starting state); CTAs run in waves of kSlots; the
+// segment scan adds a little per segment. Pure function of the sizes, so the
+// workspace query and the call agree.
+SegPlan plan_segments(long long BH, int N) {
+  SegPlan best{1, N > 0 ? N : 1};
+  if (BH <= 0 || N <= 0) return best;
+  const int nch = (N + kSegGranule - 1) / kSegGranule;
+  double best_cost = 1e300;
+  for (int P = 1; P <= nch && P <= 4096; ++P) {
+    const int L = (nch + P - 1) / P;           // chunks per segment
+    if ((nch + L - 1) / L != P) continue;      // P not reachable with equal segments
+    const long long ctas = BH * P;
+    const long long waves = (ctas + kSlots - 1) / kSlots;
+    const double cost = (double)waves * (L + 1) + 0.02 * P;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best.P = P;
+      best.seg_len = L * kSegGranule;
+    }
+  }
+  return best;
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+const char* la_status_string(la_status s) {
+  switch (s) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+  }
+  return "LA_ERR_UNKNOWN";
+}
+
+const char* la_last_error(void) { return g_last_error; }
+
+int la_version(void) { return 100; }
+
+int la_set_path(int path) {
+  if (path != LA_PATH_AUTO && path != LA_PATH_SIMT) return -1;
+  return g_path.exchange(path);
+}
+
+int la_forward_path(int dk, int dv, la_dtype dtype) {
+  if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16)) return -1;
+  return 0;
+}
+
+int la_backward_path(int dk, int dv, la_dtype dtype) {
+  if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16)) return -1;
+  return 0;
+}
+
+size_t la_forward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
+  (void)causal; (void)dtype;
+  if (B <= 0 || H <= 0 || N <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
+  const long long BH = (long long)B * H;
+  return layout(BH, N, dk, dv, plan_segments(BH, N), false).total;
+}
+
+size_t la_backward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
+  (void)causal; (void)dtype;
+  if (B <= 0 || H <= 0 || N <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
+  const long long BH = (long long)B * H;
+  return layout(BH, N, dk, dv, plan_segments(BH, N), true).total;
+}
+
+la_status la_forward(const void* q, const void* k, const void* v, void* out,
+                     int B, int H, int N, int dk, int dv, int causal, float eps,
+                     la_dtype dtype, float* S_final, float* z_final,
+                     void* workspace, size_t workspace_bytes, la_stream_t stream_) {
+  bool empty = false;
+  la_status st = check_sizes(B, H, N, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if ((S_final == nullptr) != (z_final == nullptr))
+    return fail(LA_ERR_INVALID_ARG, "S_final and z_final must be both given or both NULL");
+  if ((S_final && !aligned16(S_final)) || (z_final && !aligned16(z_final)))
+    return fail(LA_ERR_INVALID_ARG, "S_final/z_final must be 16-byte aligned");
+  cudaStream_t stream = (cudaStream_t)stream_;
+  const long long BH = (long long)B * H;
+  if (empty) {
+    if (S_final != nullptr && BH > 0) {
+      cudaError_t e = cudaMemsetAsync(S_final, 0, sizeof(float) * BH * dk * dv, stream);
+      if (e == cudaSuccess) e = cudaMemsetAsync(z_final, 0, sizeof(float) * BH * dk, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "la_forward (zero final state)");
+    }
+    return LA_OK;
+  }
+  if (!q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+  const SegPlan plan = plan_segments(BH, N);
+  const WsLayout w = layout(BH, N, dk, dv, plan, false);
+  if (workspace == nullptr || workspace_bytes < w.total)
+    return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(LA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.BH = (int)BH; a.N = N; a.dk = dk; a.dv = dv; a.causal = causal != 0;
+  a.eps = eps; a.dtype = dtype; a.S_final = S_final; a.z_final = z_final;
+  a.ws_state = (float*)((char*)workspace + w.state_off);
+  a.plan = plan; a.stream = stream;
+
+  prof_begin(LA_SPAN_FWD_STATE, stream);
+  cudaError_t e = simt_segment_state(a);
+  prof_end(LA_SPAN_FWD_STATE, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment state)");
+  prof_begin(LA_SPAN_FWD_SCAN, stream);
+  e = segment_scan(a.ws_state, a.BH, plan.P, state_words(dk, dv),
+                   a.causal ? SCAN_EXCLUSIVE_FWD : SCAN_TOTAL, S_final, z_final,
+                   dk, dv, stream);
+  prof_end(LA_SPAN_FWD_SCAN, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment scan)");
+  prof_begin(LA_SPAN_FWD_OUTPUT, stream);
+  e = simt_forward_output(a);
+  prof_end(LA_SPAN_FWD_OUTPUT, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward (output)");
+  return LA_OK;
+}
+
+la_status la_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (on) recycle_spans_locked();
+  g_prof_on.store(on != 0);
+  return LA_OK;
+}
+
+int la_profile_read(int* labels, float* ms, int max) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  const int n = (int)g_spans.size();
+  for (int i = 0; i < n && i < max; ++i) {
+    const Span& s = g_spans[i];
+    float t = -1.f;
+    if (s.start && s.stop && s.closed && cudaEventSynchronize(s.stop) == cudaSuccess) {
+      if (cudaEventElapsedTime(&t, s.start, s.stop) != cudaSuccess) t = -1.f;
+    }
+    if (labels) labels[i] = s.label;
+    if (ms) ms[i] = t;
+  }
+  return n;
+}
+
+long long la_launch_count(void) { return g_launches.load(); }
+
+la_status la_decode_step(float* S, float* z, const void* q, const void* k,
+                         const void* v, void* out, int B, int H, int dk, int dv,
+                         float eps, la_dtype dtype, la_stream_t stream) {
+  bool empty = false;
+  la_status st = check_sizes(B, H, 1, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if (empty) return LA_OK;
+  if (!S || !z || !q || !k || !v || !out)
+    return fail(LA_ERR_INVALID_ARG, "S, z, q, k, v, out must be non-NULL");
+  if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
+      !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  DecodeArgs a{};
+  a.S = S; a.z = z; a.q = q; a.k = k; a.v = v; a.out = out;
+  a.BH = B * H; a.dk = dk; a.dv = dv; a.eps = eps; a.dtype = dtype;
+  a.stream = (cudaStream_t)stream;
+  prof_begin(LA_SPAN_DECODE, a.stream);
+  cudaError_t e = la::decode_step(a);
+  prof_end(LA_SPAN_DECODE, a.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
+  return LA_OK;
+}
+
+la_status la_backward(const void* q, const void* k, const void* v,
+                      const void* dout, void* dq, void* dk_, void* dv_, int B,
+                      int H, int N, int dk, int dv, int causal, float eps,
+                      la_dtype dtype, void* workspace, size_t workspace_bytes,
+                      la_stream_t stream) {
+  bool empty = false;
+  la_status st = check_sizes(B, H, N, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if (empty) return LA_OK;
+  if (!q || !k || !v || !dout || !dq || !dk_ || !dv_)
+    return fail(LA_ERR_INVALID_ARG, "q, k, v, dout, dq, dk, dv must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk_) || !aligned16(dv_))
+    return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  const long long BH = (long long)B * H;
+  const SegPlan plan = plan_segments(BH, N);
+  const WsLayout w = layout(BH, N, dk, dv, plan, true);
+  if (workspace == nullptr || workspace_bytes < w.total)
+    return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(LA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.dout = dout; a.dq = dq; a.dk_ = dk_; a.dv_ = dv_;
+  a.BH = (int)BH; a.N = N; a.dk = dk; a.dv = dv; a.causal = causal != 0;
+  a.eps = eps; a.dtype = dtype;
+  a.ws_state = (float*)((char*)workspace + w.state_off);
+  a.ws_rev = (float*)((char*)workspace + w.rev_off);
+  a.ws_tok = (float*)((char*)workspace + w.tok_off);
+  a.plan = plan; a.stream = (cudaStream_t)stream;
+  cudaError_t e = simt_backward(a);
+  if (e != cudaSuccess) return cuda_fail(e, "la_backward");
+  return LA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Internal declarations shared by the host entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "la.h"
+
+namespace la {
+
+// ---------------------------------------------------------------------------
+// Feature map phi(x) = elu(x) + 1: x + 1 for x >= 0, exp(x) for x < 0
+// ("Transformers are RNNs" review, feature-map table). For x < 0,
+// elu(x) + 1 = exp(x) - 1 + 1 = exp(x), evaluated directly so that it stays
+// positive and accurate for very negative x.
+// phi'(x) = 1 for x >= 0 and exp(x) for x < 0, i.e. min(phi(x), 1).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float phi(float x) { return x >= 0.f ? x + 1.f : expf(x); }
+// Same map with the fast exponential (ex2.approx based); used where the
+// result is rounded to bf16 anyway.
+__device__ __forceinline__ float phi_fast(float x) { return x >= 0.f ? x + 1.f : __expf(x); }
+__device__ __forceinline__ float phi_prime_from_phi(float p) { return fminf(p, 1.f); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------
+// Sequence segmentation: each (batch, head) sequence is cut into P segments
+// of seg_len tokens (the last may be shorter); one CTA per (segment, b*h).
+// ---------------------------------------------------------------------------
+struct SegPlan {
+  int P;        // segments per sequence (>= 1)
+  int seg_len;  // tokens per segment, multiple of kSegGranule (except when N is smaller)
+};
+
+constexpr int kSegGranule = 128;   // tokens; one tensor-core chunk
+constexpr int kSlots = 152;        // CTAs resident at once: one per SM of a GB300
+
+SegPlan plan_segments(long long BH, int N);
+
+// Floats per per-segment state record: dk*dv matrix then dk vector.
+inline long long state_words(int dk, int dv) { return (long long)dk * dv + dk; }
+
+// ---------------------------------------------------------------------------
+// Launchers (return cudaError_t of the launch; enqueue only)
+// ---------------------------------------------------------------------------
+struct FwdArgs {
+  const void* q; const void* k; const void* v; void* out;
+  int BH, N, dk, dv, causal; float eps; la_dtype dtype;
+  float* S_final; float* z_final;
+  float* ws_state;  // [BH][P][dk*dv + dk]
+  SegPlan plan;
+  cudaStream_t stream;
+};
+
+struct BwdArgs {
+  const void* q; const void* k; const void* v; const void* dout;
+  void* dq; void* dk_; void* dv_;
+  int BH, N, dk, dv, causal; float eps; la_dtype dtype;
+  float* ws_state;  // [BH][P][dk*dv + dk]  forward state sums -> prefixes
+  float* ws_rev;    // [BH][P][dk*dv + dk]  reverse sums (R, r) -> suffixes
+  float* ws_tok;    // [BH][N][2]           D_t and b_t per token
+  SegPlan plan;
+  cudaStream_t stream;
+};
+
+struct DecodeArgs {
+  float* S; float* z; const void* q; const void* k; const void* v; void* out;
+  int BH, dk, dv; float eps; la_dtype dtype;
+  cudaStream_t stream;
+};
+
+// CUDA-core kernels (any supported head size, f32 or bf16)
+cudaError_t simt_segment_state(const FwdArgs& a);                 // per-segment (dS, dz)
+cudaError_t segment_scan(float* ws, int BH, int P, long long words,
+                         int mode, float* S_final, float* z_final,
+                         int dk, int dv, cudaStream_t stream);     // prefix / suffix / total
+cudaError_t simt_forward_output(const FwdArgs& a);
+cudaError_t simt_backward(const BwdArgs& a);
+cudaError_t decode_step(const DecodeArgs& a);
+
+// scan modes
+enum { SCAN_EXCLUSIVE_FWD = 0, SCAN_EXCLUSIVE_REV = 1, SCAN_TOTAL = 2 };
+
+// Measurement hooks (la_profile_enable / la_profile_read / la_launch_count):
+// prof_begin/prof_end record CUDA events around a span of launches on
+// `stream` when profiling is on; note_launch counts kernel launches.
+void prof_begin(int label, cudaStream_t stream);
+void prof_end(int label, cudaStream_t stream);
+void note_launch(int n = 1);
+
+}  // namespace la

@@ -1,0 +1,3 @@
+// CUDA-core backward kernels for key head size 64.
+#define LA_DK 64
+#include "la_simt_bwd.cuh"

@@ -13,19 +13,30 @@ returned as float32 holding exactly representable values of the storage type.
 
 from __future__ import annotations
 
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 # stream ids, so q, k, v and the upstream gradient of one seed are independent
 STREAM_Q, STREAM_K, STREAM_V, STREAM_G = 0, 1, 2, 3
 
 
-def round_to_bf16(x):
-    """Round float32 values to the nearest bfloat16 (ties to even); float32 out."""
+def round_to_bf16(x, inplace=False):
+    """Round finite float32 values to the nearest bfloat16 (ties to even).
+
+    Returns float32. Works on the bit pattern: add 0x7FFF plus the lowest kept
+    bit, then clear the low 16 bits (no overflow for finite inputs).
+    """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    bias = np.uint64(0x7FFF) + ((bits >> np.uint64(16)) & np.uint64(1))
-    rounded = ((bits + bias) & np.uint64(0xFFFF0000)).astype(np.uint32)
-    return rounded.view(np.float32).reshape(x.shape)
+    if not inplace:
+        x = x.copy()
+    bits = x.view(np.uint32)
+    bias = bits >> np.uint32(16)
+    bias &= np.uint32(1)
+    bias += np.uint32(0x7FFF)
+    bits += bias
+    bits &= np.uint32(0xFFFF0000)
+    return x
 
 
 def normal(shape, seed, stream=0, scale=1.0, dtype="bf16"):
@@ -38,7 +49,7 @@ def normal(shape, seed, stream=0, scale=1.0, dtype="bf16"):
     if scale != 1.0:
         x *= np.float32(scale)
     if dtype == "bf16":
-        return round_to_bf16(x)
+        return round_to_bf16(x, inplace=True)
     if dtype == "f32":
         return x
     raise ValueError(f"unknown dtype {dtype!r}")
@@ -46,10 +57,14 @@ def normal(shape, seed, stream=0, scale=1.0, dtype="bf16"):
 
 def qkv(B, H, N, dk, dv, seed, dtype="bf16"):
     """q, k, v of shape [B,H,N,d], each N(0,1)/sqrt(d) rounded to ``dtype``."""
-    q = normal((B, H, N, dk), seed, STREAM_Q, 1.0 / np.sqrt(dk), dtype)
-    k = normal((B, H, N, dk), seed, STREAM_K, 1.0 / np.sqrt(dk), dtype)
-    v = normal((B, H, N, dv), seed, STREAM_V, 1.0 / np.sqrt(dv), dtype)
-    return q, k, v
+    jobs = [((B, H, N, dk), STREAM_Q, dk), ((B, H, N, dk), STREAM_K, dk),
+            ((B, H, N, dv), STREAM_V, dv)]
+    if B * H * N * max(dk, dv) < (1 << 22):
+        return tuple(normal(s, seed, st, 1.0 / np.sqrt(d), dtype) for s, st, d in jobs)
+    # large tensors: the three independent streams in parallel threads
+    with ThreadPoolExecutor(max_workers=3) as ex:
+        futs = [ex.submit(normal, s, seed, st, 1.0 / np.sqrt(d), dtype) for s, st, d in jobs]
+        return tuple(f.result() for f in futs)
 
 
 def upstream_grad(B, H, N, dv, seed, dtype="bf16"):

@@ -1,0 +1,215 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) causal linear-attention library.
+ *
+ * What is computed (feature map phi(x) = elu(x) + 1 = x + 1 for x >= 0 and
+ * exp(x) for x < 0, applied elementwise to q and to k, never to v):
+ *
+ *   S_t = S_{t-1} + phi(k_t) v_t^T        state, dk x dv, rows = key components
+ *   z_t = z_{t-1} + phi(k_t)              normaliser, dk
+ *   o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps)
+ *
+ * with S_0 = 0, z_0 = 0 and the state inclusive of token t ("Linear
+ * Attention: KV를 고정 크기 상태에 누적하기", section "상태 갱신과 읽기를 식으로
+ * 정리하기": S_{t+1} = S_t + k_t v_t^T, z_{t+1} = z_t + k_t, y_t read from
+ * S_{t+1}; feature map from the "Transformers are RNNs" review, feature-map
+ * table). Non-causal attention reads the full-sequence state S_N for every
+ * query ("Linear Attention: KV를 고정 크기 상태에 누적하기", fig. 2). No
+ * 1/sqrt(d) scale is applied inside; scale the inputs if one is wanted.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: q, k are [B, H, N, dk], v, out are [B, H, N, dv], contiguous,
+ *    row-major (token-major within a head). States S are [B, H, dk, dv] and
+ *    normalisers z are [B, H, dk], fp32, contiguous.
+ *  - dtype: LA_BF16 means q, k, v, out (and gradients) are bfloat16;
+ *    LA_F32 means float32. Arithmetic, states and normalisers are fp32 in
+ *    both cases; bf16 results are rounded to nearest even.
+ *  - Supported head sizes: dk, dv in {16, 32, 64, 128}.
+ *  - Pointers: every data pointer is device memory owned by the caller and
+ *    must be 16-byte aligned. The library allocates nothing: scratch space is
+ *    passed in as `workspace` (sizes from the *_workspace_size queries).
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).
+ *    Calls validate their arguments synchronously and then only enqueue
+ *    kernels; they return before the GPU work finishes.
+ *  - Errors: a non-OK status means nothing was enqueued (LA_ERR_INVALID_ARG,
+ *    LA_ERR_UNSUPPORTED) or a launch failed (LA_ERR_CUDA). la_last_error()
+ *    gives a one-line reason, per calling thread. Empty problems (B, H or N
+ *    equal to 0) are valid and enqueue nothing except zeroing S_final/z_final.
+ *  - Device: kernels are built for sm_103a (GB300) only; on another device
+ *    the launch fails with LA_ERR_CUDA.
+ */
+#ifndef LA_H_
+#define LA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum la_status {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad eps, short workspace */
+  LA_ERR_UNSUPPORTED = 2, /* head size or dtype outside the supported set */
+  LA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  LA_ERR_TIMEOUT = 4      /* reserved: a device-side bounded wait gave up */
+} la_status;
+
+typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/* An opaque cudaStream_t. */
+typedef void* la_stream_t;
+
+/* Human-readable name of a status code. Never NULL. */
+LA_API const char* la_status_string(la_status status);
+
+/* One-line reason for the last non-OK status returned on this thread
+ * ("" if none). The pointer stays valid until the next call on this thread. */
+LA_API const char* la_last_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+LA_API int la_version(void);
+
+/*
+ * Bytes of scratch memory la_forward needs for these sizes (0 if none).
+ * Holds one fp32 (dk*dv + dk) state per (batch, head, sequence segment).
+ * Negative sizes or unsupported head sizes return 0 (la_forward then reports
+ * the error).
+ */
+LA_API size_t la_forward_workspace_size(int B, int H, int N, int dk, int dv,
+                                 int causal, la_dtype dtype);
+
+/*
+ * Forward pass over whole sequences.
+ *
+ *   causal != 0 : o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps), S_t over j <= t
+ *                 ("상태공간모델·선형 어텐션 — 어텐션의 O(N²) 대안", section 2,
+ *                 masked form = recurrence)
+ *   causal == 0 : every query reads S_N, z_N (association reorder,
+ *                 "Linear Attention, 곱의 순서를 바꾸면 생기는 일", section
+ *                 "곱의 순서를 바꾸면 기억이 요약이 된다")
+ *
+ * q, k      [B,H,N,dk]  in, dtype
+ * v         [B,H,N,dv]  in, dtype
+ * out       [B,H,N,dv]  out, dtype (must not alias the inputs)
+ * eps       >= 0, finite, added to the denominator
+ * S_final   [B,H,dk,dv] fp32 out or NULL: the full-sequence state S_N
+ * z_final   [B,H,dk]    fp32 out or NULL: z_N (both or neither)
+ * workspace device scratch of at least la_forward_workspace_size(...) bytes,
+ *           NULL allowed when that size is 0. Contents on entry are ignored.
+ *
+ * The sequence is processed in chunks on the tensor cores; segments of one
+ * sequence run on different SMs and are joined by a prefix scan of their
+ * fp32 state sums kept in `workspace`.
+ */
+LA_API la_status la_forward(const void* q, const void* k, const void* v, void* out,
+                     int B, int H, int N, int dk, int dv, int causal,
+                     float eps, la_dtype dtype, float* S_final, float* z_final,
+                     void* workspace, size_t workspace_bytes,
+                     la_stream_t stream);
+
+/*
+ * One recurrent inference step per (batch, head), in place on the state:
+ *
+ *   S <- S + phi(k) v^T;  z <- z + phi(k);  out = phi(q)^T S / (phi(q)^T z + eps)
+ *
+ * ("Linear Attention: KV를 고정 크기 상태에 누적하기", section "상태 갱신과 읽기를
+ * 식으로 정리하기"; constant work per token as in "Linear Attention, 곱의 순서를
+ * 바꾸면 생기는 일", section "곱의 순서를 바꾸면 기억이 요약이 된다").
+ *
+ * S    [B,H,dk,dv] fp32 in/out      z [B,H,dk] fp32 in/out
+ * q, k [B,H,dk] dtype in            v [B,H,dv] dtype in
+ * out  [B,H,dv] dtype out
+ * The read uses the state after the update (inclusive of this token), so a
+ * prefill of t tokens followed by this step equals la_forward's output t.
+ */
+LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k,
+                         const void* v, void* out, int B, int H, int dk,
+                         int dv, float eps, la_dtype dtype,
+                         la_stream_t stream);
+
+/*
+ * Bytes of scratch memory la_backward needs (0 if none): one fp32 state and
+ * one fp32 reverse accumulator (dk*dv + dk each) per (batch, head, segment)
+ * plus two fp32 scalars per token (the denominator and the normaliser's
+ * gradient coefficient), no per-token states.
+ */
+LA_API size_t la_backward_workspace_size(int B, int H, int N, int dk, int dv,
+                                  int causal, la_dtype dtype);
+
+/*
+ * Gradients of L = sum(dout * out) with out = la_forward(q, k, v), by
+ * forward and reverse cumulative sums, storing no per-token states ("Transformers
+ * are RNNs" review, section "그래디언트 계산 — 선형 시간·상수 메모리"; the
+ * formulas are re-derived since the page lost them):
+ *
+ *   D_t = phi(q_t).z_t + eps, o_t = S_t^T phi(q_t) / D_t,
+ *   a_t = dout_t / D_t,  b_t = -(dout_t . o_t) / D_t,
+ *   dphi(q_t) = S_t a_t + b_t z_t,
+ *   R_j = sum_{t>=j} phi(q_t) a_t^T,  r_j = sum_{t>=j} b_t phi(q_t),
+ *   dphi(k_j) = R_j v_j + r_j,  dv_j = R_j^T phi(k_j),
+ *   dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k)
+ * (non-causal: S_t -> S_N, R_j -> R_0).
+ *
+ * q, k, v, dout as in la_forward (dout has out's shape); dq [B,H,N,dk],
+ * dk_ [B,H,N,dk], dv_ [B,H,N,dv] out, dtype. workspace as in la_forward,
+ * sized by la_backward_workspace_size.
+ */
+LA_API la_status la_backward(const void* q, const void* k, const void* v,
+                      const void* dout, void* dq, void* dk_, void* dv_, int B,
+                      int H, int N, int dk, int dv, int causal, float eps,
+                      la_dtype dtype, void* workspace, size_t workspace_bytes,
+                      la_stream_t stream);
+
+/*
+ * Kernel-path selection, for tests and measurements. LA_PATH_AUTO (the
+ * default) takes the tensor-core (tcgen05) kernels where they apply (bf16,
+ * dk = dv in {64, 128}) and the CUDA-core kernels elsewhere; LA_PATH_SIMT
+ * forces the CUDA-core kernels everywhere. Process-wide; returns the
+ * previous setting, or -1 for an unknown value (setting unchanged).
+ */
+enum { LA_PATH_AUTO = 0, LA_PATH_SIMT = 1 };
+LA_API int la_set_path(int path);
+
+/* Which path la_forward / la_backward take for these arguments under the
+ * current setting: 0 = CUDA-core, 1 = tensor-core; -1 if unsupported. */
+LA_API int la_forward_path(int dk, int dv, la_dtype dtype);
+LA_API int la_backward_path(int dk, int dv, la_dtype dtype);
+
+/*
+ * Measurement hooks (no effect on results).
+ *
+ * la_profile_enable(1) clears the record and starts timing: every later call
+ * records a CUDA event pair on its stream around each kernel span listed
+ * below. la_profile_enable(0) stops recording. la_profile_read waits for the
+ * recorded events, writes up to `max` (label, milliseconds) pairs in call
+ * order and returns how many spans were recorded (possibly more than `max`).
+ * Events are created lazily with cudaEventCreate; no device memory is
+ * allocated. la_launch_count returns the number of kernels this library has
+ * launched in the process so far.
+ */
+enum {
+  LA_SPAN_FWD_STATE = 0,   /* la_forward: per-segment state sums          */
+  LA_SPAN_FWD_SCAN = 1,    /* la_forward: segment prefix scan             */
+  LA_SPAN_FWD_OUTPUT = 2,  /* la_forward: chunked output kernel           */
+  LA_SPAN_DECODE = 3,      /* la_decode_step                              */
+  LA_SPAN_BWD_STATE = 4,   /* la_backward: per-segment state sums + scan  */
+  LA_SPAN_BWD_SWEEP1 = 5,  /* la_backward: forward sweep (dq)             */
+  LA_SPAN_BWD_SCAN = 6,    /* la_backward: reverse segment scan           */
+  LA_SPAN_BWD_SWEEP2 = 7   /* la_backward: reverse sweep (dk, dv)         */
+};
+LA_API la_status la_profile_enable(int on);
+LA_API int la_profile_read(int* labels, float* ms, int max);
+LA_API long long la_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H_ */

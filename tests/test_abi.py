@@ -1,0 +1,119 @@
+"""Host-only checks of the C ABI: the library loads, exports every entry point
+declared in include/la.h, and rejects bad arguments before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_linear_attention_la_gb300 as la
+from helpers import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib()
+    return la.lib()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^LA_API\s+[^(]*?\b(la_\w+)\s*\(", txt, re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert declared, "no LA_API declarations found"
+    assert declared == set(la.exported_symbols)
+    for name in declared:
+        assert hasattr(lib, name), name
+    # and they are real exported symbols of the shared object
+    handle = ctypes.CDLL(la.LIBPATH)
+    for name in declared:
+        getattr(handle, name)
+
+
+def test_status_strings(lib):
+    assert lib.la_status_string(0) == b"LA_OK"
+    assert lib.la_status_string(1) == b"LA_ERR_INVALID_ARG"
+    assert lib.la_status_string(2) == b"LA_ERR_UNSUPPORTED"
+    assert lib.la_status_string(3) == b"LA_ERR_CUDA"
+    assert lib.la_status_string(4) == b"LA_ERR_TIMEOUT"
+    assert lib.la_status_string(99) == b"LA_ERR_UNKNOWN"
+    assert lib.la_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    f = la.la_forward_workspace_size
+    assert f(0, 1, 64, 16, 16, 1, la.LA_F32) == 0
+    assert f(1, 1, 0, 16, 16, 1, la.LA_F32) == 0
+    assert f(1, 1, 64, 48, 16, 1, la.LA_F32) == 0  # unsupported head size
+    small = f(1, 1, 64, 16, 16, 1, la.LA_F32)
+    assert small >= 4 * (16 * 16 + 16) and small % 256 == 0
+    # one record per (b, h, segment); sizes grow with B*H
+    assert f(4, 8, 4096, 64, 64, 1, la.LA_BF16) >= 32 * 4 * (64 * 64 + 64)
+    b = la.la_backward_workspace_size(4, 8, 8192, 64, 64, 1, la.LA_BF16)
+    # two records per segment plus 2 floats per token
+    assert b >= 2 * f(4, 8, 8192, 64, 64, 1, la.LA_BF16) - 256 + 4 * 2 * 32 * 8192
+
+
+def _fwd(**kw):
+    args = dict(q=16, k=32, v=48, out=64, B=1, H=1, N=64, dk=16, dv=16, causal=1,
+                eps=1e-6, dtype=la.LA_F32, S_final=None, z_final=None,
+                workspace=1024, workspace_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return la.la_forward(**args)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    # none of these reach the GPU: validation fails first
+    assert _fwd(q=None) == la.LA_ERR_INVALID_ARG
+    assert b"non-NULL" in lib.la_last_error()
+    assert _fwd(k=17) == la.LA_ERR_INVALID_ARG            # misaligned
+    assert _fwd(B=-1) == la.LA_ERR_INVALID_ARG
+    assert _fwd(dk=24) == la.LA_ERR_UNSUPPORTED
+    assert _fwd(dv=256) == la.LA_ERR_UNSUPPORTED
+    assert _fwd(dtype=7) == la.LA_ERR_UNSUPPORTED
+    assert _fwd(eps=-1.0) == la.LA_ERR_INVALID_ARG
+    assert _fwd(eps=float("nan")) == la.LA_ERR_INVALID_ARG
+    assert _fwd(eps=float("inf")) == la.LA_ERR_INVALID_ARG
+    assert _fwd(workspace=None) == la.LA_ERR_INVALID_ARG
+    assert _fwd(workspace_bytes=8) == la.LA_ERR_INVALID_ARG
+    assert b"workspace" in lib.la_last_error()
+    assert _fwd(S_final=4096) == la.LA_ERR_INVALID_ARG    # z_final missing
+    # empty problems are valid and enqueue nothing
+    assert _fwd(N=0, q=None, k=None, v=None, out=None) == la.LA_OK
+    assert _fwd(B=0) == la.LA_OK
+    assert _fwd(H=0, workspace=None, workspace_bytes=0) == la.LA_OK
+
+
+def test_decode_and_backward_reject_bad_arguments(lib):
+    d = dict(S=256, z=512, q=16, k=32, v=48, out=64, B=2, H=2, dk=64, dv=64,
+             eps=1e-6, dtype=la.LA_BF16, stream=None)
+    assert la.la_decode_step(**{**d, "S": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_step(**{**d, "z": 4}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_step(**{**d, "dk": 96}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_decode_step(**{**d, "B": 0}) == la.LA_OK
+    b = dict(q=16, k=32, v=48, dout=80, dq=96, dk_=112, dv_=128, B=1, H=1,
+             N=64, dk=16, dv=16, causal=1, eps=1e-6, dtype=la.LA_F32,
+             workspace=1024, workspace_bytes=1 << 20, stream=None)
+    assert la.la_backward(**{**b, "dout": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_backward(**{**b, "workspace_bytes": 4}) == la.LA_ERR_INVALID_ARG
+    assert la.la_backward(**{**b, "dv": 8}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_backward(**{**b, "N": 0}) == la.LA_OK
+
+
+def test_path_selection(lib):
+    assert la.la_set_path(42) == -1
+    prev = la.la_set_path(la.LA_PATH_SIMT)
+    assert la.la_forward_path(64, 64, la.LA_BF16) == 0
+    la.la_set_path(prev)
+    assert la.la_forward_path(48, 64, la.LA_BF16) == -1
+    assert la.la_forward_path(16, 16, la.LA_F32) == 0

@@ -1,0 +1,119 @@
+"""Parity at the full benchmark sizes, in the launch configuration the bench
+times (default path, one call per pass):
+
+* causal forward B=4 H=8 N=4096 d=64 bf16: every output vs the oracle recurrence
+* causal forward B=2 H=16 N=32768 d=128 bf16: sampled outputs, each computed
+  one by one by the oracle's definition, plus the final state of two heads
+* decode: fp32 states from a bf16 prefill of N=131072 tokens on B=1 H=16,
+  replicated to B=64 x H=32, then one-token steps; every state for the first
+  steps, sampled states for more
+* forward + backward B=4 H=8 N=8192 d=64 bf16: every gradient vs the oracle
+"""
+
+import numpy as np
+import pytest
+
+import oracle as orc
+import causal_linear_attention_la_gb300 as la
+from causal_linear_attention_la_gb300 import synth
+from helpers import TOL, build_lib, rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build_lib()
+    la.lib()
+
+
+def test_forward_b4_h8_n4096_d64():
+    import torch
+    q, k, v = synth.qkv(4, 8, 4096, 64, 64, seed=2, dtype="bf16")
+    want = orc.forward_recurrent(q, k, v, eps=1e-6)
+    got = la.forward(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
+    torch.cuda.synchronize()
+    err = rel_err(to_host(got), want, np.abs(v).max())
+    assert err <= TOL["bf16"], err
+
+
+def test_forward_b2_h16_n32768_d128_sampled():
+    import torch
+    B, H, N, d = 2, 16, 32768, 128
+    q, k, v = synth.qkv(B, H, N, d, d, seed=3, dtype="bf16")
+    out, S, z = la.forward(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
+                           return_state=True)
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    rng = np.random.default_rng(0)
+    vmax = np.abs(v).max()
+    worst = 0.0
+    picks = [(b, h, t) for b in range(B) for h in (0, H - 1) for t in (0, 127, 128, N - 1)]
+    picks += [(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N)))
+              for _ in range(48)]
+    for b, h, t in picks:
+        want = orc.output_at(q[b, h], k[b, h], v[b, h], t, eps=1e-6)
+        worst = max(worst, rel_err(out[b, h, t], want, vmax))
+    assert worst <= TOL["bf16"], worst
+    for b, h in ((0, 0), (1, H - 1)):
+        fk = orc.phi_elu1(k[b, h])
+        S_ref = fk.T @ v[b, h].astype(np.float64)
+        assert rel_err(to_host(S[b, h]), S_ref, np.abs(S_ref).max()) <= 1e-5
+        assert rel_err(to_host(z[b, h]), fk.sum(0), fk.sum(0).max()) <= 1e-5
+
+
+def test_decode_b64_h32_d128_from_prefill_n131072():
+    import torch
+    d, Hp, Np = 128, 16, 131072
+    B, H = 64, 32
+    qp, kp, vp = synth.qkv(1, Hp, Np, d, d, seed=4, dtype="bf16")
+    _, Sp, zp = la.forward(to_dev(qp, "bf16"), to_dev(kp, "bf16"), to_dev(vp, "bf16"),
+                           return_state=True)
+    torch.cuda.synchronize()
+    # oracle prefill states of every prefill head, fp64
+    S_or = np.stack([orc.phi_elu1(kp[0, h]).T @ vp[0, h].astype(np.float64) for h in range(Hp)])
+    z_or = np.stack([orc.phi_elu1(kp[0, h]).sum(0) for h in range(Hp)])
+    del qp, kp, vp
+    assert rel_err(to_host(Sp[0]), S_or, np.abs(S_or).max()) <= 1e-5
+    # state (b, h) starts from prefill head (b*H + h) mod Hp
+    src = (np.arange(B * H) % Hp)
+    S = Sp[0][torch.from_numpy(src).cuda()].reshape(B, H, d, d).contiguous()
+    z = zp[0][torch.from_numpy(src).cuda()].reshape(B, H, d).contiguous()
+    S_ref = S_or[src].reshape(B, H, d, d)
+    z_ref = z_or[src].reshape(B, H, d)
+    sample = [(0, 0), (5, 17), (63, 31), (31, 8)]
+    S_s = np.stack([S_ref[b, h] for b, h in sample])
+    z_s = np.stack([z_ref[b, h] for b, h in sample])
+    worst = 0.0
+    for step in range(16):
+        q, k, v = synth.decode_token(B, H, d, d, seed=1000, step=step)
+        out = la.decode_step(S, z, to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
+        torch.cuda.synchronize()
+        got = to_host(out)
+        vmax = np.abs(v).max()
+        if step < 2:   # every state
+            S_ref, z_ref, o_ref = orc.decode_step(S_ref, z_ref, q, k, v)
+            worst = max(worst, rel_err(got, o_ref, vmax))
+        idx = tuple(np.array(sample).T)
+        S_s, z_s, o_s = orc.decode_step(S_s, z_s, q[idx], k[idx], v[idx])
+        worst = max(worst, rel_err(got[idx], o_s, vmax))
+    assert worst <= TOL["bf16"], worst
+
+
+def test_forward_backward_b4_h8_n8192_d64():
+    import torch
+    B, H, N, d = 4, 8, 8192, 64
+    q, k, v = synth.qkv(B, H, N, d, d, seed=5, dtype="bf16")
+    g = synth.upstream_grad(B, H, N, d, seed=5, dtype="bf16")
+    qd, kd, vd, gd = (to_dev(x, "bf16") for x in (q, k, v, g))
+    out = la.forward(qd, kd, vd)
+    grads = la.backward(qd, kd, vd, gd)
+    torch.cuda.synchronize()
+    want_o = orc.forward_recurrent(q, k, v, eps=1e-6)
+    assert rel_err(to_host(out), want_o, np.abs(v).max()) <= TOL["bf16"]
+    want = orc.backward_recurrent(q, k, v, g, eps=1e-6)
+    for name, a, b in zip(("dq", "dk", "dv"), grads, want):
+        err = rel_err(to_host(a), b, np.abs(b).max())
+        assert err <= TOL["bf16"], (name, err)

@@ -1,0 +1,91 @@
+"""Decode and backward parity: CUDA path (through the C ABI) vs the fp64 oracle."""
+
+import numpy as np
+import pytest
+
+import oracle as orc
+import causal_linear_attention_la_gb300 as la
+from causal_linear_attention_la_gb300 import synth
+from helpers import TOL, build_lib, rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build_lib()
+    la.lib()
+    yield
+    la.la_set_path(la.LA_PATH_AUTO)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,dk,dv", [(1, 1, 16, 16), (2, 3, 32, 64),
+                                       (4, 2, 128, 128), (3, 1, 128, 16),
+                                       (2, 2, 16, 128), (64, 32, 128, 128)])
+def test_decode_steps(B, H, dk, dv, dtype):
+    import torch
+    # start from the oracle state of a short prefill, then step
+    N0 = 40
+    q0, k0, v0 = synth.qkv(B, H, N0, dk, dv, seed=dk + dv, dtype=dtype)
+    _, S_ref, z_ref = orc.forward_recurrent(q0, k0, v0, return_state=True)
+    S = torch.from_numpy(S_ref.astype(np.float32)).cuda()
+    z = torch.from_numpy(z_ref.astype(np.float32)).cuda()
+    S_ref, z_ref = S_ref.astype(np.float32).astype(np.float64), z_ref.astype(np.float32).astype(np.float64)
+    for step in range(3):
+        q, k, v = synth.decode_token(B, H, dk, dv, seed=7, step=step, dtype=dtype)
+        out = la.decode_step(S, z, to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype))
+        torch.cuda.synchronize()
+        S_ref, z_ref, o_ref = orc.decode_step(S_ref, z_ref, q, k, v)
+        err = rel_err(to_host(out), o_ref, np.abs(v).max())
+        assert err <= TOL[dtype], (step, err)
+        assert rel_err(to_host(S), S_ref, np.abs(S_ref).max()) <= 1e-6
+        assert rel_err(to_host(z), z_ref, np.abs(z_ref).max()) <= 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prefill_then_decode_matches_forward(dtype):
+    import torch
+    B, H, N, dk, dv = 2, 2, 300, 64, 64
+    q, k, v = synth.qkv(B, H, N + 1, dk, dv, seed=31, dtype=dtype)
+    full = orc.forward_recurrent(q, k, v)
+    _, S, z = la.forward(to_dev(q[:, :, :N], dtype), to_dev(k[:, :, :N], dtype),
+                         to_dev(v[:, :, :N], dtype), return_state=True)
+    out = la.decode_step(S, z, to_dev(q[:, :, N], dtype), to_dev(k[:, :, N], dtype),
+                         to_dev(v[:, :, N], dtype))
+    torch.cuda.synchronize()
+    assert rel_err(to_host(out), full[:, :, N], np.abs(v).max()) <= TOL[dtype]
+
+
+PATHS = [la.LA_PATH_AUTO, la.LA_PATH_SIMT]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,H,N,dk,dv", [
+    (1, 1, 1, 16, 16),
+    (1, 1, 64, 16, 16),
+    (2, 1, 129, 64, 64),
+    (1, 2, 700, 32, 128),
+    (1, 1, 1500, 128, 128),
+    (1, 3, 333, 128, 16),
+])
+def test_backward_shapes(B, H, N, dk, dv, causal, dtype, path):
+    import torch
+    seed = 500 + N + dk
+    q, k, v = synth.qkv(B, H, N, dk, dv, seed=seed, dtype=dtype)
+    g = synth.upstream_grad(B, H, N, dv, seed=seed, dtype=dtype)
+    want = orc.backward_recurrent(q, k, v, g, causal=causal, eps=1e-6)
+    la.la_set_path(path)
+    try:
+        got = la.backward(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype),
+                          to_dev(g, dtype), causal=causal, eps=1e-6)
+        torch.cuda.synchronize()
+    finally:
+        la.la_set_path(la.LA_PATH_AUTO)
+    for name, a, b in zip(("dq", "dk", "dv"), got, want):
+        err = rel_err(to_host(a), b, np.abs(b).max())
+        assert err <= TOL[dtype], (name, err)

@@ -1,0 +1,104 @@
+"""Forward parity: CUDA path (through the C ABI) vs the fp64 oracle.
+
+Errors are max |out_gpu - out_oracle| / max|V| over the whole tensor, bounded
+by 1e-4 for fp32 inputs and 2e-2 for bf16 inputs with fp32 accumulation.
+"""
+
+import numpy as np
+import pytest
+
+import oracle as orc
+import causal_linear_attention_la_gb300 as la
+from causal_linear_attention_la_gb300 import synth
+from helpers import TOL, build_lib, rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [la.LA_PATH_AUTO, la.LA_PATH_SIMT]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build_lib()
+    la.lib()
+    yield
+    la.la_set_path(la.LA_PATH_AUTO)
+
+
+def _run(q, k, v, causal, dtype, eps=1e-6, path=la.LA_PATH_AUTO, state=False):
+    import torch
+    la.la_set_path(path)
+    try:
+        res = la.forward(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype),
+                         causal=causal, eps=eps, return_state=state)
+        torch.cuda.synchronize()
+    finally:
+        la.la_set_path(la.LA_PATH_AUTO)
+    return res
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_tiny_config_f32(causal):
+    # B=1, H=1, N=64, dk=dv=16, fp32, seed 1, eps 1e-6
+    q, k, v = synth.qkv(1, 1, 64, 16, 16, seed=1, dtype="f32")
+    want = orc.forward_masked(q, k, v, causal=causal, eps=1e-6)
+    got = to_host(_run(q, k, v, causal, "f32"))
+    err = rel_err(got, want, np.abs(v).max())
+    assert err <= TOL["f32"], err
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,H,N,dk,dv", [
+    (1, 1, 1, 16, 16),        # single token
+    (1, 2, 31, 32, 16),       # less than one tile, dk != dv
+    (2, 1, 129, 64, 64),      # one chunk plus one token
+    (1, 1, 1000, 64, 128),    # several segments, ragged tail
+    (1, 3, 2000, 128, 128),   # many segments
+    (2, 2, 300, 128, 32),
+    (1, 1, 4100, 16, 64),
+])
+def test_forward_shapes(B, H, N, dk, dv, causal, dtype, path):
+    seed = 100 + N + dk + dv
+    q, k, v = synth.qkv(B, H, N, dk, dv, seed=seed, dtype=dtype)
+    want, S_ref, z_ref = orc.forward_recurrent(q, k, v, causal=causal, eps=1e-6,
+                                               return_state=True)
+    got, S, z = _run(q, k, v, causal, dtype, path=path, state=True)
+    err = rel_err(to_host(got), want, np.abs(v).max())
+    assert err <= TOL[dtype], err
+    # final state: relative to its own magnitude
+    s_err = rel_err(to_host(S), S_ref, np.abs(S_ref).max())
+    z_err = rel_err(to_host(z), z_ref, np.abs(z_ref).max())
+    assert s_err <= 1e-5 and z_err <= 1e-5, (s_err, z_err)
+
+
+def test_forward_eps_zero_and_large():
+    q, k, v = synth.qkv(1, 2, 257, 64, 64, seed=9, dtype="bf16")
+    for eps in (0.0, 10.0):
+        want = orc.forward_recurrent(q, k, v, eps=eps)
+        got = to_host(_run(q, k, v, True, "bf16", eps=eps))
+        assert rel_err(got, want, np.abs(v).max()) <= TOL["bf16"]
+
+
+def test_forward_extreme_inputs():
+    # large-magnitude q, k: phi saturates to exp(x) ~ 0 or x + 1 ~ large
+    rng = np.random.default_rng(3)
+    q = (rng.standard_normal((1, 1, 300, 64)) * 8).astype(np.float32)
+    k = (rng.standard_normal((1, 1, 300, 64)) * 8).astype(np.float32)
+    v = rng.standard_normal((1, 1, 300, 64)).astype(np.float32)
+    want = orc.forward_recurrent(q, k, v, eps=1e-6)
+    got = to_host(_run(q, k, v, True, "f32"))
+    assert rel_err(got, want, np.abs(v).max()) <= TOL["f32"]
+
+
+def test_empty_sequence_zeroes_state():
+    import torch
+    q = torch.zeros((2, 3, 0, 16), device="cuda")
+    v = torch.zeros((2, 3, 0, 32), device="cuda")
+    out, S, z = la.forward(q, q, v, return_state=True)
+    torch.cuda.synchronize()
+    assert out.shape == (2, 3, 0, 32)
+    assert float(S.abs().max()) == 0.0 and float(z.abs().max()) == 0.0
