@@ -93,7 +93,10 @@ cudaEvent_t take_event() {
     return e;
   }
   cudaEvent_t e = nullptr;
-  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
   return e;
 }
 
@@ -105,13 +108,24 @@ void recycle_spans_locked() {
   g_spans.clear();
 }
 
+// Record `e` on `stream`; while the stream is being captured into a CUDA graph
+// the record must be an external event-record node to take effect at replay.
+void record_event(cudaEvent_t e, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, stream, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, stream);
+}
+
 }  // namespace
 
 void prof_begin(int label, cudaStream_t stream) {
   if (!g_prof_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   Span s{label, take_event(), take_event(), false};
-  if (s.start) cudaEventRecord(s.start, stream);
+  if (s.start) record_event(s.start, stream);
+  (void)cudaGetLastError();  // a failed record must not surface as a later launch error
   g_spans.push_back(s);
 }
 
@@ -120,7 +134,8 @@ void prof_end(int label, cudaStream_t stream) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   for (auto it = g_spans.rbegin(); it != g_spans.rend(); ++it) {
     if (it->label == label && !it->closed) {
-      if (it->stop) cudaEventRecord(it->stop, stream);
+      if (it->stop) record_event(it->stop, stream);
+      (void)cudaGetLastError();
       it->closed = true;
       return;
     }
@@ -278,6 +293,7 @@ int la_profile_read(int* labels, float* ms, int max) {
     if (labels) labels[i] = s.label;
     if (ms) ms[i] = t;
   }
+  (void)cudaGetLastError();
   return n;
 }
 

@@ -30,3 +30,17 @@ def rel_err(got, want, scale):
 def build_lib():
     from causal_linear_attention_la_gb300.build import build
     return build()
+
+
+def grad_errors(got, want):
+    """Per-tensor max abs error of (dq, dk, dv), each relative to that tensor's
+    largest oracle magnitude, floored at 1e-2 x the largest magnitude of all
+    three: for very short sequences dq and dk shrink to O(eps) by cancellation
+    (a single token's output is v_0 s / (s + eps)), and a relative error of a
+    vanishing quantity says nothing about the arithmetic."""
+    want = [np.asarray(w, np.float64) for w in want]
+    floor = 1e-2 * max(float(np.abs(w).max()) for w in want)
+    out = []
+    for a, b in zip(got, want):
+        out.append(rel_err(to_host(a), b, max(float(np.abs(b).max()), floor)))
+    return out
