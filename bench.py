@@ -586,8 +586,8 @@ def main():
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
             "gpu_launches": r["launches"],
             "clocks": sampler.summary(),
-            "path": {"forward": la.la_forward_path(w["dk"], w["dv"], la.LA_BF16),
-                     "backward": la.la_backward_path(w["dk"], w["dv"], la.LA_BF16)},
+            "path": {"forward": ["cuda-core", "tensor-core"][la.la_forward_path(w["dk"], w["dv"], la.LA_BF16)],
+                     "backward": ["cuda-core", "tensor-core"][la.la_backward_path(w["dk"], w["dv"], la.LA_BF16)]},
             "sections": sections,
         }
         print(json.dumps(line), flush=True)

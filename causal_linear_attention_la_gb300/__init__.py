@@ -29,6 +29,7 @@ __all__ = [
     "la_forward_workspace_size", "la_backward_workspace_size",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
+    "la_device_status",
     "forward", "decode_step", "backward",
 ]
 
@@ -45,6 +46,7 @@ exported_symbols = (
     "la_backward_workspace_size", "la_backward",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
+    "la_device_status",
 )
 
 
@@ -94,9 +96,11 @@ def lib():
     h.la_set_path.restype = _c_int
     h.la_set_path.argtypes = [_c_int]
     h.la_forward_path.restype = _c_int
-    h.la_forward_path.argtypes = [_c_int, _c_int, _c_int]
+    h.la_forward_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
     h.la_backward_path.restype = _c_int
-    h.la_backward_path.argtypes = [_c_int, _c_int, _c_int]
+    h.la_backward_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
+    h.la_device_status.restype = _c_int
+    h.la_device_status.argtypes = [_c_int]
     h.la_profile_enable.restype = _c_int
     h.la_profile_enable.argtypes = [_c_int]
     h.la_profile_read.restype = _c_int
@@ -149,12 +153,16 @@ def la_set_path(path):
     return lib().la_set_path(path)
 
 
-def la_forward_path(dk, dv, dtype):
-    return lib().la_forward_path(dk, dv, dtype)
+def la_forward_path(dk, dv, dtype, causal=True):
+    return lib().la_forward_path(dk, dv, dtype, int(causal))
 
 
-def la_backward_path(dk, dv, dtype):
-    return lib().la_backward_path(dk, dv, dtype)
+def la_backward_path(dk, dv, dtype, causal=True):
+    return lib().la_backward_path(dk, dv, dtype, int(causal))
+
+
+def la_device_status(clear=False):
+    return lib().la_device_status(int(clear))
 
 
 def la_profile_enable(on):

@@ -14,6 +14,10 @@
 
 namespace la {
 
+// Set to LA_ERR_TIMEOUT by a kernel whose bounded wait gave up; read and
+// cleared by la_device_status. One per device (module-scope device variable).
+__device__ int g_la_device_status = 0;
+
 namespace {
 
 thread_local char g_last_error[256] = "";
@@ -144,6 +148,26 @@ void prof_end(int label, cudaStream_t stream) {
 
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int* device_status_ptr() {
+  static std::mutex mu;
+  static int* cache[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_la_device_status) == cudaSuccess)
+      cache[dev] = static_cast<int*>(p);
+    else
+      (void)cudaGetLastError();
+  }
+  return cache[dev];
+}
+
 // Pick the number of segments per sequence. Cost model in units of one
 // kSegGranule-token chunk: every CTA pays its chunks plus about one chunk of
 // prologue (loading its starting state); CTAs run in waves of kSlots; the
@@ -195,12 +219,13 @@ int la_set_path(int path) {
   return g_path.exchange(path);
 }
 
-int la_forward_path(int dk, int dv, la_dtype dtype) {
+int la_forward_path(int dk, int dv, la_dtype dtype, int causal) {
   if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16)) return -1;
-  return 0;
+  return (g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, causal != 0)) ? 1 : 0;
 }
 
-int la_backward_path(int dk, int dv, la_dtype dtype) {
+int la_backward_path(int dk, int dv, la_dtype dtype, int causal) {
+  (void)causal;
   if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16)) return -1;
   return 0;
 }
@@ -257,8 +282,11 @@ la_status la_forward(const void* q, const void* k, const void* v, void* out,
   a.ws_state = (float*)((char*)workspace + w.state_off);
   a.plan = plan; a.stream = stream;
 
+  const bool use_tc = g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, a.causal);
+  if (use_tc && device_status_ptr() == nullptr)
+    return fail(LA_ERR_CUDA, "la_forward: device status word unavailable");
   prof_begin(LA_SPAN_FWD_STATE, stream);
-  cudaError_t e = simt_segment_state(a);
+  cudaError_t e = use_tc ? tc_segment_state(a) : simt_segment_state(a);
   prof_end(LA_SPAN_FWD_STATE, stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment state)");
   prof_begin(LA_SPAN_FWD_SCAN, stream);
@@ -268,7 +296,7 @@ la_status la_forward(const void* q, const void* k, const void* v, void* out,
   prof_end(LA_SPAN_FWD_SCAN, stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment scan)");
   prof_begin(LA_SPAN_FWD_OUTPUT, stream);
-  e = simt_forward_output(a);
+  e = use_tc ? tc_forward_output(a) : simt_forward_output(a);
   prof_end(LA_SPAN_FWD_OUTPUT, stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward (output)");
   return LA_OK;
@@ -298,6 +326,19 @@ int la_profile_read(int* labels, float* ms, int max) {
 }
 
 long long la_launch_count(void) { return g_launches.load(); }
+
+la_status la_device_status(int clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_la_device_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "la_device_status");
+  if (clear && v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_la_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "la_device_status (clear)");
+  }
+  if (v != 0) return fail(LA_ERR_TIMEOUT, "a kernel's bounded wait gave up (status %d)", v);
+  return LA_OK;
+}
 
 la_status la_decode_step(float* S, float* z, const void* q, const void* k,
                          const void* v, void* out, int B, int H, int dk, int dv,

@@ -85,6 +85,15 @@ cudaError_t simt_forward_output(const FwdArgs& a);
 cudaError_t simt_backward(const BwdArgs& a);
 cudaError_t decode_step(const DecodeArgs& a);
 
+// Tensor-core kernels (bf16, dk = dv in {64, 128}, causal)
+bool tc_forward_supported(int dk, int dv, la_dtype dtype, int causal);
+cudaError_t tc_segment_state(const FwdArgs& a);
+cudaError_t tc_forward_output(const FwdArgs& a);
+
+// Device status word of the current device (set to LA_ERR_TIMEOUT by a
+// kernel whose bounded wait gave up); NULL if it cannot be resolved.
+int* device_status_ptr();
+
 // scan modes
 enum { SCAN_EXCLUSIVE_FWD = 0, SCAN_EXCLUSIVE_REV = 1, SCAN_TOTAL = 2 };
 

@@ -179,8 +179,19 @@ LA_API int la_set_path(int path);
 
 /* Which path la_forward / la_backward take for these arguments under the
  * current setting: 0 = CUDA-core, 1 = tensor-core; -1 if unsupported. */
-LA_API int la_forward_path(int dk, int dv, la_dtype dtype);
-LA_API int la_backward_path(int dk, int dv, la_dtype dtype);
+LA_API int la_forward_path(int dk, int dv, la_dtype dtype, int causal);
+LA_API int la_backward_path(int dk, int dv, la_dtype dtype, int causal);
+
+/*
+ * Device-side status. The tensor-core kernels bound every wait on another
+ * warp or on the copy engine; if one ever gives up, the kernel stops early
+ * (its outputs are then incomplete), frees its tensor memory and records
+ * LA_ERR_TIMEOUT in a per-device status word. la_device_status reads that
+ * word for the current device (a synchronous copy: synchronise the streams
+ * that ran the library's kernels first), returns LA_OK or LA_ERR_TIMEOUT and,
+ * if `clear` is non-zero, resets it.
+ */
+LA_API la_status la_device_status(int clear);
 
 /*
  * Measurement hooks (no effect on results).

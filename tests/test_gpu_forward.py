@@ -60,6 +60,13 @@ def test_tiny_config_f32(causal):
     (1, 3, 2000, 128, 128),   # many segments
     (2, 2, 300, 128, 32),
     (1, 1, 4100, 16, 64),
+    # tensor-core sizes (bf16, causal, dk = dv in {64, 128}): one token, a
+    # partial chunk, exact chunks, many segments with a ragged tail
+    (1, 1, 1, 64, 64),
+    (1, 2, 127, 128, 128),
+    (1, 1, 256, 64, 64),
+    (2, 3, 4097, 64, 64),
+    (1, 2, 5000, 128, 128),
 ])
 def test_forward_shapes(B, H, N, dk, dv, causal, dtype, path):
     seed = 100 + N + dk + dv
@@ -68,6 +75,7 @@ def test_forward_shapes(B, H, N, dk, dv, causal, dtype, path):
                                                return_state=True)
     got, S, z = _run(q, k, v, causal, dtype, path=path, state=True)
     err = rel_err(to_host(got), want, np.abs(v).max())
+    assert la.la_device_status(True) == la.LA_OK
     assert err <= TOL[dtype], err
     # final state: relative to its own magnitude
     s_err = rel_err(to_host(S), S_ref, np.abs(S_ref).max())
@@ -102,3 +110,15 @@ def test_empty_sequence_zeroes_state():
     torch.cuda.synchronize()
     assert out.shape == (2, 3, 0, 32)
     assert float(S.abs().max()) == 0.0 and float(z.abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_path_is_taken(d):
+    assert la.la_forward_path(d, d, la.LA_BF16, True) == 1
+    n0 = la.la_launch_count()
+    q, k, v = synth.qkv(1, 1, 300, d, d, seed=77, dtype="bf16")
+    want = orc.forward_recurrent(q, k, v)
+    got = to_host(_run(q, k, v, True, "bf16"))
+    assert la.la_launch_count() - n0 == 3      # state sums, scan, chunk loop
+    assert la.la_device_status(True) == la.LA_OK
+    assert rel_err(got, want, np.abs(v).max()) <= TOL["bf16"]
