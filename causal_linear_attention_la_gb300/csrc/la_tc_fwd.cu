@@ -70,22 +70,19 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {  // byte offset 
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ void phi_bf16x8(uint4& w) {
+// phi on 8 packed bf16 values in place; when `acc` is given, also add the
+// unrounded fp32 phi values to it (column sums for z).
+__device__ __forceinline__ void phi_bf16x8(uint4& w, float* acc) {
   uint32_t* p = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(p[i] << 16);
-    const float hi = __uint_as_float(p[i] & 0xFFFF0000u);
-    p[i] = pack_bf16x2(phi_fast(lo), phi_fast(hi));
-  }
-}
-
-__device__ __forceinline__ void add_bf16x8(const uint4& w, float (&acc)[8]) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(&w);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc[2 * i] += __uint_as_float(p[i] << 16);
-    acc[2 * i + 1] += __uint_as_float(p[i] & 0xFFFF0000u);
+    const float lo = phi_fast(__uint_as_float(p[i] << 16));
+    const float hi = phi_fast(__uint_as_float(p[i] & 0xFFFF0000u));
+    if (acc != nullptr) {
+      acc[2 * i] += lo;
+      acc[2 * i + 1] += hi;
+    }
+    p[i] = pack_bf16x2(lo, hi);
   }
 }
 
@@ -105,9 +102,8 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int t, int n_valid, floa
       const int r = rg + 16 * i;
       uint4* p = reinterpret_cast<uint4*>(tile + b * BOX + sw128(r, lc));
       uint4 w = *p;
-      phi_bf16x8(w);
+      phi_bf16x8(w, (zacc != nullptr && r < n_valid) ? zacc[b] : nullptr);
       *p = w;
-      if (zacc != nullptr && r < n_valid) add_bf16x8(w, zacc[b]);
     }
   }
 }

@@ -6,6 +6,13 @@ import numpy as np
 # largest oracle gradient magnitude for gradients).
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
+# Final-state tolerance (max abs error relative to max|S|). With bf16 inputs
+# the tensor cores multiply phi(k) rounded to bf16 (relative error up to
+# 2^-9 per term); the sum of N such terms with random-sign values keeps a
+# relative error near 2^-9 / sqrt(3) ~ 1e-3 (2.4e-3 observed at N = 32768),
+# bounded here at 1e-2. fp32 inputs keep fp32 phi throughout.
+STATE_TOL = {"f32": 1e-5, "bf16": 1e-2}
+
 
 def torch_dtype(name):
     import torch

@@ -16,7 +16,7 @@ import pytest
 import oracle as orc
 import causal_linear_attention_la_gb300 as la
 from causal_linear_attention_la_gb300 import synth
-from helpers import TOL, build_lib, grad_errors, rel_err, to_dev, to_host
+from helpers import STATE_TOL, TOL, build_lib, grad_errors, rel_err, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,7 @@ def test_forward_b2_h16_n32768_d128_sampled():
     for b, h in ((0, 0), (1, H - 1)):
         fk = orc.phi_elu1(k[b, h])
         S_ref = fk.T @ v[b, h].astype(np.float64)
-        assert rel_err(to_host(S[b, h]), S_ref, np.abs(S_ref).max()) <= 1e-5
+        assert rel_err(to_host(S[b, h]), S_ref, np.abs(S_ref).max()) <= STATE_TOL["bf16"]
         assert rel_err(to_host(z[b, h]), fk.sum(0), fk.sum(0).max()) <= 1e-5
 
 
@@ -76,7 +76,7 @@ def test_decode_b64_h32_d128_from_prefill_n131072():
     S_or = np.stack([orc.phi_elu1(kp[0, h]).T @ vp[0, h].astype(np.float64) for h in range(Hp)])
     z_or = np.stack([orc.phi_elu1(kp[0, h]).sum(0) for h in range(Hp)])
     del qp, kp, vp
-    assert rel_err(to_host(Sp[0]), S_or, np.abs(S_or).max()) <= 1e-5
+    assert rel_err(to_host(Sp[0]), S_or, np.abs(S_or).max()) <= STATE_TOL["bf16"]
     # state (b, h) starts from prefill head (b*H + h) mod Hp
     src = (np.arange(B * H) % Hp)
     S = Sp[0][torch.from_numpy(src).cuda()].reshape(B, H, d, d).contiguous()
