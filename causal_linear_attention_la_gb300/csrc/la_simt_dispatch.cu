@@ -20,34 +20,55 @@ namespace {
 
 // Segment scan over P records of `words` floats per (b,h): exclusive prefix
 // (forward), exclusive suffix (reverse) or the total written into every slot.
-// The inclusive total goes to S_final / z_final when given.
+// The inclusive total goes to S_final / z_final when given. Each thread owns
+// 4 consecutive words (records are 16-byte multiples) and issues its loads in
+// batches of 8 records before using them, so the dependent-latency chain is
+// P / 8 loads long rather than P.
 __global__ void scan_kernel(float* __restrict__ ws, int P, long long words,
                             int mode, float* __restrict__ S_final,
                             float* __restrict__ z_final, int dkdv, int dk) {
-  const long long e = (long long)blockIdx.y * blockDim.x + threadIdx.x;
+  const long long e = 4 * ((long long)blockIdx.y * blockDim.x + threadIdx.x);
   if (e >= words) return;
   const long long bh = blockIdx.x;
-  float* base = ws + bh * P * words + e;
-  float run = 0.f;
+  float4* base = reinterpret_cast<float4*>(ws + bh * P * words + e);
+  const long long stride = words / 4;   // in float4
+  constexpr int BATCH = 8;
+  float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
   if (mode == SCAN_TOTAL) {
-    for (int p = 0; p < P; ++p) run += base[p * words];
-    for (int p = 0; p < P; ++p) base[p * words] = run;
-  } else if (mode == SCAN_EXCLUSIVE_FWD) {
-    for (int p = 0; p < P; ++p) {
-      const float x = base[p * words];
-      base[p * words] = run;
-      run += x;
+    for (int p0 = 0; p0 < P; p0 += BATCH) {
+      float4 x[BATCH];
+#pragma unroll
+      for (int i = 0; i < BATCH; ++i) x[i] = p0 + i < P ? base[(p0 + i) * stride] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < BATCH; ++i) add(run, x[i]);
     }
+    for (int p = 0; p < P; ++p) base[p * stride] = run;
   } else {
-    for (int p = P - 1; p >= 0; --p) {
-      const float x = base[p * words];
-      base[p * words] = run;
-      run += x;
+    const bool rev = mode == SCAN_EXCLUSIVE_REV;
+    for (int p0 = 0; p0 < P; p0 += BATCH) {
+      float4 x[BATCH];
+#pragma unroll
+      for (int i = 0; i < BATCH; ++i) {
+        const int p = rev ? P - 1 - (p0 + i) : p0 + i;
+        x[i] = p0 + i < P ? base[p * stride] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < BATCH; ++i) {
+        const int p = rev ? P - 1 - (p0 + i) : p0 + i;
+        if (p0 + i < P) base[p * stride] = run;
+        add(run, x[i]);
+      }
     }
   }
   if (S_final != nullptr) {
-    if (e < dkdv) S_final[bh * dkdv + e] = run;
-    else z_final[bh * dk + (e - dkdv)] = run;
+    const float v[4] = {run.x, run.y, run.z, run.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long ej = e + j;
+      if (ej < dkdv) S_final[bh * dkdv + ej] = v[j];
+      else z_final[bh * dk + (ej - dkdv)] = v[j];
+    }
   }
 }
 
@@ -86,7 +107,8 @@ cudaError_t simt_backward(const BwdArgs& a) {
 cudaError_t segment_scan(float* ws, int BH, int P, long long words, int mode,
                          float* S_final, float* z_final, int dk, int dv,
                          cudaStream_t stream) {
-  dim3 grid(BH, (unsigned)((words + 255) / 256));
+  // records of dk*dv + dk floats: always a multiple of 4 (dk >= 16)
+  dim3 grid(BH, (unsigned)((words / 4 + 255) / 256));
   scan_kernel<<<grid, 256, 0, stream>>>(ws, P, words, mode, S_final, z_final,
                                         dk * dv, dk);
   const cudaError_t err = cudaGetLastError();

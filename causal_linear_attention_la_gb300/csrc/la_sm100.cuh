@@ -52,6 +52,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// while the phase is incomplete (it resumes as soon as the phase completes),
+// so waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up after `timeout_ns`
 // or as soon as another warp of the CTA has set *abort. Returns false on
 // give-up (and sets *abort so the whole CTA winds down).
@@ -60,9 +75,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       *abort = 1;
@@ -153,6 +166,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 2 / 1 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 16 consecutive 32-bit columns, from registers.
@@ -178,6 +198,7 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 //    along K; 8-row K groups SBO bytes apart, 64-element MN blocks LBO bytes
 //    apart. Advancing K by 16 = +2 groups = +2*SBO bytes.
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzleNone = 0;
 
 __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                                uint32_t swizzle) {
@@ -199,6 +220,24 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_m
          | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
          | ((uint32_t)(N >> 3) << 17)               // N / 8
          | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
+// phi(x) = elu(x) + 1 on a pair of bf16 values, in bf16 arithmetic:
+//   phi(x) = max(x, 0) + min(e^x, 1)
+// (x >= 0: e^x >= 1, so the sum is x + 1 with one rounding; x < 0: 0 + e^x).
+// e^x = 2^(x log2 e) with the hardware base-2 exponential on bf16 pairs; the
+// product x log2 e is formed as fma(x, a, x b) with log2 e = a + b, a its bf16
+// head (1.4453125) and b the bf16 of the remainder (-0.00262451171875), so it
+// is rounded once. Exponents below the normal range flush to zero.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
+  uint32_t u, t, e, m, r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(u) : "r"(x), "r"(0xBB2CBB2Cu));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(0x3FB93FB9u), "r"(u));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(e) : "r"(e), "r"(0x3F803F80u));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(0u));
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(e));
+  return r;
 }
 
 // Pack two floats to a bf16x2 word (round to nearest even), lo in the low half.

@@ -6,24 +6,34 @@
 // distributivity argument of "Linear Attention: KV를 고정 크기 상태에 누적하기",
 // fig. 5; the state update is the recurrence of its section "상태 갱신과 읽기를
 // 식으로 정리하기" applied to C tokens at once):
-//   P    = phi(Q_c) phi(K_c)^T, masked to j <= t          (MMA1, TMEM fp32)
-//   O    = phi(Q_c) S_prev + P V_c                         (MMA3 + MMA2)
-//   den  = phi(Q_c) z_prev + P 1 + eps                     (CUDA cores, fp32)
-//   S   += phi(K_c)^T V_c,  z += phi(K_c)^T 1              (MMA4; z on CUDA cores)
+//   P    = phi(Q_c) phi(K_c)^T, masked to j <= t            MMA1 (tensor cores)
+//   O    = phi(Q_c) S_prev + P V_c                           MMA3, MMA2
+//   S   += phi(K_c)^T V_c                                    MMA4
+//   z   += column sums of phi(K_c)                           CUDA cores, fp32
+//   den  = phi(Q_c) z_prev + P 1 + eps                       CUDA cores, fp32
 //   out  = O / den
 // S lives in tensor memory in fp32 for the whole segment; its bf16 copy in
-// shared memory is the B operand of MMA3.
+// shared memory is the B operand of MMA3. The normaliser terms stay on the
+// CUDA cores: measured on GB300, a thin (N = 16) tcgen05.mma costs nearly as
+// much as a full-width one, while the row and column sums fall out of passes
+// the CUDA cores make anyway.
 //
 // Two kernels share the machinery:
 //   tc_state_kernel   per-segment sums dS = sum phi(k) v^T, dz = sum phi(k)
 //   tc_forward_kernel the chunk loop above, starting from the segment's prefix
-// (the CUDA-core scan kernel joins them). One CTA per (segment, b*h).
+// (the scan kernel joins them). One CTA per (segment, b*h).
 //
-// Warp roles in tc_forward_kernel (320 threads):
-//   warp 0      TMA producer: Q, K, V chunk tiles into a ring of stages
-//   warp 1      TMEM allocator and MMA issuer (one elected lane)
-//   warps 2-5   group A: phi in place on Q and K, z sums, S copy to smem
-//   warps 6-9   group B: P mask/rowsum/bf16 pack, output epilogue
+// Warp roles in tc_forward_kernel (448 threads):
+//   warps 0-3    group C: phi in place on K with the column sums that update z
+//   warps 4-7    group A: phi in place on Q; state copy S -> shared memory
+//   warps 8-11   group B: P mask, bf16 pack and row sums; denominators; epilogue
+//   warp 12      TMA producer: Q, K, V chunk tiles into a ring of stages
+//   warp 13      TMEM allocator and MMA issuer (one elected lane)
+// (the CUDA-core groups take the lowest warp ids, which the warp schedulers
+// favour; each group's four warps cover the four TMEM lane quadrants)
+// phi(K) is rounded to nearest from an fp32 exponential, since z is summed
+// from it; phi(Q) uses packed bf16 arithmetic (a common scale error of
+// phi(q) cancels between numerator and denominator).
 // Every wait is bounded; on a timeout the CTA sets the device status word,
 // drains, frees its tensor memory and exits.
 #include <cudaTypedefs.h>
@@ -49,13 +59,17 @@ struct Cfg {
   static constexpr int STAGE = 3 * TILE;              // Q, K, V
   static constexpr int SBUF = NB * D * 128;           // bf16 S copy, MN-major, D rows per box
   static constexpr int KSTEPS = D / 16;               // MMA k-steps over a head dimension
+  static constexpr int NPB = 2;                       // P buffers in tensor memory
   // tensor memory columns
-  static constexpr uint32_t COL_P0 = 0, COL_P1 = 128, COL_S = 256, COL_O = 256 + D;
+  static constexpr uint32_t COL_P = 0;                // NPB x 128
+  static constexpr uint32_t COL_S = 128 * NPB;        // D
+  static constexpr uint32_t COL_O = COL_S + D;        // D
   static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
   // state kernel
   static constexpr int ST_S = D == 128 ? 2 : 3;
   static constexpr int STAGE_S = 2 * TILE;            // K, V
-  static constexpr uint32_t TMEM_COLS_S = D < 32 ? 32 : D;
+  static constexpr uint32_t TMEM_COLS_S = D == 128 ? 128 : 64;
 };
 
 // Row of the D x D state held by lane `l` of TMEM quadrant `q` (rows live in
@@ -70,83 +84,104 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {  // byte offset 
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// phi on 8 packed bf16 values in place; when `acc` is given, also add the
-// unrounded fp32 phi values to it (column sums for z).
-__device__ __forceinline__ void phi_bf16x8(uint4& w, float* acc) {
-  uint32_t* p = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = phi_fast(__uint_as_float(p[i] << 16));
-    const float hi = phi_fast(__uint_as_float(p[i] & 0xFFFF0000u));
-    if (acc != nullptr) {
-      acc[2 * i] += lo;
-      acc[2 * i + 1] += hi;
-    }
-    p[i] = pack_bf16x2(lo, hi);
-  }
-}
-
 __device__ __forceinline__ void report_timeout(int* status) { atomicExch(status, (int)LA_ERR_TIMEOUT); }
 
-// Group A: phi in place on one [C][D] tile of stage memory; when `zacc` is
-// given, also the column sums of phi over rows < n_valid (thread t owns
-// logical 16-byte chunk t % 8 of each box and rows t/8 + 16 i).
-template <int D>
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int t, int n_valid, float (*zacc)[8]) {
-  constexpr int NB = D / 64;
-  const int lc = t & 7, rg = t >> 3;
+// phi on packed bf16 values, in place on one [C][D] tile (phi is elementwise,
+// so the swizzle does not matter); NT threads, thread t owns 16-byte chunks
+// t, t + NT, ...
+template <int D, int NT>
+__device__ __forceinline__ void phi_tile_bf16(uint8_t* tile, int t) {
+  constexpr int PER = (C * D * 2 / 16) / NT;
+  constexpr int GR = 4;
+#pragma unroll 1
+  for (int i0 = 0; i0 < PER; i0 += GR) {
+    uint4 w[GR];
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
+    for (int i = 0; i < GR; ++i) w[i] = reinterpret_cast<const uint4*>(tile)[t + NT * (i0 + i)];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = rg + 16 * i;
-      uint4* p = reinterpret_cast<uint4*>(tile + b * BOX + sw128(r, lc));
-      uint4 w = *p;
-      phi_bf16x8(w, (zacc != nullptr && r < n_valid) ? zacc[b] : nullptr);
-      *p = w;
+    for (int i = 0; i < GR; ++i) {
+      w[i].x = phi_bf16x2(w[i].x);
+      w[i].y = phi_bf16x2(w[i].y);
+      w[i].z = phi_bf16x2(w[i].z);
+      w[i].w = phi_bf16x2(w[i].w);
     }
+#pragma unroll
+    for (int i = 0; i < GR; ++i) reinterpret_cast<uint4*>(tile)[t + NT * (i0 + i)] = w[i];
   }
 }
 
-// Reduce the per-thread column partials of phi_tile across group A; thread f
-// (< D) receives the column sum of feature f in *colsum. zsum: [D] floats,
-// zero on entry and left zero on exit; zbar: an mbarrier of 128 arrivals used
-// as the group's rendezvous (bounded, unlike bar.sync). Callers alternate two
-// (zsum, zbar) pairs between chunks; `parity` is the pair's use count & 1.
-template <int D>
-__device__ __forceinline__ bool reduce_colsum(float (*zacc)[8], float* zsum, uint64_t* zbar, uint32_t parity,
-                                              int t, volatile int* abort_flag, float* colsum) {
-  constexpr int NB = D / 64;
-  const int lane = t & 31, lc = t & 7;
-#pragma unroll
-  for (int b = 0; b < NB; ++b)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float x = zacc[b][e];
-      x += __shfl_xor_sync(0xffffffffu, x, 8);
-      x += __shfl_xor_sync(0xffffffffu, x, 16);
-      if (lane < 8) atomicAdd(&zsum[b * 64 + lc * 8 + e], x);
-    }
-  mbar_arrive(zbar);
-  if (!mbar_wait(zbar, parity, abort_flag, kTimeoutNs)) return false;
-  float s = 0.f;
-  if (t < D) {
-    s = zsum[t];
-    zsum[t] = 0.f;
-  }
-  *colsum = s;
-  return true;
+// phi(x) in fp32 without branches: x + 1 for x > 0, e^x otherwise, with
+// e^x = 2^(x log2 e) from the hardware base-2 exponential (results below the
+// normal range flush to zero). Rounded to bf16 by the caller.
+__device__ __forceinline__ float phi_f32(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
+  return x > 0.f ? x + 1.f : e;
 }
 
-// Copy the fp32 state rows of this thread's TMEM lane to the bf16 MN-major
-// operand buffer (row r = key component, 64 value columns per box).
-template <int D>
-__device__ __forceinline__ void copy_state_to_smem(uint32_t taddr_lane, uint8_t* sbuf, int row) {
-  constexpr int NB = D / 64;
+// phi in place on one [C][D] tile, rounded to nearest, with fp32 column sums
+// over rows < n_valid (rows >= n_valid, past the end of the sequence, become
+// zero). NT threads; warp w owns FCW = D / (NT / 4) consecutive 16-byte
+// feature chunks of every row; lane l works on chunk FCW*w + l % FCW and rows
+// l / FCW + (32 / FCW) i. The column sums are reduced inside the warp, so on
+// return lanes l < FCW hold the sums of the 8 features of chunk FCW*w + l.
+template <int D, int NT>
+struct ExactLayout {
+  static constexpr int FCW = D / (NT / 4);     // feature chunks per warp
+  static constexpr int RG = 32 / FCW;          // row groups per warp
+  static constexpr int RPT = C / RG;           // rows per thread
+  static_assert(FCW >= 1 && FCW <= 8 && (FCW & (FCW - 1)) == 0, "layout");
+};
+
+template <int D, int NT>
+__device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8]) {
+  using X = ExactLayout<D, NT>;
+  constexpr int GR = 4;                               // rows per loop trip (kept small: code size)
+  const int w = t >> 5, lane = t & 31;
+  const int fc = X::FCW * w + (lane % X::FCW);       // feature chunk 0 .. D/8-1
+  const int r0 = lane / X::FCW;
+  uint8_t* base = tile + (fc >> 3) * BOX;
+  const int ch = fc & 7;
 #pragma unroll
+  for (int e = 0; e < 8; ++e) zacc[e] = 0.f;
+#pragma unroll 1
+  for (int i0 = 0; i0 < X::RPT; i0 += GR) {
+    uint4 wv[GR];
+#pragma unroll
+    for (int i = 0; i < GR; ++i) wv[i] = *reinterpret_cast<const uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch));
+#pragma unroll
+    for (int i = 0; i < GR; ++i) {
+      const bool valid = r0 + X::RG * (i0 + i) < n_valid;
+      uint32_t* p = reinterpret_cast<uint32_t*>(&wv[i]);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float lo = valid ? phi_f32(__uint_as_float(p[h] << 16)) : 0.f;
+        const float hi = valid ? phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)) : 0.f;
+        zacc[2 * h] += lo;
+        zacc[2 * h + 1] += hi;
+        p[h] = pack_bf16x2(lo, hi);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < GR; ++i) *reinterpret_cast<uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch)) = wv[i];
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float x = zacc[e];
+#pragma unroll
+    for (int o = X::FCW; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    zacc[e] = x;
+  }
+}
+
+// Copy this thread's TMEM lane of S (fp32, D columns) to the bf16 MN-major
+// operand buffer (row = key component, 64 value columns per box).
+template <int D>
+__device__ __forceinline__ void copy_state_to_smem(uint32_t lane_addr, uint8_t* sbuf, int row) {
+#pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += 32) {
     uint32_t v[32];
-    tmem_ld32(taddr_lane + c0, v);
+    tmem_ld32(lane_addr + Cfg<D>::COL_S + c0, v);
     tmem_ld_wait();
     if (row >= 0) {
       const int b = c0 / 64, cb = (c0 % 64) / 8;  // box, first 16-byte chunk
@@ -161,18 +196,14 @@ __device__ __forceinline__ void copy_state_to_smem(uint32_t taddr_lane, uint8_t*
       }
     }
   }
-  (void)NB;
 }
 
 template <int D>
 struct FwdSmem {
-  // stage ring, then the S operand; all boxes 1024-byte aligned
-  static constexpr int OFF_STAGES = 0;
-  static constexpr int OFF_SBUF = Cfg<D>::ST * Cfg<D>::STAGE;
-  static constexpr int OFF_ZST = OFF_SBUF + Cfg<D>::SBUF;          // [ST][D] fp32
-  static constexpr int OFF_ZSUM = OFF_ZST + Cfg<D>::ST * D * 4;    // [2][D] fp32
-  static constexpr int OFF_BAR = OFF_ZSUM + 2 * D * 4;             // barriers
-  static constexpr int NBAR = 3 * Cfg<D>::ST + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 2;
+  static constexpr int OFF_SBUF = Cfg<D>::ST * Cfg<D>::STAGE;      // all boxes 1024-aligned
+  static constexpr int OFF_ZST = OFF_SBUF + Cfg<D>::SBUF;          // [ST][D] fp32: z before each staged chunk
+  static constexpr int OFF_BAR = OFF_ZST + Cfg<D>::ST * D * 4;
+  static constexpr int NBAR = 3 * Cfg<D>::ST + 2 * Cfg<D>::NPB + 5;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
 };
@@ -186,29 +217,27 @@ struct FwdParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const FwdParams prm) {
   using G = Cfg<D>;
   using L = FwdSmem<D>;
-  constexpr int ST = G::ST;
+  constexpr int ST = G::ST, NPB = G::NPB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   uint8_t* sbuf = sm + L::OFF_SBUF;
   float* zst = reinterpret_cast<float*>(sm + L::OFF_ZST);
-  float* zsum = reinterpret_cast<float*>(sm + L::OFF_ZSUM);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* phi_done = bars + ST;
   uint64_t* empty = bars + 2 * ST;
-  uint64_t* p_full = bars + 3 * ST;       // [2]
-  uint64_t* p_ready = bars + 3 * ST + 2;  // [2]
-  uint64_t* s_full = bars + 3 * ST + 4;
-  uint64_t* s_ready = bars + 3 * ST + 5;
-  uint64_t* o_full = bars + 3 * ST + 6;
-  uint64_t* o_empty = bars + 3 * ST + 7;
-  uint64_t* mma_fin = bars + 3 * ST + 8;
-  uint64_t* zbar = bars + 3 * ST + 9;     // [2]
+  uint64_t* p_full = bars + 3 * ST;              // [NPB]
+  uint64_t* p_ready = bars + 3 * ST + NPB;       // [NPB]
+  uint64_t* s_full = bars + 3 * ST + 2 * NPB;
+  uint64_t* s_ready = s_full + 1;
+  uint64_t* o_full = s_full + 2;
+  uint64_t* o_empty = s_full + 3;
+  uint64_t* mma_fin = s_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   // the swizzled operand boxes need 1024-byte alignment of the shared window
@@ -222,14 +251,15 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const float* st = prm.ws_state + ((long long)bh * prm.P + seg) * (long long)(D * D + D);
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&phi_done[i], 128);
+      mbar_init(&phi_done[i], 256);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NPB; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_ready[i], 128);
     }
@@ -238,13 +268,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     mbar_init(o_full, 1);
     mbar_init(o_empty, 128);
     mbar_init(mma_fin, 1);
-    mbar_init(&zbar[0], 128);
-    mbar_init(&zbar[1], 128);
-    for (int i = 0; i < 2 * D; ++i) zsum[i] = 0.f;
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, G::TMEM_COLS);
     tmem_relinquish();
   }
@@ -253,7 +280,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 12) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
@@ -263,14 +290,14 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % ST;
         if (c >= ST && !mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
-        uint8_t* st = sm + s * G::STAGE;
+        uint8_t* stg = sm + s * G::STAGE;
         mbar_arrive_expect_tx(&full[s], 3 * G::TILE);
         const int y = tok0 + c * C;
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
-          tma_load_3d(st + b * BOX, &map_q, &full[s], 64 * b, y, bh);
-          tma_load_3d(st + G::TILE + b * BOX, &map_k, &full[s], 64 * b, y, bh);
-          tma_load_3d(st + 2 * G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::TILE + b * BOX, &map_k, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + 2 * G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
         }
         issued = c + 1;
       }
@@ -278,7 +305,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       for (int c = max(0, issued - ST); c < issued; ++c)
         mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t id_qk = make_idesc_bf16(128, 128, false, false);   // P = phiQ phiK^T
@@ -292,7 +319,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const uint32_t qa = smem_u32(sm + s * G::STAGE);
         const uint32_t ka = qa + G::TILE;
         const uint32_t va = qa + 2 * G::TILE;
-        const uint32_t pcol = (c & 1) ? G::COL_P1 : G::COL_P0;
+        const int pb = c % NPB;
+        const uint32_t pcol = G::COL_P + 128 * pb;
         ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
@@ -302,23 +330,21 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           mma_ss(tmem + pcol, make_sdesc(qa + off, 16, 1024, kSwizzle128B),
                  make_sdesc(ka + off, 16, 1024, kSwizzle128B), id_qk, k > 0);
         }
-        tc_commit(&p_full[c & 1]);
+        tc_commit(&p_full[pb]);
         ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
         if (ok && c > 0) ok = mbar_wait(o_empty, (c - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < G::KSTEPS; ++k) {
-          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
-          mma_ss(tmem + G::COL_O, make_sdesc(qa + off, 16, 1024, kSwizzle128B),
+        for (int k = 0; k < G::KSTEPS; ++k)
+          mma_ss(tmem + G::COL_O, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
                  make_sdesc(sbuf_a + k * 2048, D * 128, 1024, kSwizzle128B), id_qs, k > 0);
-        }
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           mma_ss(tmem + G::COL_S, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B),
                  make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_kv, 1);
         tc_commit(s_full);
-        ok = mbar_wait(&p_ready[c & 1], (c >> 1) & 1, abort_flag, kTimeoutNs);
+        ok = mbar_wait(&p_ready[pb], (c / NPB) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -332,59 +358,54 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tc_commit(mma_fin);
       mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
     }
-  } else if (warp < 6) {
-    // ---------------- group A: phi, z, state copy ----------------
-    const int t = tid - 64;                 // 0..127
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- group A: phi(Q), state copy ----------------
+    const int t = tid - 128;                // 0..127
     const int q = warp & 3;                 // TMEM quadrant of this warp
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
-    // initial state: prefix of this segment, into TMEM (fp32) lanes
-    const float* st = prm.ws_state + ((long long)bh * prm.P + seg) * (long long)(D * D + D);
-    float zrun = (t < D) ? st[D * D + t] : 0.f;
+    // initial state (this segment's prefix) into TMEM
+    const float4* srow = reinterpret_cast<const float4*>(st + (row >= 0 ? row : 0) * D);
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      uint32_t v[16];
+    for (int h = 0; h < D; h += 64) {        // 64 columns per batch: 16 loads in flight
+      float4 f[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = row >= 0 ? __float_as_uint(st[row * D + c0 + j]) : 0u;
-      tmem_st16(lane_addr + G::COL_S + c0, v);
+      for (int j = 0; j < 16; ++j) f[j] = row >= 0 ? srow[h / 4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[4 * j + 0] = __float_as_uint(f[4 * g + j].x);
+          v[4 * j + 1] = __float_as_uint(f[4 * g + j].y);
+          v[4 * j + 2] = __float_as_uint(f[4 * g + j].z);
+          v[4 * j + 3] = __float_as_uint(f[4 * g + j].w);
+        }
+        tmem_st16(lane_addr + G::COL_S + h + 16 * g, v);
+      }
     }
     tmem_st_wait();
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
-      uint8_t* stg = sm + s * G::STAGE;
-      const int n_valid = min(C, tok_end - (tok0 + c * C));
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      float zacc[G::NB][8];
-#pragma unroll
-      for (int b = 0; b < G::NB; ++b)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) zacc[b][e] = 0.f;
-      phi_tile<D>(stg, t, C, nullptr);            // Q
-      phi_tile<D>(stg + G::TILE, t, n_valid, zacc);  // K, with column sums
-      float colsum = 0.f;
-      ok = reduce_colsum<D>(zacc, zsum + (c & 1) * D, &zbar[c & 1], (c >> 1) & 1, t, abort_flag, &colsum);
-      if (!ok) break;
-      if (t < D) {
-        zst[s * D + t] = zrun;  // z before this chunk, for group B's denominators
-        zrun += colsum;
-      }
+      phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);   // Q
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
-      // bf16 copy of the state before this chunk (after the previous update)
+      // bf16 copy of the state before chunk c (after the previous update)
       if (c > 0) {
         ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
       }
-      copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf, row);
+      copy_state_to_smem<D>(lane_addr, sbuf, row);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
     }
-  } else {
-    // ---------------- group B: P and the output epilogue ----------------
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------- group B: P, denominators and the output epilogue ----------------
     const int q = warp & 3;
     const int r = 32 * q + lane;            // chunk row (query token) of this thread
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
@@ -392,56 +413,72 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
-      const uint8_t* qt = sm + s * G::STAGE;
-      const uint32_t pcol = (c & 1) ? G::COL_P1 : G::COL_P0;
-      ok = mbar_wait(&p_full[c & 1], (c >> 1) & 1, abort_flag, kTimeoutNs) &&
+      const int pb = c % NPB;
+      const uint32_t pcol = G::COL_P + 128 * pb;
+      ok = mbar_wait(&p_full[pb], (c / NPB) & 1, abort_flag, kTimeoutNs) &&
            mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      // masked P row: fp32 row sum, bf16 pack back into the first 64 columns
+      // masked P row in bf16, packed into the first 64 columns of its buffer,
+      // and its fp32 row sum. Warp q holds rows 32q..32q+31: 32-column pieces
+      // left of q are kept whole, piece q is masked per lane, pieces right of
+      // q are zero.
       float rowsum = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < C; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + pcol + c0, v);
-        tmem_ld_wait();
+#pragma unroll 1
+      for (int p = 0; p < 4; ++p) {
         uint32_t pk[16];
+        if (p <= q) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + pcol + 32 * p, v);
+          tmem_ld_wait();
+          const int lim = p < q ? 32 : (r - 32 * p + 1);  // columns kept in this piece
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float a = (c0 + 2 * j <= r) ? __uint_as_float(v[2 * j]) : 0.f;
-          const float b = (c0 + 2 * j + 1 <= r) ? __uint_as_float(v[2 * j + 1]) : 0.f;
-          rowsum += a + b;
-          pk[j] = pack_bf16x2(a, b);
+          for (int j = 0; j < 16; ++j) {
+            const float a = (2 * j < lim) ? __uint_as_float(v[2 * j]) : 0.f;
+            const float b = (2 * j + 1 < lim) ? __uint_as_float(v[2 * j + 1]) : 0.f;
+            rowsum += a + b;
+            pk[j] = pack_bf16x2(a, b);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0u;
         }
-        tmem_st16(lane_addr + pcol + c0 / 2, pk);
+        tmem_st16(lane_addr + pcol + 16 * p, pk);
       }
       // phi(q_r) . z_prev from the phi-transformed Q tile (swizzled rows)
       float dot = 0.f;
-      const float* zp = zst + s * D;
+      {
+        const uint8_t* qt = sm + s * G::STAGE;
+        const float* zp = zst + s * D;
+#pragma unroll 1
+        for (int b = 0; b < G::NB; ++b)
 #pragma unroll
-      for (int b = 0; b < G::NB; ++b)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 w = *reinterpret_cast<const uint4*>(qt + b * BOX + sw128(r, ch));
-          const uint32_t* p = reinterpret_cast<const uint32_t*>(&w);
-          const int f = b * 64 + ch * 8;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            dot = fmaf(__uint_as_float(p[i] << 16), zp[f + 2 * i], dot);
-            dot = fmaf(__uint_as_float(p[i] & 0xFFFF0000u), zp[f + 2 * i + 1], dot);
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 w = *reinterpret_cast<const uint4*>(qt + b * BOX + sw128(r, ch));
+            const uint32_t* pw = reinterpret_cast<const uint32_t*>(&w);
+            const float4 z0 = *reinterpret_cast<const float4*>(zp + b * 64 + ch * 8);
+            const float4 z1 = *reinterpret_cast<const float4*>(zp + b * 64 + ch * 8 + 4);
+            dot = fmaf(__uint_as_float(pw[0] << 16), z0.x, dot);
+            dot = fmaf(__uint_as_float(pw[0] & 0xFFFF0000u), z0.y, dot);
+            dot = fmaf(__uint_as_float(pw[1] << 16), z0.z, dot);
+            dot = fmaf(__uint_as_float(pw[1] & 0xFFFF0000u), z0.w, dot);
+            dot = fmaf(__uint_as_float(pw[2] << 16), z1.x, dot);
+            dot = fmaf(__uint_as_float(pw[2] & 0xFFFF0000u), z1.y, dot);
+            dot = fmaf(__uint_as_float(pw[3] << 16), z1.z, dot);
+            dot = fmaf(__uint_as_float(pw[3] & 0xFFFF0000u), z1.w, dot);
           }
-        }
+      }
       const float inv_den = 1.f / (rowsum + dot + prm.eps);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_ready[c & 1]);
+      mbar_arrive(&p_ready[pb]);
       // output rows
       ok = mbar_wait(o_full, c & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
       const int tok = tok0 + c * C + r;
       uint4* dst = reinterpret_cast<uint4*>(outb + (long long)tok * D);
-#pragma unroll
+#pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(lane_addr + G::COL_O + c0, v);
@@ -461,28 +498,56 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tc_fence_before();
       mbar_arrive(o_empty);
     }
+  } else {
+    // ---------------- group C: phi(K) and z ----------------
+    using X = ExactLayout<D, 128>;
+    const int t = tid;                      // 0..127
+    const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    const bool owner = lane < X::FCW;       // holds the z of features 8 fc .. 8 fc + 7
+    float zrun[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) zrun[e] = owner ? st[D * D + 8 * fc + e] : 0.f;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST;
+      const int n_valid = min(C, tok_end - (tok0 + c * C));
+      ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      float colsum[8];
+      phi_tile_exact<D, 128>(sm + s * G::STAGE + G::TILE, t, n_valid, colsum);  // K
+      fence_proxy_async_smem();
+      if (owner) {
+        // z before this chunk, for group B's denominators
+        float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
+        zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
+        zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
+      }
+      mbar_arrive(&phi_done[s]);
+    }
   }
 
   // ---------------- teardown ----------------
   if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Per-segment state sums: dS = phi(K_seg)^T V_seg (tensor cores, fp32 in
-// TMEM), dz = column sums of phi(K_seg) (CUDA cores). 192 threads:
-// warp 0 TMA, warp 1 MMA, warps 2-5 phi + z + final store.
+// Per-segment state sums: dS = phi(K_seg)^T V_seg on the tensor cores into
+// TMEM (fp32), dz = column sums of phi(K_seg) on the CUDA cores (fp32).
+// 320 threads: warps 0-7 phi(K) (rounded to nearest) and z, warps 0-3 also
+// the final store of dS; warp 8 TMA, warp 9 TMEM allocator and MMA.
 // ---------------------------------------------------------------------------
 template <int D>
 struct StateSmem {
-  static constexpr int OFF_ZSUM = Cfg<D>::ST_S * Cfg<D>::STAGE_S;
-  static constexpr int OFF_BAR = OFF_ZSUM + 2 * D * 4;
-  static constexpr int NBAR = 3 * Cfg<D>::ST_S + 4;
+  static constexpr int OFF_BAR = Cfg<D>::ST_S * Cfg<D>::STAGE_S;
+  static constexpr int NBAR = 3 * Cfg<D>::ST_S + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
 };
@@ -494,7 +559,7 @@ struct StateParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const StateParams prm) {
   using G = Cfg<D>;
@@ -502,14 +567,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   constexpr int ST = G::ST_S;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
-  float* zsum = reinterpret_cast<float*>(sm + L::OFF_ZSUM);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* phi_done = bars + ST;
   uint64_t* empty = bars + 2 * ST;
   uint64_t* s_full = bars + 3 * ST;
   uint64_t* mma_fin = bars + 3 * ST + 1;
-  uint64_t* zbar = bars + 3 * ST + 2;     // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   if ((smem_u32(sm) & 1023u) != 0u) {
@@ -526,18 +589,15 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&phi_done[i], 128);
+      mbar_init(&phi_done[i], 256);
       mbar_init(&empty[i], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(mma_fin, 1);
-    mbar_init(&zbar[0], 128);
-    mbar_init(&zbar[1], 128);
-    for (int i = 0; i < 2 * D; ++i) zsum[i] = 0.f;
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, G::TMEM_COLS_S);
     tmem_relinquish();
   }
@@ -546,7 +606,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 8) {
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
@@ -554,20 +614,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % ST;
         if (c >= ST && !mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
-        uint8_t* st = sm + s * G::STAGE_S;
+        uint8_t* stg = sm + s * G::STAGE_S;
         mbar_arrive_expect_tx(&full[s], 2 * G::TILE);
         const int y = tok0 + c * C;
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
-          tma_load_3d(st + b * BOX, &map_k, &full[s], 64 * b, y, bh);
-          tma_load_3d(st + G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + b * BOX, &map_k, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
         }
         issued = c + 1;
       }
       for (int c = max(0, issued - ST); c < issued; ++c)
         mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t id_kv = make_idesc_bf16(D, D, true, true);
       bool ok = true;
@@ -589,34 +649,36 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
     }
   } else {
-    const int t = tid - 64;
+    using X = ExactLayout<D, 256>;
+    const int t = tid;                      // 0..255
     const int q = warp & 3;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
-    float zrun = 0.f;
+    const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    float zrun[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) zrun[e] = 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
-      uint8_t* stg = sm + s * G::STAGE_S;
       const int n_valid = min(C, tok_end - (tok0 + c * C));
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      float zacc[G::NB][8];
-#pragma unroll
-      for (int b = 0; b < G::NB; ++b)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) zacc[b][e] = 0.f;
-      phi_tile<D>(stg, t, n_valid, zacc);
-      float colsum = 0.f;
-      ok = reduce_colsum<D>(zacc, zsum + (c & 1) * D, &zbar[c & 1], (c >> 1) & 1, t, abort_flag, &colsum);
-      if (!ok) break;
-      zrun += colsum;
+      float colsum[8];
+      phi_tile_exact<D, 256>(sm + s * G::STAGE_S, t, n_valid, colsum);
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
     }
     float* dst = prm.ws_state + ((long long)bh * prm.P + seg) * (long long)(D * D + D);
-    if (ok) ok = mbar_wait(s_full, 0, abort_flag, kTimeoutNs);
-    if (ok) {
+    if (ok && lane < X::FCW) {
+      float4* zd = reinterpret_cast<float4*>(dst + D * D + 8 * fc);
+      zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
+      zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
+    }
+    if (ok && warp < 4) ok = mbar_wait(s_full, 0, abort_flag, kTimeoutNs);
+    if (ok && warp < 4) {
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -631,13 +693,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                             __uint_as_float(v[j + 3]));
         }
       }
-      if (t < D) dst[D * D + t] = zrun;
     }
   }
   if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS_S);
   }
@@ -686,7 +747,7 @@ cudaError_t launch_state(const FwdArgs& a) {
   e = cudaFuncSetAttribute(tc_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   StateParams p{a.N, a.plan.P, a.plan.seg_len, a.ws_state, device_status_ptr()};
-  tc_state_kernel<D><<<a.BH * a.plan.P, 192, smem, a.stream>>>(mk, mv, p);
+  tc_state_kernel<D><<<a.BH * a.plan.P, 320, smem, a.stream>>>(mk, mv, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -704,7 +765,7 @@ cudaError_t launch_forward(const FwdArgs& a) {
   e = cudaFuncSetAttribute(tc_forward_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   FwdParams p{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, (__nv_bfloat16*)a.out, device_status_ptr()};
-  tc_forward_kernel<D><<<a.BH * a.plan.P, 320, smem, a.stream>>>(mq, mk, mv, p);
+  tc_forward_kernel<D><<<a.BH * a.plan.P, 448, smem, a.stream>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;

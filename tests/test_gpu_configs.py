@@ -16,7 +16,7 @@ import pytest
 import oracle as orc
 import causal_linear_attention_la_gb300 as la
 from causal_linear_attention_la_gb300 import synth
-from helpers import STATE_TOL, TOL, build_lib, grad_errors, rel_err, to_dev, to_host
+from helpers import STATE_TOL, TOL, Z_TOL, build_lib, grad_errors, rel_err, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,7 @@ def test_forward_b2_h16_n32768_d128_sampled():
         fk = orc.phi_elu1(k[b, h])
         S_ref = fk.T @ v[b, h].astype(np.float64)
         assert rel_err(to_host(S[b, h]), S_ref, np.abs(S_ref).max()) <= STATE_TOL["bf16"]
-        assert rel_err(to_host(z[b, h]), fk.sum(0), fk.sum(0).max()) <= 1e-5
+        assert rel_err(to_host(z[b, h]), fk.sum(0), fk.sum(0).max()) <= Z_TOL["bf16"]
 
 
 def test_decode_b64_h32_d128_from_prefill_n131072():

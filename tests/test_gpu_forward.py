@@ -10,7 +10,7 @@ import pytest
 import oracle as orc
 import causal_linear_attention_la_gb300 as la
 from causal_linear_attention_la_gb300 import synth
-from helpers import STATE_TOL, TOL, build_lib, rel_err, to_dev, to_host
+from helpers import STATE_TOL, TOL, Z_TOL, build_lib, rel_err, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -80,7 +80,7 @@ def test_forward_shapes(B, H, N, dk, dv, causal, dtype, path):
     # final state, relative to its own magnitude (see STATE_TOL)
     s_err = rel_err(to_host(S), S_ref, np.abs(S_ref).max())
     z_err = rel_err(to_host(z), z_ref, np.abs(z_ref).max())
-    assert s_err <= STATE_TOL[dtype] and z_err <= 1e-5, (s_err, z_err)
+    assert s_err <= STATE_TOL[dtype] and z_err <= Z_TOL[dtype], (s_err, z_err)
 
 
 def test_forward_eps_zero_and_large():
