@@ -29,13 +29,14 @@ __all__ = [
     "la_forward_workspace_size", "la_backward_workspace_size",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
-    "la_device_status",
+    "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "forward", "decode_step", "backward",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_F32, LA_BF16 = 0, 1
 LA_PATH_AUTO, LA_PATH_SIMT = 0, 1
+LA_NOALLOC_SCRATCH_BYTES = 16 << 20   # include/la.h
 SPAN_NAMES = ("fwd_state", "fwd_scan", "fwd_output", "decode", "bwd_state",
               "bwd_sweep1", "bwd_scan", "bwd_sweep2")
 
@@ -46,7 +47,7 @@ exported_symbols = (
     "la_backward_workspace_size", "la_backward",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
-    "la_device_status",
+    "la_device_status", "la_forward_noalloc",
 )
 
 
@@ -101,6 +102,9 @@ def lib():
     h.la_backward_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
     h.la_device_status.restype = _c_int
     h.la_device_status.argtypes = [_c_int]
+    h.la_forward_noalloc.restype = _c_int
+    h.la_forward_noalloc.argtypes = ([_c_void] * 4 + [_c_int] * 6 + [_c_float, _c_int]
+                                     + [_c_void, _c_void, _c_void])
     h.la_profile_enable.restype = _c_int
     h.la_profile_enable.argtypes = [_c_int]
     h.la_profile_read.restype = _c_int
@@ -136,6 +140,14 @@ def la_forward(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype, S_final,
     return lib().la_forward(q, k, v, out, B, H, N, dk, dv, int(causal), eps,
                             dtype, S_final, z_final, workspace,
                             workspace_bytes, stream)
+
+
+def la_forward_noalloc(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype,
+                       S_final, z_final, stream):
+    """la_forward with its scratch in the library's static device array
+    (no allocation; see include/la.h)."""
+    return lib().la_forward_noalloc(q, k, v, out, B, H, N, dk, dv, int(causal),
+                                    eps, dtype, S_final, z_final, stream)
 
 
 def la_decode_step(S, z, q, k, v, out, B, H, dk, dv, eps, dtype, stream):

@@ -148,6 +148,8 @@ void prof_end(int label, cudaStream_t stream) {
 
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+la_status set_error(la_status s, const char* msg) { return fail(s, "%s", msg); }
+
 int* device_status_ptr() {
   static std::mutex mu;
   static int* cache[128] = {};

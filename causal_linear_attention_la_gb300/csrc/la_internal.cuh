@@ -94,6 +94,9 @@ cudaError_t tc_forward_output(const FwdArgs& a);
 // kernel whose bounded wait gave up); NULL if it cannot be resolved.
 int* device_status_ptr();
 
+// Record a one-line reason for `s` as this thread's la_last_error; returns s.
+la_status set_error(la_status s, const char* msg);
+
 // scan modes
 enum { SCAN_EXCLUSIVE_FWD = 0, SCAN_EXCLUSIVE_REV = 1, SCAN_TOTAL = 2 };
 

@@ -194,6 +194,41 @@ LA_API int la_backward_path(int dk, int dv, la_dtype dtype, int causal);
 LA_API la_status la_device_status(int clear);
 
 /*
+ * Forward pass for callers that cannot allocate device memory.
+ *
+ * The pages describe no counterpart to this entry point: it exists for
+ * integration. la_forward needs scratch memory, which callers normally
+ * allocate once and pass in. Some callers cannot: code that runs while a
+ * stream is being captured into a CUDA graph (cudaMalloc is not a stream
+ * operation and cannot be captured), plugin or custom-operator hosts that own
+ * all device memory and hand an operator only its input and output buffers,
+ * and latency-critical serving loops where cudaMalloc's implicit device
+ * synchronisation is unacceptable.
+ *
+ * la_forward_noalloc computes exactly what la_forward computes, with the
+ * same arguments except the workspace, which here is a file-scope device
+ * array of LA_NOALLOC_SCRATCH_BYTES inside the library. Every GPU that loads
+ * the library holds that array until the process exits.
+ *
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Problems whose scratch (la_forward_workspace_size) exceeds
+ *    LA_NOALLOC_SCRATCH_BYTES are rejected with LA_ERR_INVALID_ARG before
+ *    anything is launched.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents; nothing in it needs to start at zero (each call writes every
+ *    record it reads). Calls whose GPU work overlaps (different streams
+ *    without ordering) race on the array: order them on one stream.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+LA_API la_status la_forward_noalloc(const void* q, const void* k, const void* v, void* out,
+                                    int B, int H, int N, int dk, int dv, int causal,
+                                    float eps, la_dtype dtype, float* S_final,
+                                    float* z_final, la_stream_t stream);
+
+/*
  * Measurement hooks (no effect on results).
  *
  * la_profile_enable(1) clears the record and starts timing: every later call

@@ -1,0 +1,71 @@
+"""la_forward_noalloc, the forward entry point for callers that cannot
+allocate device memory (graph-capture regions, operator hosts that own all
+device memory, latency-critical loops): its scratch is a static device array
+inside the library instead of a caller-provided workspace.
+
+Through the C ABI, two calls in a row must each match la_forward (with a
+caller-allocated workspace) on the same inputs, within the parity tolerance
+of the other tests; a problem whose scratch exceeds the static array must be
+rejected before anything is launched. Collected last so that a failure here
+never hides the results of the other GPU tests.
+"""
+
+import numpy as np
+import pytest
+
+import causal_linear_attention_la_gb300 as la
+from causal_linear_attention_la_gb300 import synth
+from helpers import STATE_TOL, TOL, build_lib, rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build_lib()
+    la.lib()
+
+
+def _noalloc(q, k, v, causal, code):
+    import torch
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    out = torch.empty((B, H, N, dv), dtype=q.dtype, device=q.device)
+    S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    z = torch.empty((B, H, dk), dtype=torch.float32, device=q.device)
+    st = la.la_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               B, H, N, dk, dv, causal, 1e-6, code, S.data_ptr(),
+                               z.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == la.LA_OK, la.lib().la_last_error()
+    return out, S, z
+
+
+@pytest.mark.parametrize("dtype,shape", [("bf16", (4, 8, 4096, 64, 64)),
+                                         ("f32", (1, 2, 1000, 32, 64))])
+def test_noalloc_matches_forward_on_two_calls(dtype, shape):
+    import torch
+    B, H, N, dk, dv = shape
+    code = la.LA_BF16 if dtype == "bf16" else la.LA_F32
+    assert la.la_forward_workspace_size(B, H, N, dk, dv, 1, code) <= la.LA_NOALLOC_SCRATCH_BYTES
+    for seed in (41, 42):   # two calls in a row reuse the same static scratch
+        q, k, v = synth.qkv(B, H, N, dk, dv, seed=seed, dtype=dtype)
+        qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
+        ref, S_ref, z_ref = la.forward(qd, kd, vd, return_state=True)
+        out, S, z = _noalloc(qd, kd, vd, True, code)
+        torch.cuda.synchronize()
+        assert rel_err(to_host(out), to_host(ref), np.abs(v).max()) <= TOL[dtype]
+        S_ref_h = to_host(S_ref)
+        assert rel_err(to_host(S), S_ref_h, np.abs(S_ref_h).max()) <= STATE_TOL[dtype]
+        assert la.la_device_status(True) == la.LA_OK
+
+
+def test_noalloc_rejects_oversized_problem():
+    B, H, N, d = 2, 16, 32768, 128
+    need = la.la_forward_workspace_size(B, H, N, d, d, 1, la.LA_BF16)
+    assert need > la.LA_NOALLOC_SCRATCH_BYTES
+    st = la.la_forward_noalloc(None, None, None, None, B, H, N, d, d, 1, 1e-6,
+                               la.LA_BF16, None, None, None)
+    assert st == la.LA_ERR_INVALID_ARG
+    assert b"static array" in la.lib().la_last_error()
