@@ -50,7 +50,7 @@ def _digest(paths):
     h = hashlib.sha256()
     for p in paths:
         with open(p, "rb") as f:
-            h.update(p.encode())
+            h.update(os.path.relpath(p, PKG).encode())
             h.update(f.read())
     h.update(" ".join(NVCC_FLAGS).encode())
     return h.hexdigest()
