@@ -227,9 +227,8 @@ int la_forward_path(int dk, int dv, la_dtype dtype, int causal) {
 }
 
 int la_backward_path(int dk, int dv, la_dtype dtype, int causal) {
-  (void)causal;
   if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16)) return -1;
-  return 0;
+  return (g_path.load() == LA_PATH_AUTO && tc_backward_supported(dk, dv, dtype, causal != 0)) ? 1 : 0;
 }
 
 size_t la_forward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
@@ -394,7 +393,10 @@ la_status la_backward(const void* q, const void* k, const void* v,
   a.ws_rev = (float*)((char*)workspace + w.rev_off);
   a.ws_tok = (float*)((char*)workspace + w.tok_off);
   a.plan = plan; a.stream = (cudaStream_t)stream;
-  cudaError_t e = simt_backward(a);
+  const bool use_tc = g_path.load() == LA_PATH_AUTO && tc_backward_supported(dk, dv, dtype, a.causal);
+  if (use_tc && device_status_ptr() == nullptr)
+    return fail(LA_ERR_CUDA, "la_backward: device status word unavailable");
+  cudaError_t e = use_tc ? tc_backward(a) : simt_backward(a);
   if (e != cudaSuccess) return cuda_fail(e, "la_backward");
   return LA_OK;
 }

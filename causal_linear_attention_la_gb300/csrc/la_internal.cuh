@@ -89,6 +89,9 @@ cudaError_t decode_step(const DecodeArgs& a);
 bool tc_forward_supported(int dk, int dv, la_dtype dtype, int causal);
 cudaError_t tc_segment_state(const FwdArgs& a);
 cudaError_t tc_forward_output(const FwdArgs& a);
+// Tensor-core backward (bf16, dk = dv = 64, causal): state pass, scan, two sweeps
+bool tc_backward_supported(int dk, int dv, la_dtype dtype, int causal);
+cudaError_t tc_backward(const BwdArgs& a);
 
 // Device status word of the current device (set to LA_ERR_TIMEOUT by a
 // kernel whose bounded wait gave up); NULL if it cannot be resolved.

@@ -1,0 +1,1039 @@
+// Tensor-core (tcgen05) backward for bf16 inputs, causal, dk = dv = 64,
+// chunks of C = 128 tokens.
+//
+// Gradients of L = sum(dout * out) by cumulative sums, with no per-token
+// state stored ("Transformers are RNNs" review, section "그래디언트 계산 —
+// 선형 시간·상수 메모리" names the method; its formulas did not survive on
+// the page and are derived here from the forward definition). With
+// g_t = dout_t, D_t = phi(q_t).z_t + eps (inclusive z_t) and
+// o_t = S_t^T phi(q_t) / D_t:
+//   a_t = g_t / D_t,  b_t = -(g_t . o_t) / D_t
+//   dphi(q_t) = S_t a_t + b_t z_t
+//   R_j = sum_{t>=j} phi(q_t) a_t^T,  r_j = sum_{t>=j} b_t phi(q_t)
+//   dphi(k_j) = R_j v_j + r_j,  dv_j = R_j^T phi(k_j)
+//   dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k),  phi'(x) = min(phi(x), 1)
+//
+// Sweep 1 (forward through each segment, from the segment's prefix S, z):
+//   P    = phi(Q) phi(K)^T, masked j <= t           MMA (both K-major)
+//   O    = phi(Q) S_prev + P V                      MMA, MMA (P from TMEM)
+//   S   += phi(K)^T V                               MMA
+//   den  = phi(Q) z_prev + P 1 + eps;  a = g / den;  b = -(g . O) / den^2
+//   dP   = a V^T;  dP' = (dP + b) masked j <= t     MMA, CUDA cores
+//   dQ   = a S_prev^T + dP' phi(K) + b z_prev        MMA, MMA, epilogue
+//   R   += phi(Q)^T a;  r += phi(Q)^T b             MMA, CUDA cores
+// writing dq, (den, b) per token and the segment's (R, r) sums.
+// Sweep 2 (backward through each segment, from the suffix R, r after it):
+//   P^T  = phi(K) phi(Q)^T, masked t >= j           MMA
+//   dP^T = V a^T;  dP^T' = (dP^T + b_t) masked      MMA, CUDA cores
+//   dK   = V R_after^T + dP^T' phi(Q) + r_after     MMA, MMA, epilogue
+//   dV   = phi(K) R_after + P^T' a                  MMA, MMA
+//   R   += phi(Q)^T a;  r += phi(Q)^T b
+// The segment sums are joined by the state pass and the scan kernel.
+//
+// Every wait is bounded; on a timeout the CTA sets the device status word,
+// drains, frees its tensor memory and exits. Barriers that a consumer may
+// reach more than one phase late are double-buffered by chunk parity.
+#include "la_tc_common.cuh"
+
+namespace la {
+
+namespace {
+
+using namespace sm100;
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 16-byte chunk `ch` (features 8 ch .. 8 ch + 7) of row r of a [C][D] tile
+// stored as 64-feature SW128 boxes.
+__device__ __forceinline__ uint4 ld_chunk(const uint8_t* tile, int r, int ch) {
+  return *reinterpret_cast<const uint4*>(tile + (ch >> 3) * BOX + sw128(r, ch & 7));
+}
+__device__ __forceinline__ void st_chunk(uint8_t* tile, int r, int ch, uint4 v) {
+  *reinterpret_cast<uint4*>(tile + (ch >> 3) * BOX + sw128(r, ch & 7)) = v;
+}
+
+// Causal mask of one 128-column fp32 row in tensor memory (row r = 32 q +
+// lane of the chunk), packed to bf16 into the row's first 64 columns. kLower
+// keeps columns j <= r (query rows against key columns), otherwise j >= r (key
+// rows against query columns). Kept entries get `add_row` added, and with
+// kColAdd also add_col[j]. Returns the sum of the kept fp32 entries.
+template <bool kLower, bool kColAdd>
+__device__ __forceinline__ float mask_pack_row(uint32_t taddr, int q, int lane, float add_row, const float* add_col) {
+  float sum = 0.f;
+#pragma unroll 1
+  for (int p = 0; p < 4; ++p) {
+    uint32_t pk[16];
+    const bool live = kLower ? (p <= q) : (p >= q);
+    if (live) {
+      uint32_t v[32];
+      tmem_ld32(taddr + 32 * p, v);
+      float cb[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) cb[j] = 0.f;
+      if (kColAdd) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 f = reinterpret_cast<const float4*>(add_col + 32 * p)[j];
+          cb[4 * j] = f.x; cb[4 * j + 1] = f.y; cb[4 * j + 2] = f.z; cb[4 * j + 3] = f.w;
+        }
+      }
+      tmem_ld_wait();
+      const int lo = kLower ? 0 : (p == q ? lane : 0);       // kept columns [lo, hi)
+      const int hi = kLower ? (p == q ? lane + 1 : 32) : 32;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int e0 = 2 * j, e1 = 2 * j + 1;
+        const float x0 = (e0 >= lo && e0 < hi) ? __uint_as_float(v[e0]) + add_row + cb[e0] : 0.f;
+        const float x1 = (e1 >= lo && e1 < hi) ? __uint_as_float(v[e1]) + add_row + cb[e1] : 0.f;
+        sum += x0 + x1;
+        pk[j] = pack_bf16x2(x0, x1);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[j] = 0u;
+    }
+    tmem_st16(taddr + 16 * p, pk);
+  }
+  return sum;
+}
+
+// phi(q_r) . z for row r of the phi-transformed Q tile (bf16) and fp32 z.
+template <int D>
+__device__ __forceinline__ float phiq_dot(const uint8_t* qtile, int r, const float* z) {
+  float dot = 0.f;
+#pragma unroll 2
+  for (int ch = 0; ch < D / 8; ++ch) {
+    const uint4 w = ld_chunk(qtile, r, ch);
+    const uint32_t* pw = reinterpret_cast<const uint32_t*>(&w);
+    const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * ch);
+    const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * ch + 4);
+    dot = fmaf(bf_lo(pw[0]), z0.x, dot);
+    dot = fmaf(bf_hi(pw[0]), z0.y, dot);
+    dot = fmaf(bf_lo(pw[1]), z0.z, dot);
+    dot = fmaf(bf_hi(pw[1]), z0.w, dot);
+    dot = fmaf(bf_lo(pw[2]), z1.x, dot);
+    dot = fmaf(bf_hi(pw[2]), z1.y, dot);
+    dot = fmaf(bf_lo(pw[3]), z1.z, dot);
+    dot = fmaf(bf_hi(pw[3]), z1.w, dot);
+  }
+  return dot;
+}
+
+// Row pass of sweep 1: with the numerator row O_r (fp32, tensor memory) and
+// the upstream-gradient row g_r (bf16, G tile), return beta = g_r . O_r and
+// overwrite g_r in place with a_r = g_r * inv_den (bf16, nearest).
+template <int D>
+__device__ __forceinline__ float grad_row_pass(uint32_t taddr, uint8_t* gtile, int r, float inv_den) {
+  float beta = 0.f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c0, v);
+    uint4 gw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) gw[j] = ld_chunk(gtile, r, c0 / 8 + j);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(&gw[j]);
+      uint4 o;
+      uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float g0 = bf_lo(pw[h]), g1 = bf_hi(pw[h]);
+        beta = fmaf(g0, __uint_as_float(v[8 * j + 2 * h]), beta);
+        beta = fmaf(g1, __uint_as_float(v[8 * j + 2 * h + 1]), beta);
+        po[h] = pack_bf16x2(g0 * inv_den, g1 * inv_den);
+      }
+      st_chunk(gtile, r, c0 / 8 + j, o);
+    }
+  }
+  return beta;
+}
+
+// Epilogue row of a gradient: x = acc (tensor memory) + add_s * add_v, times
+// phi'(.) = min(phi, 1) read from row r of a phi-transformed tile, stored to
+// dst (bf16) unless dst is null. add_v is an fp32 vector of D entries.
+template <int D>
+__device__ __forceinline__ void grad_epilogue(uint32_t taddr, const uint8_t* ftile, int r, float add_s,
+                                              const float* add_v, __nv_bfloat16* dst) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c0, v);
+    uint4 fw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) fw[j] = ld_chunk(ftile, r, c0 / 8 + j);
+    tmem_ld_wait();
+    if (dst != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(&fw[j]);
+        const float4 a0 = *reinterpret_cast<const float4*>(add_v + c0 + 8 * j);
+        const float4 a1 = *reinterpret_cast<const float4*>(add_v + c0 + 8 * j + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        uint4 o;
+        uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float x0 = fmaf(add_s, av[2 * h], __uint_as_float(v[8 * j + 2 * h])) * fminf(bf_lo(pw[h]), 1.f);
+          const float x1 =
+              fmaf(add_s, av[2 * h + 1], __uint_as_float(v[8 * j + 2 * h + 1])) * fminf(bf_hi(pw[h]), 1.f);
+          po[h] = pack_bf16x2(x0, x1);
+        }
+        reinterpret_cast<uint4*>(dst)[c0 / 8 + j] = o;
+      }
+    }
+  }
+}
+
+// Plain bf16 store of an fp32 tensor-memory row (D columns).
+template <int D>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c0, v);
+    tmem_ld_wait();
+    if (dst != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 o;
+        o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+        o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+        o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+        o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+        reinterpret_cast<uint4*>(dst)[c0 / 8 + j] = o;
+      }
+    }
+  }
+}
+
+// A D x D fp32 state from global memory (row-major) into tensor memory at
+// column `col` (rows in the M = D accumulator layout).
+template <int D>
+__device__ __forceinline__ void load_state_to_tmem(const float* src, uint32_t lane_addr, uint32_t col, int row) {
+  const float4* srow = reinterpret_cast<const float4*>(src + (row >= 0 ? row : 0) * D);
+#pragma unroll
+  for (int h = 0; h < D; h += 64) {
+    float4 f[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = row >= 0 ? srow[h / 4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[4 * j + 0] = __float_as_uint(f[4 * g + j].x);
+        v[4 * j + 1] = __float_as_uint(f[4 * g + j].y);
+        v[4 * j + 2] = __float_as_uint(f[4 * g + j].z);
+        v[4 * j + 3] = __float_as_uint(f[4 * g + j].w);
+      }
+      tmem_st16(lane_addr + col + h + 16 * g, v);
+    }
+  }
+  tmem_st_wait();
+}
+
+// A D x D fp32 state from tensor memory (column `col`) to global memory.
+template <int D>
+__device__ __forceinline__ void store_state_from_tmem(float* dst, uint32_t lane_addr, uint32_t col, int row) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(lane_addr + col + c0, v);
+    tmem_ld_wait();
+    if (row >= 0) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dst + row * D + c0 + j) =
+            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                        __uint_as_float(v[j + 3]));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Sweep 1
+// ---------------------------------------------------------------------------
+template <int D>
+struct B1 {
+  static_assert(D == 64, "the tensor-core backward is laid out for D = 64");
+  static constexpr int NB = D / 64;
+  static constexpr int TILE = NB * BOX;
+  static constexpr int ST = 3;                        // stages of Q, K, V, G
+  static constexpr int STAGE = 4 * TILE;
+  static constexpr int SBUF = NB * D * 128;           // bf16 copy of S_prev
+  static constexpr int NSB = 2;
+  static constexpr int KSTEPS = D / 16;
+  // tensor memory columns
+  static constexpr uint32_t COL_PD = 0;               // 2 x 128: P, then dP (fp32, bf16 packed in place)
+  static constexpr uint32_t COL_OQ = 256;             // 2 x D: O, then dQ
+  static constexpr uint32_t COL_S = COL_OQ + 2 * D;   // D
+  static constexpr uint32_t COL_R = COL_S + D;        // D
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(COL_R + D <= TMEM_COLS, "tensor memory budget");
+  // shared memory
+  static constexpr int OFF_SBUF = ST * STAGE;
+  static constexpr int OFF_ZST = OFF_SBUF + NSB * SBUF;   // [ST][D] z before each staged chunk
+  static constexpr int OFF_BARR = OFF_ZST + ST * D * 4;   // [ST][C] b_t of each staged chunk
+  static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
+  static constexpr int NBAR = 3 * ST + 21;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static constexpr int THREADS = 576;
+};
+
+struct Bwd1Params {
+  int N, P, seg_len;
+  float eps;
+  const float* ws_state;   // [BH][P][D*D + D] prefixes (S, z) before each segment
+  float* ws_rev;           // [BH][P][D*D + D] segment sums (R, r)
+  float* ws_tok;           // [BH][N][2] (den, b) per token
+  __nv_bfloat16* dq;       // [BH][N][D]
+  int* status;
+};
+
+// Warp roles (576 threads):
+//   warps 0-3    group C: phi(K) in place (exact fp32, rounded) and z; the r sums
+//   warps 4-7    group A: phi(Q) in place; bf16 copies of S_prev; final R store
+//   warps 8-11   group B: P mask/pack and row sums, den, a and b (row pass)
+//   warps 12-15  group D: dP' mask/pack, dq epilogue
+//   warp 16      TMA producer (Q, K, V, G)
+//   warp 17      TMEM allocator and MMA issuer
+template <int D>
+__global__ void __launch_bounds__(576, 1)
+tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+               const Bwd1Params prm) {
+  using G = B1<D>;
+  constexpr int ST = G::ST;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  uint8_t* sbuf = sm + G::OFF_SBUF;
+  float* zst = reinterpret_cast<float*>(sm + G::OFF_ZST);
+  float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
+  uint64_t* full = bars;                 // [ST]
+  uint64_t* phi_done = bars + ST;        // [ST]
+  uint64_t* empty = bars + 2 * ST;       // [ST]
+  uint64_t* x = bars + 3 * ST;
+  uint64_t* p_full = x;                  // [2]
+  uint64_t* p_ready = x + 2;             // [2]
+  uint64_t* sb_free = x + 4;             // [2]
+  uint64_t* o_full = x + 6;              // [2]
+  uint64_t* a_ready = x + 8;             // [2]
+  uint64_t* dp_full = x + 10;            // [2]
+  uint64_t* dp_ready = x + 12;           // [2]
+  uint64_t* dq_full = x + 14;            // [2]
+  uint64_t* oq_empty = x + 16;           // [2]
+  uint64_t* s_full = x + 18;
+  uint64_t* s_ready = x + 19;
+  uint64_t* mma_fin = x + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G::OFF_MISC + 4);
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) report_timeout(prm.status);
+    return;
+  }
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / prm.P, seg = blockIdx.x % prm.P;
+  const int tok0 = seg * prm.seg_len;
+  const int tok_end = min(prm.N, tok0 + prm.seg_len);
+  const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const long long rec = ((long long)bh * prm.P + seg) * (long long)(D * D + D);
+
+  if (tid == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&phi_done[i], 256);
+      mbar_init(&empty[i], 1 + 128 + 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&p_ready[i], 128);
+      mbar_init(&sb_free[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&a_ready[i], 128);
+      mbar_init(&dp_full[i], 1);
+      mbar_init(&dp_ready[i], 128);
+      mbar_init(&dq_full[i], 1);
+      mbar_init(&oq_empty[i], 128);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_ready, 128);
+    mbar_init(mma_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 17) {
+    tmem_alloc(tmem_slot, G::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 16) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_g);
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % ST;
+        if (c >= ST && !mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
+        uint8_t* stg = sm + s * G::STAGE;
+        mbar_arrive_expect_tx(&full[s], 4 * G::TILE);
+        const int y = tok0 + c * C;
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b) {
+          tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::TILE + b * BOX, &map_k, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + 2 * G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + 3 * G::TILE + b * BOX, &map_g, &full[s], 64 * b, y, bh);
+        }
+        issued = c + 1;
+      }
+      for (int c = max(0, issued - ST); c < issued; ++c)
+        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+    }
+  } else if (warp == 17) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_qk = make_idesc_bf16(128, 128, false, false);  // P = phiQ phiK^T, dP = a V^T
+      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, true);     // O = phiQ S_prev
+      constexpr uint32_t id_as = make_idesc_bf16(128, D, false, false);    // dQ = a S_prev^T
+      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // S += phiK^T V, R += phiQ^T a
+      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V, dQ += dP' phiK
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % ST, pb = c & 1, sbi = c % G::NSB;
+        const uint32_t qa = smem_u32(sm + s * G::STAGE);
+        const uint32_t ka = qa + G::TILE, va = qa + 2 * G::TILE, ga = qa + 3 * G::TILE;
+        const uint32_t sb = smem_u32(sbuf + sbi * G::SBUF);
+        const uint32_t pd = tmem + G::COL_PD + 128 * pb;
+        const uint32_t oq = tmem + G::COL_OQ + D * pb;
+        ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        // the P/dP and O/dQ buffers of chunk c - 2 are free once its last MMA is done
+        if (ok && c >= 2) ok = mbar_wait(&dq_full[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k) {
+          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
+          mma_ss(pd, make_sdesc(qa + off, 16, 1024, kSwizzle128B), make_sdesc(ka + off, 16, 1024, kSwizzle128B),
+                 id_qk, k > 0);
+        }
+        tc_commit(&p_full[pb]);
+        ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
+        if (ok && c >= 2) ok = mbar_wait(&oq_empty[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k)
+          mma_ss(oq, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
+                 make_sdesc(sb + k * 2048, D * 128, 1024, kSwizzle128B), id_qs, k > 0);
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ss(tmem + G::COL_S, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B),
+                 make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_tt, 1);
+        tc_commit(s_full);
+        ok = mbar_wait(&p_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ts(oq, pd + k * 8, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+        tc_commit(&o_full[pb]);
+        ok = mbar_wait(&a_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k) {
+          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
+          mma_ss(pd, make_sdesc(ga + off, 16, 1024, kSwizzle128B), make_sdesc(va + off, 16, 1024, kSwizzle128B),
+                 id_qk, k > 0);
+        }
+        tc_commit(&dp_full[pb]);
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k)
+          mma_ss(oq, make_sdesc(ga + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
+                 make_sdesc(sb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_as, k > 0);
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ss(tmem + G::COL_R, make_sdesc(qa + k * 2048, BOX, 1024, kSwizzle128B),
+                 make_sdesc(ga + k * 2048, BOX, 1024, kSwizzle128B), id_tt, (c > 0 || k > 0) ? 1u : 0u);
+        tc_commit(&sb_free[sbi]);
+        ok = mbar_wait(&dp_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ts(oq, pd + k * 8, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+        tc_commit(&dq_full[pb]);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(mma_fin);
+      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- group A: phi(Q), S_prev copies, R ----------------
+    const int t = tid - 128;
+    const int q = warp & 3;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    const int row = state_row<D>(q, lane);
+    load_state_to_tmem<D>(prm.ws_state + rec, lane_addr, G::COL_S, row);
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST;
+      ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);
+      fence_proxy_async_smem();
+      mbar_arrive(&phi_done[s]);
+      if (c > 0) ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
+      if (ok && c >= G::NSB) ok = mbar_wait(&sb_free[c % G::NSB], ((c / G::NSB) - 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf + (c % G::NSB) * G::SBUF, row);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(s_ready);
+    }
+    if (ok) ok = mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    if (ok) {
+      tc_fence_after();
+      store_state_from_tmem<D>(prm.ws_rev + rec, lane_addr, G::COL_R, row);
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------- group B: P, den, a and b ----------------
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    float2* tokp = reinterpret_cast<float2*>(prm.ws_tok) + (long long)bh * prm.N;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST, pb = c & 1;
+      ok = mbar_wait(&p_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs) &&
+           mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const float rowsum = mask_pack_row<true, false>(lane_addr + G::COL_PD + 128 * pb, q, lane, 0.f, nullptr);
+      const uint8_t* qt = sm + s * G::STAGE;
+      const float den = rowsum + phiq_dot<D>(qt, r, zst + s * D) + prm.eps;
+      const float inv_den = 1.f / den;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_ready[pb]);
+      ok = mbar_wait(&o_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const float beta = grad_row_pass<D>(lane_addr + G::COL_OQ + D * pb, sm + s * G::STAGE + 3 * G::TILE, r, inv_den);
+      const float b = -beta * inv_den * inv_den;
+      barr[s * C + r] = b;
+      const int tok = tok0 + c * C + r;
+      if (tok < tok_end) tokp[tok] = make_float2(den, b);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&a_ready[pb]);
+    }
+  } else if (warp >= 12 && warp < 16) {
+    // ---------------- group D: dP', dq ----------------
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    __nv_bfloat16* dqb = prm.dq + (long long)bh * prm.N * D;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST, pb = c & 1;
+      ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs) &&
+           mbar_wait(&dp_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs) &&
+           mbar_wait(&a_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const float b = barr[s * C + r];
+      mask_pack_row<true, false>(lane_addr + G::COL_PD + 128 * pb, q, lane, b, nullptr);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&dp_ready[pb]);
+      ok = mbar_wait(&dq_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const int tok = tok0 + c * C + r;
+      grad_epilogue<D>(lane_addr + G::COL_OQ + D * pb, sm + s * G::STAGE, r, b, zst + s * D,
+                       tok < tok_end ? dqb + (long long)tok * D : nullptr);
+      tc_fence_before();
+      mbar_arrive(&oq_empty[pb]);
+      mbar_arrive(&empty[s]);
+    }
+  } else {
+    // ---------------- group C: phi(K), z, r ----------------
+    using X = ExactLayout<D, 128>;
+    const int t = tid;
+    const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    const bool owner = lane < X::FCW;
+    const float* st = prm.ws_state + rec;
+    float zrun[8], racc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      zrun[e] = owner ? st[D * D + 8 * fc + e] : 0.f;
+      racc[e] = 0.f;
+    }
+    bool ok = true;
+    for (int c = 0; c <= nchunks && ok; ++c) {
+      if (c < nchunks) {
+        const int s = c % ST;
+        const int n_valid = min(C, tok_end - (tok0 + c * C));
+        ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        float colsum[8];
+        phi_tile_exact<D, 128>(sm + s * G::STAGE + G::TILE, t, n_valid, colsum);
+        fence_proxy_async_smem();
+        if (owner) {
+          float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
+          zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
+          zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
+        }
+        mbar_arrive(&phi_done[s]);
+      }
+      if (c >= 1) {
+        // r += sum_t b_t phi(q_t) over the previous chunk
+        const int cp = c - 1, sp = cp % ST;
+        ok = mbar_wait(&a_ready[cp & 1], (cp >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        wcolsum_tile<D, 128>(sm + sp * G::STAGE, barr + sp * C, t, racc);
+        mbar_arrive(&empty[sp]);
+      }
+    }
+    reduce_row_groups<D, 128>(racc);
+    if (ok && owner) {
+      float4* rd = reinterpret_cast<float4*>(prm.ws_rev + rec + D * D + 8 * fc);
+      rd[0] = make_float4(racc[0], racc[1], racc[2], racc[3]);
+      rd[1] = make_float4(racc[4], racc[5], racc[6], racc[7]);
+    }
+  }
+
+  // ---------------- teardown ----------------
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 17) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Sweep 2
+// ---------------------------------------------------------------------------
+template <int D>
+struct B2 {
+  static_assert(D == 64, "the tensor-core backward is laid out for D = 64");
+  static constexpr int NB = D / 64;
+  static constexpr int TILE = NB * BOX;
+  static constexpr int ST = 3;
+  static constexpr int STAGE = 4 * TILE;              // Q, K, V, G (G becomes a in place)
+  static constexpr int RBUF = NB * D * 128;           // bf16 copy of R_after
+  static constexpr int KSTEPS = D / 16;
+  static constexpr uint32_t COL_PT = 0;               // 128
+  static constexpr uint32_t COL_DPT = 128;            // 128
+  static constexpr uint32_t COL_DK = 256;             // D
+  static constexpr uint32_t COL_DV = COL_DK + D;      // D
+  static constexpr uint32_t COL_R = COL_DV + D;       // D
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(COL_R + D <= TMEM_COLS, "tensor memory budget");
+  static constexpr int OFF_RBUF = ST * STAGE;
+  static constexpr int OFF_RVEC = OFF_RBUF + RBUF;        // [2][D] r_after
+  static constexpr int OFF_BARR = OFF_RVEC + 2 * D * 4;   // [ST][C] b_t
+  static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
+  static constexpr int NBAR = 3 * ST + 12;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static constexpr int THREADS = 448;
+};
+
+struct Bwd2Params {
+  int N, P, seg_len;
+  const float* ws_rev;     // [BH][P][D*D + D] suffixes (R, r) after each segment
+  const float* ws_tok;     // [BH][N][2] (den, b)
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+};
+
+// Warp roles (448 threads); chunks run from the segment's end to its start:
+//   warps 0-3    group C: phi(K) in place; a = g / den in place; b_t
+//   warps 4-7    group A: phi(Q) in place; R_after copies; r_after sums
+//   warps 8-11   group D: P^T' and dP^T' mask/pack; dk, dv epilogue
+//   warp 12      TMA producer
+//   warp 13      TMEM allocator and MMA issuer
+template <int D>
+__global__ void __launch_bounds__(448, 1)
+tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+               const Bwd2Params prm) {
+  using G = B2<D>;
+  constexpr int ST = G::ST;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  uint8_t* rbuf = sm + G::OFF_RBUF;
+  float* rvec = reinterpret_cast<float*>(sm + G::OFF_RVEC);
+  float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* prep_done = bars + ST;
+  uint64_t* empty = bars + 2 * ST;
+  uint64_t* x = bars + 3 * ST;
+  uint64_t* pt_full = x;
+  uint64_t* dpt_full = x + 1;
+  uint64_t* pt_ready = x + 2;
+  uint64_t* dpt_ready = x + 3;
+  uint64_t* rb_ready = x + 4;     // [2]
+  uint64_t* r_full = x + 6;
+  uint64_t* kv_full = x + 7;
+  uint64_t* kv_empty = x + 8;     // [2]
+  uint64_t* mma_fin = x + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G::OFF_MISC + 4);
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) report_timeout(prm.status);
+    return;
+  }
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / prm.P, seg = blockIdx.x % prm.P;
+  const int tok0 = seg * prm.seg_len;
+  const int tok_end = min(prm.N, tok0 + prm.seg_len);
+  const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const long long rec = ((long long)bh * prm.P + seg) * (long long)(D * D + D);
+
+  if (tid == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&prep_done[i], 256);
+      mbar_init(&empty[i], 1 + 128 + 128);
+    }
+    mbar_init(pt_full, 1);
+    mbar_init(dpt_full, 1);
+    mbar_init(pt_ready, 128);
+    mbar_init(dpt_ready, 128);
+    mbar_init(&rb_ready[0], 128);
+    mbar_init(&rb_ready[1], 128);
+    mbar_init(r_full, 1);
+    mbar_init(kv_full, 1);
+    mbar_init(&kv_empty[0], 128);
+    mbar_init(&kv_empty[1], 128);
+    mbar_init(mma_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(tmem_slot, G::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 12) {
+    // ---------------- TMA producer (last chunk first) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_g);
+      int issued = 0;
+      for (int i = 0; i < nchunks; ++i) {
+        const int s = i % ST;
+        if (i >= ST && !mbar_wait(&empty[s], ((i / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
+        uint8_t* stg = sm + s * G::STAGE;
+        mbar_arrive_expect_tx(&full[s], 4 * G::TILE);
+        const int y = tok0 + (nchunks - 1 - i) * C;
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b) {
+          tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::TILE + b * BOX, &map_k, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + 2 * G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + 3 * G::TILE + b * BOX, &map_g, &full[s], 64 * b, y, bh);
+        }
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - ST); i < issued; ++i)
+        mbar_wait(&full[i % ST], (i / ST) & 1, abort_flag, kTimeoutNs);
+    }
+  } else if (warp == 13) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_kq = make_idesc_bf16(128, 128, false, false);  // P^T = phiK phiQ^T, dP^T = V a^T
+      constexpr uint32_t id_vr = make_idesc_bf16(128, D, false, false);    // dK = V R^T
+      constexpr uint32_t id_kr = make_idesc_bf16(128, D, false, true);     // dV = phiK R
+      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // R += phiQ^T a
+      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // dK += dP^T' phiQ, dV += P^T' a
+      const uint32_t rb = smem_u32(rbuf);
+      const uint32_t pt = tmem + G::COL_PT, dpt = tmem + G::COL_DPT;
+      const uint32_t dkc = tmem + G::COL_DK, dvc = tmem + G::COL_DV;
+      bool ok = true;
+      for (int i = 0; i < nchunks && ok; ++i) {
+        const int s = i % ST;
+        const uint32_t qa = smem_u32(sm + s * G::STAGE);
+        const uint32_t ka = qa + G::TILE, va = qa + 2 * G::TILE, ga = qa + 3 * G::TILE;
+        ok = mbar_wait(&prep_done[s], (i / ST) & 1, abort_flag, kTimeoutNs);
+        // the P^T / dP^T buffers are free once the previous chunk's MMAs are done
+        if (ok && i >= 1) ok = mbar_wait(kv_full, (i - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k) {
+          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
+          mma_ss(pt, make_sdesc(ka + off, 16, 1024, kSwizzle128B), make_sdesc(qa + off, 16, 1024, kSwizzle128B),
+                 id_kq, k > 0);
+        }
+        tc_commit(pt_full);
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k) {
+          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
+          mma_ss(dpt, make_sdesc(va + off, 16, 1024, kSwizzle128B), make_sdesc(ga + off, 16, 1024, kSwizzle128B),
+                 id_kq, k > 0);
+        }
+        tc_commit(dpt_full);
+        ok = mbar_wait(&rb_ready[i & 1], (i >> 1) & 1, abort_flag, kTimeoutNs);
+        if (ok && i >= 1) ok = mbar_wait(&kv_empty[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k) {
+          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
+          mma_ss(dkc, make_sdesc(va + off, 16, 1024, kSwizzle128B),
+                 make_sdesc(rb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_vr, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < G::KSTEPS; ++k) {
+          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
+          mma_ss(dvc, make_sdesc(ka + off, 16, 1024, kSwizzle128B),
+                 make_sdesc(rb + k * 2048, D * 128, 1024, kSwizzle128B), id_kr, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ss(tmem + G::COL_R, make_sdesc(qa + k * 2048, BOX, 1024, kSwizzle128B),
+                 make_sdesc(ga + k * 2048, BOX, 1024, kSwizzle128B), id_tt, 1);
+        tc_commit(r_full);
+        ok = mbar_wait(pt_ready, i & 1, abort_flag, kTimeoutNs) && mbar_wait(dpt_ready, i & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ts(dkc, dpt + k * 8, make_sdesc(qa + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ts(dvc, pt + k * 8, make_sdesc(ga + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+        tc_commit(kv_full);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(mma_fin);
+      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- group A: phi(Q), R_after copies, r_after ----------------
+    using X = ExactLayout<D, 128>;
+    const int t = tid - 128;
+    const int q = warp & 3;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    const int row = state_row<D>(q, lane);
+    const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    const bool owner = lane < X::FCW;
+    const float* rr = prm.ws_rev + rec;
+    load_state_to_tmem<D>(rr, lane_addr, G::COL_R, row);
+    float rrun[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rrun[e] = owner ? rr[D * D + 8 * fc + e] : 0.f;
+    bool ok = true;
+    for (int i = 0; i < nchunks && ok; ++i) {
+      const int s = i % ST;
+      ok = mbar_wait(&full[s], (i / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);
+      fence_proxy_async_smem();
+      mbar_arrive(&prep_done[s]);
+      // R_after of chunk i: R after the updates of every later chunk
+      if (i > 0) ok = mbar_wait(r_full, (i - 1) & 1, abort_flag, kTimeoutNs);
+      // r_after of chunk i goes where chunk i - 2's epilogue read it
+      if (ok && i >= 2) ok = mbar_wait(&kv_empty[i & 1], ((i - 2) >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      copy_state_to_smem<D>(lane_addr + G::COL_R, rbuf, row);
+      if (owner) {
+        float4* rd = reinterpret_cast<float4*>(rvec + (i & 1) * D + 8 * fc);
+        rd[0] = make_float4(rrun[0], rrun[1], rrun[2], rrun[3]);
+        rd[1] = make_float4(rrun[4], rrun[5], rrun[6], rrun[7]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&rb_ready[i & 1]);
+      // r += sum_t b_t phi(q_t) over this chunk (b from group C)
+      ok = mbar_wait(&prep_done[s], (i / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      float racc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) racc[e] = 0.f;
+      wcolsum_tile<D, 128>(sm + s * G::STAGE, barr + s * C, t, racc);
+      reduce_row_groups<D, 128>(racc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rrun[e] += racc[e];
+      mbar_arrive(&empty[s]);
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------- group D: P^T', dP^T', dk, dv ----------------
+    const int q = warp & 3;
+    const int r = 32 * q + lane;            // key row j of the chunk
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    __nv_bfloat16* dkb = prm.dk + (long long)bh * prm.N * D;
+    __nv_bfloat16* dvb = prm.dv + (long long)bh * prm.N * D;
+    bool ok = true;
+    for (int i = 0; i < nchunks && ok; ++i) {
+      const int s = i % ST;
+      ok = mbar_wait(&prep_done[s], (i / ST) & 1, abort_flag, kTimeoutNs) &&
+           mbar_wait(&rb_ready[i & 1], (i >> 1) & 1, abort_flag, kTimeoutNs) &&
+           mbar_wait(pt_full, i & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      mask_pack_row<false, false>(lane_addr + G::COL_PT, q, lane, 0.f, nullptr);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(pt_ready);
+      ok = mbar_wait(dpt_full, i & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      mask_pack_row<false, true>(lane_addr + G::COL_DPT, q, lane, 0.f, barr + s * C);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(dpt_ready);
+      ok = mbar_wait(kv_full, i & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const int tok = tok0 + (nchunks - 1 - i) * C + r;
+      const bool valid = tok < tok_end;
+      grad_epilogue<D>(lane_addr + G::COL_DK, sm + s * G::STAGE + G::TILE, r, 1.f, rvec + (i & 1) * D,
+                       valid ? dkb + (long long)tok * D : nullptr);
+      store_row_bf16<D>(lane_addr + G::COL_DV, valid ? dvb + (long long)tok * D : nullptr);
+      tc_fence_before();
+      mbar_arrive(&kv_empty[i & 1]);
+      mbar_arrive(&empty[s]);
+    }
+  } else {
+    // ---------------- group C: phi(K), a = g / den, b ----------------
+    const int t = tid;                      // chunk row for the a scaling
+    const float2* tokp = reinterpret_cast<const float2*>(prm.ws_tok) + (long long)bh * prm.N;
+    bool ok = true;
+    for (int i = 0; i < nchunks && ok; ++i) {
+      const int s = i % ST;
+      const int y = tok0 + (nchunks - 1 - i) * C;
+      const bool valid = y + t < tok_end;
+      const float2 db = valid ? tokp[y + t] : make_float2(1.f, 0.f);
+      ok = mbar_wait(&full[s], (i / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      uint8_t* stg = sm + s * G::STAGE;
+      phi_tile_bf16<D, 128>(stg + G::TILE, t);
+      const float inv = valid ? 1.f / db.x : 0.f;
+      uint8_t* gt = stg + 3 * G::TILE;
+#pragma unroll 2
+      for (int ch = 0; ch < D / 8; ++ch) {
+        const uint4 w = ld_chunk(gt, t, ch);
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(&w);
+        uint4 o;
+        o.x = pack_bf16x2(bf_lo(pw[0]) * inv, bf_hi(pw[0]) * inv);
+        o.y = pack_bf16x2(bf_lo(pw[1]) * inv, bf_hi(pw[1]) * inv);
+        o.z = pack_bf16x2(bf_lo(pw[2]) * inv, bf_hi(pw[2]) * inv);
+        o.w = pack_bf16x2(bf_lo(pw[3]) * inv, bf_hi(pw[3]) * inv);
+        st_chunk(gt, t, ch, o);
+      }
+      barr[s * C + t] = valid ? db.y : 0.f;
+      fence_proxy_async_smem();
+      mbar_arrive(&prep_done[s]);
+    }
+  }
+
+  // ---------------- teardown ----------------
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+template <int D>
+cudaError_t launch_backward(const BwdArgs& a) {
+  FwdArgs f{};
+  f.q = a.q; f.k = a.k; f.v = a.v; f.out = nullptr;
+  f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = a.causal;
+  f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
+  f.stream = a.stream;
+  const long long words = state_words(D, D);
+  prof_begin(LA_SPAN_BWD_STATE, a.stream);
+  cudaError_t e = tc_segment_state(f);
+  if (e == cudaSuccess)
+    e = segment_scan(a.ws_state, a.BH, a.plan.P, words, SCAN_EXCLUSIVE_FWD, nullptr, nullptr, D, D, a.stream);
+  prof_end(LA_SPAN_BWD_STATE, a.stream);
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mq, mk, mv, mg;
+  e = make_map(&mq, a.q, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mk, a.k, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mg, a.dout, a.BH, a.N, D);
+  if (e != cudaSuccess) return e;
+  int* status = device_status_ptr();
+
+  constexpr int smem1 = B1<D>::BYTES;
+  e = cudaFuncSetAttribute(tc_bwd1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem1);
+  if (e != cudaSuccess) return e;
+  Bwd1Params p1{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dq, status};
+  prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
+  tc_bwd1_kernel<D><<<a.BH * a.plan.P, B1<D>::THREADS, smem1, a.stream>>>(mq, mk, mv, mg, p1);
+  prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  note_launch();
+
+  prof_begin(LA_SPAN_BWD_SCAN, a.stream);
+  e = segment_scan(a.ws_rev, a.BH, a.plan.P, words, SCAN_EXCLUSIVE_REV, nullptr, nullptr, D, D, a.stream);
+  prof_end(LA_SPAN_BWD_SCAN, a.stream);
+  if (e != cudaSuccess) return e;
+
+  constexpr int smem2 = B2<D>::BYTES;
+  e = cudaFuncSetAttribute(tc_bwd2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
+  if (e != cudaSuccess) return e;
+  Bwd2Params p2{a.N, a.plan.P, a.plan.seg_len, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dk_, (__nv_bfloat16*)a.dv_,
+                status};
+  prof_begin(LA_SPAN_BWD_SWEEP2, a.stream);
+  tc_bwd2_kernel<D><<<a.BH * a.plan.P, B2<D>::THREADS, smem2, a.stream>>>(mq, mk, mv, mg, p2);
+  prof_end(LA_SPAN_BWD_SWEEP2, a.stream);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
+}  // namespace
+
+bool tc_backward_supported(int dk, int dv, la_dtype dtype, int causal) {
+  return dtype == LA_BF16 && dk == 64 && dv == 64 && causal;
+}
+
+cudaError_t tc_backward(const BwdArgs& a) { return launch_backward<64>(a); }
+
+}  // namespace la

@@ -36,20 +36,13 @@
 // phi(q) cancels between numerator and denominator).
 // Every wait is bounded; on a timeout the CTA sets the device status word,
 // drains, frees its tensor memory and exits.
-#include <cudaTypedefs.h>
-
-#include "la_internal.cuh"
-#include "la_sm100.cuh"
+#include "la_tc_common.cuh"
 
 namespace la {
 
 namespace {
 
 using namespace sm100;
-
-constexpr int C = 128;                    // tokens per chunk
-constexpr int BOX = 128 * 128;            // bytes of one [128 rows][64 bf16] SW128 box
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 template <int D>
 struct Cfg {
@@ -71,132 +64,6 @@ struct Cfg {
   static constexpr int STAGE_S = 2 * TILE;            // K, V
   static constexpr uint32_t TMEM_COLS_S = D == 128 ? 128 : 64;
 };
-
-// Row of the D x D state held by lane `l` of TMEM quadrant `q` (rows live in
-// the quadrant's lanes: all 32 for M = 128, the first 16 for M = 64).
-template <int D>
-__device__ __forceinline__ int state_row(int q, int l) {
-  if (D == 128) return 32 * q + l;
-  return l < 16 ? 16 * q + l : -1;
-}
-
-__device__ __forceinline__ uint32_t sw128(int row, int chunk) {  // byte offset of a 16-byte chunk
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void report_timeout(int* status) { atomicExch(status, (int)LA_ERR_TIMEOUT); }
-
-// phi on packed bf16 values, in place on one [C][D] tile (phi is elementwise,
-// so the swizzle does not matter); NT threads, thread t owns 16-byte chunks
-// t, t + NT, ...
-template <int D, int NT>
-__device__ __forceinline__ void phi_tile_bf16(uint8_t* tile, int t) {
-  constexpr int PER = (C * D * 2 / 16) / NT;
-  constexpr int GR = 4;
-#pragma unroll 1
-  for (int i0 = 0; i0 < PER; i0 += GR) {
-    uint4 w[GR];
-#pragma unroll
-    for (int i = 0; i < GR; ++i) w[i] = reinterpret_cast<const uint4*>(tile)[t + NT * (i0 + i)];
-#pragma unroll
-    for (int i = 0; i < GR; ++i) {
-      w[i].x = phi_bf16x2(w[i].x);
-      w[i].y = phi_bf16x2(w[i].y);
-      w[i].z = phi_bf16x2(w[i].z);
-      w[i].w = phi_bf16x2(w[i].w);
-    }
-#pragma unroll
-    for (int i = 0; i < GR; ++i) reinterpret_cast<uint4*>(tile)[t + NT * (i0 + i)] = w[i];
-  }
-}
-
-// phi(x) in fp32 without branches: x + 1 for x > 0, e^x otherwise, with
-// e^x = 2^(x log2 e) from the hardware base-2 exponential (results below the
-// normal range flush to zero). Rounded to bf16 by the caller.
-__device__ __forceinline__ float phi_f32(float x) {
-  float e;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
-  return x > 0.f ? x + 1.f : e;
-}
-
-// phi in place on one [C][D] tile, rounded to nearest, with fp32 column sums
-// over rows < n_valid (rows >= n_valid, past the end of the sequence, become
-// zero). NT threads; warp w owns FCW = D / (NT / 4) consecutive 16-byte
-// feature chunks of every row; lane l works on chunk FCW*w + l % FCW and rows
-// l / FCW + (32 / FCW) i. The column sums are reduced inside the warp, so on
-// return lanes l < FCW hold the sums of the 8 features of chunk FCW*w + l.
-template <int D, int NT>
-struct ExactLayout {
-  static constexpr int FCW = D / (NT / 4);     // feature chunks per warp
-  static constexpr int RG = 32 / FCW;          // row groups per warp
-  static constexpr int RPT = C / RG;           // rows per thread
-  static_assert(FCW >= 1 && FCW <= 8 && (FCW & (FCW - 1)) == 0, "layout");
-};
-
-template <int D, int NT>
-__device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8]) {
-  using X = ExactLayout<D, NT>;
-  constexpr int GR = 4;                               // rows per loop trip (kept small: code size)
-  const int w = t >> 5, lane = t & 31;
-  const int fc = X::FCW * w + (lane % X::FCW);       // feature chunk 0 .. D/8-1
-  const int r0 = lane / X::FCW;
-  uint8_t* base = tile + (fc >> 3) * BOX;
-  const int ch = fc & 7;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) zacc[e] = 0.f;
-#pragma unroll 1
-  for (int i0 = 0; i0 < X::RPT; i0 += GR) {
-    uint4 wv[GR];
-#pragma unroll
-    for (int i = 0; i < GR; ++i) wv[i] = *reinterpret_cast<const uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch));
-#pragma unroll
-    for (int i = 0; i < GR; ++i) {
-      const bool valid = r0 + X::RG * (i0 + i) < n_valid;
-      uint32_t* p = reinterpret_cast<uint32_t*>(&wv[i]);
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float lo = valid ? phi_f32(__uint_as_float(p[h] << 16)) : 0.f;
-        const float hi = valid ? phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)) : 0.f;
-        zacc[2 * h] += lo;
-        zacc[2 * h + 1] += hi;
-        p[h] = pack_bf16x2(lo, hi);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < GR; ++i) *reinterpret_cast<uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch)) = wv[i];
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float x = zacc[e];
-#pragma unroll
-    for (int o = X::FCW; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    zacc[e] = x;
-  }
-}
-
-// Copy this thread's TMEM lane of S (fp32, D columns) to the bf16 MN-major
-// operand buffer (row = key component, 64 value columns per box).
-template <int D>
-__device__ __forceinline__ void copy_state_to_smem(uint32_t lane_addr, uint8_t* sbuf, int row) {
-#pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
-    uint32_t v[32];
-    tmem_ld32(lane_addr + Cfg<D>::COL_S + c0, v);
-    tmem_ld_wait();
-    if (row >= 0) {
-      const int b = c0 / 64, cb = (c0 % 64) / 8;  // box, first 16-byte chunk
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-        w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-        w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-        w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-        *reinterpret_cast<uint4*>(sbuf + b * (D * 128) + sw128(row, cb + j)) = w;
-      }
-    }
-  }
-}
 
 template <int D>
 struct FwdSmem {
@@ -399,7 +266,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!ok) break;
         tc_fence_after();
       }
-      copy_state_to_smem<D>(lane_addr, sbuf, row);
+      copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf, row);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
@@ -702,39 +569,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS_S);
   }
-}
-
-// ---------------------------------------------------------------------------
-// Host side
-// ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult qr;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    else
-      (void)cudaGetLastError();
-  }
-  return fn;
-}
-
-// [BH][N][D] bf16 viewed as a 3-D tensor; boxes of [C rows][64 features],
-// 128-byte swizzle, zero fill past the end of each sequence.
-cudaError_t make_map(CUtensorMap* m, const void* ptr, int BH, int N, int D) {
-  auto enc = get_encoder();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int D>
