@@ -175,7 +175,7 @@ int* device_status_ptr() {
 // prologue (loading its starting state); CTAs run in waves of kSlots; the
 // segment scan adds a little per segment. Pure function of the sizes, so the
 // workspace query and the call agree.
-SegPlan plan_segments(long long BH, int N) {
+SegPlan plan_segments(long long BH, int N, int slots) {
   SegPlan best{1, N > 0 ? N : 1};
   if (BH <= 0 || N <= 0) return best;
   const int nch = (N + kSegGranule - 1) / kSegGranule;
@@ -184,7 +184,7 @@ SegPlan plan_segments(long long BH, int N) {
     const int L = (nch + P - 1) / P;           // chunks per segment
     if ((nch + L - 1) / L != P) continue;      // P not reachable with equal segments
     const long long ctas = BH * P;
-    const long long waves = (ctas + kSlots - 1) / kSlots;
+    const long long waves = (ctas + slots - 1) / slots;
     const double cost = (double)waves * (L + 1) + 0.02 * P;
     if (cost < best_cost) {
       best_cost = cost;
@@ -193,6 +193,12 @@ SegPlan plan_segments(long long BH, int N) {
     }
   }
   return best;
+}
+
+// The forward's segment plan (one CTA per SM for every forward kernel).
+SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool causal) {
+  (void)dk; (void)dv; (void)dtype; (void)causal;
+  return plan_segments(BH, N, kSlots);
 }
 
 }  // namespace la
@@ -232,10 +238,9 @@ int la_backward_path(int dk, int dv, la_dtype dtype, int causal) {
 }
 
 size_t la_forward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
-  (void)causal; (void)dtype;
   if (B <= 0 || H <= 0 || N <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
   const long long BH = (long long)B * H;
-  return layout(BH, N, dk, dv, plan_segments(BH, N), false).total;
+  return layout(BH, N, dk, dv, forward_plan(BH, N, dk, dv, dtype, causal != 0), false).total;
 }
 
 size_t la_backward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
@@ -269,7 +274,7 @@ la_status la_forward(const void* q, const void* k, const void* v, void* out,
   if (!q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be non-NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
-  const SegPlan plan = plan_segments(BH, N);
+  const SegPlan plan = forward_plan(BH, N, dk, dv, dtype, causal != 0);
   const WsLayout w = layout(BH, N, dk, dv, plan, false);
   if (workspace == nullptr || workspace_bytes < w.total)
     return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
@@ -290,12 +295,16 @@ la_status la_forward(const void* q, const void* k, const void* v, void* out,
   cudaError_t e = use_tc ? tc_segment_state(a) : simt_segment_state(a);
   prof_end(LA_SPAN_FWD_STATE, stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment state)");
-  prof_begin(LA_SPAN_FWD_SCAN, stream);
-  e = segment_scan(a.ws_state, a.BH, plan.P, state_words(dk, dv),
-                   a.causal ? SCAN_EXCLUSIVE_FWD : SCAN_TOTAL, S_final, z_final,
-                   dk, dv, stream);
-  prof_end(LA_SPAN_FWD_SCAN, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment scan)");
+  if (!use_tc) {
+    // the tensor-core output kernel sums the earlier segments' records itself
+    // and writes the final state from its last segment
+    prof_begin(LA_SPAN_FWD_SCAN, stream);
+    e = segment_scan(a.ws_state, a.BH, plan.P, state_words(dk, dv),
+                     a.causal ? SCAN_EXCLUSIVE_FWD : SCAN_TOTAL, S_final, z_final,
+                     dk, dv, stream);
+    prof_end(LA_SPAN_FWD_SCAN, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward (segment scan)");
+  }
   prof_begin(LA_SPAN_FWD_OUTPUT, stream);
   e = use_tc ? tc_forward_output(a) : simt_forward_output(a);
   prof_end(LA_SPAN_FWD_OUTPUT, stream);

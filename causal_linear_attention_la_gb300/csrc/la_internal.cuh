@@ -42,7 +42,9 @@ struct SegPlan {
 constexpr int kSegGranule = 128;   // tokens; one tensor-core chunk
 constexpr int kSlots = 152;        // CTAs resident at once: one per SM of a GB300
 
-SegPlan plan_segments(long long BH, int N);
+// Segments per sequence for B*H sequences of N tokens when `slots` CTAs can
+// be resident at once.
+SegPlan plan_segments(long long BH, int N, int slots = kSlots);
 
 // Floats per per-segment state record: dk*dv matrix then dk vector.
 inline long long state_words(int dk, int dv) { return (long long)dk * dv + dk; }

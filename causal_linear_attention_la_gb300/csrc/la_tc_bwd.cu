@@ -13,10 +13,11 @@
 //   dphi(k_j) = R_j v_j + r_j,  dv_j = R_j^T phi(k_j)
 //   dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k),  phi'(x) = min(phi(x), 1)
 //
-// Sweep 1 (forward through each segment, from the segment's prefix S, z):
+// Sweep 1 (forward through each segment, from the segment's prefix S, z; the
+// state is held transposed, S^T, as in the forward kernel):
 //   P    = phi(Q) phi(K)^T, masked j <= t           MMA (both K-major)
 //   O    = phi(Q) S_prev + P V                      MMA, MMA (P from TMEM)
-//   S   += phi(K)^T V                               MMA
+//   S^T += V^T phi(K)                               MMA
 //   den  = phi(Q) z_prev + P 1 + eps;  a = g / den;  b = -(g . O) / den^2
 //   dP   = a V^T;  dP' = (dP + b) masked j <= t     MMA, CUDA cores
 //   dQ   = a S_prev^T + dP' phi(K) + b z_prev        MMA, MMA, epilogue
@@ -28,7 +29,11 @@
 //   dK   = V R_after^T + dP^T' phi(Q) + r_after     MMA, MMA, epilogue
 //   dV   = phi(K) R_after + P^T' a                  MMA, MMA
 //   R   += phi(Q)^T a;  r += phi(Q)^T b
-// The segment sums are joined by the state pass and the scan kernel.
+// Each segment starts from the sum of the other segments' records: sweep 1
+// adds the state pass's records of the segments before it, sweep 2 adds
+// sweep 1's (R, r) records of the segments after it. Sweep 1 is launched as a
+// dependent of the state pass and sweep 2 of sweep 1, so each fills its
+// pipeline before it waits for the records.
 //
 // Every wait is bounded; on a timeout the CTA sets the device status word,
 // drains, frees its tensor memory and exits. Barriers that a consumer may
@@ -210,50 +215,6 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
   }
 }
 
-// A D x D fp32 state from global memory (row-major) into tensor memory at
-// column `col` (rows in the M = D accumulator layout).
-template <int D>
-__device__ __forceinline__ void load_state_to_tmem(const float* src, uint32_t lane_addr, uint32_t col, int row) {
-  const float4* srow = reinterpret_cast<const float4*>(src + (row >= 0 ? row : 0) * D);
-#pragma unroll
-  for (int h = 0; h < D; h += 64) {
-    float4 f[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) f[j] = row >= 0 ? srow[h / 4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t v[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[4 * j + 0] = __float_as_uint(f[4 * g + j].x);
-        v[4 * j + 1] = __float_as_uint(f[4 * g + j].y);
-        v[4 * j + 2] = __float_as_uint(f[4 * g + j].z);
-        v[4 * j + 3] = __float_as_uint(f[4 * g + j].w);
-      }
-      tmem_st16(lane_addr + col + h + 16 * g, v);
-    }
-  }
-  tmem_st_wait();
-}
-
-// A D x D fp32 state from tensor memory (column `col`) to global memory.
-template <int D>
-__device__ __forceinline__ void store_state_from_tmem(float* dst, uint32_t lane_addr, uint32_t col, int row) {
-#pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
-    uint32_t v[32];
-    tmem_ld32(lane_addr + col + c0, v);
-    tmem_ld_wait();
-    if (row >= 0) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(dst + row * D + c0 + j) =
-            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                        __uint_as_float(v[j + 3]));
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Sweep 1
 // ---------------------------------------------------------------------------
@@ -289,8 +250,8 @@ struct B1 {
 struct Bwd1Params {
   int N, P, seg_len;
   float eps;
-  const float* ws_state;   // [BH][P][D*D + D] prefixes (S, z) before each segment
-  float* ws_rev;           // [BH][P][D*D + D] segment sums (R, r)
+  const float* ws_state;   // [BH][P][D*D + D] segment sums (S^T, z), all but the last segment
+  float* ws_rev;           // [BH][P][D*D + D] segment sums (R, r), all but the first segment
   float* ws_tok;           // [BH][N][2] (den, b) per token
   __nv_bfloat16* dq;       // [BH][N][D]
   int* status;
@@ -334,6 +295,8 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   uint64_t* mma_fin = x + 20;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G::OFF_MISC + 4);
+  // sweep 2 may start filling its pipeline while this grid runs
+  griddep_launch_dependents();
   if ((smem_u32(sm) & 1023u) != 0u) {
     if (threadIdx.x == 0) report_timeout(prm.status);
     return;
@@ -408,9 +371,9 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t id_qk = make_idesc_bf16(128, 128, false, false);  // P = phiQ phiK^T, dP = a V^T
-      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, true);     // O = phiQ S_prev
-      constexpr uint32_t id_as = make_idesc_bf16(128, D, false, false);    // dQ = a S_prev^T
-      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // S += phiK^T V, R += phiQ^T a
+      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);    // O = phiQ S_prev (S^T copy K-major)
+      constexpr uint32_t id_as = make_idesc_bf16(128, D, false, true);     // dQ = a S_prev^T (S^T copy MN-major)
+      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // S^T += V^T phiK, R += phiQ^T a
       constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V, dQ += dP' phiK
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
@@ -439,11 +402,11 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k)
           mma_ss(oq, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
-                 make_sdesc(sb + k * 2048, D * 128, 1024, kSwizzle128B), id_qs, k > 0);
+                 make_sdesc(sb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qs, k > 0);
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
-          mma_ss(tmem + G::COL_S, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B),
-                 make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_tt, 1);
+          mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
+                 make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_tt, 1);
         tc_commit(s_full);
         ok = mbar_wait(&p_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
@@ -465,7 +428,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k)
           mma_ss(oq, make_sdesc(ga + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
-                 make_sdesc(sb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_as, k > 0);
+                 make_sdesc(sb + k * 2048, D * 128, 1024, kSwizzle128B), id_as, k > 0);
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           mma_ss(tmem + G::COL_R, make_sdesc(qa + k * 2048, BOX, 1024, kSwizzle128B),
@@ -489,7 +452,9 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int q = warp & 3;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
-    load_state_to_tmem<D>(prm.ws_state + rec, lane_addr, G::COL_S, row);
+    griddep_wait();
+    sum_states_to_tmem<D>(prm.ws_state + (long long)bh * prm.P * (D * D + D), D * D + D, 0, seg, lane_addr,
+                          G::COL_S, row);
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -507,8 +472,9 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tc_fence_before();
       mbar_arrive(s_ready);
     }
-    if (ok) ok = mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
-    if (ok) {
+    // the first segment's (R, r) sums are never read
+    if (ok && seg > 0) ok = mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    if (ok && seg > 0) {
       tc_fence_after();
       store_state_from_tmem<D>(prm.ws_rev + rec, lane_addr, G::COL_R, row);
     }
@@ -579,13 +545,11 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int t = tid;
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;
-    const float* st = prm.ws_state + rec;
     float zrun[8], racc[8];
+    griddep_wait();
+    sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * (D * D + D), D * D + D, 0, seg, 8 * fc, zrun);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      zrun[e] = owner ? st[D * D + 8 * fc + e] : 0.f;
-      racc[e] = 0.f;
-    }
+    for (int e = 0; e < 8; ++e) racc[e] = 0.f;
     bool ok = true;
     for (int c = 0; c <= nchunks && ok; ++c) {
       if (c < nchunks) {
@@ -615,7 +579,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     reduce_row_groups<D, 128>(racc);
-    if (ok && owner) {
+    if (ok && owner && seg > 0) {
       float4* rd = reinterpret_cast<float4*>(prm.ws_rev + rec + D * D + 8 * fc);
       rd[0] = make_float4(racc[0], racc[1], racc[2], racc[3]);
       rd[1] = make_float4(racc[4], racc[5], racc[6], racc[7]);
@@ -664,7 +628,7 @@ struct B2 {
 
 struct Bwd2Params {
   int N, P, seg_len;
-  const float* ws_rev;     // [BH][P][D*D + D] suffixes (R, r) after each segment
+  const float* ws_rev;     // [BH][P][D*D + D] segment sums (R, r), all but the first segment
   const float* ws_tok;     // [BH][N][2] (den, b)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -715,7 +679,6 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
-  const long long rec = ((long long)bh * prm.P + seg) * (long long)(D * D + D);
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -852,11 +815,12 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int row = state_row<D>(q, lane);
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;
-    const float* rr = prm.ws_rev + rec;
-    load_state_to_tmem<D>(rr, lane_addr, G::COL_R, row);
+    // R_after, r_after of the segment: the sums of the segments after it
+    const float* recs = prm.ws_rev + (long long)bh * prm.P * (D * D + D);
     float rrun[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) rrun[e] = owner ? rr[D * D + 8 * fc + e] : 0.f;
+    griddep_wait();
+    sum_states_to_tmem<D>(recs, D * D + D, seg + 1, prm.P, lane_addr, G::COL_R, row);
+    sum_vectors8<D>(recs, D * D + D, seg + 1, prm.P, 8 * fc, rrun);
     bool ok = true;
     for (int i = 0; i < nchunks && ok; ++i) {
       const int s = i % ST;
@@ -934,6 +898,7 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     // ---------------- group C: phi(K), a = g / den, b ----------------
     const int t = tid;                      // chunk row for the a scaling
     const float2* tokp = reinterpret_cast<const float2*>(prm.ws_tok) + (long long)bh * prm.N;
+    griddep_wait();
     bool ok = true;
     for (int i = 0; i < nchunks && ok; ++i) {
       const int s = i % ST;
@@ -976,6 +941,22 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+template <typename Kernel, typename... Args>
+cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <int D>
 cudaError_t launch_backward(const BwdArgs& a) {
   FwdArgs f{};
@@ -983,11 +964,8 @@ cudaError_t launch_backward(const BwdArgs& a) {
   f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = a.causal;
   f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
   f.stream = a.stream;
-  const long long words = state_words(D, D);
   prof_begin(LA_SPAN_BWD_STATE, a.stream);
-  cudaError_t e = tc_segment_state(f);
-  if (e == cudaSuccess)
-    e = segment_scan(a.ws_state, a.BH, a.plan.P, words, SCAN_EXCLUSIVE_FWD, nullptr, nullptr, D, D, a.stream);
+  cudaError_t e = tc_segment_state(f);    // sums of S^T, z for segments 0 .. P-2
   prof_end(LA_SPAN_BWD_STATE, a.stream);
   if (e != cudaSuccess) return e;
 
@@ -1004,16 +982,10 @@ cudaError_t launch_backward(const BwdArgs& a) {
   if (e != cudaSuccess) return e;
   Bwd1Params p1{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dq, status};
   prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
-  tc_bwd1_kernel<D><<<a.BH * a.plan.P, B1<D>::THREADS, smem1, a.stream>>>(mq, mk, mv, mg, p1);
+  e = launch_dependent(tc_bwd1_kernel<D>, a.BH * a.plan.P, B1<D>::THREADS, smem1, a.stream, mq, mk, mv, mg, p1);
   prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   note_launch();
-
-  prof_begin(LA_SPAN_BWD_SCAN, a.stream);
-  e = segment_scan(a.ws_rev, a.BH, a.plan.P, words, SCAN_EXCLUSIVE_REV, nullptr, nullptr, D, D, a.stream);
-  prof_end(LA_SPAN_BWD_SCAN, a.stream);
-  if (e != cudaSuccess) return e;
 
   constexpr int smem2 = B2<D>::BYTES;
   e = cudaFuncSetAttribute(tc_bwd2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
@@ -1021,9 +993,8 @@ cudaError_t launch_backward(const BwdArgs& a) {
   Bwd2Params p2{a.N, a.plan.P, a.plan.seg_len, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dk_, (__nv_bfloat16*)a.dv_,
                 status};
   prof_begin(LA_SPAN_BWD_SWEEP2, a.stream);
-  tc_bwd2_kernel<D><<<a.BH * a.plan.P, B2<D>::THREADS, smem2, a.stream>>>(mq, mk, mv, mg, p2);
+  e = launch_dependent(tc_bwd2_kernel<D>, a.BH * a.plan.P, B2<D>::THREADS, smem2, a.stream, mq, mk, mv, mg, p2);
   prof_end(LA_SPAN_BWD_SWEEP2, a.stream);
-  e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }

@@ -196,6 +196,120 @@ __device__ __forceinline__ void copy_state_to_smem(uint32_t taddr, uint8_t* sbuf
   }
 }
 
+// A D x D fp32 state from global memory (row-major) into tensor memory at
+// column `col` (rows in the M = D accumulator layout).
+template <int D>
+__device__ __forceinline__ void load_state_to_tmem(const float* src, uint32_t lane_addr, uint32_t col, int row) {
+  const float4* srow = reinterpret_cast<const float4*>(src + (row >= 0 ? row : 0) * D);
+#pragma unroll
+  for (int h = 0; h < D; h += 64) {
+    float4 f[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = row >= 0 ? srow[h / 4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[4 * j + 0] = __float_as_uint(f[4 * g + j].x);
+        v[4 * j + 1] = __float_as_uint(f[4 * g + j].y);
+        v[4 * j + 2] = __float_as_uint(f[4 * g + j].z);
+        v[4 * j + 3] = __float_as_uint(f[4 * g + j].w);
+      }
+      tmem_st16(lane_addr + col + h + 16 * g, v);
+    }
+  }
+  tmem_st_wait();
+}
+
+// A D x D fp32 state from tensor memory (column `col`) to global memory.
+template <int D>
+__device__ __forceinline__ void store_state_from_tmem(float* dst, uint32_t lane_addr, uint32_t col, int row) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(lane_addr + col + c0, v);
+    tmem_ld_wait();
+    if (row >= 0) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dst + row * D + c0 + j) =
+            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                        __uint_as_float(v[j + 3]));
+    }
+  }
+}
+
+// Sum of the D x D parts of the state records p0 .. p1-1 (`stride` floats
+// apart, row-major) for this thread's state row, into tensor memory at column
+// `col` (rows in the M = D accumulator layout; row < 0: lane unused).
+template <int D>
+__device__ __forceinline__ void sum_states_to_tmem(const float* recs, long long stride, int p0, int p1,
+                                                   uint32_t lane_addr, uint32_t col, int row) {
+#pragma unroll 1
+  for (int h = 0; h < D; h += 64) {
+    float4 acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row >= 0) {
+#pragma unroll 1
+      for (int p = p0; p < p1; ++p) {
+        const float4* src = reinterpret_cast<const float4*>(recs + p * stride + (long long)row * D + h);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float4 f = src[j];
+          acc[j].x += f.x; acc[j].y += f.y; acc[j].z += f.z; acc[j].w += f.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[4 * j + 0] = __float_as_uint(acc[4 * g + j].x);
+        v[4 * j + 1] = __float_as_uint(acc[4 * g + j].y);
+        v[4 * j + 2] = __float_as_uint(acc[4 * g + j].z);
+        v[4 * j + 3] = __float_as_uint(acc[4 * g + j].w);
+      }
+      tmem_st16(lane_addr + col + h + 16 * g, v);
+    }
+  }
+  tmem_st_wait();
+}
+
+// Sum of the 8-entry slices [off, off + 8) of the vector parts (at D*D) of the
+// state records p0 .. p1-1.
+template <int D>
+__device__ __forceinline__ void sum_vectors8(const float* recs, long long stride, int p0, int p1, int off,
+                                             float (&acc)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 1
+  for (int p = p0; p < p1; ++p) {
+    const float4* src = reinterpret_cast<const float4*>(recs + p * stride + D * D + off);
+    const float4 a = src[0], b = src[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+}
+
+// The transpose of a D x D state held in tensor memory (this thread's lane is
+// row `row` of the held matrix) to global memory, row-major: dst[c][row].
+template <int D>
+__device__ __forceinline__ void store_state_transposed(float* dst, uint32_t lane_addr, uint32_t col, int row) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(lane_addr + col + c0, v);
+    tmem_ld_wait();
+    if (row >= 0) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dst[(long long)(c0 + j) * D + row] = __uint_as_float(v[j]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------

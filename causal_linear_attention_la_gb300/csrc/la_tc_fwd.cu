@@ -6,26 +6,33 @@
 // distributivity argument of "Linear Attention: KV를 고정 크기 상태에 누적하기",
 // fig. 5; the state update is the recurrence of its section "상태 갱신과 읽기를
 // 식으로 정리하기" applied to C tokens at once):
-//   P    = phi(Q_c) phi(K_c)^T, masked to j <= t            MMA1 (tensor cores)
-//   O    = phi(Q_c) S_prev + P V_c                           MMA3, MMA2
-//   S   += phi(K_c)^T V_c                                    MMA4
+//   P    = phi(Q_c) phi(K_c)^T, masked to j <= t            tensor cores
+//   O    = phi(Q_c) S_prev + P V_c                           tensor cores
+//   S   += phi(K_c)^T V_c                                    tensor cores
 //   z   += column sums of phi(K_c)                           CUDA cores, fp32
 //   den  = phi(Q_c) z_prev + P 1 + eps                       CUDA cores, fp32
 //   out  = O / den
-// S lives in tensor memory in fp32 for the whole segment; its bf16 copy in
-// shared memory is the B operand of MMA3. The normaliser terms stay on the
-// CUDA cores: measured on GB300, a thin (N = 16) tcgen05.mma costs nearly as
-// much as a full-width one, while the row and column sums fall out of passes
-// the CUDA cores make anyway.
+// The state is held transposed (S^T, value index first) in fp32 tensor
+// memory for the whole segment: S^T += V^T phi(K) reads both tiles as they
+// arrive, and its bf16 copy in shared memory is then a K-major operand. At
+// D = 64 that copy sits right after the K tile, so P and phi(Q) S_prev come
+// out of one N = 192 MMA (on GB300 an MMA instruction costs about the same
+// for any N up to 256, so fewer, wider instructions are faster). The
+// normaliser terms stay on the CUDA cores, where the row and column sums fall
+// out of passes they make anyway.
 //
-// Two kernels share the machinery:
-//   tc_state_kernel   per-segment sums dS = sum phi(k) v^T, dz = sum phi(k)
-//   tc_forward_kernel the chunk loop above, starting from the segment's prefix
-// (the scan kernel joins them). One CTA per (segment, b*h).
+// Two kernels:
+//   tc_state_kernel   per-segment sums dS^T = V^T phi(K), dz = sum phi(k), for
+//                     every segment but the last of each sequence
+//   tc_forward_kernel the chunk loop above; it starts from the sum of the
+//                     records of the earlier segments (the exclusive prefix),
+//                     and the last segment writes the final state.
+// One CTA per (segment, b*h). The forward kernel is launched as a dependent
+// of the state kernel: it fills its pipeline before waiting for the records.
 //
 // Warp roles in tc_forward_kernel (448 threads):
 //   warps 0-3    group C: phi in place on K with the column sums that update z
-//   warps 4-7    group A: phi in place on Q; state copy S -> shared memory
+//   warps 4-7    group A: phi in place on Q; state copy S^T -> shared memory
 //   warps 8-11   group B: P mask, bf16 pack and row sums; denominators; epilogue
 //   warp 12      TMA producer: Q, K, V chunk tiles into a ring of stages
 //   warp 13      TMEM allocator and MMA issuer (one elected lane)
@@ -48,17 +55,23 @@ template <int D>
 struct Cfg {
   static constexpr int NB = D / 64;                   // 64-feature boxes per tile
   static constexpr int TILE = NB * BOX;               // one [C][D] bf16 tile
-  static constexpr int ST = D == 128 ? 2 : 3;         // forward pipeline stages
-  static constexpr int STAGE = 3 * TILE;              // Q, K, V
-  static constexpr int SBUF = NB * D * 128;           // bf16 S copy, MN-major, D rows per box
+  static constexpr int SBUF = NB * D * 128;           // bf16 copy of S^T, D rows per box
+  static constexpr bool MERGE = D == 64;              // P and phi(Q) S_prev in one MMA
+  static constexpr int ST = D == 64 ? 3 : 2;          // forward pipeline stages
+  // stage layout: Q, K, [S^T copy if MERGE], V
+  static constexpr int OFF_K = TILE;
+  static constexpr int OFF_SB = 2 * TILE;             // MERGE only: rows 128.. of the K operand
+  static constexpr int OFF_V = MERGE ? 2 * TILE + SBUF : 2 * TILE;
+  static constexpr int STAGE = OFF_V + TILE;
   static constexpr int KSTEPS = D / 16;               // MMA k-steps over a head dimension
   static constexpr int NPB = 2;                       // P buffers in tensor memory
+  static constexpr int NOB = MERGE ? 2 : 1;           // O buffers (each follows its P when MERGE)
   // tensor memory columns
-  static constexpr uint32_t COL_P = 0;                // NPB x 128
-  static constexpr uint32_t COL_S = 128 * NPB;        // D
-  static constexpr uint32_t COL_O = COL_S + D;        // D
+  __host__ __device__ static constexpr uint32_t pcol(int pb) { return MERGE ? pb * (128 + D) : 128 * pb; }
+  __host__ __device__ static constexpr uint32_t ocol(int ob) { return MERGE ? ob * (128 + D) + 128 : 128 * NPB + D; }
+  static constexpr uint32_t COL_S = MERGE ? 2 * (128 + D) : 128 * NPB;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
+  static_assert(COL_S + D <= TMEM_COLS && ocol(NOB - 1) + D <= TMEM_COLS, "tensor memory budget");
   // state kernel
   static constexpr int ST_S = D == 128 ? 2 : 3;
   static constexpr int STAGE_S = 2 * TILE;            // K, V
@@ -67,19 +80,23 @@ struct Cfg {
 
 template <int D>
 struct FwdSmem {
-  static constexpr int OFF_SBUF = Cfg<D>::ST * Cfg<D>::STAGE;      // all boxes 1024-aligned
-  static constexpr int OFF_ZST = OFF_SBUF + Cfg<D>::SBUF;          // [ST][D] fp32: z before each staged chunk
-  static constexpr int OFF_BAR = OFF_ZST + Cfg<D>::ST * D * 4;
-  static constexpr int NBAR = 3 * Cfg<D>::ST + 2 * Cfg<D>::NPB + 5;
+  using G = Cfg<D>;
+  static constexpr int OFF_SBUF = G::ST * G::STAGE;                // !MERGE: the S^T copy (1024-aligned)
+  static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // [ST][D] fp32: z before each staged chunk
+  static constexpr int OFF_BAR = OFF_ZST + G::ST * D * 4;
+  static constexpr int NBAR = 3 * G::ST + 2 * G::NPB + 2 * G::NOB + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
+  static_assert(BYTES <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
   int N, P, seg_len;
   float eps;
-  const float* ws_state;   // [BH][P][D*D + D] prefixes
+  const float* ws_state;   // [BH][P][D*D + D] sums of S^T, z over each segment (all but the last)
   __nv_bfloat16* out;      // [BH][N][D]
+  float* S_final;          // [BH][D][D] or null (written by the last segment)
+  float* z_final;          // [BH][D] or null
   int* status;             // device status word (set on a bounded-wait timeout)
 };
 
@@ -89,22 +106,21 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                   const __grid_constant__ CUtensorMap map_v, const FwdParams prm) {
   using G = Cfg<D>;
   using L = FwdSmem<D>;
-  constexpr int ST = G::ST, NPB = G::NPB;
+  constexpr int ST = G::ST, NPB = G::NPB, NOB = G::NOB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
-  uint8_t* sbuf = sm + L::OFF_SBUF;
   float* zst = reinterpret_cast<float*>(sm + L::OFF_ZST);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
-  uint64_t* full = bars;
-  uint64_t* phi_done = bars + ST;
-  uint64_t* empty = bars + 2 * ST;
-  uint64_t* p_full = bars + 3 * ST;              // [NPB]
-  uint64_t* p_ready = bars + 3 * ST + NPB;       // [NPB]
-  uint64_t* s_full = bars + 3 * ST + 2 * NPB;
+  uint64_t* full = bars;                          // [ST]
+  uint64_t* phi_done = bars + ST;                 // [ST]
+  uint64_t* empty = bars + 2 * ST;                // [ST]
+  uint64_t* p_full = bars + 3 * ST;               // [NPB]
+  uint64_t* p_ready = p_full + NPB;               // [NPB]
+  uint64_t* o_full = p_ready + NPB;               // [NOB]
+  uint64_t* o_empty = o_full + NOB;               // [NOB]
+  uint64_t* s_full = o_empty + NOB;
   uint64_t* s_ready = s_full + 1;
-  uint64_t* o_full = s_full + 2;
-  uint64_t* o_empty = s_full + 3;
-  uint64_t* mma_fin = s_full + 4;
+  uint64_t* mma_fin = s_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   // the swizzled operand boxes need 1024-byte alignment of the shared window
@@ -118,7 +134,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
-  const float* st = prm.ws_state + ((long long)bh * prm.P + seg) * (long long)(D * D + D);
+  const bool last_seg = seg == prm.P - 1;
+  const bool write_final = last_seg && prm.S_final != nullptr;
+  // the state update after the last chunk is only needed for the final state
+  const int nupdates = write_final ? nchunks : nchunks - 1;
+  const long long rstride = (long long)(D * D + D);
+  const float* recs = prm.ws_state + (long long)bh * prm.P * rstride;
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -130,10 +151,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       mbar_init(&p_full[i], 1);
       mbar_init(&p_ready[i], 128);
     }
+    for (int i = 0; i < NOB; ++i) {
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 128);
+    }
     mbar_init(s_full, 1);
     mbar_init(s_ready, 128);
-    mbar_init(o_full, 1);
-    mbar_init(o_empty, 128);
     mbar_init(mma_fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -163,8 +186,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
           tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + G::TILE + b * BOX, &map_k, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + 2 * G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::OFF_K + b * BOX, &map_k, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::OFF_V + b * BOX, &map_v, &full[s], 64 * b, y, bh);
         }
         issued = c + 1;
       }
@@ -175,50 +198,57 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t id_qk = make_idesc_bf16(128, 128, false, false);   // P = phiQ phiK^T
-      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, true);      // O = phiQ S
-      constexpr uint32_t id_kv = make_idesc_bf16(D, D, true, true);         // S += phiK^T V
-      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);      // O += P V
-      const uint32_t sbuf_a = smem_u32(sbuf);
+      constexpr uint32_t id_qk = make_idesc_bf16(128, G::MERGE ? 128 + D : 128, false, false);  // [P | O] or P
+      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);    // O = phiQ S_prev (!MERGE)
+      constexpr uint32_t id_vk = make_idesc_bf16(D, D, true, true);        // S^T += V^T phiK
+      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V
+      const uint32_t sbuf_a = smem_u32(sm + L::OFF_SBUF);
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST;
         const uint32_t qa = smem_u32(sm + s * G::STAGE);
-        const uint32_t ka = qa + G::TILE;
-        const uint32_t va = qa + 2 * G::TILE;
-        const int pb = c % NPB;
-        const uint32_t pcol = G::COL_P + 128 * pb;
+        const uint32_t ka = qa + G::OFF_K;
+        const uint32_t va = qa + G::OFF_V;
+        const int pb = c % NPB, ob = c % NOB;
+        const uint32_t pc = tmem + G::pcol(pb), oc = tmem + G::ocol(ob);
         ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        // O buffer ob is free once the epilogue of chunk c - NOB has read it
+        if (ok && G::MERGE && c >= NOB) ok = mbar_wait(&o_empty[ob], ((c / NOB) - 1) & 1, abort_flag, kTimeoutNs);
+        if (ok && G::MERGE) ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        // P (and with MERGE, O = phiQ S_prev in the next D columns)
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
-          mma_ss(tmem + pcol, make_sdesc(qa + off, 16, 1024, kSwizzle128B),
-                 make_sdesc(ka + off, 16, 1024, kSwizzle128B), id_qk, k > 0);
+          mma_ss(pc, make_sdesc(qa + off, 16, 1024, kSwizzle128B), make_sdesc(ka + off, 16, 1024, kSwizzle128B),
+                 id_qk, k > 0);
         }
         tc_commit(&p_full[pb]);
-        ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
-        if (ok && c > 0) ok = mbar_wait(o_empty, (c - 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
+        if (!G::MERGE) {
+          ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
+          if (ok && c >= NOB) ok = mbar_wait(&o_empty[ob], ((c / NOB) - 1) & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < G::KSTEPS; ++k)
-          mma_ss(tmem + G::COL_O, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
-                 make_sdesc(sbuf_a + k * 2048, D * 128, 1024, kSwizzle128B), id_qs, k > 0);
+          for (int k = 0; k < G::KSTEPS; ++k)
+            mma_ss(oc, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
+                   make_sdesc(sbuf_a + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qs, k > 0);
+        }
+        if (c < nupdates) {
 #pragma unroll
-        for (int k = 0; k < C / 16; ++k)
-          mma_ss(tmem + G::COL_S, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B),
-                 make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_kv, 1);
-        tc_commit(s_full);
+          for (int k = 0; k < C / 16; ++k)
+            mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
+                   make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_vk, 1);
+          tc_commit(s_full);
+        }
         ok = mbar_wait(&p_ready[pb], (c / NPB) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
-          mma_ts(tmem + G::COL_O, tmem + pcol + k * 8, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
-                 id_pv, 1);
-        tc_commit(o_full);
+          mma_ts(oc, pc + k * 8, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+        tc_commit(&o_full[ob]);
         tc_commit(&empty[s]);
       }
       // every MMA issued must have finished before tensor memory is released
@@ -230,28 +260,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int t = tid - 128;                // 0..127
     const int q = warp & 3;                 // TMEM quadrant of this warp
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    const int row = state_row<D>(q, lane);
-    // initial state (this segment's prefix) into TMEM
-    const float4* srow = reinterpret_cast<const float4*>(st + (row >= 0 ? row : 0) * D);
-#pragma unroll
-    for (int h = 0; h < D; h += 64) {        // 64 columns per batch: 16 loads in flight
-      float4 f[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) f[j] = row >= 0 ? srow[h / 4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t v[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[4 * j + 0] = __float_as_uint(f[4 * g + j].x);
-          v[4 * j + 1] = __float_as_uint(f[4 * g + j].y);
-          v[4 * j + 2] = __float_as_uint(f[4 * g + j].z);
-          v[4 * j + 3] = __float_as_uint(f[4 * g + j].w);
-        }
-        tmem_st16(lane_addr + G::COL_S + h + 16 * g, v);
-      }
-    }
-    tmem_st_wait();
+    const int row = state_row<D>(q, lane);  // value index m of this lane's S^T row
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -260,16 +269,27 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);   // Q
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
-      // bf16 copy of the state before chunk c (after the previous update)
-      if (c > 0) {
+      if (c == 0) {
+        // this segment's starting state: the sum of the earlier segments' records
+        griddep_wait();
+        sum_states_to_tmem<D>(recs, rstride, 0, seg, lane_addr, G::COL_S, row);
+      } else {
+        // the state after chunk c - 1's update
         ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
       }
-      copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf, row);
+      copy_state_to_smem<D>(lane_addr + G::COL_S, G::MERGE ? sm + s * G::STAGE + G::OFF_SB : sm + L::OFF_SBUF, row);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
+    }
+    if (ok && write_final) {
+      ok = mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      if (ok) {
+        tc_fence_after();
+        store_state_transposed<D>(prm.S_final + (long long)bh * D * D, lane_addr, G::COL_S, row);
+      }
     }
   } else if (warp >= 8 && warp < 12) {
     // ---------------- group B: P, denominators and the output epilogue ----------------
@@ -280,8 +300,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
-      const int pb = c % NPB;
-      const uint32_t pcol = G::COL_P + 128 * pb;
+      const int pb = c % NPB, ob = c % NOB;
+      const uint32_t pcol = G::pcol(pb), ocol = G::ocol(ob);
       ok = mbar_wait(&p_full[pb], (c / NPB) & 1, abort_flag, kTimeoutNs) &&
            mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
@@ -340,7 +360,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tc_fence_before();
       mbar_arrive(&p_ready[pb]);
       // output rows
-      ok = mbar_wait(o_full, c & 1, abort_flag, kTimeoutNs);
+      ok = mbar_wait(&o_full[ob], (c / NOB) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
       const int tok = tok0 + c * C + r;
@@ -348,7 +368,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(lane_addr + G::COL_O + c0, v);
+        tmem_ld32(lane_addr + ocol + c0, v);
         tmem_ld_wait();
         if (tok < tok_end) {
 #pragma unroll
@@ -363,7 +383,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
       }
       tc_fence_before();
-      mbar_arrive(o_empty);
+      mbar_arrive(&o_empty[ob]);
     }
   } else {
     // ---------------- group C: phi(K) and z ----------------
@@ -372,8 +392,6 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;       // holds the z of features 8 fc .. 8 fc + 7
     float zrun[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) zrun[e] = owner ? st[D * D + 8 * fc + e] : 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -381,17 +399,26 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       float colsum[8];
-      phi_tile_exact<D, 128>(sm + s * G::STAGE + G::TILE, t, n_valid, colsum);  // K
+      phi_tile_exact<D, 128>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
       fence_proxy_async_smem();
+      if (c == 0) {
+        griddep_wait();
+        sum_vectors8<D>(recs, rstride, 0, seg, 8 * fc, zrun);
+      }
       if (owner) {
         // z before this chunk, for group B's denominators
         float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
         zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
         zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
       }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
       mbar_arrive(&phi_done[s]);
+    }
+    if (ok && write_final && owner) {
+      float4* zd = reinterpret_cast<float4*>(prm.z_final + (long long)bh * D + 8 * fc);
+      zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
+      zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
     }
   }
 
@@ -406,10 +433,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 }
 
 // ---------------------------------------------------------------------------
-// Per-segment state sums: dS = phi(K_seg)^T V_seg on the tensor cores into
-// TMEM (fp32), dz = column sums of phi(K_seg) on the CUDA cores (fp32).
+// Per-segment state sums: dS^T = V_seg^T phi(K_seg) on the tensor cores into
+// TMEM (fp32), dz = column sums of phi(K_seg) on the CUDA cores (fp32), for
+// segments 0 .. P-2 of each sequence (the last segment's sum is never read:
+// the forward kernel's last segment carries the state to its end itself).
 // 320 threads: warps 0-7 phi(K) (rounded to nearest) and z, warps 0-3 also
-// the final store of dS; warp 8 TMA, warp 9 TMEM allocator and MMA.
+// the final store of dS^T; warp 8 TMA, warp 9 TMEM allocator and MMA.
 // ---------------------------------------------------------------------------
 template <int D>
 struct StateSmem {
@@ -442,13 +471,16 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   uint64_t* mma_fin = bars + 3 * ST + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
+  // the dependent forward kernel may start filling its pipeline right away
+  griddep_launch_dependents();
   if ((smem_u32(sm) & 1023u) != 0u) {
     if (threadIdx.x == 0) report_timeout(prm.status);
     return;
   }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / prm.P, seg = blockIdx.x % prm.P;
+  const int nseg = prm.P - 1;
+  const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
@@ -496,7 +528,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t id_kv = make_idesc_bf16(D, D, true, true);
+      constexpr uint32_t id_vk = make_idesc_bf16(D, D, true, true);
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % ST;
@@ -507,8 +539,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
-          mma_ss(tmem, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B),
-                 make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_kv, (c > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tmem, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
+                 make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_vk, (c > 0 || k > 0) ? 1u : 0u);
         tc_commit(&empty[s]);
       }
       tc_commit(s_full);
@@ -547,19 +579,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     if (ok && warp < 4) ok = mbar_wait(s_full, 0, abort_flag, kTimeoutNs);
     if (ok && warp < 4) {
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + c0, v);
-        tmem_ld_wait();
-        if (row >= 0) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + row * D + c0 + j) =
-                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                            __uint_as_float(v[j + 3]));
-        }
-      }
+      store_state_from_tmem<D>(dst, lane_addr, 0, row);
     }
   }
   if (*abort_flag && tid == 0) report_timeout(prm.status);
@@ -573,6 +593,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 
 template <int D>
 cudaError_t launch_state(const FwdArgs& a) {
+  if (a.plan.P < 2) return cudaSuccess;     // one segment: no earlier segments to sum
   CUtensorMap mk, mv;
   cudaError_t e = make_map(&mk, a.k, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
@@ -581,7 +602,7 @@ cudaError_t launch_state(const FwdArgs& a) {
   e = cudaFuncSetAttribute(tc_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   StateParams p{a.N, a.plan.P, a.plan.seg_len, a.ws_state, device_status_ptr()};
-  tc_state_kernel<D><<<a.BH * a.plan.P, 320, smem, a.stream>>>(mk, mv, p);
+  tc_state_kernel<D><<<a.BH * (a.plan.P - 1), 320, smem, a.stream>>>(mk, mv, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -595,12 +616,24 @@ cudaError_t launch_forward(const FwdArgs& a) {
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
   if (e != cudaSuccess) return e;
   constexpr int smem = FwdSmem<D>::BYTES;
-  static_assert(smem <= 232448, "shared memory budget");
   e = cudaFuncSetAttribute(tc_forward_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  FwdParams p{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, (__nv_bfloat16*)a.out, device_status_ptr()};
-  tc_forward_kernel<D><<<a.BH * a.plan.P, 448, smem, a.stream>>>(mq, mk, mv, p);
-  e = cudaGetLastError();
+  FwdParams p{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, (__nv_bfloat16*)a.out,
+              a.S_final, a.z_final, device_status_ptr()};
+  // a dependent of the state kernel (when there is one): it may start before
+  // that kernel ends and waits for its records only where it reads them
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.BH * a.plan.P);
+  cfg.blockDim = dim3(448);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.plan.P > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D>, mq, mk, mv, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }

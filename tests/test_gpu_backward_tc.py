@@ -59,7 +59,8 @@ def test_backward_path_is_tensor_core():
 def test_backward_tensor_core(B, H, N):
     n0 = la.la_launch_count()
     got, want = _grads(B, H, N, seed=900 + N + B * H)
-    assert la.la_launch_count() - n0 == 5      # state, scan, sweep 1, reverse scan, sweep 2
+    # segment sums (only with more than one segment), sweep 1, sweep 2
+    assert la.la_launch_count() - n0 in (2, 3)
     assert la.la_device_status(True) == la.LA_OK
     errs = grad_errors(got, want)
     assert max(errs) <= TOL["bf16"], errs
