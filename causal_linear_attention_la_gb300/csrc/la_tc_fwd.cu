@@ -81,10 +81,12 @@ struct Cfg {
 template <int D>
 struct FwdSmem {
   using G = Cfg<D>;
+  static constexpr bool TMA_OUT = D == 64;                          // output tiles leave through TMA stores
   static constexpr int OFF_SBUF = G::ST * G::STAGE;                // !MERGE: the S^T copy (1024-aligned)
-  static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // [ST][D] fp32: z before each staged chunk
+  static constexpr int OFF_OST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // TMA_OUT: 2 bf16 output tiles
+  static constexpr int OFF_ZST = OFF_OST + (TMA_OUT ? 2 * G::TILE : 0);  // [ST][D] fp32: z before each staged chunk
   static constexpr int OFF_BAR = OFF_ZST + G::ST * D * 4;
-  static constexpr int NBAR = 3 * G::ST + 2 * G::NPB + 2 * G::NOB + 3;
+  static constexpr int NBAR = 3 * G::ST + 2 * G::NPB + 2 * G::NOB + 3 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -103,7 +105,8 @@ struct FwdParams {
 template <int D>
 __global__ void __launch_bounds__(448, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const FwdParams prm) {
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                  const FwdParams prm) {
   using G = Cfg<D>;
   using L = FwdSmem<D>;
   constexpr int ST = G::ST, NPB = G::NPB, NOB = G::NOB;
@@ -121,6 +124,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint64_t* s_full = o_empty + NOB;
   uint64_t* s_ready = s_full + 1;
   uint64_t* mma_fin = s_full + 2;
+  uint64_t* ost_full = s_full + 3;                // [2] output tile written (group B)
+  uint64_t* ost_free = s_full + 5;                // [2] output tile read by its TMA store
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   // the swizzled operand boxes need 1024-byte alignment of the shared window
@@ -158,6 +163,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     mbar_init(s_full, 1);
     mbar_init(s_ready, 128);
     mbar_init(mma_fin, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ost_full[i], 128);
+      mbar_init(&ost_free[i], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -364,6 +373,44 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (!ok) break;
       tc_fence_after();
       const int tok = tok0 + c * C + r;
+      if (L::TMA_OUT) {
+        // Stage the bf16 row in a swizzled tile; one thread stores the whole
+        // tile with TMA (rows past the end of the sequence are clipped).
+        const int i = c & 1;
+        uint8_t* ost = sm + L::OFF_OST + i * G::TILE;
+        if (c >= 2) ok = mbar_wait(&ost_free[i], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + ocol + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * inv_den, __uint_as_float(v[8 * j + 1]) * inv_den);
+            w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv_den, __uint_as_float(v[8 * j + 3]) * inv_den);
+            w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv_den, __uint_as_float(v[8 * j + 5]) * inv_den);
+            w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv_den, __uint_as_float(v[8 * j + 7]) * inv_den);
+            *reinterpret_cast<uint4*>(ost + (c0 / 64) * BOX + sw128(r, (c0 % 64) / 8 + j)) = w;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&o_empty[ob]);
+        fence_proxy_async_smem();
+        mbar_arrive(&ost_full[i]);
+        if (r == 0) {
+          ok = mbar_wait(&ost_full[i], (c >> 1) & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+#pragma unroll
+          for (int b = 0; b < G::NB; ++b) tma_store_3d(&map_o, ost + b * BOX, 64 * b, tok0 + c * C, bh);
+          tma_store_commit();
+          // the previous tile's store has read its buffer once at most one group is left
+          tma_store_wait_read<1>();
+          if (c >= 1) mbar_arrive(&ost_free[(c - 1) & 1]);
+        }
+        continue;
+      }
       uint4* dst = reinterpret_cast<uint4*>(outb + (long long)tok * D);
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -385,6 +432,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tc_fence_before();
       mbar_arrive(&o_empty[ob]);
     }
+    // every TMA store of this CTA must be complete before it exits
+    if (L::TMA_OUT && r == 0) tma_store_wait<0>();
   } else {
     // ---------------- group C: phi(K) and z ----------------
     using X = ExactLayout<D, 128>;
@@ -610,10 +659,11 @@ cudaError_t launch_state(const FwdArgs& a) {
 
 template <int D>
 cudaError_t launch_forward(const FwdArgs& a) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   cudaError_t e = make_map(&mq, a.q, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mk, a.k, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mo, a.out, a.BH, a.N, D);
   if (e != cudaSuccess) return e;
   constexpr int smem = FwdSmem<D>::BYTES;
   e = cudaFuncSetAttribute(tc_forward_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -632,7 +682,7 @@ cudaError_t launch_forward(const FwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.plan.P > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D>, mq, mk, mv, p);
+  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D>, mq, mk, mv, mo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
