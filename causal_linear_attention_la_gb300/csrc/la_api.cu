@@ -67,7 +67,7 @@ WsLayout layout(long long BH, int N, int dk, int dv, const SegPlan& plan, bool b
   WsLayout w{};
   const size_t rec = sizeof(float) * (size_t)state_words(dk, dv) * (size_t)plan.P * (size_t)BH;
   w.state_off = 0;
-  size_t off = align_up(rec, 256);
+  size_t off = align_up(rec * (size_t)plan.F, 256);
   if (backward) {
     w.rev_off = off;
     off += align_up(rec, 256);
@@ -195,10 +195,30 @@ SegPlan plan_segments(long long BH, int N, int slots) {
   return best;
 }
 
-// The forward's segment plan (one CTA per SM for every forward kernel).
+// The forward's segment plan (one CTA per SM for the output kernels). On the
+// tensor-core path the state pass may split each segment over F CTAs (F
+// records per segment) while it still fits in one CTA per SM: the output
+// kernel's CTAs, which need a whole SM, start on the SMs the state pass
+// leaves free (measured: a state pass spread over every SM delays them more
+// than its shorter CTAs save).
 SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool causal) {
-  (void)dk; (void)dv; (void)dtype; (void)causal;
-  return plan_segments(BH, N, kSlots);
+  SegPlan plan = plan_segments(BH, N, kSlots);
+  const bool tc = g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, causal);
+  if (!tc || plan.P < 2) return plan;
+  const int L = plan.seg_len / kSegGranule;
+  double best = 1e300;
+  for (int F = 1; F <= 8 && F <= L; ++F) {
+    const int sub = (L + F - 1) / F;
+    if ((F - 1) * sub >= L) continue;          // every part must hold a chunk
+    const long long ctas = BH * (plan.P - 1) * F;
+    if (F > 1 && ctas > kSlots) break;
+    const double cost = (double)((ctas + kSlots - 1) / kSlots) * (sub + 1);
+    if (cost < best) {
+      best = cost;
+      plan.F = F;
+    }
+  }
+  return plan;
 }
 
 }  // namespace la

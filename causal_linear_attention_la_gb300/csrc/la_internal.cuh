@@ -30,6 +30,8 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+constexpr int kSegGranuleDecl = 128;  // = kSegGranule (declared below)
+
 // ---------------------------------------------------------------------------
 // Sequence segmentation: each (batch, head) sequence is cut into P segments
 // of seg_len tokens (the last may be shorter); one CTA per (segment, b*h).
@@ -37,9 +39,16 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 struct SegPlan {
   int P;        // segments per sequence (>= 1)
   int seg_len;  // tokens per segment, multiple of kSegGranule (except when N is smaller)
+  int F = 1;    // tensor-core state pass: CTAs (and sum records) per segment
 };
 
-constexpr int kSegGranule = 128;   // tokens; one tensor-core chunk
+// Tokens summed by one state-pass CTA: ceil(chunks per segment / F) chunks.
+inline int state_sub_len(const SegPlan& p) {
+  const int L = (p.seg_len + kSegGranuleDecl - 1) / kSegGranuleDecl;
+  return ((L + p.F - 1) / p.F) * kSegGranuleDecl;
+}
+
+constexpr int kSegGranule = kSegGranuleDecl;   // tokens; one tensor-core chunk
 constexpr int kSlots = 152;        // CTAs resident at once: one per SM of a GB300
 
 // Segments per sequence for B*H sequences of N tokens when `slots` CTAs can

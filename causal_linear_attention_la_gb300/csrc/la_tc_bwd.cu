@@ -248,9 +248,9 @@ struct B1 {
 };
 
 struct Bwd1Params {
-  int N, P, seg_len;
+  int N, P, seg_len, F;
   float eps;
-  const float* ws_state;   // [BH][P][D*D + D] segment sums (S^T, z), all but the last segment
+  const float* ws_state;   // [BH][P*F][D*D + D] state-pass sums (S^T, z) of segments 0..P-2
   float* ws_rev;           // [BH][P][D*D + D] segment sums (R, r), all but the first segment
   float* ws_tok;           // [BH][N][2] (den, b) per token
   __nv_bfloat16* dq;       // [BH][N][D]
@@ -453,8 +453,8 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
     griddep_wait();
-    sum_states_to_tmem<D>(prm.ws_state + (long long)bh * prm.P * (D * D + D), D * D + D, 0, seg, lane_addr,
-                          G::COL_S, row);
+    sum_states_to_tmem<D>(prm.ws_state + (long long)bh * prm.P * prm.F * (D * D + D), D * D + D, 0,
+                          seg * prm.F, lane_addr, G::COL_S, row);
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -547,7 +547,8 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const bool owner = lane < X::FCW;
     float zrun[8], racc[8];
     griddep_wait();
-    sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * (D * D + D), D * D + D, 0, seg, 8 * fc, zrun);
+    sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * prm.F * (D * D + D), D * D + D, 0, seg * prm.F,
+                    8 * fc, zrun);
 #pragma unroll
     for (int e = 0; e < 8; ++e) racc[e] = 0.f;
     bool ok = true;
@@ -980,7 +981,7 @@ cudaError_t launch_backward(const BwdArgs& a) {
   constexpr int smem1 = B1<D>::BYTES;
   e = cudaFuncSetAttribute(tc_bwd1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem1);
   if (e != cudaSuccess) return e;
-  Bwd1Params p1{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dq, status};
+  Bwd1Params p1{a.N, a.plan.P, a.plan.seg_len, a.plan.F, a.eps, a.ws_state, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dq, status};
   prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
   e = launch_dependent(tc_bwd1_kernel<D>, a.BH * a.plan.P, B1<D>::THREADS, smem1, a.stream, mq, mk, mv, mg, p1);
   prof_end(LA_SPAN_BWD_SWEEP1, a.stream);

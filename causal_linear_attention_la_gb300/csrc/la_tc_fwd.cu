@@ -93,9 +93,9 @@ struct FwdSmem {
 };
 
 struct FwdParams {
-  int N, P, seg_len;
+  int N, P, seg_len, F;
   float eps;
-  const float* ws_state;   // [BH][P][D*D + D] sums of S^T, z over each segment (all but the last)
+  const float* ws_state;   // [BH][P*F][D*D + D] sums of S^T, z over each state-pass part (segments 0..P-2)
   __nv_bfloat16* out;      // [BH][N][D]
   float* S_final;          // [BH][D][D] or null (written by the last segment)
   float* z_final;          // [BH][D] or null
@@ -135,7 +135,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / prm.P, seg = blockIdx.x % prm.P;
+  // segment-major order: the first segments (which wait for no records) come first
+  const int BH = gridDim.x / prm.P;
+  const int bh = blockIdx.x % BH, seg = blockIdx.x / BH;
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
@@ -144,7 +146,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   // the state update after the last chunk is only needed for the final state
   const int nupdates = write_final ? nchunks : nchunks - 1;
   const long long rstride = (long long)(D * D + D);
-  const float* recs = prm.ws_state + (long long)bh * prm.P * rstride;
+  const float* recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
+  const int nrec = seg * prm.F;           // records of the earlier segments
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -280,8 +283,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       mbar_arrive(&phi_done[s]);
       if (c == 0) {
         // this segment's starting state: the sum of the earlier segments' records
-        griddep_wait();
-        sum_states_to_tmem<D>(recs, rstride, 0, seg, lane_addr, G::COL_S, row);
+        if (nrec > 0) griddep_wait();
+        sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row);
       } else {
         // the state after chunk c - 1's update
         ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
@@ -451,8 +454,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       phi_tile_exact<D, 128>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
       fence_proxy_async_smem();
       if (c == 0) {
-        griddep_wait();
-        sum_vectors8<D>(recs, rstride, 0, seg, 8 * fc, zrun);
+        if (nrec > 0) griddep_wait();
+        sum_vectors8<D>(recs, rstride, 0, nrec, 8 * fc, zrun);
       }
       if (owner) {
         // z before this chunk, for group B's denominators
@@ -498,8 +501,8 @@ struct StateSmem {
 };
 
 struct StateParams {
-  int N, P, seg_len;
-  float* ws_state;  // [BH][P][D*D + D]
+  int N, P, seg_len, F, sub_len;
+  float* ws_state;  // [BH][P*F][D*D + D]
   int* status;
 };
 
@@ -528,10 +531,13 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nseg = prm.P - 1;
-  const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
-  const int tok0 = seg * prm.seg_len;
-  const int tok_end = min(prm.N, tok0 + prm.seg_len);
+  // part j of segment j / F covers sub_len tokens from j % F * sub_len
+  const int nparts = (prm.P - 1) * prm.F;
+  const int bh = blockIdx.x / nparts, j = blockIdx.x % nparts;
+  const int seg = j / prm.F, part = j % prm.F;
+  const int seg_end = min(prm.N, (seg + 1) * prm.seg_len);
+  const int tok0 = seg * prm.seg_len + part * prm.sub_len;
+  const int tok_end = min(seg_end, tok0 + prm.sub_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
 
   if (tid == 0) {
@@ -619,7 +625,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 #pragma unroll
       for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
     }
-    float* dst = prm.ws_state + ((long long)bh * prm.P + seg) * (long long)(D * D + D);
+    float* dst = prm.ws_state + ((long long)bh * prm.P * prm.F + j) * (long long)(D * D + D);
     if (ok && lane < X::FCW) {
       float4* zd = reinterpret_cast<float4*>(dst + D * D + 8 * fc);
       zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
@@ -650,8 +656,8 @@ cudaError_t launch_state(const FwdArgs& a) {
   constexpr int smem = StateSmem<D>::BYTES;
   e = cudaFuncSetAttribute(tc_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  StateParams p{a.N, a.plan.P, a.plan.seg_len, a.ws_state, device_status_ptr()};
-  tc_state_kernel<D><<<a.BH * (a.plan.P - 1), 320, smem, a.stream>>>(mk, mv, p);
+  StateParams p{a.N, a.plan.P, a.plan.seg_len, a.plan.F, state_sub_len(a.plan), a.ws_state, device_status_ptr()};
+  tc_state_kernel<D><<<a.BH * (a.plan.P - 1) * a.plan.F, 320, smem, a.stream>>>(mk, mv, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -668,7 +674,7 @@ cudaError_t launch_forward(const FwdArgs& a) {
   constexpr int smem = FwdSmem<D>::BYTES;
   e = cudaFuncSetAttribute(tc_forward_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  FwdParams p{a.N, a.plan.P, a.plan.seg_len, a.eps, a.ws_state, (__nv_bfloat16*)a.out,
+  FwdParams p{a.N, a.plan.P, a.plan.seg_len, a.plan.F, a.eps, a.ws_state, (__nv_bfloat16*)a.out,
               a.S_final, a.z_final, device_status_ptr()};
   // a dependent of the state kernel (when there is one): it may start before
   // that kernel ends and waits for its records only where it reads them

@@ -60,8 +60,13 @@ def test_workspace_sizes(lib):
     # one record per (b, h, segment); sizes grow with B*H
     assert f(4, 8, 4096, 64, 64, 1, la.LA_BF16) >= 32 * 4 * (64 * 64 + 64)
     b = la.la_backward_workspace_size(4, 8, 8192, 64, 64, 1, la.LA_BF16)
-    # two records per segment plus 2 floats per token
-    assert b >= 2 * f(4, 8, 8192, 64, 64, 1, la.LA_BF16) - 256 + 4 * 2 * 32 * 8192
+    # state and reverse records (at least one segment each) plus 2 floats per token
+    assert b >= 2 * 32 * 4 * (64 * 64 + 64) + 4 * 2 * 32 * 8192
+    # the CUDA-core path (fp32 inputs): one state and one reverse record per
+    # segment, so the backward needs twice the forward's records plus the tokens
+    fs = f(4, 8, 8192, 64, 64, 1, la.LA_F32)
+    bs = la.la_backward_workspace_size(4, 8, 8192, 64, 64, 1, la.LA_F32)
+    assert bs >= 2 * fs - 256 + 4 * 2 * 32 * 8192
 
 
 def _fwd(**kw):

@@ -124,3 +124,25 @@ def test_tensor_core_path_is_taken(d):
     assert la.la_launch_count() - n0 == 2
     assert la.la_device_status(True) == la.LA_OK
     assert rel_err(got, want, np.abs(v).max()) <= TOL["bf16"]
+
+
+def test_state_pass_split_over_ctas():
+    """60 sequences of 2048 tokens: two segments per sequence, and the segment
+    sums of the first are split over two CTAs of the state pass (its workspace
+    then holds more records than the CUDA-core plan). Sampled heads, final
+    state included, are checked against the oracle."""
+    import torch
+    B, H, N, d = 6, 10, 2048, 64
+    ws_tc = la.la_forward_workspace_size(B, H, N, d, d, 1, la.LA_BF16)
+    ws_f32 = la.la_forward_workspace_size(B, H, N, d, d, 1, la.LA_F32)
+    assert ws_tc > ws_f32
+    q, k, v = synth.qkv(B, H, N, d, d, seed=606, dtype="bf16")
+    out, S, z = _run(q, k, v, True, "bf16", state=True)
+    assert la.la_device_status(True) == la.LA_OK
+    out, S, z = to_host(out), to_host(S), to_host(z)
+    for b, h in [(0, 0), (2, 5), (5, 9)]:
+        want, S_w, z_w = orc.forward_recurrent(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                               v[b:b + 1, h:h + 1], return_state=True)
+        assert rel_err(out[b:b + 1, h:h + 1], want, np.abs(v).max()) <= TOL["bf16"]
+        assert rel_err(S[b, h], S_w[0, 0], np.abs(S_w).max()) <= STATE_TOL["bf16"]
+        assert rel_err(z[b, h], z_w[0, 0], np.abs(z_w).max()) <= Z_TOL["bf16"]
