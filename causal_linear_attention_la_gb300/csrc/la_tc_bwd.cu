@@ -223,21 +223,25 @@ struct B1 {
   static_assert(D == 64, "the tensor-core backward is laid out for D = 64");
   static constexpr int NB = D / 64;
   static constexpr int TILE = NB * BOX;
-  static constexpr int ST = 3;                        // stages of Q, K, V, G
-  static constexpr int STAGE = 4 * TILE;
-  static constexpr int SBUF = NB * D * 128;           // bf16 copy of S_prev
-  static constexpr int NSB = 2;
+  static constexpr int ST = 3;                        // stages of Q, K, S^T copy, V, G
+  static constexpr int SBUF = NB * D * 128;           // bf16 copy of S_prev^T
+  // stage layout: the S_prev^T copy follows the K tile, so that
+  // [phi(K) ; S_prev^T] is one K-major operand of 128 + D rows
+  static constexpr int OFF_K = TILE;
+  static constexpr int OFF_SC = 2 * TILE;
+  static constexpr int OFF_V = 2 * TILE + SBUF;
+  static constexpr int OFF_G = 3 * TILE + SBUF;
+  static constexpr int STAGE = 4 * TILE + SBUF;
   static constexpr int KSTEPS = D / 16;
-  // tensor memory columns
-  static constexpr uint32_t COL_PD = 0;               // 2 x 128: P, then dP (fp32, bf16 packed in place)
-  static constexpr uint32_t COL_OQ = 256;             // 2 x D: O, then dQ
-  static constexpr uint32_t COL_S = COL_OQ + 2 * D;   // D
+  // tensor memory columns: two [P | O] pairs (P then dP in place, O then dQ)
+  __host__ __device__ static constexpr uint32_t col_pd(int pb) { return pb * (128 + D); }
+  __host__ __device__ static constexpr uint32_t col_oq(int pb) { return pb * (128 + D) + 128; }
+  static constexpr uint32_t COL_S = 2 * (128 + D);    // D
   static constexpr uint32_t COL_R = COL_S + D;        // D
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(COL_R + D <= TMEM_COLS, "tensor memory budget");
   // shared memory
-  static constexpr int OFF_SBUF = ST * STAGE;
-  static constexpr int OFF_ZST = OFF_SBUF + NSB * SBUF;   // [ST][D] z before each staged chunk
+  static constexpr int OFF_ZST = ST * STAGE;              // [ST][D] z before each staged chunk
   static constexpr int OFF_BARR = OFF_ZST + ST * D * 4;   // [ST][C] b_t of each staged chunk
   static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
   static constexpr int NBAR = 3 * ST + 21;
@@ -273,7 +277,6 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   constexpr int ST = G::ST;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
-  uint8_t* sbuf = sm + G::OFF_SBUF;
   float* zst = reinterpret_cast<float*>(sm + G::OFF_ZST);
   float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
@@ -283,7 +286,6 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   uint64_t* x = bars + 3 * ST;
   uint64_t* p_full = x;                  // [2]
   uint64_t* p_ready = x + 2;             // [2]
-  uint64_t* sb_free = x + 4;             // [2]
   uint64_t* o_full = x + 6;              // [2]
   uint64_t* a_ready = x + 8;             // [2]
   uint64_t* dp_full = x + 10;            // [2]
@@ -318,7 +320,6 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_ready[i], 128);
-      mbar_init(&sb_free[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&a_ready[i], 128);
       mbar_init(&dp_full[i], 1);
@@ -358,9 +359,9 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
           tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + G::TILE + b * BOX, &map_k, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + 2 * G::TILE + b * BOX, &map_v, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + 3 * G::TILE + b * BOX, &map_g, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::OFF_K + b * BOX, &map_k, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::OFF_V + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + G::OFF_G + b * BOX, &map_g, &full[s], 64 * b, y, bh);
         }
         issued = c + 1;
       }
@@ -370,39 +371,34 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   } else if (warp == 17) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t id_qk = make_idesc_bf16(128, 128, false, false);  // P = phiQ phiK^T, dP = a V^T
-      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);    // O = phiQ S_prev (S^T copy K-major)
+      constexpr uint32_t id_qk = make_idesc_bf16(128, 128, false, false);  // dP = a V^T
+      constexpr uint32_t id_qs = make_idesc_bf16(128, 128 + D, false, false);  // [P | O] = phiQ [phiK ; S_prev^T]^T
       constexpr uint32_t id_as = make_idesc_bf16(128, D, false, true);     // dQ = a S_prev^T (S^T copy MN-major)
       constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // S^T += V^T phiK, R += phiQ^T a
       constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V, dQ += dP' phiK
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int s = c % ST, pb = c & 1, sbi = c % G::NSB;
+        const int s = c % ST, pb = c & 1;
         const uint32_t qa = smem_u32(sm + s * G::STAGE);
-        const uint32_t ka = qa + G::TILE, va = qa + 2 * G::TILE, ga = qa + 3 * G::TILE;
-        const uint32_t sb = smem_u32(sbuf + sbi * G::SBUF);
-        const uint32_t pd = tmem + G::COL_PD + 128 * pb;
-        const uint32_t oq = tmem + G::COL_OQ + D * pb;
+        const uint32_t ka = qa + G::OFF_K, va = qa + G::OFF_V, ga = qa + G::OFF_G, sb = qa + G::OFF_SC;
+        const uint32_t pd = tmem + G::col_pd(pb);
+        const uint32_t oq = tmem + G::col_oq(pb);
         ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
-        // the P/dP and O/dQ buffers of chunk c - 2 are free once its last MMA is done
+        // the P/dP and O/dQ buffers of chunk c - 2 are free once its last MMA
+        // is done and its dq epilogue has read them
         if (ok && c >= 2) ok = mbar_wait(&dq_full[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
+        if (ok) ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
+        if (ok && c >= 2) ok = mbar_wait(&oq_empty[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        // P and O = phiQ S_prev share A = phiQ: one MMA over [phiK ; S_prev^T]
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
           mma_ss(pd, make_sdesc(qa + off, 16, 1024, kSwizzle128B), make_sdesc(ka + off, 16, 1024, kSwizzle128B),
-                 id_qk, k > 0);
+                 id_qs, k > 0);
         }
         tc_commit(&p_full[pb]);
-        ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
-        if (ok && c >= 2) ok = mbar_wait(&oq_empty[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < G::KSTEPS; ++k)
-          mma_ss(oq, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
-                 make_sdesc(sb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qs, k > 0);
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
@@ -433,7 +429,6 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         for (int k = 0; k < C / 16; ++k)
           mma_ss(tmem + G::COL_R, make_sdesc(qa + k * 2048, BOX, 1024, kSwizzle128B),
                  make_sdesc(ga + k * 2048, BOX, 1024, kSwizzle128B), id_tt, (c > 0 || k > 0) ? 1u : 0u);
-        tc_commit(&sb_free[sbi]);
         ok = mbar_wait(&dp_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
@@ -464,10 +459,9 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
       if (c > 0) ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
-      if (ok && c >= G::NSB) ok = mbar_wait(&sb_free[c % G::NSB], ((c / G::NSB) - 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf + (c % G::NSB) * G::SBUF, row);
+      copy_state_to_smem<D>(lane_addr + G::COL_S, sm + s * G::STAGE + G::OFF_SC, row);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
@@ -491,7 +485,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
            mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const float rowsum = mask_pack_row<true, false>(lane_addr + G::COL_PD + 128 * pb, q, lane, 0.f, nullptr);
+      const float rowsum = mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, 0.f, nullptr);
       const uint8_t* qt = sm + s * G::STAGE;
       const float den = rowsum + phiq_dot<D>(qt, r, zst + s * D) + prm.eps;
       const float inv_den = 1.f / den;
@@ -501,7 +495,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = mbar_wait(&o_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const float beta = grad_row_pass<D>(lane_addr + G::COL_OQ + D * pb, sm + s * G::STAGE + 3 * G::TILE, r, inv_den);
+      const float beta = grad_row_pass<D>(lane_addr + G::col_oq(pb), sm + s * G::STAGE + G::OFF_G, r, inv_den);
       const float b = -beta * inv_den * inv_den;
       barr[s * C + r] = b;
       const int tok = tok0 + c * C + r;
@@ -525,7 +519,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const float b = barr[s * C + r];
-      mask_pack_row<true, false>(lane_addr + G::COL_PD + 128 * pb, q, lane, b, nullptr);
+      mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, b, nullptr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&dp_ready[pb]);
@@ -533,7 +527,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const int tok = tok0 + c * C + r;
-      grad_epilogue<D>(lane_addr + G::COL_OQ + D * pb, sm + s * G::STAGE, r, b, zst + s * D,
+      grad_epilogue<D>(lane_addr + G::col_oq(pb), sm + s * G::STAGE, r, b, zst + s * D,
                        tok < tok_end ? dqb + (long long)tok * D : nullptr);
       tc_fence_before();
       mbar_arrive(&oq_empty[pb]);
@@ -559,7 +553,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         float colsum[8];
-        phi_tile_exact<D, 128>(sm + s * G::STAGE + G::TILE, t, n_valid, colsum);
+        phi_tile_exact<D, 128>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);
         fence_proxy_async_smem();
         if (owner) {
           float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
@@ -606,18 +600,21 @@ struct B2 {
   static constexpr int NB = D / 64;
   static constexpr int TILE = NB * BOX;
   static constexpr int ST = 3;
-  static constexpr int STAGE = 4 * TILE;              // Q, K, V, G (G becomes a in place)
   static constexpr int RBUF = NB * D * 128;           // bf16 copy of R_after
+  // stage: Q, K, V, G (becomes a in place), then the R_after copy right after
+  // the a tile, so that [a ; R_after] is one K-major operand of 128 + D rows
+  static constexpr int OFF_R = 4 * TILE;
+  static constexpr int STAGE = OFF_R + RBUF;
   static constexpr int KSTEPS = D / 16;
   static constexpr uint32_t COL_PT = 0;               // 128
-  static constexpr uint32_t COL_DPT = 128;            // 128
+  static constexpr uint32_t COL_DPT = 128;            // 128, followed by dK: [dP^T | dK] from one MMA
   static constexpr uint32_t COL_DK = 256;             // D
   static constexpr uint32_t COL_DV = COL_DK + D;      // D
   static constexpr uint32_t COL_R = COL_DV + D;       // D
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(COL_R + D <= TMEM_COLS, "tensor memory budget");
-  static constexpr int OFF_RBUF = ST * STAGE;
-  static constexpr int OFF_RVEC = OFF_RBUF + RBUF;        // [2][D] r_after
+  static_assert(COL_DK == COL_DPT + 128, "dK must follow dP^T");
+  static constexpr int OFF_RVEC = ST * STAGE;             // [2][D] r_after
   static constexpr int OFF_BARR = OFF_RVEC + 2 * D * 4;   // [ST][C] b_t
   static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
   static constexpr int NBAR = 3 * ST + 12;
@@ -651,7 +648,6 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   constexpr int ST = G::ST;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
-  uint8_t* rbuf = sm + G::OFF_RBUF;
   float* rvec = reinterpret_cast<float*>(sm + G::OFF_RVEC);
   float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
@@ -739,19 +735,18 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t id_kq = make_idesc_bf16(128, 128, false, false);  // P^T = phiK phiQ^T, dP^T = V a^T
-      constexpr uint32_t id_vr = make_idesc_bf16(128, D, false, false);    // dK = V R^T
+      constexpr uint32_t id_kq = make_idesc_bf16(128, 128, false, false);  // P^T = phiK phiQ^T
+      constexpr uint32_t id_vr = make_idesc_bf16(128, 128 + D, false, false);  // [dP^T | dK] = V [a ; R]^T
       constexpr uint32_t id_kr = make_idesc_bf16(128, D, false, true);     // dV = phiK R
       constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // R += phiQ^T a
       constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // dK += dP^T' phiQ, dV += P^T' a
-      const uint32_t rb = smem_u32(rbuf);
       const uint32_t pt = tmem + G::COL_PT, dpt = tmem + G::COL_DPT;
       const uint32_t dkc = tmem + G::COL_DK, dvc = tmem + G::COL_DV;
       bool ok = true;
       for (int i = 0; i < nchunks && ok; ++i) {
         const int s = i % ST;
         const uint32_t qa = smem_u32(sm + s * G::STAGE);
-        const uint32_t ka = qa + G::TILE, va = qa + 2 * G::TILE, ga = qa + 3 * G::TILE;
+        const uint32_t ka = qa + G::TILE, va = qa + 2 * G::TILE, ga = qa + 3 * G::TILE, rb = qa + G::OFF_R;
         ok = mbar_wait(&prep_done[s], (i / ST) & 1, abort_flag, kTimeoutNs);
         // the P^T / dP^T buffers are free once the previous chunk's MMAs are done
         if (ok && i >= 1) ok = mbar_wait(kv_full, (i - 1) & 1, abort_flag, kTimeoutNs);
@@ -764,23 +759,18 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                  id_kq, k > 0);
         }
         tc_commit(pt_full);
-#pragma unroll
-        for (int k = 0; k < G::KSTEPS; ++k) {
-          const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
-          mma_ss(dpt, make_sdesc(va + off, 16, 1024, kSwizzle128B), make_sdesc(ga + off, 16, 1024, kSwizzle128B),
-                 id_kq, k > 0);
-        }
-        tc_commit(dpt_full);
         ok = mbar_wait(&rb_ready[i & 1], (i >> 1) & 1, abort_flag, kTimeoutNs);
         if (ok && i >= 1) ok = mbar_wait(&kv_empty[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        // dP^T = V a^T and dK = V R_after^T share A = V: one MMA over [a ; R_after]
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
-          mma_ss(dkc, make_sdesc(va + off, 16, 1024, kSwizzle128B),
-                 make_sdesc(rb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_vr, k > 0);
+          mma_ss(dpt, make_sdesc(va + off, 16, 1024, kSwizzle128B), make_sdesc(ga + off, 16, 1024, kSwizzle128B),
+                 id_vr, k > 0);
         }
+        tc_commit(dpt_full);
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
@@ -836,7 +826,7 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       if (ok && i >= 2) ok = mbar_wait(&kv_empty[i & 1], ((i - 2) >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      copy_state_to_smem<D>(lane_addr + G::COL_R, rbuf, row);
+      copy_state_to_smem<D>(lane_addr + G::COL_R, sm + s * G::STAGE + G::OFF_R, row);
       if (owner) {
         float4* rd = reinterpret_cast<float4*>(rvec + (i & 1) * D + 8 * fc);
         rd[0] = make_float4(rrun[0], rrun[1], rrun[2], rrun[3]);
