@@ -73,7 +73,7 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(COL_S + D <= TMEM_COLS && ocol(NOB - 1) + D <= TMEM_COLS, "tensor memory budget");
   // state kernel
-  static constexpr int ST_S = D == 128 ? 2 : 3;
+  static constexpr int ST_S = D == 128 ? 3 : 6;    // state-pass stages (bytes in flight hide DRAM latency)
   static constexpr int STAGE_S = 2 * TILE;            // K, V
   static constexpr uint32_t TMEM_COLS_S = D == 128 ? 128 : 64;
 };
