@@ -80,17 +80,10 @@ struct ExactLayout {
   static_assert(FCW >= 1 && FCW <= 8 && (FCW & (FCW - 1)) == 0, "layout");
 };
 
-template <int D, int NT>
-__device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8]) {
+template <int D, int NT, bool kCheck>
+__device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r0, int n_valid, float (&zacc)[8]) {
   using X = ExactLayout<D, NT>;
   constexpr int GR = 4;                               // rows per loop trip (kept small: code size)
-  const int w = t >> 5, lane = t & 31;
-  const int fc = X::FCW * w + (lane % X::FCW);       // feature chunk 0 .. D/8-1
-  const int r0 = lane / X::FCW;
-  uint8_t* base = tile + (fc >> 3) * BOX;
-  const int ch = fc & 7;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) zacc[e] = 0.f;
 #pragma unroll 1
   for (int i0 = 0; i0 < X::RPT; i0 += GR) {
     uint4 wv[GR];
@@ -98,7 +91,7 @@ __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid
     for (int i = 0; i < GR; ++i) wv[i] = *reinterpret_cast<const uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch));
 #pragma unroll
     for (int i = 0; i < GR; ++i) {
-      const bool valid = r0 + X::RG * (i0 + i) < n_valid;
+      const bool valid = !kCheck || r0 + X::RG * (i0 + i) < n_valid;
       uint32_t* p = reinterpret_cast<uint32_t*>(&wv[i]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
@@ -112,12 +105,36 @@ __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid
 #pragma unroll
     for (int i = 0; i < GR; ++i) *reinterpret_cast<uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch)) = wv[i];
   }
+}
+
+// kReduce: zacc is cleared first and, on return, reduced inside the warp as
+// above. Otherwise this thread's partial sums are added to zacc, and the
+// caller reduces them (reduce_row_groups) when it needs the totals.
+template <int D, int NT, bool kReduce = true>
+__device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8]) {
+  using X = ExactLayout<D, NT>;
+  const int w = t >> 5, lane = t & 31;
+  const int fc = X::FCW * w + (lane % X::FCW);       // feature chunk 0 .. D/8-1
+  const int r0 = lane / X::FCW;
+  uint8_t* base = tile + (fc >> 3) * BOX;
+  const int ch = fc & 7;
+  if (kReduce) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float x = zacc[e];
+    for (int e = 0; e < 8; ++e) zacc[e] = 0.f;
+  }
+  // full tiles skip the per-row validity test
+  if (n_valid >= C)
+    phi_tile_exact_rows<D, NT, false>(base, ch, r0, n_valid, zacc);
+  else
+    phi_tile_exact_rows<D, NT, true>(base, ch, r0, n_valid, zacc);
+  if (kReduce) {
 #pragma unroll
-    for (int o = X::FCW; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    zacc[e] = x;
+    for (int e = 0; e < 8; ++e) {
+      float x = zacc[e];
+#pragma unroll
+      for (int o = X::FCW; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      zacc[e] = x;
+    }
   }
 }
 

@@ -609,6 +609,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    // per-thread partial column sums, reduced once after the last chunk
     float zrun[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) zrun[e] = 0.f;
@@ -618,13 +619,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       const int n_valid = min(C, tok_end - (tok0 + c * C));
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      float colsum[8];
-      phi_tile_exact<D, 256>(sm + s * G::STAGE_S, t, n_valid, colsum);
+      phi_tile_exact<D, 256, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
     }
+    reduce_row_groups<D, 256>(zrun);
     float* dst = prm.ws_state + ((long long)bh * prm.P * prm.F + j) * (long long)(D * D + D);
     if (ok && lane < X::FCW) {
       float4* zd = reinterpret_cast<float4*>(dst + D * D + 8 * fc);
