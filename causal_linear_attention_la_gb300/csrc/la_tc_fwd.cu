@@ -81,12 +81,10 @@ struct Cfg {
 template <int D>
 struct FwdSmem {
   using G = Cfg<D>;
-  static constexpr bool TMA_OUT = D == 64;                          // output tiles leave through TMA stores
   static constexpr int OFF_SBUF = G::ST * G::STAGE;                // !MERGE: the S^T copy (1024-aligned)
-  static constexpr int OFF_OST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // TMA_OUT: 2 bf16 output tiles
-  static constexpr int OFF_ZST = OFF_OST + (TMA_OUT ? 2 * G::TILE : 0);  // [ST][D] fp32: z before each staged chunk
+  static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // [ST][D] fp32: z before each staged chunk
   static constexpr int OFF_BAR = OFF_ZST + G::ST * D * 4;
-  static constexpr int NBAR = 3 * G::ST + 2 * G::NPB + 2 * G::NOB + 3 + 4;
+  static constexpr int NBAR = 4 * G::ST + 2 * G::NPB + 2 * G::NOB + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -124,8 +122,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint64_t* s_full = o_empty + NOB;
   uint64_t* s_ready = s_full + 1;
   uint64_t* mma_fin = s_full + 2;
-  uint64_t* ost_full = s_full + 3;                // [2] output tile written (group B)
-  uint64_t* ost_free = s_full + 5;                // [2] output tile read by its TMA store
+  uint64_t* ost_full = s_full + 3;                // [ST] output tile of the staged chunk written (group B)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   // the swizzled operand boxes need 1024-byte alignment of the shared window
@@ -166,10 +163,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     mbar_init(s_full, 1);
     mbar_init(s_ready, 128);
     mbar_init(mma_fin, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ost_full[i], 128);
-      mbar_init(&ost_free[i], 1);
-    }
+    for (int i = 0; i < ST; ++i) mbar_init(&ost_full[i], 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -188,10 +182,29 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      int issued = 0;
-      for (int c = 0; c < nchunks; ++c) {
+      tma_prefetch_desc(&map_o);
+      // The output tile of a chunk is staged in its stage's Q region (dead
+      // once the chunk's MMAs are done); this thread stores it with TMA and
+      // waits until the store has read it before refilling the stage.
+      auto store_out = [&](int c) {
         const int s = c % ST;
-        if (c >= ST && !mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
+        if (!mbar_wait(&ost_full[s], (c / ST) & 1, abort_flag, kTimeoutNs)) return false;
+        uint8_t* stg = sm + s * G::STAGE;
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b) tma_store_3d(&map_o, stg + b * BOX, 64 * b, tok0 + c * C, bh);
+        tma_store_commit();
+        tma_store_wait_read<0>();
+        return true;
+      };
+      int issued = 0, stored = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % ST;
+        if (c >= ST) {
+          ok = mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs) && store_out(c - ST);
+          if (!ok) break;
+          stored = c - ST + 1;
+        }
         uint8_t* stg = sm + s * G::STAGE;
         mbar_arrive_expect_tx(&full[s], 3 * G::TILE);
         const int y = tok0 + c * C;
@@ -203,7 +216,11 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         issued = c + 1;
       }
-      // drain: every issued load must land before the CTA's smem is released
+      // the chunks still in the ring: their outputs
+      for (int c = stored; c < issued && ok; ++c) ok = store_out(c);
+      // every store must be complete, and every issued load must have landed,
+      // before the CTA's shared memory is released
+      tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
         mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
     }
@@ -308,7 +325,6 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int q = warp & 3;
     const int r = 32 * q + lane;            // chunk row (query token) of this thread
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    __nv_bfloat16* outb = prm.out + (long long)bh * prm.N * D;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -375,68 +391,30 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       ok = mbar_wait(&o_full[ob], (c / NOB) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const int tok = tok0 + c * C + r;
-      if (L::TMA_OUT) {
-        // Stage the bf16 row in a swizzled tile; one thread stores the whole
-        // tile with TMA (rows past the end of the sequence are clipped).
-        const int i = c & 1;
-        uint8_t* ost = sm + L::OFF_OST + i * G::TILE;
-        if (c >= 2) ok = mbar_wait(&ost_free[i], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + ocol + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * inv_den, __uint_as_float(v[8 * j + 1]) * inv_den);
-            w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv_den, __uint_as_float(v[8 * j + 3]) * inv_den);
-            w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv_den, __uint_as_float(v[8 * j + 5]) * inv_den);
-            w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv_den, __uint_as_float(v[8 * j + 7]) * inv_den);
-            *reinterpret_cast<uint4*>(ost + (c0 / 64) * BOX + sw128(r, (c0 % 64) / 8 + j)) = w;
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&o_empty[ob]);
-        fence_proxy_async_smem();
-        mbar_arrive(&ost_full[i]);
-        if (r == 0) {
-          ok = mbar_wait(&ost_full[i], (c >> 1) & 1, abort_flag, kTimeoutNs);
-          if (!ok) break;
-#pragma unroll
-          for (int b = 0; b < G::NB; ++b) tma_store_3d(&map_o, ost + b * BOX, 64 * b, tok0 + c * C, bh);
-          tma_store_commit();
-          // the previous tile's store has read its buffer once at most one group is left
-          tma_store_wait_read<1>();
-          if (c >= 1) mbar_arrive(&ost_free[(c - 1) & 1]);
-        }
-        continue;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(outb + (long long)tok * D);
+      // Stage the bf16 row in the chunk's Q tile region (swizzled rows); the
+      // TMA producer stores the whole tile (rows past the end of the sequence
+      // are clipped) before it refills the stage.
+      uint8_t* ost = sm + s * G::STAGE;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(lane_addr + ocol + c0, v);
         tmem_ld_wait();
-        if (tok < tok_end) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * inv_den, __uint_as_float(v[8 * j + 1]) * inv_den);
-            w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv_den, __uint_as_float(v[8 * j + 3]) * inv_den);
-            w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv_den, __uint_as_float(v[8 * j + 5]) * inv_den);
-            w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv_den, __uint_as_float(v[8 * j + 7]) * inv_den);
-            dst[c0 / 8 + j] = w;
-          }
+        for (int j = 0; j < 4; ++j) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * inv_den, __uint_as_float(v[8 * j + 1]) * inv_den);
+          w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv_den, __uint_as_float(v[8 * j + 3]) * inv_den);
+          w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv_den, __uint_as_float(v[8 * j + 5]) * inv_den);
+          w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv_den, __uint_as_float(v[8 * j + 7]) * inv_den);
+          *reinterpret_cast<uint4*>(ost + (c0 / 64) * BOX + sw128(r, (c0 % 64) / 8 + j)) = w;
         }
       }
       tc_fence_before();
       mbar_arrive(&o_empty[ob]);
+      fence_proxy_async_smem();
+      mbar_arrive(&ost_full[s]);
     }
-    // every TMA store of this CTA must be complete before it exits
-    if (L::TMA_OUT && r == 0) tma_store_wait<0>();
   } else {
     // ---------------- group C: phi(K) and z ----------------
     using X = ExactLayout<D, 128>;
