@@ -158,11 +158,12 @@ __device__ __forceinline__ float grad_row_pass(uint32_t taddr, uint8_t* gtile, i
 }
 
 // Epilogue row of a gradient: x = acc (tensor memory) + add_s * add_v, times
-// phi'(.) = min(phi, 1) read from row r of a phi-transformed tile, stored to
-// dst (bf16) unless dst is null. add_v is an fp32 vector of D entries.
+// phi'(.) = min(phi, 1) read from row r of a phi-transformed tile, written in
+// bf16 to row r of the swizzled output tile `otile` (stored later with TMA).
+// add_v is an fp32 vector of D entries.
 template <int D>
 __device__ __forceinline__ void grad_epilogue(uint32_t taddr, const uint8_t* ftile, int r, float add_s,
-                                              const float* add_v, __nv_bfloat16* dst) {
+                                              const float* add_v, uint8_t* otile) {
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += 32) {
     uint32_t v[32];
@@ -171,46 +172,42 @@ __device__ __forceinline__ void grad_epilogue(uint32_t taddr, const uint8_t* fti
 #pragma unroll
     for (int j = 0; j < 4; ++j) fw[j] = ld_chunk(ftile, r, c0 / 8 + j);
     tmem_ld_wait();
-    if (dst != nullptr) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t* pw = reinterpret_cast<const uint32_t*>(&fw[j]);
-        const float4 a0 = *reinterpret_cast<const float4*>(add_v + c0 + 8 * j);
-        const float4 a1 = *reinterpret_cast<const float4*>(add_v + c0 + 8 * j + 4);
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        uint4 o;
-        uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(&fw[j]);
+      const float4 a0 = *reinterpret_cast<const float4*>(add_v + c0 + 8 * j);
+      const float4 a1 = *reinterpret_cast<const float4*>(add_v + c0 + 8 * j + 4);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      uint4 o;
+      uint32_t* po = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float x0 = fmaf(add_s, av[2 * h], __uint_as_float(v[8 * j + 2 * h])) * fminf(bf_lo(pw[h]), 1.f);
-          const float x1 =
-              fmaf(add_s, av[2 * h + 1], __uint_as_float(v[8 * j + 2 * h + 1])) * fminf(bf_hi(pw[h]), 1.f);
-          po[h] = pack_bf16x2(x0, x1);
-        }
-        reinterpret_cast<uint4*>(dst)[c0 / 8 + j] = o;
+      for (int h = 0; h < 4; ++h) {
+        const float x0 = fmaf(add_s, av[2 * h], __uint_as_float(v[8 * j + 2 * h])) * fminf(bf_lo(pw[h]), 1.f);
+        const float x1 =
+            fmaf(add_s, av[2 * h + 1], __uint_as_float(v[8 * j + 2 * h + 1])) * fminf(bf_hi(pw[h]), 1.f);
+        po[h] = pack_bf16x2(x0, x1);
       }
+      st_chunk(otile, r, c0 / 8 + j, o);
     }
   }
 }
 
-// Plain bf16 store of an fp32 tensor-memory row (D columns).
+// An fp32 tensor-memory row (D columns) in bf16 to row r of a swizzled tile.
 template <int D>
-__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst) {
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint8_t* otile, int r) {
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += 32) {
     uint32_t v[32];
     tmem_ld32(taddr + c0, v);
     tmem_ld_wait();
-    if (dst != nullptr) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 o;
-        o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-        o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-        o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-        o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-        reinterpret_cast<uint4*>(dst)[c0 / 8 + j] = o;
-      }
+    for (int j = 0; j < 4; ++j) {
+      uint4 o;
+      o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+      o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+      o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+      o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+      st_chunk(otile, r, c0 / 8 + j, o);
     }
   }
 }
@@ -272,7 +269,7 @@ template <int D>
 __global__ void __launch_bounds__(576, 1)
 tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
-               const Bwd1Params prm) {
+               const __grid_constant__ CUtensorMap map_dq, const Bwd1Params prm) {
   using G = B1<D>;
   constexpr int ST = G::ST;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -349,10 +346,24 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
       tma_prefetch_desc(&map_g);
+      // dq of a chunk is staged in its stage's K region; it is stored here,
+      // once the stage's consumers are done, before the stage is refilled
+      auto store_dq = [&](int c) {
+        uint8_t* stg = sm + (c % ST) * G::STAGE;
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b) tma_store_3d(&map_dq, stg + G::OFF_K + b * BOX, 64 * b, tok0 + c * C, bh);
+        tma_store_commit();
+        tma_store_wait_read<0>();
+      };
       int issued = 0;
+      bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % ST;
-        if (c >= ST && !mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
+        if (c >= ST) {
+          ok = mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          store_dq(c - ST);
+        }
         uint8_t* stg = sm + s * G::STAGE;
         mbar_arrive_expect_tx(&full[s], 4 * G::TILE);
         const int y = tok0 + c * C;
@@ -365,6 +376,12 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         }
         issued = c + 1;
       }
+      // the chunks still in the ring
+      for (int c = max(0, issued - ST); c < issued && ok; ++c) {
+        ok = mbar_wait(&empty[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        if (ok) store_dq(c);
+      }
+      tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
         mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
     }
@@ -509,7 +526,6 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    __nv_bfloat16* dqb = prm.dq + (long long)bh * prm.N * D;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST, pb = c & 1;
@@ -526,11 +542,13 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = mbar_wait(&dq_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const int tok = tok0 + c * C + r;
+      // dq staged in the chunk's K region (dead once dQ += dP' phiK is done);
+      // the TMA producer stores it before refilling the stage
       grad_epilogue<D>(lane_addr + G::col_oq(pb), sm + s * G::STAGE, r, b, zst + s * D,
-                       tok < tok_end ? dqb + (long long)tok * D : nullptr);
+                       sm + s * G::STAGE + G::OFF_K);
       tc_fence_before();
       mbar_arrive(&oq_empty[pb]);
+      fence_proxy_async_smem();
       mbar_arrive(&empty[s]);
     }
   } else {
@@ -643,6 +661,7 @@ template <int D>
 __global__ void __launch_bounds__(448, 1)
 tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+               const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                const Bwd2Params prm) {
   using G = B2<D>;
   constexpr int ST = G::ST;
@@ -713,10 +732,28 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
       tma_prefetch_desc(&map_g);
+      // dk and dv of iteration i are staged in its stage's V and a tiles;
+      // they are stored here, once the stage's consumers are done
+      auto store_dkv = [&](int i) {
+        uint8_t* stg = sm + (i % ST) * G::STAGE;
+        const int y = tok0 + (nchunks - 1 - i) * C;
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b) {
+          tma_store_3d(&map_dk, stg + 2 * G::TILE + b * BOX, 64 * b, y, bh);
+          tma_store_3d(&map_dv, stg + 3 * G::TILE + b * BOX, 64 * b, y, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_read<0>();
+      };
       int issued = 0;
+      bool ok = true;
       for (int i = 0; i < nchunks; ++i) {
         const int s = i % ST;
-        if (i >= ST && !mbar_wait(&empty[s], ((i / ST) - 1) & 1, abort_flag, kTimeoutNs)) break;
+        if (i >= ST) {
+          ok = mbar_wait(&empty[s], ((i / ST) - 1) & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          store_dkv(i - ST);
+        }
         uint8_t* stg = sm + s * G::STAGE;
         mbar_arrive_expect_tx(&full[s], 4 * G::TILE);
         const int y = tok0 + (nchunks - 1 - i) * C;
@@ -729,6 +766,12 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         }
         issued = i + 1;
       }
+      // the chunks still in the ring
+      for (int i = max(0, issued - ST); i < issued && ok; ++i) {
+        ok = mbar_wait(&empty[i % ST], (i / ST) & 1, abort_flag, kTimeoutNs);
+        if (ok) store_dkv(i);
+      }
+      tma_store_wait<0>();
       for (int i = max(0, issued - ST); i < issued; ++i)
         mbar_wait(&full[i % ST], (i / ST) & 1, abort_flag, kTimeoutNs);
     }
@@ -852,8 +895,6 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int q = warp & 3;
     const int r = 32 * q + lane;            // key row j of the chunk
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    __nv_bfloat16* dkb = prm.dk + (long long)bh * prm.N * D;
-    __nv_bfloat16* dvb = prm.dv + (long long)bh * prm.N * D;
     bool ok = true;
     for (int i = 0; i < nchunks && ok; ++i) {
       const int s = i % ST;
@@ -876,13 +917,14 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = mbar_wait(kv_full, i & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const int tok = tok0 + (nchunks - 1 - i) * C + r;
-      const bool valid = tok < tok_end;
-      grad_epilogue<D>(lane_addr + G::COL_DK, sm + s * G::STAGE + G::TILE, r, 1.f, rvec + (i & 1) * D,
-                       valid ? dkb + (long long)tok * D : nullptr);
-      store_row_bf16<D>(lane_addr + G::COL_DV, valid ? dvb + (long long)tok * D : nullptr);
+      // dk and dv staged in the chunk's V and a tiles (dead once its MMAs are
+      // done); the TMA producer stores them before refilling the stage
+      uint8_t* stg = sm + s * G::STAGE;
+      grad_epilogue<D>(lane_addr + G::COL_DK, stg + G::TILE, r, 1.f, rvec + (i & 1) * D, stg + 2 * G::TILE);
+      store_row_bf16<D>(lane_addr + G::COL_DV, stg + 3 * G::TILE, r);
       tc_fence_before();
       mbar_arrive(&kv_empty[i & 1]);
+      fence_proxy_async_smem();
       mbar_arrive(&empty[s]);
     }
   } else {
@@ -965,6 +1007,10 @@ cudaError_t launch_backward(const BwdArgs& a) {
   if (e == cudaSuccess) e = make_map(&mk, a.k, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mg, a.dout, a.BH, a.N, D);
+  CUtensorMap mdq, mdk, mdv;
+  if (e == cudaSuccess) e = make_map(&mdq, a.dq, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mdk, a.dk_, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mdv, a.dv_, a.BH, a.N, D);
   if (e != cudaSuccess) return e;
   int* status = device_status_ptr();
 
@@ -973,7 +1019,7 @@ cudaError_t launch_backward(const BwdArgs& a) {
   if (e != cudaSuccess) return e;
   Bwd1Params p1{a.N, a.plan.P, a.plan.seg_len, a.plan.F, a.eps, a.ws_state, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dq, status};
   prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
-  e = launch_dependent(tc_bwd1_kernel<D>, a.BH * a.plan.P, B1<D>::THREADS, smem1, a.stream, mq, mk, mv, mg, p1);
+  e = launch_dependent(tc_bwd1_kernel<D>, a.BH * a.plan.P, B1<D>::THREADS, smem1, a.stream, mq, mk, mv, mg, mdq, p1);
   prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
   if (e != cudaSuccess) return e;
   note_launch();
@@ -984,7 +1030,8 @@ cudaError_t launch_backward(const BwdArgs& a) {
   Bwd2Params p2{a.N, a.plan.P, a.plan.seg_len, a.ws_rev, a.ws_tok, (__nv_bfloat16*)a.dk_, (__nv_bfloat16*)a.dv_,
                 status};
   prof_begin(LA_SPAN_BWD_SWEEP2, a.stream);
-  e = launch_dependent(tc_bwd2_kernel<D>, a.BH * a.plan.P, B2<D>::THREADS, smem2, a.stream, mq, mk, mv, mg, p2);
+  e = launch_dependent(tc_bwd2_kernel<D>, a.BH * a.plan.P, B2<D>::THREADS, smem2, a.stream, mq, mk, mv, mg, mdk, mdv,
+                       p2);
   prof_end(LA_SPAN_BWD_SWEEP2, a.stream);
   if (e == cudaSuccess) note_launch();
   return e;
