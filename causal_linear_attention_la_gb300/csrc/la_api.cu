@@ -204,13 +204,15 @@ SegPlan plan_segments(long long BH, int N, int slots) {
 SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool causal) {
   SegPlan plan = plan_segments(BH, N, kSlots);
   const bool tc = g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, causal);
-  if (!tc || plan.P < 2) return plan;
+  // segments the state pass sums: the earlier ones (causal) or all of them
+  const int nseg = causal ? plan.P - 1 : plan.P;
+  if (!tc || nseg < 1) return plan;
   const int L = plan.seg_len / kSegGranule;
   double best = 1e300;
   for (int F = 1; F <= 8 && F <= L; ++F) {
     const int sub = (L + F - 1) / F;
     if ((F - 1) * sub >= L) continue;          // every part must hold a chunk
-    const long long ctas = BH * (plan.P - 1) * F;
+    const long long ctas = BH * nseg * F;
     if (F > 1 && ctas > kSlots) break;
     const double cost = (double)((ctas + kSlots - 1) / kSlots) * (sub + 1);
     if (cost < best) {

@@ -96,7 +96,7 @@ cudaError_t simt_forward_output(const FwdArgs& a);
 cudaError_t simt_backward(const BwdArgs& a);
 cudaError_t decode_step(const DecodeArgs& a);
 
-// Tensor-core kernels (bf16, dk = dv in {64, 128}, causal)
+// Tensor-core kernels (bf16, dk = dv in {64, 128}; causal and non-causal)
 bool tc_forward_supported(int dk, int dv, la_dtype dtype, int causal);
 cudaError_t tc_segment_state(const FwdArgs& a);
 cudaError_t tc_forward_output(const FwdArgs& a);

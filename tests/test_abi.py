@@ -120,9 +120,11 @@ def test_path_selection(lib):
     prev = la.la_set_path(la.LA_PATH_SIMT)
     assert la.la_forward_path(64, 64, la.LA_BF16) == 0
     la.la_set_path(la.LA_PATH_AUTO)
-    # tensor cores for bf16 causal with dk = dv in {64, 128}
+    # tensor cores for bf16 with dk = dv in {64, 128}, causal or not
     assert la.la_forward_path(64, 64, la.LA_BF16) == 1
     assert la.la_forward_path(128, 128, la.LA_BF16) == 1
+    assert la.la_forward_path(64, 64, la.LA_BF16, False) == 1
+    assert la.la_forward_path(128, 128, la.LA_BF16, False) == 1
     assert la.la_forward_path(128, 64, la.LA_BF16) == 0
     assert la.la_forward_path(64, 64, la.LA_F32) == 0
     assert la.la_forward_path(32, 32, la.LA_BF16) == 0

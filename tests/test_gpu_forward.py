@@ -60,7 +60,7 @@ def test_tiny_config_f32(causal):
     (1, 3, 2000, 128, 128),   # many segments
     (2, 2, 300, 128, 32),
     (1, 1, 4100, 16, 64),
-    # tensor-core sizes (bf16, causal, dk = dv in {64, 128}): one token, a
+    # tensor-core sizes (bf16, dk = dv in {64, 128}): one token, a
     # partial chunk, exact chunks, many segments with a ragged tail
     (1, 1, 1, 64, 64),
     (1, 2, 127, 128, 128),
@@ -124,6 +124,32 @@ def test_tensor_core_path_is_taken(d):
     assert la.la_launch_count() - n0 == 2
     assert la.la_device_status(True) == la.LA_OK
     assert rel_err(got, want, np.abs(v).max()) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,N", [
+    (1, 1, 1),        # one token
+    (1, 1, 300),      # one segment, ragged chunk
+    (1, 1, 4100),     # many segments, a short last segment
+    (6, 10, 2049),    # segments split over several state CTAs, one-token tail
+    (2, 3, 9000),
+])
+def test_noncausal_tensor_core(B, H, N, d):
+    """Non-causal: every query reads the whole-sequence state S_N, z_N; the
+    state pass sums all segments and a second kernel applies the total."""
+    assert la.la_forward_path(d, d, la.LA_BF16, False) == 1
+    q, k, v = synth.qkv(B, H, N, d, d, seed=500 + N + d, dtype="bf16")
+    want, S_ref, z_ref = orc.forward_recurrent(q, k, v, causal=False, eps=1e-6,
+                                               return_state=True)
+    n0 = la.la_launch_count()
+    got, S, z = _run(q, k, v, False, "bf16", state=True)
+    assert la.la_launch_count() - n0 == 2
+    assert la.la_device_status(True) == la.LA_OK
+    err = rel_err(to_host(got), want, np.abs(v).max())
+    assert err <= TOL["bf16"], err
+    s_err = rel_err(to_host(S), S_ref, np.abs(S_ref).max())
+    z_err = rel_err(to_host(z), z_ref, np.abs(z_ref).max())
+    assert s_err <= STATE_TOL["bf16"] and z_err <= Z_TOL["bf16"], (s_err, z_err)
 
 
 def test_state_pass_split_over_ctas():
