@@ -80,7 +80,7 @@ struct ExactLayout {
   static_assert(FCW >= 1 && FCW <= 8 && (FCW & (FCW - 1)) == 0, "layout");
 };
 
-template <int D, int NT, bool kCheck>
+template <int D, int NT, bool kCheck, bool kSum>
 __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r0, int n_valid, float (&zacc)[8]) {
   using X = ExactLayout<D, NT>;
   constexpr int GR = 4;                               // rows per loop trip (kept small: code size)
@@ -97,8 +97,10 @@ __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r
       for (int h = 0; h < 4; ++h) {
         const float lo = valid ? phi_f32(__uint_as_float(p[h] << 16)) : 0.f;
         const float hi = valid ? phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)) : 0.f;
-        zacc[2 * h] += lo;
-        zacc[2 * h + 1] += hi;
+        if (kSum) {
+          zacc[2 * h] += lo;
+          zacc[2 * h + 1] += hi;
+        }
         p[h] = pack_bf16x2(lo, hi);
       }
     }
@@ -110,7 +112,8 @@ __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r
 // kReduce: zacc is cleared first and, on return, reduced inside the warp as
 // above. Otherwise this thread's partial sums are added to zacc, and the
 // caller reduces them (reduce_row_groups) when it needs the totals.
-template <int D, int NT, bool kReduce = true>
+// kSum = false: phi only, zacc untouched.
+template <int D, int NT, bool kReduce = true, bool kSum = true>
 __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8]) {
   using X = ExactLayout<D, NT>;
   const int w = t >> 5, lane = t & 31;
@@ -118,16 +121,16 @@ __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid
   const int r0 = lane / X::FCW;
   uint8_t* base = tile + (fc >> 3) * BOX;
   const int ch = fc & 7;
-  if (kReduce) {
+  if (kReduce && kSum) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) zacc[e] = 0.f;
   }
   // full tiles skip the per-row validity test
   if (n_valid >= C)
-    phi_tile_exact_rows<D, NT, false>(base, ch, r0, n_valid, zacc);
+    phi_tile_exact_rows<D, NT, false, kSum>(base, ch, r0, n_valid, zacc);
   else
-    phi_tile_exact_rows<D, NT, true>(base, ch, r0, n_valid, zacc);
-  if (kReduce) {
+    phi_tile_exact_rows<D, NT, true, kSum>(base, ch, r0, n_valid, zacc);
+  if (kReduce && kSum) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       float x = zacc[e];

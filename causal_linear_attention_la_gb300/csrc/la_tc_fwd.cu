@@ -58,20 +58,28 @@ struct Cfg {
   static constexpr int NB = D / 64;                   // 64-feature boxes per tile
   static constexpr int TILE = NB * BOX;               // one [C][D] bf16 tile
   static constexpr int SBUF = NB * D * 128;           // bf16 copy of S^T, D rows per box
-  static constexpr bool MERGE = D == 64;              // P and phi(Q) S_prev in one MMA
+  static constexpr bool MERGE = D == 64;              // P, phi(Q) S_prev and phi(Q) z_prev in one MMA
   static constexpr int ST = D == 64 ? 3 : 2;          // forward pipeline stages
-  // stage layout: Q, K, [S^T copy if MERGE], V
+  // MERGE: the state is held as one M = 128 accumulator [S^T ; z ... z]
+  // (lanes 0..D-1 the rows of S^T, lanes D..127 copies of z), and its bf16
+  // copy (D rows of S^T, then ZR rows of z) follows the K tile, so that one
+  // MMA with N = 128 + D + ZR gives [P | phi(Q) S_prev | phi(Q) z_prev].
+  static constexpr int ZR = 16;                       // z rows in the copy (N granule)
+  static constexpr int NQK = MERGE ? 128 + D + ZR : 128;
+  static constexpr int SBM = (D + ZR) * 128;          // MERGE: bytes of the copy
+  // stage layout: Q, K, [S^T and z copy if MERGE], V
   static constexpr int OFF_K = TILE;
   static constexpr int OFF_SB = 2 * TILE;             // MERGE only: rows 128.. of the K operand
-  static constexpr int OFF_V = MERGE ? 2 * TILE + SBUF : 2 * TILE;
+  static constexpr int OFF_V = MERGE ? 2 * TILE + SBM : 2 * TILE;
   static constexpr int STAGE = OFF_V + TILE;
+  static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static constexpr int KSTEPS = D / 16;               // MMA k-steps over a head dimension
   static constexpr int NPB = 2;                       // P buffers in tensor memory
   static constexpr int NOB = MERGE ? 2 : 1;           // O buffers (each follows its P when MERGE)
-  // tensor memory columns
-  __host__ __device__ static constexpr uint32_t pcol(int pb) { return MERGE ? pb * (128 + D) : 128 * pb; }
-  __host__ __device__ static constexpr uint32_t ocol(int ob) { return MERGE ? ob * (128 + D) + 128 : 128 * NPB + D; }
-  static constexpr uint32_t COL_S = MERGE ? 2 * (128 + D) : 128 * NPB;
+  // tensor memory columns; MERGE: per buffer [P 128 | O D | den ZR], 224 apart
+  __host__ __device__ static constexpr uint32_t pcol(int pb) { return MERGE ? pb * 224 : 128 * pb; }
+  __host__ __device__ static constexpr uint32_t ocol(int ob) { return MERGE ? ob * 224 + 128 : 128 * NPB + D; }
+  static constexpr uint32_t COL_S = MERGE ? 448 : 128 * NPB;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(COL_S + D <= TMEM_COLS && ocol(NOB - 1) + D <= TMEM_COLS, "tensor memory budget");
   // state kernel
@@ -83,9 +91,13 @@ struct Cfg {
 template <int D>
 struct FwdSmem {
   using G = Cfg<D>;
-  static constexpr int OFF_SBUF = G::ST * G::STAGE;                // !MERGE: the S^T copy (1024-aligned)
-  static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // [ST][D] fp32: z before each staged chunk
-  static constexpr int OFF_BAR = OFF_ZST + G::ST * D * 4;
+  // MERGE: a [C][64] tile of bf16 ones, the second 64-wide block of the V
+  // operands: rows D.. of V^T (so the state MMA also sums z) and columns D..
+  // of [V | 1] (so P V also sums the rows of P)
+  static constexpr int OFF_ONES = G::ST * G::STAGE;
+  static constexpr int OFF_SBUF = OFF_ONES + (G::MERGE ? BOX : 0);    // !MERGE: the S^T copy (1024-aligned)
+  static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // !MERGE: [ST][D] fp32 z before each staged chunk
+  static constexpr int OFF_BAR = OFF_ZST + (G::MERGE ? 0 : G::ST * D * 4);
   static constexpr int NBAR = 4 * G::ST + 2 * G::NPB + 2 * G::NOB + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
@@ -169,6 +181,11 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (G::MERGE) {
+    uint4* ones = reinterpret_cast<uint4*>(sm + L::OFF_ONES);
+    for (int i = tid; i < BOX / 16; i += blockDim.x) ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   if (warp == 13) {
     tmem_alloc(tmem_slot, G::TMEM_COLS);
     tmem_relinquish();
@@ -229,17 +246,23 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t id_qk = make_idesc_bf16(128, G::MERGE ? 128 + D : 128, false, false);  // [P | O] or P
+      constexpr uint32_t id_qk = make_idesc_bf16(128, G::NQK, false, false);  // [P | O | den] or P
       constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);    // O = phiQ S_prev (!MERGE)
-      constexpr uint32_t id_vk = make_idesc_bf16(D, D, true, true);        // S^T += V^T phiK
-      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V
+      // S^T += V^T phiK; MERGE: [S^T ; z] += [V^T ; 1] phiK
+      constexpr uint32_t id_vk = make_idesc_bf16(G::MERGE ? 128 : D, D, true, true);
+      // O += P V; MERGE: [O | den] += P [V | 1]
+      constexpr uint32_t id_pv = make_idesc_bf16(128, G::MERGE ? D + G::ZR : D, false, true);
       const uint32_t sbuf_a = smem_u32(sm + L::OFF_SBUF);
+      const uint32_t ones_a = smem_u32(sm + L::OFF_ONES);
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST;
         const uint32_t qa = smem_u32(sm + s * G::STAGE);
         const uint32_t ka = qa + G::OFF_K;
         const uint32_t va = qa + G::OFF_V;
+        // the second 64-wide block of an MN-major V operand: the next feature
+        // box, or (MERGE) the ones tile
+        const uint32_t v_lbo = G::MERGE ? ones_a - va : (uint32_t)BOX;
         const int pb = c % NPB, ob = c % NOB;
         const uint32_t pc = tmem + G::pcol(pb), oc = tmem + G::ocol(ob);
         ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
@@ -269,7 +292,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (c < nupdates) {
 #pragma unroll
           for (int k = 0; k < C / 16; ++k)
-            mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
+            mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, v_lbo, 1024, kSwizzle128B),
                    make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_vk, 1);
           tc_commit(s_full);
         }
@@ -278,7 +301,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
-          mma_ts(oc, pc + k * 8, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+          mma_ts(oc, pc + k * 8, make_sdesc(va + k * 2048, v_lbo, 1024, kSwizzle128B), id_pv, 1);
         tc_commit(&o_full[ob]);
         tc_commit(&empty[s]);
       }
@@ -291,7 +314,13 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int t = tid - 128;                // 0..127
     const int q = warp & 3;                 // TMEM quadrant of this warp
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    const int row = state_row<D>(q, lane);  // value index m of this lane's S^T row
+    // this lane's row of the held state: value index m of S^T (row < 0: none).
+    // MERGE (M = 128 layout): lanes 0..D-1 hold S^T; lanes D.. hold z, whose
+    // record slice starts right after the D x D part (row D); the copy takes
+    // ZR of them as its rows D..D+ZR-1
+    const int row = G::MERGE ? (q < 2 ? 32 * q + lane : -1) : state_row<D>(q, lane);
+    const int row_sum = G::MERGE && q >= 2 ? D : row;
+    const int row_copy = G::MERGE && q == 2 ? (lane < G::ZR ? D + lane : -1) : row;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -303,14 +332,15 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (c == 0) {
         // this segment's starting state: the sum of the earlier segments' records
         if (nrec > 0) griddep_wait();
-        sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row);
+        sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum);
       } else {
         // the state after chunk c - 1's update
         ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
       }
-      copy_state_to_smem<D>(lane_addr + G::COL_S, G::MERGE ? sm + s * G::STAGE + G::OFF_SB : sm + L::OFF_SBUF, row);
+      copy_state_to_smem<D>(lane_addr + G::COL_S, G::MERGE ? sm + s * G::STAGE + G::OFF_SB : sm + L::OFF_SBUF,
+                            row_copy);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
@@ -320,6 +350,21 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (ok) {
         tc_fence_after();
         store_state_transposed<D>(prm.S_final + (long long)bh * D * D, lane_addr, G::COL_S, row);
+        if (G::MERGE && q == 2) {
+          // z from the first z lane
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + G::COL_S + c0, v);
+            tmem_ld_wait();
+            if (lane == 0)
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(prm.z_final + (long long)bh * D + c0 + j) =
+                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                __uint_as_float(v[j + 3]));
+          }
+        }
       }
     }
   } else if (warp >= 8 && warp < 12) {
@@ -332,28 +377,38 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const int s = c % ST;
       const int pb = c % NPB, ob = c % NOB;
       const uint32_t pcol = G::pcol(pb), ocol = G::ocol(ob);
+      // (!MERGE: the phi(Q) tile is read below for phi(q) . z_prev)
       ok = mbar_wait(&p_full[pb], (c / NPB) & 1, abort_flag, kTimeoutNs) &&
-           mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+           (G::MERGE || mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs));
       if (!ok) break;
       tc_fence_after();
-      // masked P row in bf16, packed into the first 64 columns of its buffer,
-      // and its fp32 row sum. Warp q holds rows 32q..32q+31: 32-column pieces
-      // left of q are kept whole, piece q is masked per lane, pieces right of
-      // q are zero.
+      // masked P row in bf16, packed into the first 64 columns of its buffer
+      // (!MERGE: and its fp32 row sum; MERGE: P V sums the packed row).
+      // Warp q holds rows 32q..32q+31: 32-column pieces left of q are kept
+      // whole, piece q keeps columns <= lane, pieces right of q are zero.
       float rowsum = 0.f;
 #pragma unroll 1
       for (int p = 0; p < 4; ++p) {
         uint32_t pk[16];
-        if (p <= q) {
+        if (p < q) {
           uint32_t v[32];
           tmem_ld32(lane_addr + pcol + 32 * p, v);
           tmem_ld_wait();
-          const int lim = p < q ? 32 : (r - 32 * p + 1);  // columns kept in this piece
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a = (2 * j < lim) ? __uint_as_float(v[2 * j]) : 0.f;
-            const float b = (2 * j + 1 < lim) ? __uint_as_float(v[2 * j + 1]) : 0.f;
-            rowsum += a + b;
+            const float a = __uint_as_float(v[2 * j]), b = __uint_as_float(v[2 * j + 1]);
+            if (!G::MERGE) rowsum += a + b;
+            pk[j] = pack_bf16x2(a, b);
+          }
+        } else if (p == q) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + pcol + 32 * p, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a = (2 * j <= lane) ? __uint_as_float(v[2 * j]) : 0.f;
+            const float b = (2 * j + 1 <= lane) ? __uint_as_float(v[2 * j + 1]) : 0.f;
+            if (!G::MERGE) rowsum += a + b;
             pk[j] = pack_bf16x2(a, b);
           }
         } else {
@@ -362,9 +417,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         tmem_st16(lane_addr + pcol + 16 * p, pk);
       }
-      // phi(q_r) . z_prev from the phi-transformed Q tile (swizzled rows)
+      // !MERGE: phi(q_r) . z_prev from the phi-transformed Q tile (swizzled rows)
       float dot = 0.f;
-      {
+      if constexpr (!G::MERGE) {
         const uint8_t* qt = sm + s * G::STAGE;
         const float* zp = zst + s * D;
 #pragma unroll 1
@@ -385,7 +440,6 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             dot = fmaf(__uint_as_float(pw[3] & 0xFFFF0000u), z1.w, dot);
           }
       }
-      const float inv_den = 1.f / (rowsum + dot + prm.eps);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_ready[pb]);
@@ -393,6 +447,16 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       ok = mbar_wait(&o_full[ob], (c / NOB) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
+      float inv_den;
+      if constexpr (G::MERGE) {
+        // den = phi(q_r) . z_prev + the row sum of the packed P row
+        uint32_t dw;
+        tmem_ld1(lane_addr + ocol + D, dw);
+        tmem_ld_wait();
+        inv_den = 1.f / (__uint_as_float(dw) + prm.eps);
+      } else {
+        inv_den = 1.f / (rowsum + dot + prm.eps);
+      }
       // Stage the bf16 row in the chunk's Q tile region (swizzled rows); the
       // TMA producer stores the whole tile (rows past the end of the sequence
       // are clipped) before it refills the stage.
@@ -418,7 +482,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       mbar_arrive(&ost_full[s]);
     }
   } else {
-    // ---------------- group C: phi(K) and z ----------------
+    // ---------------- group C: phi(K) and (!MERGE) z ----------------
     using X = ExactLayout<D, 128>;
     const int t = tid;                      // 0..127
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
@@ -431,6 +495,13 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       float colsum[8];
+      if constexpr (G::MERGE) {
+        // z is summed by the state MMA
+        phi_tile_exact<D, 128, false, false>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
+        fence_proxy_async_smem();
+        mbar_arrive(&phi_done[s]);
+        continue;
+      }
       phi_tile_exact<D, 128>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
       fence_proxy_async_smem();
       if (c == 0) {
@@ -447,7 +518,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
       mbar_arrive(&phi_done[s]);
     }
-    if (ok && write_final && owner) {
+    if (!G::MERGE && ok && write_final && owner) {
       float4* zd = reinterpret_cast<float4*>(prm.z_final + (long long)bh * D + 8 * fc);
       zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
       zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);

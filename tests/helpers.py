@@ -13,10 +13,13 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}
 # bounded here at 1e-2. fp32 inputs keep fp32 phi throughout.
 STATE_TOL = {"f32": 1e-5, "bf16": 1e-2}
 
-# Normaliser tolerance (max abs error relative to max z). z sums N positive
-# terms phi(k) rounded to bf16 (nearest even, unbiased): the error grows like
-# sqrt(N) ulp against a sum that grows like N; 4e-5 observed at N = 32768.
-Z_TOL = {"f32": 1e-5, "bf16": 2e-4}
+# Normaliser tolerance (max abs error relative to max z). With bf16 inputs at
+# d = 64 the tensor cores sum z from the same bf16-rounded phi(k) that feed S
+# (so S and z weight every token alike): each term carries a relative error
+# of at most half a bf16 ulp, 2^-8, which is the bound at N = 1 (2.8e-3
+# observed); over N terms the unbiased rounding errors shrink like 1/sqrt(N).
+# Bounded like the state, at 1e-2.
+Z_TOL = {"f32": 1e-5, "bf16": 1e-2}
 
 
 def torch_dtype(name):
