@@ -350,12 +350,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 
 // [BH][N][D] bf16 viewed as a 3-D tensor; boxes of [C rows][64 features],
 // 128-byte swizzle, zero fill past the end of each sequence.
-cudaError_t make_map(CUtensorMap* m, const void* ptr, int BH, int N, int D) {
+// [BH][N][D] bf16 tensor, boxes of 64 features x `rows` tokens, 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* ptr, int BH, int N, int D, int rows = C) {
   auto enc = get_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

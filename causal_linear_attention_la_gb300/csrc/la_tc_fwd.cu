@@ -95,7 +95,11 @@ struct FwdSmem {
   // operands: rows D.. of V^T (so the state MMA also sums z) and columns D..
   // of [V | 1] (so P V also sums the rows of P)
   static constexpr int OFF_ONES = G::ST * G::STAGE;
-  static constexpr int OFF_SBUF = OFF_ONES + (G::MERGE ? BOX : 0);    // !MERGE: the S^T copy (1024-aligned)
+  // MERGE: two output tiles; each warp of group B stores its 32 rows with TMA,
+  // so a stage is free as soon as its chunk's MMAs are done (!MERGE: the
+  // output is staged in the chunk's Q tile and stored by the producer)
+  static constexpr int OFF_OUT = OFF_ONES + (G::MERGE ? BOX : 0);
+  static constexpr int OFF_SBUF = OFF_OUT + (G::MERGE ? 2 * G::TILE : 0);  // !MERGE: the S^T copy (1024-aligned)
   static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // !MERGE: [ST][D] fp32 z before each staged chunk
   static constexpr int OFF_BAR = OFF_ZST + (G::MERGE ? 0 : G::ST * D * 4);
   static constexpr int NBAR = 4 * G::ST + 2 * G::NPB + 2 * G::NOB + 3;
@@ -118,7 +122,7 @@ template <int D>
 __global__ void __launch_bounds__(448, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
-                  const FwdParams prm) {
+                  const __grid_constant__ CUtensorMap map_o32, const FwdParams prm) {
   using G = Cfg<D>;
   using L = FwdSmem<D>;
   constexpr int ST = G::ST, NPB = G::NPB, NOB = G::NOB;
@@ -201,7 +205,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      tma_prefetch_desc(&map_o);
+      if (!G::MERGE) tma_prefetch_desc(&map_o);
       // The output tile of a chunk is staged in its stage's Q region (dead
       // once the chunk's MMAs are done); this thread stores it with TMA and
       // waits until the store has read it before refilling the stage.
@@ -220,7 +224,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST;
         if (c >= ST) {
-          ok = mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs) && store_out(c - ST);
+          ok = mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs) && (G::MERGE || store_out(c - ST));
           if (!ok) break;
           stored = c - ST + 1;
         }
@@ -236,7 +240,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         issued = c + 1;
       }
       // the chunks still in the ring: their outputs
-      for (int c = stored; c < issued && ok; ++c) ok = store_out(c);
+      if (!G::MERGE)
+        for (int c = stored; c < issued && ok; ++c) ok = store_out(c);
       // every store must be complete, and every issued load must have landed,
       // before the CTA's shared memory is released
       tma_store_wait<0>();
@@ -457,10 +462,16 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       } else {
         inv_den = 1.f / (rowsum + dot + prm.eps);
       }
-      // Stage the bf16 row in the chunk's Q tile region (swizzled rows); the
-      // TMA producer stores the whole tile (rows past the end of the sequence
-      // are clipped) before it refills the stage.
-      uint8_t* ost = sm + s * G::STAGE;
+      // Stage the bf16 row (swizzled rows). !MERGE: in the chunk's Q tile
+      // region; the TMA producer stores the whole tile (rows past the end of
+      // the sequence are clipped) before it refills the stage. MERGE: in output
+      // tile ob; this warp stores its 32 rows itself once the store of chunk
+      // c - 2 has finished reading the tile.
+      uint8_t* ost = G::MERGE ? sm + L::OFF_OUT + ob * G::TILE : sm + s * G::STAGE;
+      if (G::MERGE && c >= 2) {
+        if (lane == 0) tma_store_wait_read<1>();
+        __syncwarp();
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
@@ -479,8 +490,21 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       tc_fence_before();
       mbar_arrive(&o_empty[ob]);
       fence_proxy_async_smem();
-      mbar_arrive(&ost_full[s]);
+      if constexpr (G::MERGE) {
+        __syncwarp();
+        if (lane == 0) {
+          // one bulk group per chunk (empty past the end of the sequence), so
+          // that waiting for all but the newest group frees tile ob
+          const int y = tok0 + c * C + 32 * q;
+          if (y < prm.N) tma_store_3d(&map_o32, ost + 32 * q * 128, 0, y, bh);
+          tma_store_commit();
+        }
+      } else {
+        mbar_arrive(&ost_full[s]);
+      }
     }
+    // every store must be complete before the CTA's shared memory is released
+    if (G::MERGE && lane == 0) tma_store_wait<0>();
   } else {
     // ---------------- group C: phi(K) and (!MERGE) z ----------------
     using X = ExactLayout<D, 128>;
@@ -993,11 +1017,12 @@ cudaError_t launch_noncausal(const FwdArgs& a) {
 template <int D>
 cudaError_t launch_forward(const FwdArgs& a) {
   if (!a.causal) return launch_noncausal<D>(a);
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mo32;
   cudaError_t e = make_map(&mq, a.q, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mk, a.k, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mo, a.out, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mo32, a.out, a.BH, a.N, D, 32);
   if (e != cudaSuccess) return e;
   constexpr int smem = FwdSmem<D>::BYTES;
   e = cudaFuncSetAttribute(tc_forward_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1016,7 +1041,7 @@ cudaError_t launch_forward(const FwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.plan.P > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D>, mq, mk, mv, mo, p);
+  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D>, mq, mk, mv, mo, mo32, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
