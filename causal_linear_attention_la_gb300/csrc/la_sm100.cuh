@@ -257,6 +257,11 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The descriptor of the same operand `bytes` further on: the start address
+// is the low 14-bit field (address / 16) and stays below 2^14 for any shared
+// memory address, so the offset adds without carry into the other fields.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                  // D: fp32

@@ -259,6 +259,20 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       constexpr uint32_t id_pv = make_idesc_bf16(128, G::MERGE ? D + G::ZR : D, false, true);
       const uint32_t sbuf_a = smem_u32(sm + L::OFF_SBUF);
       const uint32_t ones_a = smem_u32(sm + L::OFF_ONES);
+      // O += P V of chunk c once group B has packed its P; frees the stage
+      auto issue_pv = [&](int c) -> bool {
+        const int s = c % ST, pb = c % NPB, ob = c % NOB;
+        const uint32_t va = smem_u32(sm + s * G::STAGE) + G::OFF_V;
+        const uint64_t dv = make_sdesc(va, G::MERGE ? ones_a - va : (uint32_t)BOX, 1024, kSwizzle128B);
+        if (!mbar_wait(&p_ready[pb], (c / NPB) & 1, abort_flag, kTimeoutNs)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ts(tmem + G::ocol(ob), tmem + G::pcol(pb) + k * 8, sdesc_add(dv, k * 2048), id_pv, 1);
+        tc_commit(&o_full[ob]);
+        tc_commit(&empty[s]);
+        return true;
+      };
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST;
@@ -276,12 +290,23 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (ok && G::MERGE) ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        // operand descriptors of this stage; each k-step adds a constant
+        const uint64_t dq = make_sdesc(qa, 16, 1024, kSwizzle128B);
+        const uint64_t dk = make_sdesc(ka, 16, 1024, kSwizzle128B);
+        // V (MN-major, second 64-wide block at v_lbo) and phi(K) (MN-major)
+        const uint64_t dv = make_sdesc(va, v_lbo, 1024, kSwizzle128B);
+        const uint64_t dkm = make_sdesc(ka, BOX, 1024, kSwizzle128B);
+        auto issue_state = [&]() {
+#pragma unroll
+          for (int k = 0; k < C / 16; ++k)
+            mma_ss(tmem + G::COL_S, sdesc_add(dv, k * 2048), sdesc_add(dkm, k * 2048), id_vk, 1);
+          tc_commit(s_full);
+        };
         // P (and with MERGE, O = phiQ S_prev in the next D columns)
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
-          mma_ss(pc, make_sdesc(qa + off, 16, 1024, kSwizzle128B), make_sdesc(ka + off, 16, 1024, kSwizzle128B),
-                 id_qk, k > 0);
+          mma_ss(pc, sdesc_add(dq, off), sdesc_add(dk, off), id_qk, k > 0);
         }
         tc_commit(&p_full[pb]);
         if (!G::MERGE) {
@@ -289,27 +314,27 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           if (ok && c >= NOB) ok = mbar_wait(&o_empty[ob], ((c / NOB) - 1) & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
+          const uint64_t ds = make_sdesc(sbuf_a, 16, 1024, kSwizzle128B);
 #pragma unroll
           for (int k = 0; k < G::KSTEPS; ++k)
-            mma_ss(oc, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
-                   make_sdesc(sbuf_a + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qs, k > 0);
+            mma_ss(oc, sdesc_add(dq, (k >> 2) * BOX + (k & 3) * 32), sdesc_add(ds, (k >> 2) * (D * 128) + (k & 3) * 32),
+                   id_qs, k > 0);
         }
-        if (c < nupdates) {
-#pragma unroll
-          for (int k = 0; k < C / 16; ++k)
-            mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, v_lbo, 1024, kSwizzle128B),
-                   make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_vk, 1);
-          tc_commit(s_full);
+        // MERGE: P V lags one chunk and goes before this chunk's state
+        // update, so the tensor pipe runs it while group B packs P of this
+        // chunk, and its O buffer is released early.
+        // !MERGE: the state copy buffer is shared by all stages and may be
+        // refilled once s_full shows that every earlier MMA is done, so the
+        // update comes after this chunk's O MMA.
+        if (G::MERGE) {
+          if (c > 0) ok = issue_pv(c - 1);
+          if (ok && c < nupdates) issue_state();
+        } else {
+          if (c < nupdates) issue_state();
+          ok = issue_pv(c);
         }
-        ok = mbar_wait(&p_ready[pb], (c / NPB) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < C / 16; ++k)
-          mma_ts(oc, pc + k * 8, make_sdesc(va + k * 2048, v_lbo, 1024, kSwizzle128B), id_pv, 1);
-        tc_commit(&o_full[ob]);
-        tc_commit(&empty[s]);
       }
+      if (G::MERGE && ok && nchunks > 0) ok = issue_pv(nchunks - 1);
       // every MMA issued must have finished before tensor memory is released
       tc_commit(mma_fin);
       mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
@@ -377,21 +402,19 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int q = warp & 3;
     const int r = 32 * q + lane;            // chunk row (query token) of this thread
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    bool ok = true;
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int s = c % ST;
-      const int pb = c % NPB, ob = c % NOB;
-      const uint32_t pcol = G::pcol(pb), ocol = G::ocol(ob);
-      // (!MERGE: the phi(Q) tile is read below for phi(q) . z_prev)
-      ok = mbar_wait(&p_full[pb], (c / NPB) & 1, abort_flag, kTimeoutNs) &&
-           (G::MERGE || mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs));
-      if (!ok) break;
+    // Masked P row of chunk c in bf16, packed into the first 64 columns of its
+    // buffer (!MERGE: with its fp32 row sum; MERGE: P V sums the packed row).
+    // Warp q holds rows 32q..32q+31: 32-column pieces left of q are kept
+    // whole, piece q keeps columns <= lane, pieces right of q are zero.
+    // Returns with the packed row written (tmem_st_wait) but not yet published.
+    auto p_pass = [&](int c, float& rowsum) -> bool {
+      const int s = c % ST, pb = c % NPB;
+      const uint32_t pcol = G::pcol(pb);
+      // (!MERGE: the phi(Q) tile is read afterwards for phi(q) . z_prev)
+      if (!mbar_wait(&p_full[pb], (c / NPB) & 1, abort_flag, kTimeoutNs)) return false;
+      if (!G::MERGE && !mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs)) return false;
       tc_fence_after();
-      // masked P row in bf16, packed into the first 64 columns of its buffer
-      // (!MERGE: and its fp32 row sum; MERGE: P V sums the packed row).
-      // Warp q holds rows 32q..32q+31: 32-column pieces left of q are kept
-      // whole, piece q keeps columns <= lane, pieces right of q are zero.
-      float rowsum = 0.f;
+      rowsum = 0.f;
 #pragma unroll 1
       for (int p = 0; p < 4; ++p) {
         uint32_t pk[16];
@@ -422,61 +445,23 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         tmem_st16(lane_addr + pcol + 16 * p, pk);
       }
-      // !MERGE: phi(q_r) . z_prev from the phi-transformed Q tile (swizzled rows)
-      float dot = 0.f;
-      if constexpr (!G::MERGE) {
-        const uint8_t* qt = sm + s * G::STAGE;
-        const float* zp = zst + s * D;
-#pragma unroll 1
-        for (int b = 0; b < G::NB; ++b)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint4 w = *reinterpret_cast<const uint4*>(qt + b * BOX + sw128(r, ch));
-            const uint32_t* pw = reinterpret_cast<const uint32_t*>(&w);
-            const float4 z0 = *reinterpret_cast<const float4*>(zp + b * 64 + ch * 8);
-            const float4 z1 = *reinterpret_cast<const float4*>(zp + b * 64 + ch * 8 + 4);
-            dot = fmaf(__uint_as_float(pw[0] << 16), z0.x, dot);
-            dot = fmaf(__uint_as_float(pw[0] & 0xFFFF0000u), z0.y, dot);
-            dot = fmaf(__uint_as_float(pw[1] << 16), z0.z, dot);
-            dot = fmaf(__uint_as_float(pw[1] & 0xFFFF0000u), z0.w, dot);
-            dot = fmaf(__uint_as_float(pw[2] << 16), z1.x, dot);
-            dot = fmaf(__uint_as_float(pw[2] & 0xFFFF0000u), z1.y, dot);
-            dot = fmaf(__uint_as_float(pw[3] << 16), z1.z, dot);
-            dot = fmaf(__uint_as_float(pw[3] & 0xFFFF0000u), z1.w, dot);
-          }
-      }
       tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_ready[pb]);
-      // output rows
-      ok = mbar_wait(&o_full[ob], (c / NOB) & 1, abort_flag, kTimeoutNs);
-      if (!ok) break;
+      return true;
+    };
+    // Output rows of chunk c, scaled by inv_den (MERGE: read from the den
+    // column here), staged as swizzled bf16 rows. !MERGE: in the chunk's Q
+    // tile region; the TMA producer stores the whole tile (rows past the end
+    // of the sequence are clipped) before it refills the stage. MERGE: in
+    // output tile c % 2; this warp stores its 32 rows itself once the store of
+    // chunk c - 2 has finished reading the tile.
+    auto epilogue = [&](int c, float inv_den) -> bool {
+      const int s = c % ST, ob = c % NOB;
+      const uint32_t ocol = G::ocol(ob);
+      if (!mbar_wait(&o_full[ob], (c / NOB) & 1, abort_flag, kTimeoutNs)) return false;
       tc_fence_after();
-      float inv_den;
-      if constexpr (G::MERGE) {
-        // den = phi(q_r) . z_prev + the row sum of the packed P row
-        uint32_t dw;
-        tmem_ld1(lane_addr + ocol + D, dw);
-        tmem_ld_wait();
-        inv_den = 1.f / (__uint_as_float(dw) + prm.eps);
-      } else {
-        inv_den = 1.f / (rowsum + dot + prm.eps);
-      }
-      // Stage the bf16 row (swizzled rows). !MERGE: in the chunk's Q tile
-      // region; the TMA producer stores the whole tile (rows past the end of
-      // the sequence are clipped) before it refills the stage. MERGE: in output
-      // tile ob; this warp stores its 32 rows itself once the store of chunk
-      // c - 2 has finished reading the tile.
       uint8_t* ost = G::MERGE ? sm + L::OFF_OUT + ob * G::TILE : sm + s * G::STAGE;
-      if (G::MERGE && c >= 2) {
-        if (lane == 0) tma_store_wait_read<1>();
-        __syncwarp();
-      }
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + ocol + c0, v);
-        tmem_ld_wait();
+      // scale, pack and stage 32 columns of the row
+      auto put32 = [&](int c0, const uint32_t (&v)[32]) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint4 w;
@@ -486,9 +471,35 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv_den, __uint_as_float(v[8 * j + 7]) * inv_den);
           *reinterpret_cast<uint4*>(ost + (c0 / 64) * BOX + sw128(r, (c0 % 64) / 8 + j)) = w;
         }
+      };
+      if constexpr (G::MERGE) {
+        // the whole row and den = phi(q_r) . z_prev + the row sum of the
+        // packed P row, read at once, so the O buffer is released early
+        uint32_t v0[32], v1[32], dw;
+        tmem_ld32(lane_addr + ocol, v0);
+        tmem_ld32(lane_addr + ocol + 32, v1);
+        tmem_ld1(lane_addr + ocol + D, dw);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&o_empty[ob]);
+        inv_den = 1.f / (__uint_as_float(dw) + prm.eps);
+        if (c >= 2) {
+          if (lane == 0) tma_store_wait_read<1>();
+          __syncwarp();
+        }
+        put32(0, v0);
+        put32(32, v1);
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + ocol + c0, v);
+          tmem_ld_wait();
+          put32(c0, v);
+        }
+        tc_fence_before();
+        mbar_arrive(&o_empty[ob]);
       }
-      tc_fence_before();
-      mbar_arrive(&o_empty[ob]);
       fence_proxy_async_smem();
       if constexpr (G::MERGE) {
         __syncwarp();
@@ -501,6 +512,55 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
       } else {
         mbar_arrive(&ost_full[s]);
+      }
+      return true;
+    };
+    bool ok = true;
+    if constexpr (G::MERGE) {
+      // P V of chunk c is issued after the MMAs of chunk c + 1, so the P pass
+      // of chunk c + 1 comes before the epilogue of chunk c
+      for (int c = 0; c <= nchunks && ok; ++c) {
+        if (c < nchunks) {
+          float unused;
+          ok = p_pass(c, unused);
+          if (!ok) break;
+          tc_fence_before();
+          mbar_arrive(&p_ready[c % NPB]);
+        }
+        if (c >= 1) ok = epilogue(c - 1, 0.f);
+      }
+    } else {
+      for (int c = 0; c < nchunks && ok; ++c) {
+        float rowsum;
+        ok = p_pass(c, rowsum);
+        if (!ok) break;
+        // phi(q_r) . z_prev from the phi-transformed Q tile (swizzled rows)
+        float dot = 0.f;
+        {
+          const int s = c % ST;
+          const uint8_t* qt = sm + s * G::STAGE;
+          const float* zp = zst + s * D;
+#pragma unroll 1
+          for (int b = 0; b < G::NB; ++b)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 w = *reinterpret_cast<const uint4*>(qt + b * BOX + sw128(r, ch));
+              const uint32_t* pw = reinterpret_cast<const uint32_t*>(&w);
+              const float4 z0 = *reinterpret_cast<const float4*>(zp + b * 64 + ch * 8);
+              const float4 z1 = *reinterpret_cast<const float4*>(zp + b * 64 + ch * 8 + 4);
+              dot = fmaf(__uint_as_float(pw[0] << 16), z0.x, dot);
+              dot = fmaf(__uint_as_float(pw[0] & 0xFFFF0000u), z0.y, dot);
+              dot = fmaf(__uint_as_float(pw[1] << 16), z0.z, dot);
+              dot = fmaf(__uint_as_float(pw[1] & 0xFFFF0000u), z0.w, dot);
+              dot = fmaf(__uint_as_float(pw[2] << 16), z1.x, dot);
+              dot = fmaf(__uint_as_float(pw[2] & 0xFFFF0000u), z1.y, dot);
+              dot = fmaf(__uint_as_float(pw[3] << 16), z1.z, dot);
+              dot = fmaf(__uint_as_float(pw[3] & 0xFFFF0000u), z1.w, dot);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&p_ready[c % NPB]);
+        ok = epilogue(c, 1.f / (rowsum + dot + prm.eps));
       }
     }
     // every store must be complete before the CTA's shared memory is released
