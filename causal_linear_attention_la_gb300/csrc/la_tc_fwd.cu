@@ -229,8 +229,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           stored = c - ST + 1;
         }
         uint8_t* stg = sm + s * G::STAGE;
-        mbar_arrive_expect_tx(&full[s], 3 * G::TILE);
         const int y = tok0 + c * C;
+        mbar_arrive_expect_tx(&full[s], 3 * G::TILE);
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
           tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
@@ -296,11 +296,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // V (MN-major, second 64-wide block at v_lbo) and phi(K) (MN-major)
         const uint64_t dv = make_sdesc(va, v_lbo, 1024, kSwizzle128B);
         const uint64_t dkm = make_sdesc(ka, BOX, 1024, kSwizzle128B);
-        auto issue_state = [&]() {
+        auto issue_state = [&]() -> bool {
 #pragma unroll
           for (int k = 0; k < C / 16; ++k)
             mma_ss(tmem + G::COL_S, sdesc_add(dv, k * 2048), sdesc_add(dkm, k * 2048), id_vk, 1);
           tc_commit(s_full);
+          return true;
         };
         // P (and with MERGE, O = phiQ S_prev in the next D columns)
 #pragma unroll
@@ -328,10 +329,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // update comes after this chunk's O MMA.
         if (G::MERGE) {
           if (c > 0) ok = issue_pv(c - 1);
-          if (ok && c < nupdates) issue_state();
+          if (ok && c < nupdates) ok = issue_state();
         } else {
-          if (c < nupdates) issue_state();
-          ok = issue_pv(c);
+          if (c < nupdates) ok = issue_state();
+          if (ok) ok = issue_pv(c);
         }
       }
       if (G::MERGE && ok && nchunks > 0) ok = issue_pv(nchunks - 1);
@@ -629,7 +630,11 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 // ---------------------------------------------------------------------------
 template <int D>
 struct StateSmem {
-  static constexpr int OFF_BAR = Cfg<D>::ST_S * Cfg<D>::STAGE_S;
+  // D = 64: the state MMA runs with M = 128, A = [V^T ; 1] (ones tile as the
+  // second 64-wide block of A), so lanes 64.. of the accumulator hold dz
+  static constexpr bool ZMMA = D == 64;
+  static constexpr int OFF_ONES = Cfg<D>::ST_S * Cfg<D>::STAGE_S;
+  static constexpr int OFF_BAR = OFF_ONES + (ZMMA ? BOX : 0);
   static constexpr int NBAR = 3 * Cfg<D>::ST_S + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
@@ -688,6 +693,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (L::ZMMA) {
+    uint4* ones = reinterpret_cast<uint4*>(sm + L::OFF_ONES);
+    for (int i = tid; i < BOX / 16; i += blockDim.x) ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   if (warp == 9) {
     tmem_alloc(tmem_slot, G::TMEM_COLS_S);
     tmem_relinquish();
@@ -720,19 +730,22 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t id_vk = make_idesc_bf16(D, D, true, true);
+      // S^T += V^T phi(K); ZMMA: [S^T ; z] += [V^T ; 1] phi(K)
+      constexpr uint32_t id_vk = make_idesc_bf16(L::ZMMA ? 128 : D, D, true, true);
+      const uint32_t ones_a = smem_u32(sm + L::OFF_ONES);
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % ST;
         const uint32_t ka = smem_u32(sm + s * G::STAGE_S);
         const uint32_t va = ka + G::TILE;
+        const uint64_t dv = make_sdesc(va, L::ZMMA ? ones_a - va : (uint32_t)BOX, 1024, kSwizzle128B);
+        const uint64_t dk = make_sdesc(ka, BOX, 1024, kSwizzle128B);
         ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
-          mma_ss(tmem, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
-                 make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_vk, (c > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tmem, sdesc_add(dv, k * 2048), sdesc_add(dk, k * 2048), id_vk, (c > 0 || k > 0) ? 1u : 0u);
         tc_commit(&empty[s]);
       }
       tc_commit(s_full);
@@ -744,7 +757,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int t = tid;                      // 0..255
     const int q = warp & 3;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    const int row = state_row<D>(q, lane);
+    // row of S^T held by this lane (ZMMA: M = 128 layout, lanes 0..D-1)
+    const int row = L::ZMMA ? (q < 2 ? 32 * q + lane : -1) : state_row<D>(q, lane);
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     // per-thread partial column sums, reduced once after the last chunk
     float zrun[8];
@@ -756,13 +770,16 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       const int n_valid = min(C, tok_end - (tok0 + c * C));
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      phi_tile_exact<D, 256, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
+      if (L::ZMMA)
+        phi_tile_exact<D, 256, false, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
+      else
+        phi_tile_exact<D, 256, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
     }
     reduce_row_groups<D, 256>(zrun);
     float* dst = prm.ws_state + ((long long)bh * prm.P * prm.F + j) * (long long)(D * D + D);
-    if (ok && lane < X::FCW) {
+    if (!L::ZMMA && ok && lane < X::FCW) {
       float4* zd = reinterpret_cast<float4*>(dst + D * D + 8 * fc);
       zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
       zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
@@ -772,9 +789,24 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       tc_fence_after();
       if (nchunks > 0) {
         store_state_from_tmem<D>(dst, lane_addr, 0, row);
+        if (L::ZMMA && q == 2) {
+          // dz from the first z lane
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + c0, v);
+            tmem_ld_wait();
+            if (lane == 0)
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(dst + D * D + c0 + e) =
+                    make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                __uint_as_float(v[e + 3]));
+          }
+        }
       } else {
         // no MMA wrote the accumulator: the empty part's record is zero
-        for (int i = t; i < D * D; i += 128) dst[i] = 0.f;
+        for (int i = t; i < (L::ZMMA ? D * D + D : D * D); i += 128) dst[i] = 0.f;
       }
     }
   }
