@@ -84,15 +84,26 @@ __device__ __forceinline__ float mask_pack_row(uint32_t taddr, int q, int lane, 
         }
       }
       tmem_ld_wait();
-      const int lo = kLower ? 0 : (p == q ? lane : 0);       // kept columns [lo, hi)
-      const int hi = kLower ? (p == q ? lane + 1 : 32) : 32;
+      if (p != q) {
+        // a piece wholly on the kept side of the diagonal
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e0 = 2 * j, e1 = 2 * j + 1;
-        const float x0 = (e0 >= lo && e0 < hi) ? __uint_as_float(v[e0]) + add_row + cb[e0] : 0.f;
-        const float x1 = (e1 >= lo && e1 < hi) ? __uint_as_float(v[e1]) + add_row + cb[e1] : 0.f;
-        sum += x0 + x1;
-        pk[j] = pack_bf16x2(x0, x1);
+        for (int j = 0; j < 16; ++j) {
+          const float x0 = __uint_as_float(v[2 * j]) + add_row + cb[2 * j];
+          const float x1 = __uint_as_float(v[2 * j + 1]) + add_row + cb[2 * j + 1];
+          sum += x0 + x1;
+          pk[j] = pack_bf16x2(x0, x1);
+        }
+      } else {
+        const int lo = kLower ? 0 : lane;       // kept columns [lo, hi)
+        const int hi = kLower ? lane + 1 : 32;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int e0 = 2 * j, e1 = 2 * j + 1;
+          const float x0 = (e0 >= lo && e0 < hi) ? __uint_as_float(v[e0]) + add_row + cb[e0] : 0.f;
+          const float x1 = (e1 >= lo && e1 < hi) ? __uint_as_float(v[e1]) + add_row + cb[e1] : 0.f;
+          sum += x0 + x1;
+          pk[j] = pack_bf16x2(x0, x1);
+        }
       }
     } else {
 #pragma unroll
