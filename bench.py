@@ -12,7 +12,8 @@ call with pinned host buffers and the host<->device copies inside the timed
 region. The other workloads of the method are measured in the same run and
 reported under "sections": the causal forward B=2 H=16 N=32768 d=128, the
 decode step on B=64 x H=32 fp32 states of d=128 (1024 steps in a CUDA graph),
-and forward + backward B=4 H=8 N=8192 d=64.
+the same decode with 16 tokens per call (64 calls of la_decode_steps), and
+forward + backward B=4 H=8 N=8192 d=64.
 
 Timing: W eager warm-up steps, then the K timed steps are captured once in a
 CUDA graph and replayed, bracketed by CUDA events on the launching stream
@@ -54,6 +55,9 @@ WORKLOADS = {
     "decode_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                 prefill=dict(B=1, H=16, N=131072), steps=1024),
     "fwdbwd_b4_h8_n8192_d64": dict(kind="fwdbwd", B=4, H=8, N=8192, dk=64, dv=64, causal=True, seed=5),
+    # the same states, 16 tokens per call (la_decode_steps): 64 calls = 1024 tokens
+    "decode16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
+                                  prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16),
 }
 MAIN = "fwd_b4_h8_n4096_d64"
 EPS = 1e-6
@@ -320,17 +324,23 @@ def run_decode(w, K, W, barrier):
     S = Sp[0][src].reshape(B, H, dk, dv).contiguous()
     z = zp[0][src].reshape(B, H, dk).contiguous()
     T = w["steps"]
-    qs = (torch.randn((T, B, H, dk), generator=gen, device=dev) * dk ** -0.5).to(torch.bfloat16)
-    ks = (torch.randn((T, B, H, dk), generator=gen, device=dev) * dk ** -0.5).to(torch.bfloat16)
-    vs = (torch.randn((T, B, H, dv), generator=gen, device=dev) * dv ** -0.5).to(torch.bfloat16)
-    out = torch.empty((T, B, H, dv), dtype=torch.bfloat16, device=dev)
+    nt = w.get("tokens", 1)             # tokens per call
+    qs = (torch.randn((T, B, H, nt, dk), generator=gen, device=dev) * dk ** -0.5).to(torch.bfloat16)
+    ks = (torch.randn((T, B, H, nt, dk), generator=gen, device=dev) * dk ** -0.5).to(torch.bfloat16)
+    vs = (torch.randn((T, B, H, nt, dv), generator=gen, device=dev) * dv ** -0.5).to(torch.bfloat16)
+    out = torch.empty((T, B, H, nt, dv), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream()
 
     def step(i):
         sp = torch.cuda.current_stream().cuda_stream
-        st = la.la_decode_step(S.data_ptr(), z.data_ptr(), qs[i].data_ptr(), ks[i].data_ptr(),
-                               vs[i].data_ptr(), out[i].data_ptr(), B, H, dk, dv, EPS,
-                               la.LA_BF16, sp)
+        if nt == 1:
+            st = la.la_decode_step(S.data_ptr(), z.data_ptr(), qs[i].data_ptr(), ks[i].data_ptr(),
+                                   vs[i].data_ptr(), out[i].data_ptr(), B, H, dk, dv, EPS,
+                                   la.LA_BF16, sp)
+        else:
+            st = la.la_decode_steps(S.data_ptr(), z.data_ptr(), qs[i].data_ptr(), ks[i].data_ptr(),
+                                    vs[i].data_ptr(), out[i].data_ptr(), B, H, nt, dk, dv, EPS,
+                                    la.LA_BF16, sp)
         assert st == 0, la.lib().la_last_error()
 
     with torch.cuda.stream(stream):
@@ -532,14 +542,18 @@ def main():
             rr = run_decode(ws, K, W, barrier)
             t = max_over_ranks(rr["ms"]) / 1e3
             per = t / rr["steps"]
+            nt = ws.get("tokens", 1)
+            # bytes of one call: the state once, q, k, v, out once per token
+            call_bytes = decode_state_bytes(ws) + nt * decode_io_bytes(ws)
             gbs = decode_state_bytes(ws) / per / 1e9
             sections[name] = {
                 "value": gbs, "unit": "GB/s (S/z traffic)", "ms_per_step": 1e3 * per,
-                "steps": rr["steps"], "tokens_per_s": world * ws["B"] / per,
+                "steps": rr["steps"], "tokens_per_call": nt,
+                "tokens_per_s": world * ws["B"] * nt / per,
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"], "kernel": "decode",
                              "traffic": ncu_traffic("decode_" + name)},
-                "bytes_per_step": decode_state_bytes(ws) + decode_io_bytes(ws),
+                "bytes_per_step": call_bytes,
                 "prefill_s_eager": rr["prefill_s"], "gpu_launches": rr["launches"],
                 "l2": f"state {decode_state_bytes(ws) / 2 / 1e6:.0f} MB > L2",
             }

@@ -3,10 +3,10 @@
 The compute lives in ``lib/liblagb300.so`` (CUDA kernels for sm_103a); this
 module only marshals arguments. Two layers:
 
-* ``la_forward``, ``la_decode_step``, ``la_backward`` (and the workspace-size
+* ``la_forward``, ``la_decode_step``, ``la_decode_steps``, ``la_backward`` (and the workspace-size
   queries) mirror the C entry points of ``include/la.h`` one to one and take
   raw device pointers (ints) and sizes.
-* ``forward``, ``decode_step``, ``backward`` take torch CUDA tensors, allocate
+* ``forward``, ``decode_step``, ``decode_steps``, ``backward`` take torch CUDA tensors, allocate
   outputs and workspace with torch, and call the C entry points on the current
   torch stream.
 
@@ -25,12 +25,12 @@ from .build import LIBPATH
 __all__ = [
     "LA_OK", "LA_F32", "LA_BF16", "LA_PATH_AUTO", "LA_PATH_SIMT",
     "LaError", "LibraryNotBuilt", "lib", "exported_symbols",
-    "la_forward", "la_decode_step", "la_backward",
+    "la_forward", "la_decode_step", "la_decode_steps", "la_backward",
     "la_forward_workspace_size", "la_backward_workspace_size",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
-    "forward", "decode_step", "backward",
+    "forward", "decode_step", "decode_steps", "backward",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
@@ -43,7 +43,7 @@ SPAN_NAMES = ("fwd_state", "fwd_scan", "fwd_output", "decode", "bwd_state",
 # every entry point of include/la.h
 exported_symbols = (
     "la_status_string", "la_last_error", "la_version",
-    "la_forward_workspace_size", "la_forward", "la_decode_step",
+    "la_forward_workspace_size", "la_forward", "la_decode_step", "la_decode_steps",
     "la_backward_workspace_size", "la_backward",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
@@ -91,6 +91,8 @@ def lib():
                              + [_c_void, _c_void, _c_void, _c_size, _c_void])
     h.la_decode_step.restype = _c_int
     h.la_decode_step.argtypes = [_c_void] * 6 + [_c_int] * 4 + [_c_float, _c_int, _c_void]
+    h.la_decode_steps.restype = _c_int
+    h.la_decode_steps.argtypes = [_c_void] * 6 + [_c_int] * 5 + [_c_float, _c_int, _c_void]
     h.la_backward.restype = _c_int
     h.la_backward.argtypes = ([_c_void] * 7 + [_c_int] * 6 + [_c_float, _c_int]
                               + [_c_void, _c_size, _c_void])
@@ -152,6 +154,10 @@ def la_forward_noalloc(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype,
 
 def la_decode_step(S, z, q, k, v, out, B, H, dk, dv, eps, dtype, stream):
     return lib().la_decode_step(S, z, q, k, v, out, B, H, dk, dv, eps, dtype, stream)
+
+
+def la_decode_steps(S, z, q, k, v, out, B, H, T, dk, dv, eps, dtype, stream):
+    return lib().la_decode_steps(S, z, q, k, v, out, B, H, T, dk, dv, eps, dtype, stream)
 
 
 def la_backward(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps,
@@ -269,6 +275,25 @@ def decode_step(S, z, q, k, v, eps=1e-6, out=None):
     _check(la_decode_step(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
                           v.data_ptr(), out.data_ptr(), B, H, dk, dv, eps, code,
                           _stream_ptr(q)))
+    return out
+
+
+def decode_steps(S, z, q, k, v, eps=1e-6, out=None):
+    """T in-place recurrent steps on fp32 S [B,H,dk,dv], z [B,H,dk] with
+    q, k [B,H,T,dk], v [B,H,T,dv]; returns out [B,H,T,dv]."""
+    import torch
+    B, H, dk, dv = S.shape
+    T = q.shape[2]
+    code = _dtype_code(q)
+    _need(S, "S", torch.float32)
+    _need(z, "z", torch.float32)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype)
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    _check(la_decode_steps(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
+                           v.data_ptr(), out.data_ptr(), B, H, T, dk, dv, eps, code,
+                           _stream_ptr(q)))
     return out
 
 

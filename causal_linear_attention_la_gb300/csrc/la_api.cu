@@ -395,6 +395,31 @@ la_status la_decode_step(float* S, float* z, const void* q, const void* k,
   return LA_OK;
 }
 
+la_status la_decode_steps(float* S, float* z, const void* q, const void* k,
+                          const void* v, void* out, int B, int H, int T, int dk,
+                          int dv, float eps, la_dtype dtype, la_stream_t stream) {
+  if (T < 0) return fail(LA_ERR_INVALID_ARG, "T must be >= 0");
+  bool empty = false;
+  la_status st = check_sizes(B, H, T, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if (empty) return LA_OK;
+  if (!S || !z || !q || !k || !v || !out)
+    return fail(LA_ERR_INVALID_ARG, "S, z, q, k, v, out must be non-NULL");
+  if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
+      !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  DecodeArgs a{};
+  a.S = S; a.z = z; a.q = q; a.k = k; a.v = v; a.out = out;
+  a.BH = B * H; a.dk = dk; a.dv = dv; a.eps = eps; a.dtype = dtype;
+  a.stream = (cudaStream_t)stream;
+  a.ntok = T;
+  prof_begin(LA_SPAN_DECODE, a.stream);
+  cudaError_t e = la::decode_step(a);
+  prof_end(LA_SPAN_DECODE, a.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps");
+  return LA_OK;
+}
+
 la_status la_backward(const void* q, const void* k, const void* v,
                       const void* dout, void* dq, void* dk_, void* dv_, int B,
                       int H, int N, int dk, int dv, int causal, float eps,

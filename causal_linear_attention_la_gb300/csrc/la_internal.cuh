@@ -85,6 +85,7 @@ struct DecodeArgs {
   float* S; float* z; const void* q; const void* k; const void* v; void* out;
   int BH, dk, dv; float eps; la_dtype dtype;
   cudaStream_t stream;
+  int ntok = 1;     // tokens per (b,h) in this call (q, k, v, out hold ntok rows each)
 };
 
 // CUDA-core kernels (any supported head size, f32 or bf16)

@@ -135,6 +135,25 @@ LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k
                          la_stream_t stream);
 
 /*
+ * T consecutive decode steps per (batch, head) in one call: for t = 0 .. T-1,
+ * the step of la_decode_step with token t (same formulas, same inclusive read).
+ * The state is read and written once per call, not once per token, so its
+ * traffic is shared by the T tokens (multi-token decode: a prompt appended to
+ * a cached state, or several tokens verified at once; "Linear Attention: KV를
+ * 고정 크기 상태에 누적하기", section "상태 갱신과 읽기를 식으로 정리하기").
+ *
+ * S    [B,H,dk,dv] fp32 in/out      z [B,H,dk] fp32 in/out
+ * q, k [B,H,T,dk] dtype in          v [B,H,T,dv] dtype in
+ * out  [B,H,T,dv] dtype out
+ * T >= 0 (T = 0 leaves S and z unchanged). With T = 1 it equals
+ * la_decode_step; from a prefill of t tokens its outputs equal la_forward's
+ * outputs t .. t+T-1 on the appended tokens. Errors as la_decode_step.
+ */
+LA_API la_status la_decode_steps(float* S, float* z, const void* q, const void* k,
+                          const void* v, void* out, int B, int H, int T, int dk,
+                          int dv, float eps, la_dtype dtype, la_stream_t stream);
+
+/*
  * Bytes of scratch memory la_backward needs (0 if none): one fp32 state and
  * one fp32 reverse accumulator (dk*dv + dk each) per (batch, head, segment)
  * plus two fp32 scalars per token (the denominator and the normaliser's

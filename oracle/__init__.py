@@ -18,6 +18,7 @@ from .la_oracle import (  # noqa: F401
     forward_masked,
     forward_recurrent,
     decode_step,
+    decode_steps,
     output_at,
     backward_recurrent,
     backward_masked,

@@ -196,6 +196,24 @@ def decode_step(S, z, q, k, v, eps=1e-6, feature="elu1"):
     return S_new, z_new, num / den[..., None]
 
 
+def decode_steps(S, z, q, k, v, eps=1e-6, feature="elu1"):
+    """T consecutive recurrent steps on a given state, one per token.
+
+    The step of decode_step applied to tokens 0 .. T-1 in order (the
+    recurrence of [LA-state] section "상태 갱신과 읽기를 식으로 정리하기",
+    started from (S, z) instead of zero).
+    Shapes: S [..., dk, dv], z [..., dk], q,k [..., T, dk], v [..., T, dv].
+    Returns (S', z', out [..., T, dv]); the inputs are not modified.
+    """
+    S, z, q, k, v = _as64(S, z, q, k, v)
+    T = q.shape[-2]
+    out = np.zeros(q.shape[:-1] + (v.shape[-1],))
+    for t in range(T):
+        S, z, out[..., t, :] = decode_step(S, z, q[..., t, :], k[..., t, :], v[..., t, :],
+                                           eps=eps, feature=feature)
+    return S, z, out
+
+
 def output_at(q_bh, k_bh, v_bh, t, causal=True, eps=1e-6, feature="elu1"):
     """Output of one query position of one (batch, head), by the definition.
 

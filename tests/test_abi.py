@@ -115,6 +115,20 @@ def test_decode_and_backward_reject_bad_arguments(lib):
     assert la.la_backward(**{**b, "N": 0}) == la.LA_OK
 
 
+def test_decode_steps_validation(lib):
+    """Argument checks of la_decode_steps happen before any device work."""
+    d = dict(S=1024, z=1024, q=1024, k=1024, v=1024, out=1024, B=2, H=3, T=4,
+             dk=64, dv=64, eps=1e-6, dtype=la.LA_BF16, stream=None)
+    assert la.la_decode_steps(**{**d, "T": -1}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps(**{**d, "q": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps(**{**d, "S": 1032}) == la.LA_ERR_INVALID_ARG   # unaligned
+    assert la.la_decode_steps(**{**d, "dk": 48}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_decode_steps(**{**d, "eps": -1.0}) == la.LA_ERR_INVALID_ARG
+    # nothing to do: no device access
+    assert la.la_decode_steps(**{**d, "T": 0}) == la.LA_OK
+    assert la.la_decode_steps(**{**d, "B": 0}) == la.LA_OK
+
+
 def test_path_selection(lib):
     assert la.la_set_path(42) == -1
     prev = la.la_set_path(la.LA_PATH_SIMT)

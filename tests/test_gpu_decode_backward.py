@@ -45,6 +45,54 @@ def test_decode_steps(B, H, dk, dv, dtype):
         assert rel_err(to_host(z), z_ref, np.abs(z_ref).max()) <= 1e-6
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,T,dk,dv", [(1, 1, 2, 16, 16), (2, 3, 5, 32, 64),
+                                         (4, 2, 16, 128, 128), (3, 1, 33, 128, 16),
+                                         (2, 2, 7, 16, 128), (1, 2, 64, 64, 64),
+                                         (64, 32, 16, 128, 128)])
+def test_decode_tokens(B, H, T, dk, dv, dtype):
+    """T tokens per call (la_decode_steps) from a prefill state vs the oracle's
+    T single steps: outputs, and the state after the call."""
+    import torch
+    N0 = 24
+    q0, k0, v0 = synth.qkv(B, H, N0, dk, dv, seed=3 * dk + dv, dtype=dtype)
+    _, S_ref, z_ref = orc.forward_recurrent(q0, k0, v0, return_state=True)
+    S_ref, z_ref = S_ref.astype(np.float32), z_ref.astype(np.float32)
+    S = torch.from_numpy(S_ref).cuda()
+    z = torch.from_numpy(z_ref).cuda()
+    q, k, v = synth.qkv(B, H, T, dk, dv, seed=900 + T, dtype=dtype)
+    out = la.decode_steps(S, z, to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype))
+    torch.cuda.synchronize()
+    S_w, z_w, o_w = orc.decode_steps(S_ref, z_ref, q, k, v)
+    assert la.la_device_status(True) == la.LA_OK
+    err = rel_err(to_host(out), o_w, np.abs(v).max())
+    assert err <= TOL[dtype], err
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-6
+    assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= 1e-6
+
+
+def test_decode_tokens_edge_cases():
+    """T = 0 leaves the state untouched; T = 1 is la_decode_step bit for bit."""
+    import torch
+    B, H, dk, dv = 2, 3, 64, 32
+    S0 = torch.randn(B, H, dk, dv, device="cuda").abs()
+    z0 = torch.randn(B, H, dk, device="cuda").abs() + 1.0
+    S, z = S0.clone(), z0.clone()
+    e = torch.empty(B, H, 0, dk, device="cuda", dtype=torch.bfloat16)
+    out = la.decode_steps(S, z, e, e, torch.empty(B, H, 0, dv, device="cuda", dtype=torch.bfloat16))
+    torch.cuda.synchronize()
+    assert out.shape == (B, H, 0, dv)
+    assert torch.equal(S, S0) and torch.equal(z, z0)
+    q, k, v = synth.qkv(B, H, 1, dk, dv, seed=77, dtype="bf16")
+    S1, z1 = S0.clone(), z0.clone()
+    o1 = la.decode_steps(S1, z1, to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
+    S2, z2 = S0.clone(), z0.clone()
+    o2 = la.decode_step(S2, z2, to_dev(q[:, :, 0], "bf16"), to_dev(k[:, :, 0], "bf16"),
+                        to_dev(v[:, :, 0], "bf16"))
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, :, 0], o2) and torch.equal(S1, S2) and torch.equal(z1, z2)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_prefill_then_decode_matches_forward(dtype):
     import torch

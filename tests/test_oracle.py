@@ -252,6 +252,43 @@ def test_decode_two_steps_on_page_example():
     np.testing.assert_array_equal(outs[2], np.array(g["normaliser"]["y2"], float))
 
 
+def test_decode_steps_on_page_example():
+    """Three tokens in one multi-token call from the zero state reproduce the
+    worked example's S_3 (fig. 4) and its outputs (fig. 6: y_2 = [1.5, 0.5])."""
+    g = _load("la_state_three_tokens.json")
+    S, z, out = orc.decode_steps(np.zeros((2, 2)), np.zeros(2),
+                                 np.array(g["q"], float), np.array(g["k"], float),
+                                 np.array(g["v"], float), eps=0.0, feature="identity")
+    np.testing.assert_array_equal(S, np.array(g["states"]["S3"], float))
+    np.testing.assert_array_equal(z, np.array(g["normaliser"]["z3"], float))
+    np.testing.assert_array_equal(out[0], [2.0, 0.0])
+    np.testing.assert_array_equal(out[1], [0.0, 3.0])
+    np.testing.assert_array_equal(out[2], np.array(g["normaliser"]["y2"], float))
+
+
+def test_decode_steps_continue_prefill():
+    """From the state of a prefill of t tokens, T steps give the whole-sequence
+    outputs t .. t+T-1 and the state of the first t+T tokens; T = 0 changes
+    nothing."""
+    q, k, v = _rand(B=2, H=2, N=20, dk=4, dv=3, seed=12)
+    full, S_all, z_all = orc.forward_recurrent(q, k, v, return_state=True)
+    for t, T in ((0, 20), (5, 1), (7, 9), (19, 1)):
+        _, S, z = orc.forward_recurrent(q[:, :, :t], k[:, :, :t], v[:, :, :t],
+                                        return_state=True)
+        S2, z2, out = orc.decode_steps(S, z, q[:, :, t:t + T], k[:, :, t:t + T],
+                                       v[:, :, t:t + T])
+        np.testing.assert_allclose(out, full[:, :, t:t + T], rtol=1e-12, atol=1e-14)
+        _, S_ref, z_ref = orc.forward_recurrent(q[:, :, :t + T], k[:, :, :t + T],
+                                                v[:, :, :t + T], return_state=True)
+        np.testing.assert_allclose(S2, S_ref, rtol=1e-13)
+        np.testing.assert_allclose(z2, z_ref, rtol=1e-13)
+    S0, z0 = S_all.copy(), z_all.copy()
+    S1, z1, out = orc.decode_steps(S0, z0, q[:, :, :0], k[:, :, :0], v[:, :, :0])
+    assert out.shape == (2, 2, 0, 3)
+    np.testing.assert_array_equal(S1, S_all)
+    np.testing.assert_array_equal(z1, z_all)
+
+
 # ---------------------------------------------------------------------------
 # Backward: finite differences (brute force) and the two derivations
 # ---------------------------------------------------------------------------
