@@ -143,14 +143,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(loaded)}
 
 
+# source files of the kernels behind each measured span (the traffic lines in
+# profiles/ncu_dram_traffic.txt carry the digest of these files)
+_COMMON_TC = ["la_tc_common.cuh", "la_sm100.cuh", "la_internal.cuh"]
+KERNEL_SOURCES = {
+    "fwd_output": ["la_tc_fwd.cu"] + _COMMON_TC,
+    "bwd": ["la_tc_bwd.cu"] + _COMMON_TC,
+    "decode": ["la_decode.cu", "la_internal.cuh"],
+}
+
+
 def ncu_traffic(span):
     """DRAM bytes per launch of a kernel span from the committed ncu summary,
-    if it was taken on the library currently built (digest match), else None."""
-    import causal_linear_attention_la_gb300 as la
-    stamp = la.LIBPATH + ".sha256"
+    if it was taken on the kernel sources currently built (digest match), else None."""
+    from causal_linear_attention_la_gb300.build import kernel_digest
     path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
+    key = next((k for k in KERNEL_SOURCES if span.startswith(k + "_")), None)
+    if key is None:
+        return None
     try:
-        digest = open(stamp).read().strip()
+        digest = kernel_digest(KERNEL_SOURCES[key])
         for line in open(path):
             parts = line.split()
             if len(parts) >= 4 and not line.startswith("#") and parts[0] == span and parts[1] == digest[:16]:

@@ -56,6 +56,13 @@ def _digest(paths):
     return h.hexdigest()
 
 
+def kernel_digest(names):
+    """Digest of the named csrc files (kernel sources and the headers they
+    include) and the compile flags: identifies one kernel's build, so that a
+    measurement taken on it can be matched to the code that produced it."""
+    return _digest([os.path.join(CSRC, n) for n in sorted(names)])
+
+
 def _deps():
     hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     hdrs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]

@@ -3,7 +3,7 @@
     python -m causal_linear_attention_la_gb300.run_once --workload fwd --B 4 --H 8 --N 4096 --d 64 --calls 2
 
 Workloads: fwd (la_forward), bwd (la_forward then la_backward), decode
-(la_decode_step on zero-initialised states). Inputs are seeded normal
+(la_decode_step on zero-initialised states, or la_decode_steps with --tokens T). Inputs are seeded normal
 values scaled by 1/sqrt(d), bf16 unless --f32.
 """
 
@@ -23,6 +23,7 @@ def main(argv=None):
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--d", type=int, default=64)
     ap.add_argument("--calls", type=int, default=2)
+    ap.add_argument("--tokens", type=int, default=1, help="decode: tokens per call (la_decode_steps when > 1)")
     ap.add_argument("--noncausal", action="store_true")
     ap.add_argument("--f32", action="store_true")
     args = ap.parse_args(argv)
@@ -40,9 +41,15 @@ def main(argv=None):
     if args.workload == "decode":
         S = torch.zeros((B, H, d, d), device="cuda")
         z = torch.zeros((B, H, d), device="cuda")
-        q, k, v = rnd(B, H, d), rnd(B, H, d), rnd(B, H, d)
-        for _ in range(args.calls):
-            la.decode_step(S, z, q, k, v)
+        if args.tokens > 1:
+            T = args.tokens
+            q, k, v = rnd(B, H, T, d), rnd(B, H, T, d), rnd(B, H, T, d)
+            for _ in range(args.calls):
+                la.decode_steps(S, z, q, k, v)
+        else:
+            q, k, v = rnd(B, H, d), rnd(B, H, d), rnd(B, H, d)
+            for _ in range(args.calls):
+                la.decode_step(S, z, q, k, v)
     else:
         q, k, v = rnd(B, H, N, d), rnd(B, H, N, d), rnd(B, H, N, d)
         gout = rnd(B, H, N, d, scale=1.0)
