@@ -24,3 +24,9 @@ from .la_oracle import (  # noqa: F401
     backward_masked,
     loss_dot,
 )
+from .variants import (  # noqa: F401
+    decode_steps_decay,
+    decode_steps_delta,
+    impulse_response,
+    half_life,
+)
