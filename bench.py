@@ -12,8 +12,9 @@ call with pinned host buffers and the host<->device copies inside the timed
 region. The other workloads of the method are measured in the same run and
 reported under "sections": the causal forward B=2 H=16 N=32768 d=128, the
 decode step on B=64 x H=32 fp32 states of d=128 (1024 steps in a CUDA graph),
-the same decode with 16 tokens per call (64 calls of la_decode_steps), and
-forward + backward B=4 H=8 N=8192 d=64.
+the same decode with 16 tokens per call (64 calls of la_decode_steps), the
+decay-gated and delta-rule variants in the same shape, and forward + backward
+B=4 H=8 N=8192 d=64.
 
 Timing: W eager warm-up steps, then the K timed steps are captured once in a
 CUDA graph and replayed, bracketed by CUDA events on the launching stream
@@ -58,6 +59,13 @@ WORKLOADS = {
     # the same states, 16 tokens per call (la_decode_steps): 64 calls = 1024 tokens
     "decode16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                   prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16),
+    # the state-update variants on the same states, 16 tokens per call
+    "decay16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
+                                 prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16,
+                                 variant="decay"),
+    "delta16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
+                                 prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16,
+                                 variant="delta"),
 }
 MAIN = "fwd_b4_h8_n4096_d64"
 EPS = 1e-6
@@ -193,8 +201,9 @@ def bwd_bytes(w, elt=2):
 
 
 def decode_state_bytes(w):
-    """S and z read and written once per step, fp32."""
-    return w["B"] * w["H"] * (w["dk"] * w["dv"] + w["dk"]) * 4 * 2
+    """S and z read and written once per step (call), fp32; the delta rule keeps no z."""
+    zwords = 0 if w.get("variant") == "delta" else w["dk"]
+    return w["B"] * w["H"] * (w["dk"] * w["dv"] + zwords) * 4 * 2
 
 
 def decode_io_bytes(w, elt=2):
@@ -343,9 +352,23 @@ def run_decode(w, K, W, barrier):
     out = torch.empty((T, B, H, nt, dv), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream()
 
+    variant = w.get("variant")
+    alpha = torch.linspace(0.9, 0.999, H, device=dev)       # per-head decay factors
+    if variant == "delta":
+        # unit-norm keys: each write replaces what its key held
+        ks = ks / ks.float().norm(dim=-1, keepdim=True).to(ks.dtype)
+
     def step(i):
         sp = torch.cuda.current_stream().cuda_stream
-        if nt == 1:
+        if variant == "decay":
+            st = la.la_decode_steps_decay(S.data_ptr(), z.data_ptr(), qs[i].data_ptr(), ks[i].data_ptr(),
+                                          vs[i].data_ptr(), out[i].data_ptr(), B, H, nt, dk, dv,
+                                          alpha.data_ptr(), EPS, la.LA_BF16, sp)
+        elif variant == "delta":
+            st = la.la_decode_steps_delta(S.data_ptr(), qs[i].data_ptr(), ks[i].data_ptr(),
+                                          vs[i].data_ptr(), out[i].data_ptr(), B, H, nt, dk, dv,
+                                          la.LA_BF16, sp)
+        elif nt == 1:
             st = la.la_decode_step(S.data_ptr(), z.data_ptr(), qs[i].data_ptr(), ks[i].data_ptr(),
                                    vs[i].data_ptr(), out[i].data_ptr(), B, H, dk, dv, EPS,
                                    la.LA_BF16, sp)
@@ -563,7 +586,9 @@ def main():
                 "steps": rr["steps"], "tokens_per_call": nt,
                 "tokens_per_s": world * ws["B"] * nt / per,
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": gbs / peaks["hbm_gbs"], "kernel": "decode",
+                             "frac": gbs / peaks["hbm_gbs"],
+                             "kernel": {"decay": "decay_tokens", "delta": "delta_tokens"}.get(
+                                 ws.get("variant"), "decode"),
                              "traffic": ncu_traffic("decode_" + name)},
                 "bytes_per_step": call_bytes,
                 "prefill_s_eager": rr["prefill_s"], "gpu_launches": rr["launches"],

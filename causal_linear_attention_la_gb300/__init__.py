@@ -26,11 +26,13 @@ __all__ = [
     "LA_OK", "LA_F32", "LA_BF16", "LA_PATH_AUTO", "LA_PATH_SIMT",
     "LaError", "LibraryNotBuilt", "lib", "exported_symbols",
     "la_forward", "la_decode_step", "la_decode_steps", "la_backward",
+    "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy",
     "la_forward_workspace_size", "la_backward_workspace_size",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "forward", "decode_step", "decode_steps", "backward",
+    "decode_steps_decay", "decode_steps_delta", "state_copy",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
@@ -44,6 +46,7 @@ SPAN_NAMES = ("fwd_state", "fwd_scan", "fwd_output", "decode", "bwd_state",
 exported_symbols = (
     "la_status_string", "la_last_error", "la_version",
     "la_forward_workspace_size", "la_forward", "la_decode_step", "la_decode_steps",
+    "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy",
     "la_backward_workspace_size", "la_backward",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
@@ -93,6 +96,12 @@ def lib():
     h.la_decode_step.argtypes = [_c_void] * 6 + [_c_int] * 4 + [_c_float, _c_int, _c_void]
     h.la_decode_steps.restype = _c_int
     h.la_decode_steps.argtypes = [_c_void] * 6 + [_c_int] * 5 + [_c_float, _c_int, _c_void]
+    h.la_decode_steps_decay.restype = _c_int
+    h.la_decode_steps_decay.argtypes = [_c_void] * 6 + [_c_int] * 5 + [_c_void, _c_float, _c_int, _c_void]
+    h.la_decode_steps_delta.restype = _c_int
+    h.la_decode_steps_delta.argtypes = [_c_void] * 5 + [_c_int] * 6 + [_c_void]
+    h.la_state_copy.restype = _c_int
+    h.la_state_copy.argtypes = [_c_void] * 4 + [_c_int] * 4 + [_c_void]
     h.la_backward.restype = _c_int
     h.la_backward.argtypes = ([_c_void] * 7 + [_c_int] * 6 + [_c_float, _c_int]
                               + [_c_void, _c_size, _c_void])
@@ -158,6 +167,18 @@ def la_decode_step(S, z, q, k, v, out, B, H, dk, dv, eps, dtype, stream):
 
 def la_decode_steps(S, z, q, k, v, out, B, H, T, dk, dv, eps, dtype, stream):
     return lib().la_decode_steps(S, z, q, k, v, out, B, H, T, dk, dv, eps, dtype, stream)
+
+
+def la_decode_steps_decay(S, z, q, k, v, out, B, H, T, dk, dv, alpha, eps, dtype, stream):
+    return lib().la_decode_steps_decay(S, z, q, k, v, out, B, H, T, dk, dv, alpha, eps, dtype, stream)
+
+
+def la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream):
+    return lib().la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream)
+
+
+def la_state_copy(dst_S, dst_z, src_S, src_z, B, H, dk, dv, stream):
+    return lib().la_state_copy(dst_S, dst_z, src_S, src_z, B, H, dk, dv, stream)
 
 
 def la_backward(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps,
@@ -295,6 +316,53 @@ def decode_steps(S, z, q, k, v, eps=1e-6, out=None):
                            v.data_ptr(), out.data_ptr(), B, H, T, dk, dv, eps, code,
                            _stream_ptr(q)))
     return out
+
+
+def decode_steps_decay(S, z, q, k, v, alpha, eps=1e-6, out=None):
+    """decode_steps with the summary decayed by alpha [H] (fp32 CUDA) before each token."""
+    import torch
+    B, H, dk, dv = S.shape
+    T = q.shape[2]
+    code = _dtype_code(q)
+    _need(S, "S", torch.float32)
+    _need(z, "z", torch.float32)
+    _need(alpha, "alpha", torch.float32)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype)
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    _check(la_decode_steps_decay(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                 v.data_ptr(), out.data_ptr(), B, H, T, dk, dv,
+                                 alpha.data_ptr(), eps, code, _stream_ptr(q)))
+    return out
+
+
+def decode_steps_delta(S, q, k, v, out=None):
+    """T delta-rule steps in place on fp32 S [B,H,dk,dv]; returns out [B,H,T,dv]."""
+    import torch
+    B, H, dk, dv = S.shape
+    T = q.shape[2]
+    code = _dtype_code(q)
+    _need(S, "S", torch.float32)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype)
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    _check(la_decode_steps_delta(S.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                 out.data_ptr(), B, H, T, dk, dv, code, _stream_ptr(q)))
+    return out
+
+
+def state_copy(dst_S, src_S, dst_z=None, src_z=None):
+    """dst_S <- src_S and dst_z <- src_z (snapshot or restore of a state)."""
+    import torch
+    B, H, dk, dv = src_S.shape
+    for t, n in ((dst_S, "dst_S"), (src_S, "src_S")):
+        _need(t, n, torch.float32)
+    _check(la_state_copy(dst_S.data_ptr(), dst_z.data_ptr() if dst_z is not None else None,
+                         src_S.data_ptr(), src_z.data_ptr() if src_z is not None else None,
+                         B, H, dk, dv, _stream_ptr(src_S)))
+    return dst_S
 
 
 def backward(q, k, v, dout, causal=True, eps=1e-6, workspace=None):

@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "la_internal.cuh"
+#include "la_variants.cuh"
 
 namespace la {
 
@@ -417,6 +418,67 @@ la_status la_decode_steps(float* S, float* z, const void* q, const void* k,
   cudaError_t e = la::decode_step(a);
   prof_end(LA_SPAN_DECODE, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps");
+  return LA_OK;
+}
+
+la_status la_decode_steps_decay(float* S, float* z, const void* q, const void* k,
+                                const void* v, void* out, int B, int H, int T, int dk,
+                                int dv, const float* alpha, float eps, la_dtype dtype,
+                                la_stream_t stream) {
+  if (T < 0) return fail(LA_ERR_INVALID_ARG, "T must be >= 0");
+  bool empty = false;
+  la_status st = check_sizes(B, H, T, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if (empty) return LA_OK;
+  if (!S || !z || !q || !k || !v || !out || !alpha)
+    return fail(LA_ERR_INVALID_ARG, "S, z, q, k, v, out, alpha must be non-NULL");
+  if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
+      !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "S, z, q, k, v, out must be 16-byte aligned");
+  VariantArgs a{};
+  a.S = S; a.z = z; a.q = q; a.k = k; a.v = v; a.out = out; a.alpha = alpha;
+  a.H = H; a.BH = B * H; a.ntok = T; a.dk = dk; a.dv = dv; a.eps = eps; a.dtype = dtype;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = la::decode_steps_decay(a);
+  if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps_decay");
+  return LA_OK;
+}
+
+la_status la_decode_steps_delta(float* S, const void* q, const void* k, const void* v,
+                                void* out, int B, int H, int T, int dk, int dv,
+                                la_dtype dtype, la_stream_t stream) {
+  if (T < 0) return fail(LA_ERR_INVALID_ARG, "T must be >= 0");
+  bool empty = false;
+  la_status st = check_sizes(B, H, T, dk, dv, dtype, 0.f, &empty);
+  if (st != LA_OK) return st;
+  if (empty) return LA_OK;
+  if (!S || !q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "S, q, k, v, out must be non-NULL");
+  if (!aligned16(S) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  VariantArgs a{};
+  a.S = S; a.q = q; a.k = k; a.v = v; a.out = out;
+  a.H = H; a.BH = B * H; a.ntok = T; a.dk = dk; a.dv = dv; a.dtype = dtype;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = la::decode_steps_delta(a);
+  if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps_delta");
+  return LA_OK;
+}
+
+la_status la_state_copy(float* dst_S, float* dst_z, const float* src_S, const float* src_z,
+                        int B, int H, int dk, int dv, la_stream_t stream) {
+  bool empty = false;
+  la_status st = check_sizes(B, H, 1, dk, dv, LA_F32, 0.f, &empty);
+  if (st != LA_OK) return st;
+  if ((dst_z == nullptr) != (src_z == nullptr))
+    return fail(LA_ERR_INVALID_ARG, "dst_z and src_z must be both given or both NULL");
+  if (empty) return LA_OK;
+  if (!dst_S || !src_S) return fail(LA_ERR_INVALID_ARG, "dst_S and src_S must be non-NULL");
+  if (!aligned16(dst_S) || !aligned16(src_S) || !aligned16(dst_z) || !aligned16(src_z))
+    return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  const long long BH = (long long)B * H;
+  cudaError_t e = la::copy_floats(dst_S, src_S, BH * dk * dv, (cudaStream_t)stream);
+  if (e == cudaSuccess && dst_z) e = la::copy_floats(dst_z, src_z, BH * dk, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "la_state_copy");
   return LA_OK;
 }
 

@@ -1,0 +1,24 @@
+// Declarations of the state-update variants (decay gating, delta rule) and the
+// state copy; host launchers defined in la_variants.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "la.h"
+
+namespace la {
+
+struct VariantArgs {
+  float* S; float* z;                 // state (z unused by the delta rule)
+  const void* q; const void* k; const void* v; void* out;
+  const float* alpha;                 // decay: [H] per-head factors (device)
+  int H, BH, ntok, dk, dv; float eps; la_dtype dtype;
+  cudaStream_t stream;
+};
+
+cudaError_t decode_steps_decay(const VariantArgs& a);
+cudaError_t decode_steps_delta(const VariantArgs& a);
+// dst <- src for n floats (16-byte aligned pointers)
+cudaError_t copy_floats(float* dst, const float* src, long long n, cudaStream_t stream);
+
+}  // namespace la

@@ -154,6 +154,51 @@ LA_API la_status la_decode_steps(float* S, float* z, const void* q, const void* 
                           int dv, float eps, la_dtype dtype, la_stream_t stream);
 
 /*
+ * Decay-gated decode: T steps per (batch, head) in one call, the whole summary
+ * multiplied by a per-head factor alpha before each token is added ("Linear
+ * Attention, 곱의 순서를 바꾸면 생기는 일", the paragraph on 감쇠 게이팅; the
+ * recurrence h_t = a h_{t-1} + x_t of "상태공간모델·선형 어텐션", section 3):
+ *
+ *   S <- alpha S + phi(k) v^T;  z <- alpha z + phi(k);
+ *   out = phi(q)^T S / (phi(q)^T z + eps)
+ *
+ * alpha [H] fp32 device memory, one factor per head (alpha = 1 gives
+ * la_decode_steps; values above 1 make the state grow without bound and are
+ * not checked). Other arguments and errors as la_decode_steps.
+ */
+LA_API la_status la_decode_steps_decay(float* S, float* z, const void* q, const void* k,
+                                const void* v, void* out, int B, int H, int T, int dk,
+                                int dv, const float* alpha, float eps, la_dtype dtype,
+                                la_stream_t stream);
+
+/*
+ * Delta-rule decode: T steps per (batch, head) in one call; each step reads
+ * the state with the key and adds only the difference to the value (the
+ * paragraph on 델타 규칙 of the same page):
+ *
+ *   u = S^T k;  S <- S + k (v - u)^T;  out = S^T q
+ *
+ * q and k are used as given (no feature map) and the read is not normalised,
+ * as in the page's example; with unit-norm keys a write replaces what the key
+ * held. S [B,H,dk,dv] fp32 in/out; q, k [B,H,T,dk], v [B,H,T,dv] in, out
+ * [B,H,T,dv] out, dtype. Errors as la_decode_steps.
+ */
+LA_API la_status la_decode_steps_delta(float* S, const void* q, const void* k, const void* v,
+                                void* out, int B, int H, int T, int dk, int dv,
+                                la_dtype dtype, la_stream_t stream);
+
+/*
+ * State snapshot / restore: dst_S <- src_S ([B,H,dk,dv] fp32) and, if both
+ * are given, dst_z <- src_z ([B,H,dk] fp32), on `stream`. The same call saves
+ * a state (prefix caching) and puts it back; a later step from the restored
+ * state repeats the original bit for bit. Pointers 16-byte aligned, device
+ * memory, not overlapping; dst_z and src_z both NULL or both non-NULL.
+ */
+LA_API la_status la_state_copy(float* dst_S, float* dst_z, const float* src_S,
+                        const float* src_z, int B, int H, int dk, int dv,
+                        la_stream_t stream);
+
+/*
  * Bytes of scratch memory la_backward needs (0 if none): one fp32 state and
  * one fp32 reverse accumulator (dk*dv + dk each) per (batch, head, segment)
  * plus two fp32 scalars per token (the denominator and the normaliser's

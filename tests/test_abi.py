@@ -129,6 +129,28 @@ def test_decode_steps_validation(lib):
     assert la.la_decode_steps(**{**d, "B": 0}) == la.LA_OK
 
 
+def test_variant_validation(lib):
+    """Argument checks of the variant entry points happen before any device work."""
+    d = dict(S=1024, z=1024, q=1024, k=1024, v=1024, out=1024, B=2, H=3, T=4,
+             dk=64, dv=64, alpha=2048, eps=1e-6, dtype=la.LA_BF16, stream=None)
+    assert la.la_decode_steps_decay(**{**d, "T": -1}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps_decay(**{**d, "alpha": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps_decay(**{**d, "z": 1028}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps_decay(**{**d, "dv": 24}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_decode_steps_decay(**{**d, "T": 0}) == la.LA_OK
+    e = dict(S=1024, q=1024, k=1024, v=1024, out=1024, B=2, H=3, T=4, dk=64, dv=64,
+             dtype=la.LA_F32, stream=None)
+    assert la.la_decode_steps_delta(**{**e, "T": -2}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps_delta(**{**e, "k": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_decode_steps_delta(**{**e, "dtype": 7}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_decode_steps_delta(**{**e, "H": 0}) == la.LA_OK
+    c = dict(dst_S=1024, dst_z=2048, src_S=4096, src_z=8192, B=2, H=3, dk=64, dv=64, stream=None)
+    assert la.la_state_copy(**{**c, "dst_z": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_state_copy(**{**c, "src_S": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_state_copy(**{**c, "dst_S": 1030}) == la.LA_ERR_INVALID_ARG
+    assert la.la_state_copy(**{**c, "B": 0}) == la.LA_OK
+
+
 def test_path_selection(lib):
     assert la.la_set_path(42) == -1
     prev = la.la_set_path(la.LA_PATH_SIMT)

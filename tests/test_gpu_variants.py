@@ -1,0 +1,141 @@
+"""Decay-gated and delta-rule decode, and the state copy: CUDA path (through the
+C ABI) vs the fp64 oracle."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as orc
+import causal_linear_attention_la_gb300 as la
+from causal_linear_attention_la_gb300 import synth
+from helpers import TOL, build_lib, rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build_lib()
+    la.lib()
+    yield
+
+
+def _prefill_state(B, H, dk, dv, dtype, seed):
+    q0, k0, v0 = synth.qkv(B, H, 24, dk, dv, seed=seed, dtype=dtype)
+    _, S, z = orc.forward_recurrent(q0, k0, v0, return_state=True)
+    return S.astype(np.float32), z.astype(np.float32)
+
+
+SHAPES = [(1, 1, 3, 16, 16), (2, 3, 5, 32, 64), (2, 2, 16, 128, 128), (3, 1, 33, 128, 16),
+          (2, 2, 7, 16, 128), (64, 32, 16, 128, 128)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,T,dk,dv", SHAPES)
+def test_decay_tokens(B, H, T, dk, dv, dtype):
+    import torch
+    S_ref, z_ref = _prefill_state(B, H, dk, dv, dtype, seed=5 * dk + dv)
+    alpha_h = np.random.default_rng(T + H).uniform(0.5, 1.0, H).astype(np.float32)
+    S = torch.from_numpy(S_ref).cuda()
+    z = torch.from_numpy(z_ref).cuda()
+    q, k, v = synth.qkv(B, H, T, dk, dv, seed=700 + T, dtype=dtype)
+    out = la.decode_steps_decay(S, z, to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype),
+                                torch.from_numpy(alpha_h).cuda())
+    torch.cuda.synchronize()
+    S_w, z_w, o_w = orc.decode_steps_decay(S_ref, z_ref, q, k, v,
+                                           alpha=alpha_h.astype(np.float64)[None, :])
+    assert rel_err(to_host(out), o_w, np.abs(v).max()) <= TOL[dtype]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-6
+    assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= 1e-6
+
+
+def test_decay_one_matches_plain_decode():
+    import torch
+    B, H, T, dk, dv = 2, 4, 20, 64, 64
+    S_ref, z_ref = _prefill_state(B, H, dk, dv, "bf16", seed=8)
+    q, k, v = [to_dev(x, "bf16") for x in synth.qkv(B, H, T, dk, dv, seed=9, dtype="bf16")]
+    S1, z1 = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+    S2, z2 = S1.clone(), z1.clone()
+    o1 = la.decode_steps_decay(S1, z1, q, k, v, torch.ones(H, device="cuda"))
+    o2 = la.decode_steps(S2, z2, q, k, v)
+    torch.cuda.synchronize()
+    assert rel_err(to_host(o1), to_host(o2), 1.0) <= 1e-6
+    assert rel_err(to_host(S1), to_host(S2), float(S2.abs().max())) <= 1e-6
+
+
+def test_delta_rule_page_example_on_gpu():
+    """The worked example, embedded in dk = dv = 16 (zeros elsewhere):
+    (5, 3) then key (0.6, 0.8) with value 10 -> (7.76, 6.68); reads 10 and 7.76."""
+    import torch
+    with open(os.path.join(GOLDEN, "la_order_delta_rule.json")) as f:
+        g = json.load(f)
+    S = torch.zeros(1, 1, 16, 16, device="cuda")
+    keys = g["k"] + [g["write"]["k"]]
+    vals = [x[0] for x in g["v"]] + [g["write"]["v"][0]]
+    k = torch.zeros(1, 1, 3, 16, device="cuda")
+    v = torch.zeros(1, 1, 3, 16, device="cuda")
+    q = torch.zeros(1, 1, 3, 16, device="cuda")
+    for t in range(3):
+        k[0, 0, t, :2] = torch.tensor(keys[t])
+        v[0, 0, t, 0] = vals[t]
+        q[0, 0, t, :2] = torch.tensor(g["reads_after"]["queries"][0])
+    out = la.decode_steps_delta(S, q, k, v)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to_host(S)[0, 0, :2, 0], g["S_after"], rtol=0, atol=1e-5)
+    assert abs(float(out[0, 0, 2, 0]) - g["reads_after"]["values"][0]) <= 1e-5
+    q1 = torch.zeros(1, 1, 1, 16, device="cuda")
+    q1[0, 0, 0, 0] = 1.0
+    o1 = la.decode_steps_delta(S, q1, torch.zeros_like(q1), torch.zeros(1, 1, 1, 16, device="cuda"))
+    torch.cuda.synchronize()
+    assert abs(float(o1[0, 0, 0, 0]) - g["reads_after"]["values"][1]) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,T,dk,dv", SHAPES)
+def test_delta_tokens(B, H, T, dk, dv, dtype):
+    """Random unit-norm keys (rounded to the input dtype) on a random state."""
+    import torch
+    rng = np.random.default_rng(dk * 7 + dv + T)
+    S0 = rng.standard_normal((B, H, dk, dv)).astype(np.float32)
+    q, k, v = synth.qkv(B, H, T, dk, dv, seed=300 + T, dtype=dtype)
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    q = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    qd, kd, vd = to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype)
+    q, k = to_host(qd), to_host(kd)            # the values the kernel sees
+    S = torch.from_numpy(S0).cuda()
+    out = la.decode_steps_delta(S, qd, kd, vd)
+    torch.cuda.synchronize()
+    S_w, o_w = orc.decode_steps_delta(S0, q, k, v)
+    scale = max(np.abs(o_w).max(), np.abs(v).max())
+    assert rel_err(to_host(out), o_w, scale) <= TOL[dtype]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+
+
+def test_state_snapshot_restore_round_trip():
+    """Save a state, step it, put the copy back and repeat the same steps: the
+    outputs and states repeat bit for bit; without z only S is copied."""
+    import torch
+    B, H, T, dk, dv = 4, 8, 9, 128, 64
+    S_ref, z_ref = _prefill_state(B, H, dk, dv, "bf16", seed=12)
+    S, z = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+    snapS, snapz = torch.empty_like(S), torch.empty_like(z)
+    la.state_copy(snapS, S, snapz, z)
+    q, k, v = [to_dev(x, "bf16") for x in synth.qkv(B, H, T, dk, dv, seed=13, dtype="bf16")]
+    o1 = la.decode_steps(S, z, q, k, v)
+    S1, z1 = S.clone(), z.clone()
+    la.state_copy(S, snapS, z, snapz)
+    torch.cuda.synchronize()
+    assert torch.equal(S, torch.from_numpy(S_ref).cuda()) and torch.equal(z, torch.from_numpy(z_ref).cuda())
+    o2 = la.decode_steps(S, z, q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(S, S1) and torch.equal(z, z1)
+    only = torch.zeros_like(S)
+    la.state_copy(only, S)
+    torch.cuda.synchronize()
+    assert torch.equal(only, S)
