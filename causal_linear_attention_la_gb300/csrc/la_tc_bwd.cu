@@ -509,13 +509,16 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST, pb = c & 1;
-      ok = mbar_wait(&p_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs) &&
-           mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      // phi(q_r) . z_prev needs only the phi tiles: formed while the MMAs of
+      // the chunk run, before P is ready
+      ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      const float qz = phiq_dot<D>(sm + s * G::STAGE, r, zst + s * D);
+      ok = mbar_wait(&p_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
       const float rowsum = mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, 0.f, nullptr);
-      const uint8_t* qt = sm + s * G::STAGE;
-      const float den = rowsum + phiq_dot<D>(qt, r, zst + s * D) + prm.eps;
+      const float den = rowsum + qz + prm.eps;
       const float inv_den = 1.f / den;
       tmem_st_wait();
       tc_fence_before();
