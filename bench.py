@@ -13,8 +13,8 @@ region. The other workloads of the method are measured in the same run and
 reported under "sections": the causal forward B=2 H=16 N=32768 d=128, the
 decode step on B=64 x H=32 fp32 states of d=128 (1024 steps in a CUDA graph),
 the same decode with 16 tokens per call (64 calls of la_decode_steps), the
-decay-gated and delta-rule variants in the same shape, and forward + backward
-B=4 H=8 N=8192 d=64.
+decay-gated and delta-rule variants in the same shape, forward + backward
+B=4 H=8 N=8192 d=64, and the decay-gated forward in the headline shape.
 
 Timing: W eager warm-up steps, then the K timed steps are captured once in a
 CUDA graph and replayed, bracketed by CUDA events on the launching stream
@@ -56,6 +56,9 @@ WORKLOADS = {
     "decode_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                 prefill=dict(B=1, H=16, N=131072), steps=1024),
     "fwdbwd_b4_h8_n8192_d64": dict(kind="fwdbwd", B=4, H=8, N=8192, dk=64, dv=64, causal=True, seed=5),
+    # decay-gated forward (per-head factors 0.9 .. 0.999), the headline shape
+    "fwd_decay_b4_h8_n4096_d64": dict(kind="forward", B=4, H=8, N=4096, dk=64, dv=64, causal=True, seed=2,
+                                      decay=True),
     # the same states, 16 tokens per call (la_decode_steps): 64 calls = 1024 tokens
     "decode16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                   prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16),
@@ -290,13 +293,19 @@ def run_forward(w, K, W, barrier, with_bwd=False):
     ws_b = la.la_backward_workspace_size(B, H, N, dk, dv, w["causal"], code) if with_bwd else 0
     ws = torch.empty(max(ws_f, ws_b, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream()
+    alpha = torch.linspace(0.9, 0.999, H, device=dev)       # decay: per-head factors
 
     def step(i):
         s = sets[i % R]
         sp = torch.cuda.current_stream().cuda_stream
-        st = la.la_forward(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(),
-                           s["out"].data_ptr(), B, H, N, dk, dv, w["causal"], EPS, code,
-                           None, None, ws.data_ptr(), ws.numel(), sp)
+        if w.get("decay"):
+            st = la.la_forward_decay(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(),
+                                     s["out"].data_ptr(), B, H, N, dk, dv, alpha.data_ptr(), EPS, code,
+                                     None, None, ws.data_ptr(), ws.numel(), sp)
+        else:
+            st = la.la_forward(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(),
+                               s["out"].data_ptr(), B, H, N, dk, dv, w["causal"], EPS, code,
+                               None, None, ws.data_ptr(), ws.numel(), sp)
         assert st == 0, la.lib().la_last_error()
         if with_bwd:
             st = la.la_backward(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(),

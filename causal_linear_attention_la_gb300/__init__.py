@@ -26,13 +26,13 @@ __all__ = [
     "LA_OK", "LA_F32", "LA_BF16", "LA_PATH_AUTO", "LA_PATH_SIMT",
     "LaError", "LibraryNotBuilt", "lib", "exported_symbols",
     "la_forward", "la_decode_step", "la_decode_steps", "la_backward",
-    "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy",
+    "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy", "la_forward_decay",
     "la_forward_workspace_size", "la_backward_workspace_size",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "forward", "decode_step", "decode_steps", "backward",
-    "decode_steps_decay", "decode_steps_delta", "state_copy",
+    "decode_steps_decay", "decode_steps_delta", "state_copy", "forward_decay",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
@@ -46,7 +46,7 @@ SPAN_NAMES = ("fwd_state", "fwd_scan", "fwd_output", "decode", "bwd_state",
 exported_symbols = (
     "la_status_string", "la_last_error", "la_version",
     "la_forward_workspace_size", "la_forward", "la_decode_step", "la_decode_steps",
-    "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy",
+    "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy", "la_forward_decay",
     "la_backward_workspace_size", "la_backward",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
@@ -100,6 +100,9 @@ def lib():
     h.la_decode_steps_decay.argtypes = [_c_void] * 6 + [_c_int] * 5 + [_c_void, _c_float, _c_int, _c_void]
     h.la_decode_steps_delta.restype = _c_int
     h.la_decode_steps_delta.argtypes = [_c_void] * 5 + [_c_int] * 6 + [_c_void]
+    h.la_forward_decay.restype = _c_int
+    h.la_forward_decay.argtypes = [_c_void] * 4 + [_c_int] * 5 + [_c_void, _c_float, _c_int] + \
+        [_c_void] * 3 + [ctypes.c_size_t, _c_void]
     h.la_state_copy.restype = _c_int
     h.la_state_copy.argtypes = [_c_void] * 4 + [_c_int] * 4 + [_c_void]
     h.la_backward.restype = _c_int
@@ -175,6 +178,12 @@ def la_decode_steps_decay(S, z, q, k, v, out, B, H, T, dk, dv, alpha, eps, dtype
 
 def la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream):
     return lib().la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream)
+
+
+def la_forward_decay(q, k, v, out, B, H, N, dk, dv, alpha, eps, dtype, S_final, z_final,
+                     workspace, workspace_bytes, stream):
+    return lib().la_forward_decay(q, k, v, out, B, H, N, dk, dv, alpha, eps, dtype, S_final,
+                                  z_final, workspace, workspace_bytes, stream)
 
 
 def la_state_copy(dst_S, dst_z, src_S, src_z, B, H, dk, dv, stream):
@@ -334,6 +343,34 @@ def decode_steps_decay(S, z, q, k, v, alpha, eps=1e-6, out=None):
     _check(la_decode_steps_decay(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
                                  v.data_ptr(), out.data_ptr(), B, H, T, dk, dv,
                                  alpha.data_ptr(), eps, code, _stream_ptr(q)))
+    return out
+
+
+def forward_decay(q, k, v, alpha, eps=1e-6, return_state=False, out=None, workspace=None):
+    """Decay-gated causal forward (bf16, d = 64) with per-head factors alpha [H]."""
+    import torch
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype)
+    _need(alpha, "alpha", torch.float32)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=q.dtype, device=q.device)
+    S = z = None
+    if return_state:
+        S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+        z = torch.empty((B, H, dk), dtype=torch.float32, device=q.device)
+    ws_bytes = la_forward_workspace_size(B, H, N, dk, dv, True, code)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    _check(la_forward_decay(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            B, H, N, dk, dv, alpha.data_ptr(), eps, code,
+                            S.data_ptr() if S is not None else None,
+                            z.data_ptr() if z is not None else None,
+                            workspace.data_ptr(), workspace.numel(), _stream_ptr(q)))
+    if return_state:
+        return out, S, z
     return out
 
 

@@ -421,6 +421,50 @@ la_status la_decode_steps(float* S, float* z, const void* q, const void* k,
   return LA_OK;
 }
 
+la_status la_forward_decay(const void* q, const void* k, const void* v, void* out,
+                           int B, int H, int N, int dk, int dv, const float* alpha, float eps,
+                           la_dtype dtype, float* S_final, float* z_final,
+                           void* workspace, size_t workspace_bytes, la_stream_t stream_) {
+  bool empty = false;
+  la_status st = check_sizes(B, H, N, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if (dtype != LA_BF16 || dk != 64 || dv != 64)
+    return fail(LA_ERR_UNSUPPORTED, "la_forward_decay: bf16 with dk = dv = 64 only");
+  if ((S_final == nullptr) != (z_final == nullptr))
+    return fail(LA_ERR_INVALID_ARG, "S_final and z_final must be both given or both NULL");
+  if ((S_final && !aligned16(S_final)) || (z_final && !aligned16(z_final)))
+    return fail(LA_ERR_INVALID_ARG, "S_final/z_final must be 16-byte aligned");
+  cudaStream_t stream = (cudaStream_t)stream_;
+  const long long BH = (long long)B * H;
+  if (empty) {
+    if (S_final != nullptr && BH > 0) {
+      cudaError_t e = cudaMemsetAsync(S_final, 0, sizeof(float) * BH * dk * dv, stream);
+      if (e == cudaSuccess) e = cudaMemsetAsync(z_final, 0, sizeof(float) * BH * dk, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "la_forward_decay (zero final state)");
+    }
+    return LA_OK;
+  }
+  if (!q || !k || !v || !out || !alpha) return fail(LA_ERR_INVALID_ARG, "q, k, v, out, alpha must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+  const SegPlan plan = forward_plan(BH, N, dk, dv, dtype, true);
+  const WsLayout w = layout(BH, N, dk, dv, plan, false);
+  if (workspace == nullptr || workspace_bytes < w.total)
+    return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(LA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (device_status_ptr() == nullptr) return fail(LA_ERR_CUDA, "la_forward_decay: device status word unavailable");
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.BH = (int)BH; a.N = N; a.dk = dk; a.dv = dv; a.causal = 1;
+  a.eps = eps; a.dtype = dtype; a.S_final = S_final; a.z_final = z_final;
+  a.ws_state = (float*)((char*)workspace + w.state_off);
+  a.plan = plan; a.stream = stream;
+  cudaError_t e = tc_forward_decay(a, alpha, H);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward_decay");
+  return LA_OK;
+}
+
 la_status la_decode_steps_decay(float* S, float* z, const void* q, const void* k,
                                 const void* v, void* out, int B, int H, int T, int dk,
                                 int dv, const float* alpha, float eps, la_dtype dtype,

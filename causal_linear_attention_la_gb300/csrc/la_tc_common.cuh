@@ -80,8 +80,9 @@ struct ExactLayout {
   static_assert(FCW >= 1 && FCW <= 8 && (FCW & (FCW - 1)) == 0, "layout");
 };
 
-template <int D, int NT, bool kCheck, bool kSum>
-__device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r0, int n_valid, float (&zacc)[8]) {
+template <int D, int NT, bool kCheck, bool kSum, bool kScale = false>
+__device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r0, int n_valid, float (&zacc)[8],
+                                                    float log2a = 0.f, int wbase = 0) {
   using X = ExactLayout<D, NT>;
   constexpr int GR = 4;                               // rows per loop trip (kept small: code size)
 #pragma unroll 1
@@ -91,12 +92,19 @@ __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r
     for (int i = 0; i < GR; ++i) wv[i] = *reinterpret_cast<const uint4*>(base + sw128(r0 + X::RG * (i0 + i), ch));
 #pragma unroll
     for (int i = 0; i < GR; ++i) {
-      const bool valid = !kCheck || r0 + X::RG * (i0 + i) < n_valid;
+      const int rr = r0 + X::RG * (i0 + i);
+      const bool valid = !kCheck || rr < n_valid;
+      // kScale: row rr is weighted by 2^((wbase - rr) log2a) = a^(wbase - rr)
+      const float w = kScale ? (valid ? exp2f((float)(wbase - rr) * log2a) : 0.f) : 1.f;
       uint32_t* p = reinterpret_cast<uint32_t*>(&wv[i]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const float lo = valid ? phi_f32(__uint_as_float(p[h] << 16)) : 0.f;
-        const float hi = valid ? phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)) : 0.f;
+        float lo = valid ? phi_f32(__uint_as_float(p[h] << 16)) : 0.f;
+        float hi = valid ? phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)) : 0.f;
+        if (kScale) {
+          lo *= w;
+          hi *= w;
+        }
         if (kSum) {
           zacc[2 * h] += lo;
           zacc[2 * h + 1] += hi;
@@ -112,9 +120,11 @@ __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r
 // kReduce: zacc is cleared first and, on return, reduced inside the warp as
 // above. Otherwise this thread's partial sums are added to zacc, and the
 // caller reduces them (reduce_row_groups) when it needs the totals.
-// kSum = false: phi only, zacc untouched.
-template <int D, int NT, bool kReduce = true, bool kSum = true>
-__device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8]) {
+// kSum = false: phi only, zacc untouched. kScale: row r (of the tile) is
+// multiplied by a^(wbase - r), a = 2^log2a (decay weights), before rounding.
+template <int D, int NT, bool kReduce = true, bool kSum = true, bool kScale = false>
+__device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8],
+                                               float log2a = 0.f, int wbase = 0) {
   using X = ExactLayout<D, NT>;
   const int w = t >> 5, lane = t & 31;
   const int fc = X::FCW * w + (lane % X::FCW);       // feature chunk 0 .. D/8-1
@@ -127,9 +137,9 @@ __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid
   }
   // full tiles skip the per-row validity test
   if (n_valid >= C)
-    phi_tile_exact_rows<D, NT, false, kSum>(base, ch, r0, n_valid, zacc);
+    phi_tile_exact_rows<D, NT, false, kSum, kScale>(base, ch, r0, n_valid, zacc, log2a, wbase);
   else
-    phi_tile_exact_rows<D, NT, true, kSum>(base, ch, r0, n_valid, zacc);
+    phi_tile_exact_rows<D, NT, true, kSum, kScale>(base, ch, r0, n_valid, zacc, log2a, wbase);
   if (kReduce && kSum) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {

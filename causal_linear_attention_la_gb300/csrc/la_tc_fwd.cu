@@ -116,9 +116,122 @@ struct FwdParams {
   float* S_final;          // [BH][D][D] or null (written by the last segment)
   float* z_final;          // [BH][D] or null
   int* status;             // device status word (set on a bounded-wait timeout)
+  // decay gating (the kDecay kernels): per-head factors and the state-pass part length
+  const float* alpha = nullptr;   // [H]
+  int H = 1;
+  int sub_len = 0;
 };
 
+// With decay gating (kDecay, D = 64): S_t = a S_{t-1} + phi(k_t) v_t^T and the
+// same for z ("Linear Attention, 곱의 순서를 바꾸면 생기는 일", paragraph on 감쇠
+// 게이팅). For a chunk of n tokens starting from S_prev:
+//   row r reads a^(r+1) S_prev: phi(Q) rows are weighted a^(r+1);
+//   token j enters the state as a^(n-1-j) phi(k_j) v_j^T: phi(K) rows are
+//   weighted a^(n-1-j), so the state update and z keep their MMAs;
+//   P_rj then carries a^(r+1) a^(n-1-j) and the mask keeps a^(r-j) of it
+//   (times a^(-n));
+//   the held state is multiplied by a^n before the chunk's update.
+// A state-pass part's record is its sum decayed to the part's last token;
+// segment s starts from sum_p a^(tok0_s - end_p) record_p.
+
+// Weighted sum of state records p0 .. p1-1 (as sum_states_to_tmem): record p
+// covers tokens up to part_end(p) - 1 and is weighted a^(tok0 - part_end(p)).
 template <int D>
+__device__ __forceinline__ void sum_states_decayed(const float* recs, long long stride, int p0, int p1,
+                                                   uint32_t lane_addr, uint32_t col, int row, float log2a,
+                                                   int tok0, int F, int seg_len, int sub_len) {
+#pragma unroll 1
+  for (int h = 0; h < D; h += 64) {
+    float4 acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row >= 0) {
+#pragma unroll 1
+      for (int p = p0; p < p1; ++p) {
+        const int sg = p / F, part = p % F;
+        const int pend = min(sg * seg_len + (part + 1) * sub_len, (sg + 1) * seg_len);
+        const float w = exp2f((float)(tok0 - pend) * log2a);
+        const float4* src = reinterpret_cast<const float4*>(recs + p * stride + (long long)row * D + h);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float4 f = src[j];
+          acc[j].x = fmaf(w, f.x, acc[j].x); acc[j].y = fmaf(w, f.y, acc[j].y);
+          acc[j].z = fmaf(w, f.z, acc[j].z); acc[j].w = fmaf(w, f.w, acc[j].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[4 * j + 0] = __float_as_uint(acc[4 * g + j].x);
+        v[4 * j + 1] = __float_as_uint(acc[4 * g + j].y);
+        v[4 * j + 2] = __float_as_uint(acc[4 * g + j].z);
+        v[4 * j + 3] = __float_as_uint(acc[4 * g + j].w);
+      }
+      tmem_st16(lane_addr + col + h + 16 * g, v);
+    }
+  }
+  tmem_st_wait();
+}
+
+// The bf16 copy of the held state (as copy_state_to_smem) and, in the same
+// pass, the held state multiplied by `f` in tensor memory (every lane).
+template <int D>
+__device__ __forceinline__ void copy_state_and_scale(uint32_t taddr, uint8_t* sbuf, int row, float f) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c0, v);
+    tmem_ld_wait();
+    if (row >= 0) {
+      const int b = c0 / 64, cb = (c0 % 64) / 8;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+        w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+        w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+        w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+        *reinterpret_cast<uint4*>(sbuf + b * (D * 128) + sw128(row, cb + j)) = w;
+      }
+    }
+    uint32_t lo[16], hi[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      lo[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+      hi[j] = __float_as_uint(__uint_as_float(v[16 + j]) * f);
+    }
+    tmem_st16(taddr + c0, lo);
+    tmem_st16(taddr + c0 + 16, hi);
+  }
+  tmem_st_wait();
+}
+
+// phi in place on a [C][D] tile in packed bf16 (as phi_tile_bf16), row r
+// multiplied by a^(r+1) = 2^((r+1) log2a).
+template <int D, int NT>
+__device__ __forceinline__ void phi_tile_bf16_decayed(uint8_t* tile, int t, float log2a) {
+  constexpr int PER = (C * D * 2 / 16) / NT;
+#pragma unroll 1
+  for (int i = 0; i < PER; ++i) {
+    const int idx = t + NT * i;
+    const int r = (idx & 1023) >> 3;                // 8 chunks of 16 bytes per 128-byte row
+    const float w = exp2f((float)(r + 1) * log2a);
+    const uint32_t w2 = pack_bf16x2(w, w);
+    uint4 x = reinterpret_cast<const uint4*>(tile)[idx];
+    uint32_t* px = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t f = phi_bf16x2(px[h]);
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(px[h]) : "r"(f), "r"(w2));
+    }
+    reinterpret_cast<uint4*>(tile)[idx] = x;
+  }
+}
+
+template <int D, bool kDecay = false>
 __global__ void __launch_bounds__(448, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -126,6 +239,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   using G = Cfg<D>;
   using L = FwdSmem<D>;
   constexpr int ST = G::ST, NPB = G::NPB, NOB = G::NOB;
+  static_assert(!kDecay || G::MERGE, "decay gating is laid out for D = 64");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   float* zst = reinterpret_cast<float*>(sm + L::OFF_ZST);
@@ -156,6 +270,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const float log2a = kDecay ? log2f(prm.alpha[bh % prm.H]) : 0.f;
   const bool last_seg = seg == prm.P - 1;
   const bool write_final = last_seg && prm.S_final != nullptr;
   // the state update after the last chunk is only needed for the final state
@@ -357,21 +472,36 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const int s = c % ST;
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);   // Q
+      if constexpr (kDecay)
+        phi_tile_bf16_decayed<D, 128>(sm + s * G::STAGE, t, log2a);   // Q, row r times a^(r+1)
+      else
+        phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);   // Q
       fence_proxy_async_smem();
       mbar_arrive(&phi_done[s]);
       if (c == 0) {
         // this segment's starting state: the sum of the earlier segments' records
         if (nrec > 0) griddep_wait();
-        sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum);
+        if constexpr (kDecay)
+          sum_states_decayed<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum, log2a, tok0, prm.F,
+                                prm.seg_len, prm.sub_len);
+        else
+          sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum);
       } else {
         // the state after chunk c - 1's update
         ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
       }
-      copy_state_to_smem<D>(lane_addr + G::COL_S, G::MERGE ? sm + s * G::STAGE + G::OFF_SB : sm + L::OFF_SBUF,
-                            row_copy);
+      if constexpr (kDecay) {
+        // the copy of S_prev, and the held state decayed by a^n before this
+        // chunk's n tokens are added
+        const int n_valid = min(C, tok_end - (tok0 + c * C));
+        copy_state_and_scale<D>(lane_addr + G::COL_S, sm + s * G::STAGE + G::OFF_SB, row_copy,
+                                exp2f((float)n_valid * log2a));
+      } else {
+        copy_state_to_smem<D>(lane_addr + G::COL_S, G::MERGE ? sm + s * G::STAGE + G::OFF_SB : sm + L::OFF_SBUF,
+                              row_copy);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
@@ -416,6 +546,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (!G::MERGE && !mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs)) return false;
       tc_fence_after();
       rowsum = 0.f;
+      // with decay, the kept entries carry a^(r-j+n): times a^(-n)
+      const float dfac = kDecay ? exp2f(-(float)min(C, tok_end - (tok0 + c * C)) * log2a) : 1.f;
 #pragma unroll 1
       for (int p = 0; p < 4; ++p) {
         uint32_t pk[16];
@@ -425,7 +557,11 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a = __uint_as_float(v[2 * j]), b = __uint_as_float(v[2 * j + 1]);
+            float a = __uint_as_float(v[2 * j]), b = __uint_as_float(v[2 * j + 1]);
+            if (kDecay) {
+              a *= dfac;
+              b *= dfac;
+            }
             if (!G::MERGE) rowsum += a + b;
             pk[j] = pack_bf16x2(a, b);
           }
@@ -435,8 +571,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a = (2 * j <= lane) ? __uint_as_float(v[2 * j]) : 0.f;
-            const float b = (2 * j + 1 <= lane) ? __uint_as_float(v[2 * j + 1]) : 0.f;
+            const float a = (2 * j <= lane) ? __uint_as_float(v[2 * j]) * dfac : 0.f;
+            const float b = (2 * j + 1 <= lane) ? __uint_as_float(v[2 * j + 1]) * dfac : 0.f;
             if (!G::MERGE) rowsum += a + b;
             pk[j] = pack_bf16x2(a, b);
           }
@@ -581,8 +717,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (!ok) break;
       float colsum[8];
       if constexpr (G::MERGE) {
-        // z is summed by the state MMA
-        phi_tile_exact<D, 128, false, false>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
+        // z is summed by the state MMA; with decay, row j is weighted a^(n-1-j)
+        if constexpr (kDecay)
+          phi_tile_exact<D, 128, false, false, true>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum, log2a,
+                                                     n_valid - 1);
+        else
+          phi_tile_exact<D, 128, false, false>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
         fence_proxy_async_smem();
         mbar_arrive(&phi_done[s]);
         continue;
@@ -645,9 +785,13 @@ struct StateParams {
   int nseg;         // segments summed: P - 1 (causal) or P (non-causal)
   float* ws_state;  // [BH][P*F][D*D + D]
   int* status;
+  const float* alpha = nullptr;   // kDecay: [H] per-head factors
+  int H = 1;
 };
 
-template <int D>
+// kDecay: each record is decayed to its part's last token (row j of a chunk
+// weighted a^(part_end - 1 - token)).
+template <int D, bool kDecay = false>
 __global__ void __launch_bounds__(320, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const StateParams prm) {
@@ -681,6 +825,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   const int tok_end = min(seg_end, tok0 + prm.sub_len);
   // a part past the end of a short last segment (non-causal) holds no token
   const int nchunks = max(0, (tok_end - tok0 + C - 1) / C);
+  static_assert(!kDecay || StateSmem<D>::ZMMA, "decay gating is laid out for D = 64");
+  const float log2a = kDecay ? log2f(prm.alpha[bh % prm.H]) : 0.f;
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -770,7 +916,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       const int n_valid = min(C, tok_end - (tok0 + c * C));
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      if (L::ZMMA)
+      if (kDecay)
+        phi_tile_exact<D, 256, false, false, true>(sm + s * G::STAGE_S, t, n_valid, zrun, log2a,
+                                                   tok_end - 1 - (tok0 + c * C));
+      else if (L::ZMMA)
         phi_tile_exact<D, 256, false, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
       else
         phi_tile_exact<D, 256, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
@@ -1057,8 +1206,8 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
   }
 }
 
-template <int D>
-cudaError_t launch_state(const FwdArgs& a) {
+template <int D, bool kDecay = false>
+cudaError_t launch_state(const FwdArgs& a, const float* alpha = nullptr, int H = 1) {
   // causal: the segments before the last (none with one segment); non-causal: all
   const int nseg = a.causal ? a.plan.P - 1 : a.plan.P;
   if (nseg < 1) return cudaSuccess;
@@ -1067,11 +1216,13 @@ cudaError_t launch_state(const FwdArgs& a) {
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
   if (e != cudaSuccess) return e;
   constexpr int smem = StateSmem<D>::BYTES;
-  e = cudaFuncSetAttribute(tc_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(tc_state_kernel<D, kDecay>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   StateParams p{a.N, a.plan.P, a.plan.seg_len, a.plan.F, state_sub_len(a.plan), nseg, a.ws_state,
                 device_status_ptr()};
-  tc_state_kernel<D><<<a.BH * nseg * a.plan.F, 320, smem, a.stream>>>(mk, mv, p);
+  p.alpha = alpha;
+  p.H = H;
+  tc_state_kernel<D, kDecay><<<a.BH * nseg * a.plan.F, 320, smem, a.stream>>>(mk, mv, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -1106,9 +1257,9 @@ cudaError_t launch_noncausal(const FwdArgs& a) {
   return e;
 }
 
-template <int D>
-cudaError_t launch_forward(const FwdArgs& a) {
-  if (!a.causal) return launch_noncausal<D>(a);
+template <int D, bool kDecay = false>
+cudaError_t launch_forward(const FwdArgs& a, const float* alpha = nullptr, int H = 1) {
+  if (!kDecay && !a.causal) return launch_noncausal<D>(a);
   CUtensorMap mq, mk, mv, mo, mo32;
   cudaError_t e = make_map(&mq, a.q, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mk, a.k, a.BH, a.N, D);
@@ -1117,10 +1268,13 @@ cudaError_t launch_forward(const FwdArgs& a) {
   if (e == cudaSuccess) e = make_map(&mo32, a.out, a.BH, a.N, D, 32);
   if (e != cudaSuccess) return e;
   constexpr int smem = FwdSmem<D>::BYTES;
-  e = cudaFuncSetAttribute(tc_forward_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(tc_forward_kernel<D, kDecay>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   FwdParams p{a.N, a.plan.P, a.plan.seg_len, a.plan.F, a.eps, a.ws_state, (__nv_bfloat16*)a.out,
               a.S_final, a.z_final, device_status_ptr()};
+  p.alpha = alpha;
+  p.H = H;
+  p.sub_len = state_sub_len(a.plan);
   // a dependent of the state kernel (when there is one): it may start before
   // that kernel ends and waits for its records only where it reads them
   cudaLaunchConfig_t cfg{};
@@ -1133,7 +1287,7 @@ cudaError_t launch_forward(const FwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.plan.P > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D>, mq, mk, mv, mo, mo32, p);
+  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D, kDecay>, mq, mk, mv, mo, mo32, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -1144,6 +1298,18 @@ cudaError_t launch_forward(const FwdArgs& a) {
 bool tc_forward_supported(int dk, int dv, la_dtype dtype, int causal) {
   (void)causal;
   return dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128);
+}
+
+cudaError_t tc_forward_decay(const FwdArgs& a, const float* alpha, int H) {
+  if (a.dk != 64 || a.dv != 64 || a.dtype != LA_BF16 || !a.causal) return cudaErrorInvalidValue;
+  prof_begin(LA_SPAN_FWD_STATE, a.stream);
+  cudaError_t e = launch_state<64, true>(a, alpha, H);
+  prof_end(LA_SPAN_FWD_STATE, a.stream);
+  if (e != cudaSuccess) return e;
+  prof_begin(LA_SPAN_FWD_OUTPUT, a.stream);
+  e = launch_forward<64, true>(a, alpha, H);
+  prof_end(LA_SPAN_FWD_OUTPUT, a.stream);
+  return e;
 }
 
 cudaError_t tc_segment_state(const FwdArgs& a) {

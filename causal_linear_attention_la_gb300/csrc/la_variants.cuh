@@ -18,6 +18,11 @@ struct VariantArgs {
 
 cudaError_t decode_steps_decay(const VariantArgs& a);
 cudaError_t decode_steps_delta(const VariantArgs& a);
+// Decay-gated causal forward on the tensor cores (bf16, dk = dv = 64): the
+// state pass and the chunk loop with per-head factors alpha [H]; FwdArgs as
+// for la_forward (its segment plan and workspace).
+struct FwdArgs;
+cudaError_t tc_forward_decay(const FwdArgs& a, const float* alpha, int H);
 // dst <- src for n floats (16-byte aligned pointers)
 cudaError_t copy_floats(float* dst, const float* src, long long n, cudaStream_t stream);
 

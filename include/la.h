@@ -172,6 +172,24 @@ LA_API la_status la_decode_steps_decay(float* S, float* z, const void* q, const 
                                 la_stream_t stream);
 
 /*
+ * Decay-gated causal forward: the outputs of la_decode_steps_decay run over
+ * the whole sequence from the zero state, computed chunk by chunk on the
+ * tensor cores (the chunked form of the same recurrence: inside a chunk the
+ * causal weights phi(q_t).phi(k_j) carry alpha^(t-j); across chunks the
+ * carried state decays by alpha per token).
+ *
+ * q, k, v, out as la_forward (bf16, dk = dv = 64 only; LA_ERR_UNSUPPORTED
+ * otherwise); alpha [H] fp32 device memory, each in [0.5, 1] (smaller factors
+ * underflow the chunk's weights; not checked); S_final, z_final as la_forward
+ * (the decayed state after the last token); workspace sized by
+ * la_forward_workspace_size(B, H, N, 64, 64, 1, LA_BF16).
+ */
+LA_API la_status la_forward_decay(const void* q, const void* k, const void* v, void* out,
+                           int B, int H, int N, int dk, int dv, const float* alpha, float eps,
+                           la_dtype dtype, float* S_final, float* z_final,
+                           void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
  * Delta-rule decode: T steps per (batch, head) in one call; each step reads
  * the state with the key and adds only the difference to the value (the
  * paragraph on 델타 규칙 of the same page):

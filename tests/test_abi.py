@@ -144,6 +144,15 @@ def test_variant_validation(lib):
     assert la.la_decode_steps_delta(**{**e, "k": None}) == la.LA_ERR_INVALID_ARG
     assert la.la_decode_steps_delta(**{**e, "dtype": 7}) == la.LA_ERR_UNSUPPORTED
     assert la.la_decode_steps_delta(**{**e, "H": 0}) == la.LA_OK
+    f = dict(q=1024, k=1024, v=1024, out=1024, B=2, H=3, N=100, dk=64, dv=64, alpha=2048, eps=1e-6,
+             dtype=la.LA_BF16, S_final=None, z_final=None, workspace=4096, workspace_bytes=1 << 20,
+             stream=None)
+    assert la.la_forward_decay(**{**f, "dk": 128, "dv": 128}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_forward_decay(**{**f, "dtype": la.LA_F32}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_forward_decay(**{**f, "alpha": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_decay(**{**f, "S_final": 8192}) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_decay(**{**f, "workspace_bytes": 8}) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_decay(**{**f, "N": 0}) == la.LA_OK
     c = dict(dst_S=1024, dst_z=2048, src_S=4096, src_z=8192, B=2, H=3, dk=64, dv=64, stream=None)
     assert la.la_state_copy(**{**c, "dst_z": None}) == la.LA_ERR_INVALID_ARG
     assert la.la_state_copy(**{**c, "src_S": None}) == la.LA_ERR_INVALID_ARG

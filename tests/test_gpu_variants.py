@@ -139,3 +139,44 @@ def test_state_snapshot_restore_round_trip():
     la.state_copy(only, S)
     torch.cuda.synchronize()
     assert torch.equal(only, S)
+
+
+# ---------------------------------------------------------------------------
+# Decay-gated forward (chunked, tensor cores) vs the oracle recurrence
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("B,H,N", [
+    (1, 1, 1),         # one token
+    (1, 1, 100),       # one partial chunk
+    (2, 1, 129),       # a chunk and one token
+    (2, 3, 1000),      # several segments, ragged tail
+    (1, 1, 4096),      # many one-chunk segments
+    (6, 10, 2049),     # state pass in several parts per segment, one-token tail
+])
+def test_forward_decay(B, H, N):
+    import torch
+    from helpers import STATE_TOL, Z_TOL
+    q, k, v = synth.qkv(B, H, N, 64, 64, seed=40 + N + H, dtype="bf16")
+    alpha_h = np.random.default_rng(N).uniform(0.5, 1.0, H).astype(np.float32)
+    out, S, z = la.forward_decay(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
+                                 torch.from_numpy(alpha_h).cuda(), return_state=True)
+    torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
+    S_w, z_w, o_w = orc.decode_steps_decay(np.zeros((B, H, 64, 64)), np.zeros((B, H, 64)), q, k, v,
+                                           alpha=alpha_h.astype(np.float64)[None, :])
+    err = rel_err(to_host(out), o_w, np.abs(v).max())
+    assert err <= TOL["bf16"], err
+    s_err = rel_err(to_host(S), S_w, np.abs(S_w).max())
+    z_err = rel_err(to_host(z), z_w, np.abs(z_w).max())
+    assert s_err <= STATE_TOL["bf16"] and z_err <= Z_TOL["bf16"], (s_err, z_err)
+
+
+def test_forward_decay_one_is_forward():
+    import torch
+    B, H, N = 2, 4, 3000
+    q, k, v = [to_dev(x, "bf16") for x in synth.qkv(B, H, N, 64, 64, seed=61, dtype="bf16")]
+    o1 = la.forward_decay(q, k, v, torch.ones(H, device="cuda"))
+    o2 = la.forward(q, k, v)
+    torch.cuda.synchronize()
+    assert rel_err(to_host(o1), to_host(o2), float(v.abs().max())) <= 1e-6
