@@ -56,6 +56,8 @@ WORKLOADS = {
     "decode_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                 prefill=dict(B=1, H=16, N=131072), steps=1024),
     "fwdbwd_b4_h8_n8192_d64": dict(kind="fwdbwd", B=4, H=8, N=8192, dk=64, dv=64, causal=True, seed=5),
+    # the same shape without the causal mask (every query reads the whole sequence)
+    "fwdbwd_nc_b4_h8_n8192_d64": dict(kind="fwdbwd", B=4, H=8, N=8192, dk=64, dv=64, causal=False, seed=5),
     # decay-gated forward (per-head factors 0.9 .. 0.999), the headline shape
     "fwd_decay_b4_h8_n4096_d64": dict(kind="forward", B=4, H=8, N=4096, dk=64, dv=64, causal=True, seed=2,
                                       decay=True),

@@ -1,5 +1,5 @@
-// Tensor-core (tcgen05) backward for bf16 inputs, causal, dk = dv = 64,
-// chunks of C = 128 tokens.
+// Tensor-core (tcgen05) backward for bf16 inputs, dk = dv = 64, chunks of
+// C = 128 tokens: causal (two sweeps), and non-causal (passes A and B below).
 //
 // Gradients of L = sum(dout * out) by cumulative sums, with no per-token
 // state stored ("Transformers are RNNs" review, section "그래디언트 계산 —
@@ -986,6 +986,511 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
+// Non-causal backward (every query reads S_N, z_N; every key sees R_0, r_0):
+//   D_t = phi(q_t).z_N + eps,  a_t = g_t / D_t,  b_t = -(g_t . o_t) / D_t,
+//   dphi(q_t) = S_N a_t + b_t z_N,
+//   R_0 = sum_t phi(q_t) a_t^T,  r_0 = sum_t b_t phi(q_t),
+//   dphi(k_j) = R_0 v_j + r_0,  dv_j = R_0^T phi(k_j)
+// (the non-causal case of the gradient above: S_t -> S_N, R_j -> R_0).
+// Three launches: the forward's state pass over all segments (S_N, z_N
+// records), pass A per segment (dq and the segment's (R, r) record), pass B
+// per segment (dk, dv from the sum of all (R, r) records). No masks: each
+// chunk is a dense product with the totals.
+// ---------------------------------------------------------------------------
+template <int D>
+struct NA {
+  static_assert(D == 64, "the tensor-core backward is laid out for D = 64");
+  static constexpr int TILE = BOX;
+  static constexpr int ST = 4;                        // stages of Q, G
+  static constexpr int OFF_G = TILE;
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int OFF_SBUF = ST * STAGE;         // bf16 S_N^T copy, D rows
+  static constexpr int OFF_ZN = OFF_SBUF + D * 128;   // [D] z_N
+  static constexpr int OFF_BARR = OFF_ZN + D * 4;     // [ST][C] b_t
+  static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
+  static constexpr int NBAR = 5 * ST + 8 + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static constexpr uint32_t COL_S = 0;                // S_N^T (M = D layout)
+  __host__ __device__ static constexpr uint32_t col_oq(int ob) { return D + D * ob; }  // O, then dQ in place
+  static constexpr uint32_t COL_R = 3 * D;            // R (M = D layout)
+  static constexpr uint32_t TMEM_COLS = 256;
+};
+
+struct NcBwdParams {
+  int N, P, seg_len, F;
+  float eps;
+  const float* ws_state;   // [BH][P*F][D*D + D] S^T, z sums of every part (pass A reads)
+  float* ws_rev;           // [BH][P][D*D + D] (R, r) of each segment (A writes, B reads)
+  int* status;
+};
+
+// Pass A. Warps 0-3: phi(Q), the S_N / z_N sums and copies, r sums, the R
+// record; warps 4-7: den, the row pass (a, b) and the dq epilogue; warp 8 TMA
+// (Q, G in; dq out from the dead G tile); warp 9 TMEM and MMA.
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
+                   const __grid_constant__ CUtensorMap map_dq, const NcBwdParams prm) {
+  using G = NA<D>;
+  constexpr int ST = G::ST;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  uint8_t* sbuf = sm + G::OFF_SBUF;
+  float* zn = reinterpret_cast<float*>(sm + G::OFF_ZN);
+  float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
+  uint64_t* full = bars;               // [ST]
+  uint64_t* phi_done = bars + ST;      // [ST]
+  uint64_t* empty = bars + 2 * ST;     // [ST] MMAs of the stage's chunk done
+  uint64_t* ost_full = bars + 3 * ST;  // [ST] dq staged (group B)
+  uint64_t* rdone = bars + 4 * ST;     // [ST] r sums read the stage (group A)
+  uint64_t* x = bars + 5 * ST;
+  uint64_t* o_full = x;                // [2]
+  uint64_t* a_ready = x + 2;           // [2]
+  uint64_t* dq_full = x + 4;           // [2]
+  uint64_t* oq_empty = x + 6;          // [2]
+  uint64_t* s_ready = x + 8;
+  uint64_t* mma_fin = x + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G::OFF_MISC + 4);
+  // pass B may start filling its pipeline while this grid runs
+  griddep_launch_dependents();
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) report_timeout(prm.status);
+    return;
+  }
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / prm.P, seg = blockIdx.x % prm.P;
+  const int tok0 = seg * prm.seg_len;
+  const int tok_end = min(prm.N, tok0 + prm.seg_len);
+  const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const long long rstride = (long long)(D * D + D);
+  const float* recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
+  const int nrec = prm.P * prm.F;
+  float* rec_out = prm.ws_rev + ((long long)bh * prm.P + seg) * rstride;
+
+  if (tid == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&phi_done[i], 128);
+      mbar_init(&empty[i], 1);
+      mbar_init(&ost_full[i], 128);
+      mbar_init(&rdone[i], 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&o_full[i], 1);
+      mbar_init(&a_ready[i], 128);
+      mbar_init(&dq_full[i], 1);
+      mbar_init(&oq_empty[i], 128);
+    }
+    mbar_init(s_ready, 128);
+    mbar_init(mma_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, G::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_g);
+      tma_prefetch_desc(&map_dq);
+      // the stage of chunk c is free once its MMAs, its dq epilogue and its
+      // r sums are done; its dq (in the dead G tile) is stored first
+      auto retire = [&](int c) -> bool {
+        const int s = c % ST;
+        const uint32_t par = (c / ST) & 1;
+        if (!mbar_wait(&empty[s], par, abort_flag, kTimeoutNs) ||
+            !mbar_wait(&ost_full[s], par, abort_flag, kTimeoutNs) ||
+            !mbar_wait(&rdone[s], par, abort_flag, kTimeoutNs))
+          return false;
+        tma_store_3d(&map_dq, sm + s * G::STAGE + G::OFF_G, 0, tok0 + c * C, bh);
+        tma_store_commit();
+        tma_store_wait_read<0>();
+        return true;
+      };
+      int issued = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % ST;
+        if (c >= ST && !(ok = retire(c - ST))) break;
+        uint8_t* stg = sm + s * G::STAGE;
+        mbar_arrive_expect_tx(&full[s], 2 * G::TILE);
+        tma_load_3d(stg, &map_q, &full[s], 0, tok0 + c * C, bh);
+        tma_load_3d(stg + G::OFF_G, &map_g, &full[s], 0, tok0 + c * C, bh);
+        issued = c + 1;
+      }
+      for (int c = max(0, issued - ST); c < issued && ok; ++c) ok = retire(c);
+      tma_store_wait<0>();
+      for (int c = max(0, issued - ST); c < issued; ++c)
+        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);   // O = phiQ S_N (S^T copy K-major)
+      constexpr uint32_t id_as = make_idesc_bf16(128, D, false, true);    // dQ = a S_N^T (copy MN-major)
+      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);       // R += phiQ^T a
+      const uint32_t sb = smem_u32(sbuf);
+      const uint64_t dsk = make_sdesc(sb, 16, 1024, kSwizzle128B);
+      const uint64_t dsm = make_sdesc(sb, D * 128, 1024, kSwizzle128B);
+      bool ok = mbar_wait(s_ready, 0, abort_flag, kTimeoutNs);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % ST, ob = c & 1;
+        const uint32_t qa = smem_u32(sm + s * G::STAGE), ga = qa + G::OFF_G;
+        const uint32_t oq = tmem + G::col_oq(ob);
+        ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        if (ok && c >= 2) ok = mbar_wait(&oq_empty[ob], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dq = make_sdesc(qa, 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(oq, sdesc_add(dq, k * 32), sdesc_add(dsk, k * 32), id_qs, k > 0);
+        tc_commit(&o_full[ob]);
+        ok = mbar_wait(&a_ready[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dg = make_sdesc(ga, 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(oq, sdesc_add(dg, k * 32), sdesc_add(dsm, k * 2048), id_as, k > 0);
+        const uint64_t dqm = make_sdesc(qa, BOX, 1024, kSwizzle128B);
+        const uint64_t dgm = make_sdesc(ga, BOX, 1024, kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          mma_ss(tmem + G::COL_R, sdesc_add(dqm, k * 2048), sdesc_add(dgm, k * 2048), id_tt,
+                 (c > 0 || k > 0) ? 1u : 0u);
+        tc_commit(&dq_full[ob]);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(mma_fin);
+      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    }
+  } else if (warp < 4) {
+    // ---------------- group A: phi(Q), totals, r, R ----------------
+    using X = ExactLayout<D, 128>;
+    const int t = tid;
+    const int q = warp & 3;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    const int row = state_row<D>(q, lane);
+    const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    float racc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) racc[e] = 0.f;
+    griddep_wait();
+    sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row);
+    copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf, row);
+    for (int i = t; i < D; i += 128) {
+      float acc = 0.f;
+      for (int p = 0; p < nrec; ++p) acc += recs[p * rstride + D * D + i];
+      zn[i] = acc;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(s_ready);
+    bool ok = true;
+    for (int c = 0; c <= nchunks && ok; ++c) {
+      if (c < nchunks) {
+        const int s = c % ST;
+        ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);
+        fence_proxy_async_smem();
+        mbar_arrive(&phi_done[s]);
+      }
+      if (c >= 1) {
+        // r += sum_t b_t phi(q_t) over the previous chunk
+        const int cp = c - 1, sp = cp % ST;
+        ok = mbar_wait(&a_ready[cp & 1], (cp >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        wcolsum_tile<D, 128>(sm + sp * G::STAGE, barr + sp * C, t, racc);
+        mbar_arrive(&rdone[sp]);
+      }
+    }
+    reduce_row_groups<D, 128>(racc);
+    if (ok && lane < X::FCW) {
+      float4* rd = reinterpret_cast<float4*>(rec_out + D * D + 8 * fc);
+      rd[0] = make_float4(racc[0], racc[1], racc[2], racc[3]);
+      rd[1] = make_float4(racc[4], racc[5], racc[6], racc[7]);
+    }
+    if (ok) ok = mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    if (ok) {
+      tc_fence_after();
+      store_state_from_tmem<D>(rec_out, lane_addr, G::COL_R, row);
+    }
+  } else {
+    // ---------------- group B: den, a and b, dq ----------------
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    bool ok = mbar_wait(s_ready, 0, abort_flag, kTimeoutNs);
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST, ob = c & 1;
+      uint8_t* stg = sm + s * G::STAGE;
+      ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      const float inv_den = 1.f / (phiq_dot<D>(stg, r, zn) + prm.eps);
+      ok = mbar_wait(&o_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const float beta = grad_row_pass<D>(lane_addr + G::col_oq(ob), stg + G::OFF_G, r, inv_den);
+      const float b = -beta * inv_den * inv_den;
+      barr[s * C + r] = b;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&a_ready[ob]);
+      ok = mbar_wait(&dq_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      // dq staged in the dead G tile (a has been read by the MMAs); the
+      // producer stores it before refilling the stage
+      grad_epilogue<D>(lane_addr + G::col_oq(ob), stg, r, b, zn, stg + G::OFF_G);
+      tc_fence_before();
+      mbar_arrive(&oq_empty[ob]);
+      fence_proxy_async_smem();
+      mbar_arrive(&ost_full[s]);
+    }
+  }
+
+  // ---------------- teardown ----------------
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::TMEM_COLS);
+  }
+}
+
+template <int D>
+struct NB {
+  static_assert(D == 64, "the tensor-core backward is laid out for D = 64");
+  static constexpr int TILE = BOX;
+  static constexpr int ST = 4;                        // stages of K, V
+  static constexpr int OFF_V = TILE;
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int OFF_RBUF = ST * STAGE;         // bf16 R_0 copy, D rows
+  static constexpr int OFF_RVEC = OFF_RBUF + D * 128; // [D] r_0
+  static constexpr int OFF_BAR = OFF_RVEC + D * 4;
+  static constexpr int NBAR = 4 * ST + 4 + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static constexpr uint32_t COL_R = 0;                // R_0 (M = D layout)
+  __host__ __device__ static constexpr uint32_t col_dk(int ob) { return D + 2 * D * ob; }
+  __host__ __device__ static constexpr uint32_t col_dv(int ob) { return 2 * D + 2 * D * ob; }
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(col_dv(1) + D <= TMEM_COLS, "tensor memory budget");
+};
+
+struct NcBwdBParams {
+  int N, P, seg_len;
+  const float* ws_rev;     // [BH][P][D*D + D] (R, r) of every segment
+  int* status;
+};
+
+// Pass B. Warps 0-3: phi(K) in place; warps 4-7: the R_0 / r_0 sums and the
+// R_0 copy, then the dk, dv epilogue (dk staged in the dead V tile, dv in the
+// dead K tile, row by row); warp 8 TMA; warp 9 TMEM and MMA.
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+tc_bwd_nc_b_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
+                   const NcBwdBParams prm) {
+  using G = NB<D>;
+  constexpr int ST = G::ST;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  uint8_t* rbuf = sm + G::OFF_RBUF;
+  float* rvec = reinterpret_cast<float*>(sm + G::OFF_RVEC);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
+  uint64_t* full = bars;               // [ST]
+  uint64_t* phi_done = bars + ST;      // [ST]
+  uint64_t* empty = bars + 2 * ST;     // [ST] MMAs of the stage's chunk done
+  uint64_t* ost_full = bars + 3 * ST;  // [ST] dk, dv staged
+  uint64_t* x = bars + 4 * ST;
+  uint64_t* kv_full = x;               // [2]
+  uint64_t* kv_empty = x + 2;          // [2]
+  uint64_t* r_ready = x + 4;
+  uint64_t* mma_fin = x + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G::OFF_MISC + 4);
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) report_timeout(prm.status);
+    return;
+  }
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / prm.P, seg = blockIdx.x % prm.P;
+  const int tok0 = seg * prm.seg_len;
+  const int tok_end = min(prm.N, tok0 + prm.seg_len);
+  const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const long long rstride = (long long)(D * D + D);
+  const float* recs = prm.ws_rev + (long long)bh * prm.P * rstride;
+
+  if (tid == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&phi_done[i], 128);
+      mbar_init(&empty[i], 1);
+      mbar_init(&ost_full[i], 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 128);
+    }
+    mbar_init(r_ready, 128);
+    mbar_init(mma_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, G::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_dk);
+      tma_prefetch_desc(&map_dv);
+      auto retire = [&](int c) -> bool {
+        const int s = c % ST;
+        const uint32_t par = (c / ST) & 1;
+        if (!mbar_wait(&empty[s], par, abort_flag, kTimeoutNs) ||
+            !mbar_wait(&ost_full[s], par, abort_flag, kTimeoutNs))
+          return false;
+        uint8_t* stg = sm + s * G::STAGE;
+        tma_store_3d(&map_dk, stg + G::OFF_V, 0, tok0 + c * C, bh);
+        tma_store_3d(&map_dv, stg, 0, tok0 + c * C, bh);
+        tma_store_commit();
+        tma_store_wait_read<0>();
+        return true;
+      };
+      int issued = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % ST;
+        if (c >= ST && !(ok = retire(c - ST))) break;
+        uint8_t* stg = sm + s * G::STAGE;
+        mbar_arrive_expect_tx(&full[s], 2 * G::TILE);
+        tma_load_3d(stg, &map_k, &full[s], 0, tok0 + c * C, bh);
+        tma_load_3d(stg + G::OFF_V, &map_v, &full[s], 0, tok0 + c * C, bh);
+        issued = c + 1;
+      }
+      for (int c = max(0, issued - ST); c < issued && ok; ++c) ok = retire(c);
+      tma_store_wait<0>();
+      for (int c = max(0, issued - ST); c < issued; ++c)
+        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_vr = make_idesc_bf16(128, D, false, false);   // dK = V R_0^T (R copy K-major)
+      constexpr uint32_t id_kr = make_idesc_bf16(128, D, false, true);    // dV = phiK R_0 (copy MN-major)
+      const uint32_t rb = smem_u32(rbuf);
+      const uint64_t drk = make_sdesc(rb, 16, 1024, kSwizzle128B);
+      const uint64_t drm = make_sdesc(rb, D * 128, 1024, kSwizzle128B);
+      bool ok = mbar_wait(r_ready, 0, abort_flag, kTimeoutNs);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % ST, ob = c & 1;
+        const uint32_t ka = smem_u32(sm + s * G::STAGE), va = ka + G::OFF_V;
+        ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        if (ok && c >= 2) ok = mbar_wait(&kv_empty[ob], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dv_ = make_sdesc(va, 16, 1024, kSwizzle128B);
+        const uint64_t dk_ = make_sdesc(ka, 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + G::col_dk(ob), sdesc_add(dv_, k * 32), sdesc_add(drk, k * 32), id_vr, k > 0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + G::col_dv(ob), sdesc_add(dk_, k * 32), sdesc_add(drm, k * 2048), id_kr, k > 0);
+        tc_commit(&kv_full[ob]);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(mma_fin);
+      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+    }
+  } else if (warp < 4) {
+    // ---------------- group C: phi(K) ----------------
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST;
+      ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      phi_tile_bf16<D, 128>(sm + s * G::STAGE, tid);
+      fence_proxy_async_smem();
+      mbar_arrive(&phi_done[s]);
+    }
+  } else {
+    // ---------------- group E: R_0, r_0; dk, dv ----------------
+    const int t = tid - 128;
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    const int row = state_row<D>(q, lane);
+    griddep_wait();
+    sum_states_to_tmem<D>(recs, rstride, 0, prm.P, lane_addr, G::COL_R, row);
+    tc_fence_before();
+    tc_fence_after();
+    copy_state_to_smem<D>(lane_addr + G::COL_R, rbuf, row);
+    for (int i = t; i < D; i += 128) {
+      float acc = 0.f;
+      for (int p = 0; p < prm.P; ++p) acc += recs[p * rstride + D * D + i];
+      rvec[i] = acc;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(r_ready);
+    bool ok = mbar_wait(r_ready, 0, abort_flag, kTimeoutNs);   // rvec complete
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST, ob = c & 1;
+      uint8_t* stg = sm + s * G::STAGE;
+      ok = mbar_wait(&kv_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      // dk = (dK + r_0) phi'(k) into the V tile, then dv into this row of
+      // the K tile (the row's phi(k) has been read)
+      grad_epilogue<D>(lane_addr + G::col_dk(ob), stg, r, 1.f, rvec, stg + G::OFF_V);
+      store_row_bf16<D>(lane_addr + G::col_dv(ob), stg, r);
+      tc_fence_before();
+      mbar_arrive(&kv_empty[ob]);
+      fence_proxy_async_smem();
+      mbar_arrive(&ost_full[s]);
+    }
+  }
+
+  // ---------------- teardown ----------------
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 template <typename Kernel, typename... Args>
@@ -1051,12 +1556,60 @@ cudaError_t launch_backward(const BwdArgs& a) {
   return e;
 }
 
+// Non-causal: the state pass over every segment (S_N, z_N records), then
+// pass A (dq, (R, r) records) and pass B (dk, dv), each a dependent of the
+// launch before it.
+template <int D>
+cudaError_t launch_backward_nc(const BwdArgs& a) {
+  FwdArgs f{};
+  f.q = a.q; f.k = a.k; f.v = a.v; f.out = nullptr;
+  f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = 0;
+  f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
+  f.stream = a.stream;
+  prof_begin(LA_SPAN_BWD_STATE, a.stream);
+  cudaError_t e = tc_segment_state(f);    // sums of S^T, z for every segment
+  prof_end(LA_SPAN_BWD_STATE, a.stream);
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv;
+  e = make_map(&mq, a.q, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mk, a.k, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mg, a.dout, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mdq, a.dq, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mdk, a.dk_, a.BH, a.N, D);
+  if (e == cudaSuccess) e = make_map(&mdv, a.dv_, a.BH, a.N, D);
+  if (e != cudaSuccess) return e;
+  int* status = device_status_ptr();
+
+  constexpr int smema = NA<D>::BYTES;
+  e = cudaFuncSetAttribute(tc_bwd_nc_a_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smema);
+  if (e != cudaSuccess) return e;
+  NcBwdParams pa{a.N, a.plan.P, a.plan.seg_len, a.plan.F, a.eps, a.ws_state, a.ws_rev, status};
+  prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
+  e = launch_dependent(tc_bwd_nc_a_kernel<D>, a.BH * a.plan.P, 320, smema, a.stream, mq, mg, mdq, pa);
+  prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
+  if (e != cudaSuccess) return e;
+  note_launch();
+
+  constexpr int smemb = NB<D>::BYTES;
+  e = cudaFuncSetAttribute(tc_bwd_nc_b_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smemb);
+  if (e != cudaSuccess) return e;
+  NcBwdBParams pb{a.N, a.plan.P, a.plan.seg_len, a.ws_rev, status};
+  prof_begin(LA_SPAN_BWD_SWEEP2, a.stream);
+  e = launch_dependent(tc_bwd_nc_b_kernel<D>, a.BH * a.plan.P, 320, smemb, a.stream, mk, mv, mdk, mdv, pb);
+  prof_end(LA_SPAN_BWD_SWEEP2, a.stream);
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
 }  // namespace
 
 bool tc_backward_supported(int dk, int dv, la_dtype dtype, int causal) {
-  return dtype == LA_BF16 && dk == 64 && dv == 64 && causal;
+  (void)causal;
+  return dtype == LA_BF16 && dk == 64 && dv == 64;
 }
 
-cudaError_t tc_backward(const BwdArgs& a) { return launch_backward<64>(a); }
+cudaError_t tc_backward(const BwdArgs& a) { return a.causal ? launch_backward<64>(a) : launch_backward_nc<64>(a); }
 
 }  // namespace la

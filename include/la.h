@@ -251,8 +251,9 @@ LA_API la_status la_backward(const void* q, const void* k, const void* v,
 
 /*
  * Kernel-path selection, for tests and measurements. LA_PATH_AUTO (the
- * default) takes the tensor-core (tcgen05) kernels where they apply (bf16,
- * dk = dv in {64, 128}) and the CUDA-core kernels elsewhere; LA_PATH_SIMT
+ * default) takes the tensor-core (tcgen05) kernels where they apply (bf16;
+ * forward dk = dv in {64, 128}, backward dk = dv = 64, causal or not) and the
+ * CUDA-core kernels elsewhere; LA_PATH_SIMT
  * forces the CUDA-core kernels everywhere. Process-wide; returns the
  * previous setting, or -1 for an unknown value (setting unchanged).
  */

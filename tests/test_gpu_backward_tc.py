@@ -1,9 +1,11 @@
-"""Tensor-core backward (bf16, dk = dv = 64, causal) vs the fp64 oracle.
+"""Tensor-core backward (bf16, dk = dv = 64, causal and non-causal) vs the
+fp64 oracle.
 
 Shapes span one token, one partial chunk, exact chunk boundaries, a ragged
 tail, segments of one and of several chunks (the segment plan depends on B*H
 and N), so that both sweeps, the forward prefix scan and the reverse suffix
-scan are all exercised.
+scan are all exercised; non-causal, the state pass over every segment and
+passes A (dq, segment (R, r) records) and B (dk, dv from their total).
 """
 
 import numpy as np
@@ -28,20 +30,20 @@ def _lib():
     la.la_set_path(la.LA_PATH_AUTO)
 
 
-def _grads(B, H, N, seed, eps=1e-6):
+def _grads(B, H, N, seed, eps=1e-6, causal=True):
     import torch
     q, k, v = synth.qkv(B, H, N, 64, 64, seed=seed, dtype="bf16")
     g = synth.upstream_grad(B, H, N, 64, seed=seed, dtype="bf16")
     got = la.backward(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
-                      to_dev(g, "bf16"), causal=True, eps=eps)
+                      to_dev(g, "bf16"), causal=causal, eps=eps)
     torch.cuda.synchronize()
-    want = orc.backward_recurrent(q, k, v, g, causal=True, eps=eps)
+    want = orc.backward_recurrent(q, k, v, g, causal=causal, eps=eps)
     return got, want
 
 
 def test_backward_path_is_tensor_core():
     assert la.la_backward_path(64, 64, la.LA_BF16, True) == 1
-    assert la.la_backward_path(64, 64, la.LA_BF16, False) == 0
+    assert la.la_backward_path(64, 64, la.LA_BF16, False) == 1
     assert la.la_backward_path(64, 64, la.LA_F32, True) == 0
     assert la.la_backward_path(128, 128, la.LA_BF16, True) == 0
 
@@ -66,7 +68,27 @@ def test_backward_tensor_core(B, H, N):
     assert max(errs) <= TOL["bf16"], errs
 
 
-def test_backward_tensor_core_matches_cuda_core():
+@pytest.mark.parametrize("B,H,N", [
+    (1, 1, 1),        # single token
+    (1, 1, 100),      # one partial chunk
+    (2, 1, 129),      # one chunk plus one token
+    (1, 2, 300),      # ragged, one segment per chunk
+    (1, 1, 4096),     # 32 one-chunk segments: 32 records in every total
+    (4, 8, 1000),     # segments of two chunks, ragged last segment
+    (2, 16, 3000),    # segments of six chunks
+])
+def test_backward_tensor_core_noncausal(B, H, N):
+    n0 = la.la_launch_count()
+    got, want = _grads(B, H, N, seed=1900 + N + B * H, causal=False)
+    # state pass, pass A, pass B
+    assert la.la_launch_count() - n0 == 3
+    assert la.la_device_status(True) == la.LA_OK
+    errs = grad_errors(got, want)
+    assert max(errs) <= TOL["bf16"], errs
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_tensor_core_matches_cuda_core(causal):
     """Both paths implement the same gradient; on the same bf16 inputs they
     agree to the bf16 tolerance (each is also checked against the oracle)."""
     import torch
@@ -74,10 +96,10 @@ def test_backward_tensor_core_matches_cuda_core():
     q, k, v = synth.qkv(B, H, N, 64, 64, seed=31, dtype="bf16")
     g = synth.upstream_grad(B, H, N, 64, seed=31, dtype="bf16")
     args = [to_dev(x, "bf16") for x in (q, k, v, g)]
-    tc = [t.clone() for t in la.backward(*args, causal=True)]
+    tc = [t.clone() for t in la.backward(*args, causal=causal)]
     la.la_set_path(la.LA_PATH_SIMT)
     try:
-        simt = [to_host(t) for t in la.backward(*args, causal=True)]
+        simt = [to_host(t) for t in la.backward(*args, causal=causal)]
         torch.cuda.synchronize()
     finally:
         la.la_set_path(la.LA_PATH_AUTO)
@@ -85,9 +107,10 @@ def test_backward_tensor_core_matches_cuda_core():
     assert max(errs) <= TOL["bf16"], errs
 
 
-def test_backward_tensor_core_eps_zero():
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_tensor_core_eps_zero(causal):
     """eps = 0 is allowed; phi > 0 keeps every denominator positive."""
-    got, want = _grads(1, 2, 513, seed=4242, eps=0.0)
+    got, want = _grads(1, 2, 513, seed=4242, eps=0.0, causal=causal)
     assert la.la_device_status(True) == la.LA_OK
     errs = grad_errors(got, want)
     assert max(errs) <= TOL["bf16"], errs
