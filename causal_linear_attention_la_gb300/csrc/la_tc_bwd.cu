@@ -1001,21 +1001,31 @@ template <int D>
 struct NA {
   static_assert(D == 64, "the tensor-core backward is laid out for D = 64");
   static constexpr int TILE = BOX;
-  static constexpr int ST = 4;                        // stages of Q, G
+  // stages of Q, G: a stage lives from its load through the row pass, the
+  // MMAs, the dq epilogue and the store (~5 us), so six keep the loads going
+  static constexpr int ST = 6;
   static constexpr int OFF_G = TILE;
   static constexpr int STAGE = 2 * TILE;
-  static constexpr int OFF_SBUF = ST * STAGE;         // bf16 S_N^T copy, D rows
-  static constexpr int OFF_ZN = OFF_SBUF + D * 128;   // [D] z_N
+  // bf16 [S_N^T ; z_hi ; z_lo ; 0] (D + 16 rows): O and den from one MMA
+  static constexpr int NO = D + 16;
+  static constexpr uint32_t G_NO = NO;
+  static constexpr int OFF_SBUF = ST * STAGE;
+  static constexpr int OFF_ZN = OFF_SBUF + NO * 128;  // [D] z_N (fp32)
   static constexpr int OFF_BARR = OFF_ZN + D * 4;     // [ST][C] b_t
   static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
-  static constexpr int NBAR = 5 * ST + 8 + 2;
+  static constexpr int NBAR = 6 * ST + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
-  static constexpr uint32_t COL_S = 0;                // S_N^T (M = D layout)
-  __host__ __device__ static constexpr uint32_t col_oq(int ob) { return D + D * ob; }  // O, then dQ in place
-  static constexpr uint32_t COL_R = 3 * D;            // R (M = D layout)
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t COL_S = 0;                // S_N^T (M = D layout), start only
+  static constexpr uint32_t COL_R = 64;               // R (M = D layout)
+  // [O | den parts] of a chunk (free once its row pass is done) and dQ of a
+  // chunk (free once its epilogue is done), each double-buffered
+  __host__ __device__ static constexpr uint32_t col_o(int ob) { return 128 + G_NO * ob; }
+  __host__ __device__ static constexpr uint32_t col_dq(int ob) { return 128 + 2 * G_NO + D * ob; }
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(col_dq(1) + D <= TMEM_COLS, "tensor memory budget");
+  static constexpr int THREADS = 448;
 };
 
 struct NcBwdParams {
@@ -1026,11 +1036,12 @@ struct NcBwdParams {
   int* status;
 };
 
-// Pass A. Warps 0-3: phi(Q), the S_N / z_N sums and copies, r sums, the R
-// record; warps 4-7: den, the row pass (a, b) and the dq epilogue; warp 8 TMA
-// (Q, G in; dq out from the dead G tile); warp 9 TMEM and MMA.
+// Pass A (448 threads). Warps 0-3: phi(Q), the S_N / z_N sums and copy, the
+// r sums and the (R, r) record; warps 4-7: the row pass (a, b) from
+// [O | den]; warps 8-11: the dq epilogue; warp 12 TMA (Q, G in; dq out from
+// the dead G tile); warp 13 TMEM and MMA.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
 tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
                    const __grid_constant__ CUtensorMap map_dq, const NcBwdParams prm) {
   using G = NA<D>;
@@ -1044,13 +1055,14 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
   uint64_t* full = bars;               // [ST]
   uint64_t* phi_done = bars + ST;      // [ST]
   uint64_t* empty = bars + 2 * ST;     // [ST] MMAs of the stage's chunk done
-  uint64_t* ost_full = bars + 3 * ST;  // [ST] dq staged (group B)
+  uint64_t* ost_full = bars + 3 * ST;  // [ST] dq staged (group D)
   uint64_t* rdone = bars + 4 * ST;     // [ST] r sums read the stage (group A)
-  uint64_t* x = bars + 5 * ST;
+  uint64_t* b_ready = bars + 5 * ST;   // [ST] b of the stage's chunk written (group B)
+  uint64_t* x = bars + 6 * ST;
   uint64_t* o_full = x;                // [2]
   uint64_t* a_ready = x + 2;           // [2]
   uint64_t* dq_full = x + 4;           // [2]
-  uint64_t* oq_empty = x + 6;          // [2]
+  uint64_t* dq_empty = x + 6;          // [2]
   uint64_t* s_ready = x + 8;
   uint64_t* mma_fin = x + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::OFF_MISC);
@@ -1079,19 +1091,20 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
       mbar_init(&empty[i], 1);
       mbar_init(&ost_full[i], 128);
       mbar_init(&rdone[i], 128);
+      mbar_init(&b_ready[i], 128);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&o_full[i], 1);
       mbar_init(&a_ready[i], 128);
       mbar_init(&dq_full[i], 1);
-      mbar_init(&oq_empty[i], 128);
+      mbar_init(&dq_empty[i], 128);
     }
     mbar_init(s_ready, 128);
     mbar_init(mma_fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, G::TMEM_COLS);
     tmem_relinquish();
   }
@@ -1100,7 +1113,7 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
@@ -1136,42 +1149,51 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
       for (int c = max(0, issued - ST); c < issued; ++c)
         mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);   // O = phiQ S_N (S^T copy K-major)
-      constexpr uint32_t id_as = make_idesc_bf16(128, D, false, true);    // dQ = a S_N^T (copy MN-major)
-      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);       // R += phiQ^T a
+      constexpr uint32_t id_qs = make_idesc_bf16(128, G::NO, false, false);  // [O | den] = phiQ [S_N^T ; z]^T
+      constexpr uint32_t id_as = make_idesc_bf16(128, D, false, true);       // dQ = a S_N^T (copy MN-major)
+      constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);          // R += phiQ^T a
       const uint32_t sb = smem_u32(sbuf);
       const uint64_t dsk = make_sdesc(sb, 16, 1024, kSwizzle128B);
       const uint64_t dsm = make_sdesc(sb, D * 128, 1024, kSwizzle128B);
+      // [O | den] of chunk c + 1 is issued before the wait for chunk c's row
+      // pass, so that the row pass of c + 1 can follow that of c at once; its
+      // buffer was last read by the row pass of c - 1, which the issuer has
+      // already waited for
+      auto issue_o = [&](int c) -> bool {
+        const int s = c % ST, ob = c & 1;
+        if (!mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs)) return false;
+        tc_fence_after();
+        const uint64_t dq = make_sdesc(smem_u32(sm + s * G::STAGE), 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + G::col_o(ob), sdesc_add(dq, k * 32), sdesc_add(dsk, k * 32), id_qs, k > 0);
+        tc_commit(&o_full[ob]);
+        return true;
+      };
       bool ok = mbar_wait(s_ready, 0, abort_flag, kTimeoutNs);
+      if (ok && nchunks > 0) ok = issue_o(0);
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST, ob = c & 1;
         const uint32_t qa = smem_u32(sm + s * G::STAGE), ga = qa + G::OFF_G;
-        const uint32_t oq = tmem + G::col_oq(ob);
-        ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
-        if (ok && c >= 2) ok = mbar_wait(&oq_empty[ob], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t dq = make_sdesc(qa, 16, 1024, kSwizzle128B);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss(oq, sdesc_add(dq, k * 32), sdesc_add(dsk, k * 32), id_qs, k > 0);
-        tc_commit(&o_full[ob]);
+        if (c + 1 < nchunks && !(ok = issue_o(c + 1))) break;
         ok = mbar_wait(&a_ready[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
+        if (ok && c >= 2) ok = mbar_wait(&dq_empty[ob], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         const uint64_t dg = make_sdesc(ga, 16, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(oq, sdesc_add(dg, k * 32), sdesc_add(dsm, k * 2048), id_as, k > 0);
+          mma_ss(tmem + G::col_dq(ob), sdesc_add(dg, k * 32), sdesc_add(dsm, k * 2048), id_as, k > 0);
         const uint64_t dqm = make_sdesc(qa, BOX, 1024, kSwizzle128B);
         const uint64_t dgm = make_sdesc(ga, BOX, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           mma_ss(tmem + G::COL_R, sdesc_add(dqm, k * 2048), sdesc_add(dgm, k * 2048), id_tt,
                  (c > 0 || k > 0) ? 1u : 0u);
+        // dq_full covers the R MMA too: the epilogue overwrites a
         tc_commit(&dq_full[ob]);
         tc_commit(&empty[s]);
       }
@@ -1192,11 +1214,20 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     griddep_wait();
     sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row);
     copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf, row);
-    for (int i = t; i < D; i += 128) {
+    // z_N: fp32 for the epilogue; as bf16 hi + lo rows D, D + 1 of the MMA
+    // operand (den = phi(q).z_hi + phi(q).z_lo, about 16 bits), rows D + 2 ..
+    // zero
+    if (t < D) {
       float acc = 0.f;
-      for (int p = 0; p < nrec; ++p) acc += recs[p * rstride + D * D + i];
-      zn[i] = acc;
+      for (int p = 0; p < nrec; ++p) acc += recs[p * rstride + D * D + t];
+      zn[t] = acc;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+      *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D, t >> 3) + 2 * (t & 7)) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D + 1, t >> 3) + 2 * (t & 7)) = lo;
     }
+    for (int i = t; i < (G::NO - D - 2) * 8; i += 128)
+      *reinterpret_cast<uint4*>(sbuf + sw128(D + 2 + (i >> 3), i & 7)) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(s_ready);
@@ -1230,35 +1261,50 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
       tc_fence_after();
       store_state_from_tmem<D>(rec_out, lane_addr, G::COL_R, row);
     }
-  } else {
-    // ---------------- group B: den, a and b, dq ----------------
+  } else if (warp < 8) {
+    // ---------------- group B: a and b from [O | den] ----------------
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    bool ok = mbar_wait(s_ready, 0, abort_flag, kTimeoutNs);
+    bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST, ob = c & 1;
       uint8_t* stg = sm + s * G::STAGE;
-      ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
-      if (!ok) break;
-      const float inv_den = 1.f / (phiq_dot<D>(stg, r, zn) + prm.eps);
       ok = mbar_wait(&o_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const float beta = grad_row_pass<D>(lane_addr + G::col_oq(ob), stg + G::OFF_G, r, inv_den);
-      const float b = -beta * inv_den * inv_den;
-      barr[s * C + r] = b;
+      uint32_t dz[2];
+      tmem_ld2(lane_addr + G::col_o(ob) + D, dz);
+      tmem_ld_wait();
+      const float inv_den = 1.f / (__uint_as_float(dz[0]) + __uint_as_float(dz[1]) + prm.eps);
+      const float beta = grad_row_pass<D>(lane_addr + G::col_o(ob), stg + G::OFF_G, r, inv_den);
+      barr[s * C + r] = -beta * inv_den * inv_den;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&a_ready[ob]);
-      ok = mbar_wait(&dq_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
+      mbar_arrive(&b_ready[s]);
+    }
+  } else {
+    // ---------------- group D: dq ----------------
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    bool ok = mbar_wait(s_ready, 0, abort_flag, kTimeoutNs);     // zn
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST, ob = c & 1;
+      uint8_t* stg = sm + s * G::STAGE;
+      // b of the chunk from group B (per stage: group B cannot refill the
+      // stage before this epilogue is done); then dQ (and the R update,
+      // which reads a) done
+      ok = mbar_wait(&b_ready[s], (c / ST) & 1, abort_flag, kTimeoutNs) &&
+           mbar_wait(&dq_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      // dq staged in the dead G tile (a has been read by the MMAs); the
-      // producer stores it before refilling the stage
-      grad_epilogue<D>(lane_addr + G::col_oq(ob), stg, r, b, zn, stg + G::OFF_G);
+      // dq staged in the dead G tile; the producer stores it before
+      // refilling the stage
+      grad_epilogue<D>(lane_addr + G::col_dq(ob), stg, r, barr[s * C + r], zn, stg + G::OFF_G);
       tc_fence_before();
-      mbar_arrive(&oq_empty[ob]);
+      mbar_arrive(&dq_empty[ob]);
       fence_proxy_async_smem();
       mbar_arrive(&ost_full[s]);
     }
@@ -1268,7 +1314,7 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
   if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
   }
@@ -1587,7 +1633,7 @@ cudaError_t launch_backward_nc(const BwdArgs& a) {
   if (e != cudaSuccess) return e;
   NcBwdParams pa{a.N, a.plan.P, a.plan.seg_len, a.plan.F, a.eps, a.ws_state, a.ws_rev, status};
   prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
-  e = launch_dependent(tc_bwd_nc_a_kernel<D>, a.BH * a.plan.P, 320, smema, a.stream, mq, mg, mdq, pa);
+  e = launch_dependent(tc_bwd_nc_a_kernel<D>, a.BH * a.plan.P, NA<D>::THREADS, smema, a.stream, mq, mg, mdq, pa);
   prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
   if (e != cudaSuccess) return e;
   note_launch();
