@@ -163,6 +163,7 @@ KERNEL_SOURCES = {
     "fwd_output": ["la_tc_fwd.cu"] + _COMMON_TC,
     "bwd": ["la_tc_bwd.cu"] + _COMMON_TC,
     "decode": ["la_decode.cu", "la_internal.cuh"],
+    "variants": ["la_variants.cu", "la_variants.cuh", "la_internal.cuh"],
 }
 
 
@@ -600,7 +601,7 @@ def main():
                              "frac": gbs / peaks["hbm_gbs"],
                              "kernel": {"decay": "decay_tokens", "delta": "delta_tokens"}.get(
                                  ws.get("variant"), "decode"),
-                             "traffic": ncu_traffic("decode_" + name)},
+                             "traffic": ncu_traffic(("variants_" if ws.get("variant") else "decode_") + name)},
                 "bytes_per_step": call_bytes,
                 "prefill_s_eager": rr["prefill_s"], "gpu_launches": rr["launches"],
                 "l2": f"state {decode_state_bytes(ws) / 2 / 1e6:.0f} MB > L2",

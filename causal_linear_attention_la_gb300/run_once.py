@@ -2,9 +2,11 @@
 
     python -m causal_linear_attention_la_gb300.run_once --workload fwd --B 4 --H 8 --N 4096 --d 64 --calls 2
 
-Workloads: fwd (la_forward), bwd (la_forward then la_backward), decode
-(la_decode_step on zero-initialised states, or la_decode_steps with --tokens T). Inputs are seeded normal
-values scaled by 1/sqrt(d), bf16 unless --f32.
+Workloads: fwd (la_forward; la_forward_decay with --decay), bwd (la_forward
+then la_backward), decode (la_decode_step on zero-initialised states, or
+la_decode_steps with --tokens T; --variant decay|delta for the gated and
+delta-rule updates). Inputs are seeded normal values scaled by 1/sqrt(d),
+bf16 unless --f32; decay factors 0.9 .. 0.999 over the heads.
 """
 
 import argparse
@@ -25,6 +27,9 @@ def main(argv=None):
     ap.add_argument("--calls", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=1, help="decode: tokens per call (la_decode_steps when > 1)")
     ap.add_argument("--noncausal", action="store_true")
+    ap.add_argument("--decay", action="store_true", help="fwd: decay-gated forward")
+    ap.add_argument("--variant", choices=["plain", "decay", "delta"], default="plain",
+                    help="decode: state update variant")
     ap.add_argument("--f32", action="store_true")
     args = ap.parse_args(argv)
     from causal_linear_attention_la_gb300.build import build
@@ -38,10 +43,19 @@ def main(argv=None):
         return (torch.randn(shape, generator=g, device="cuda") * scale).to(dt)
 
     causal = not args.noncausal
+    alpha = torch.linspace(0.9, 0.999, H, device="cuda")
     if args.workload == "decode":
         S = torch.zeros((B, H, d, d), device="cuda")
         z = torch.zeros((B, H, d), device="cuda")
-        if args.tokens > 1:
+        if args.variant != "plain":
+            T = args.tokens
+            q, k, v = rnd(B, H, T, d), rnd(B, H, T, d), rnd(B, H, T, d)
+            for _ in range(args.calls):
+                if args.variant == "decay":
+                    la.decode_steps_decay(S, z, q, k, v, alpha)
+                else:
+                    la.decode_steps_delta(S, q, k, v)
+        elif args.tokens > 1:
             T = args.tokens
             q, k, v = rnd(B, H, T, d), rnd(B, H, T, d), rnd(B, H, T, d)
             for _ in range(args.calls):
@@ -54,7 +68,10 @@ def main(argv=None):
         q, k, v = rnd(B, H, N, d), rnd(B, H, N, d), rnd(B, H, N, d)
         gout = rnd(B, H, N, d, scale=1.0)
         for _ in range(args.calls):
-            la.forward(q, k, v, causal=causal)
+            if args.decay:
+                la.forward_decay(q, k, v, alpha)
+            else:
+                la.forward(q, k, v, causal=causal)
             if args.workload == "bwd":
                 la.backward(q, k, v, gout, causal=causal)
     torch.cuda.synchronize()
