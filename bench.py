@@ -7,9 +7,11 @@ Prints ONE JSON line (rank 0). The headline workload is the causal forward
 B=4 H=8 N=4096 dk=dv=64 bf16 (one step = one la_forward over the batch: the
 per-segment state sums, the segment scan and the chunked output kernel).
 `value` is tokens/s (a token = one position of one sequence, all heads) with
-inputs resident in HBM; `e2e` is the same metric through the public Python
-call with pinned host buffers and the host<->device copies inside the timed
-region. The other workloads of the method are measured in the same run and
+inputs resident in HBM; `e2e` is the same metric through the host-buffer
+C-ABI call la_forward_host (pinned host q, k, v, out; every step's
+host<->device copies inside the timed region; sequence groups overlap their
+copies with their neighbours' compute, and the unpipelined call is reported
+beside it). The other workloads of the method are measured in the same run and
 reported under "sections": the causal forward B=2 H=16 N=32768 d=128, the
 decode step on B=64 x H=32 fp32 states of d=128 (1024 steps in a CUDA graph),
 the same decode with 16 tokens per call (64 calls of la_decode_steps), the
@@ -74,6 +76,7 @@ WORKLOADS = {
 }
 MAIN = "fwd_b4_h8_n4096_d64"
 EPS = 1e-6
+E2E_SLICES = 2          # la_forward_host: sequence groups whose copies overlap compute (best measured)
 
 
 # ---------------------------------------------------------------------------
@@ -398,9 +401,12 @@ def run_decode(w, K, W, barrier):
     return dict(ms=ms, launches=launches, steps=T, prefill_s=prefill_s)
 
 
-def run_e2e(w, K, W):
-    """Same forward metric through la.forward with pinned host buffers:
-    per step H2D of q, k, v, the call, D2H of out; timed with CUDA events."""
+def run_e2e(w, K, W, slices=E2E_SLICES):
+    """Same forward metric through the host-buffer C-ABI call la_forward_host:
+    per step the H2D copies of q, k, v from pinned host memory, the forward,
+    and the D2H copy of out, timed with CUDA events on the calling stream.
+    ``slices`` groups of sequences overlap their copies with the compute of
+    their neighbours (1: copy, compute, copy in sequence)."""
     import torch
     import causal_linear_attention_la_gb300 as la
     B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
@@ -410,19 +416,11 @@ def run_e2e(w, K, W):
     hk = (torch.randn((B, H, N, dk), generator=g) * dk ** -0.5).to(torch.bfloat16).pin_memory()
     hv = (torch.randn((B, H, N, dv), generator=g) * dv ** -0.5).to(torch.bfloat16).pin_memory()
     ho = torch.empty((B, H, N, dv), dtype=torch.bfloat16).pin_memory()
-    dq = torch.empty_like(hq, device="cuda")
-    dk_ = torch.empty_like(hk, device="cuda")
-    dv_ = torch.empty_like(hv, device="cuda")
-    do = torch.empty_like(ho, device="cuda")
-    ws = torch.empty(max(1, la.la_forward_workspace_size(B, H, N, dk, dv, w["causal"], la.LA_BF16)),
+    ws = torch.empty(max(1, la.la_forward_host_workspace_size(B, H, N, dk, dv, w["causal"], la.LA_BF16, slices)),
                      dtype=torch.uint8, device="cuda")
 
     def step():
-        dq.copy_(hq, non_blocking=True)
-        dk_.copy_(hk, non_blocking=True)
-        dv_.copy_(hv, non_blocking=True)
-        la.forward(dq, dk_, dv_, causal=w["causal"], eps=EPS, out=do, workspace=ws)
-        ho.copy_(do, non_blocking=True)
+        la.forward_host(hq, hk, hv, causal=w["causal"], eps=EPS, out=ho, slices=slices, workspace=ws)
 
     for _ in range(W):
         step()
@@ -437,7 +435,7 @@ def run_e2e(w, K, W):
     ms = e0.elapsed_time(e1)
     h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
     d2h = ho.numel() * 2
-    return dict(ms=ms, h2d=h2d, d2h=d2h)
+    return dict(ms=ms, h2d=h2d, d2h=d2h, slices=slices)
 
 
 # ---------------------------------------------------------------------------
@@ -561,6 +559,7 @@ def main():
     achieved = alg_bytes / (out_span["avg_ms"] / 1e3) / 1e9
     e2e = run_e2e(w, K, W)
     e2e_ms = max_over_ranks(e2e["ms"])
+    e2e_serial_ms = max_over_ranks(run_e2e(w, K, W, slices=1)["ms"])
 
     sections = {}
     wanted = list(WORKLOADS) if args.sections == "all" else (
@@ -646,7 +645,9 @@ def main():
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_threads,
                              "kind": "oracle", "sample": cpu_desc},
             "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "call": f"la_forward_host, {e2e['slices']} sequence groups",
+                    "unpipelined_value": world * tokens / (e2e_serial_ms / 1e3)},
             "gpu_launches": r["launches"],
             "clocks": sampler.summary(),
             "path": {"forward": ["cuda-core", "tensor-core"][la.la_forward_path(w["dk"], w["dv"], la.LA_BF16)],

@@ -31,6 +31,7 @@ __all__ = [
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
+    "la_forward_host", "la_forward_host_workspace_size", "forward_host",
     "forward", "decode_step", "decode_steps", "backward",
     "decode_steps_decay", "decode_steps_delta", "state_copy", "forward_decay",
 ]
@@ -51,6 +52,7 @@ exported_symbols = (
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
     "la_device_status", "la_forward_noalloc",
+    "la_forward_host_workspace_size", "la_forward_host",
 )
 
 
@@ -92,6 +94,11 @@ def lib():
     h.la_forward.restype = _c_int
     h.la_forward.argtypes = ([_c_void] * 4 + [_c_int] * 6 + [_c_float, _c_int]
                              + [_c_void, _c_void, _c_void, _c_size, _c_void])
+    h.la_forward_host_workspace_size.restype = _c_size
+    h.la_forward_host_workspace_size.argtypes = [_c_int] * 8
+    h.la_forward_host.restype = _c_int
+    h.la_forward_host.argtypes = ([_c_void] * 4 + [_c_int] * 6 + [_c_float, _c_int, _c_int]
+                                  + [_c_void, _c_size, _c_void])
     h.la_decode_step.restype = _c_int
     h.la_decode_step.argtypes = [_c_void] * 6 + [_c_int] * 4 + [_c_float, _c_int, _c_void]
     h.la_decode_steps.restype = _c_int
@@ -154,6 +161,16 @@ def la_forward(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype, S_final,
     return lib().la_forward(q, k, v, out, B, H, N, dk, dv, int(causal), eps,
                             dtype, S_final, z_final, workspace,
                             workspace_bytes, stream)
+
+
+def la_forward_host_workspace_size(B, H, N, dk, dv, causal, dtype, slices):
+    return lib().la_forward_host_workspace_size(B, H, N, dk, dv, int(causal), dtype, slices)
+
+
+def la_forward_host(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype, slices,
+                    workspace, workspace_bytes, stream):
+    return lib().la_forward_host(q, k, v, out, B, H, N, dk, dv, int(causal), eps,
+                                 dtype, slices, workspace, workspace_bytes, stream)
 
 
 def la_forward_noalloc(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype,
@@ -288,6 +305,34 @@ def forward(q, k, v, causal=True, eps=1e-6, return_state=False, out=None,
                       workspace.data_ptr(), workspace.numel(), _stream_ptr(q)))
     if return_state:
         return out, S, z
+    return out
+
+
+def forward_host(q, k, v, causal=True, eps=1e-6, out=None, slices=2, workspace=None,
+                 device=None):
+    """la_forward_host: q, k [B,H,N,dk], v [B,H,N,dv] CPU tensors (pinned for
+    overlap), out a CPU tensor [B,H,N,dv] (allocated pinned when None). The
+    copies and the forward are enqueued on the current stream of ``device``;
+    synchronise it before reading ``out``."""
+    import torch
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, cuda=False)
+        if t.is_cuda:
+            raise ValueError(f"{n} must be a host tensor")
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=q.dtype).pin_memory()
+    _need(out, "out", q.dtype, cuda=False)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws_bytes = la_forward_host_workspace_size(B, H, N, dk, dv, causal, code, slices)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check(la_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           B, H, N, dk, dv, causal, eps, code, slices,
+                           workspace.data_ptr(), workspace.numel(),
+                           torch.cuda.current_stream(dev).cuda_stream))
     return out
 
 

@@ -224,6 +224,60 @@ SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool c
   return plan;
 }
 
+// la_forward_host: internal copy streams and events, created on first use
+// for the current device and reused under a lock (enqueueing is short).
+struct HostPipe {
+  std::mutex mu;
+  int device = -1;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+};
+HostPipe g_pipe;
+
+cudaError_t host_pipe_ready_locked(int device) {
+  if (g_pipe.device == device) return cudaSuccess;
+  if (g_pipe.device >= 0) return cudaErrorInvalidDevice;   // one device per process
+  cudaError_t e = cudaStreamCreateWithFlags(&g_pipe.h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_pipe.d2h, cudaStreamNonBlocking);
+  cudaEvent_t* evs[8] = {&g_pipe.start, &g_pipe.end, &g_pipe.in[0], &g_pipe.in[1],
+                         &g_pipe.done[0], &g_pipe.done[1], &g_pipe.freed[0], &g_pipe.freed[1]};
+  for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+  if (e == cudaSuccess) g_pipe.device = device;
+  return e;
+}
+
+// Staging layout of la_forward_host: two slots of [q | k | v | out] for the
+// largest slice, then one la_forward workspace; regions 256-byte aligned.
+struct HostLayout {
+  int S, base, extra;            // slices; sequences per slice: base (+1 for the first `extra`)
+  size_t qb, vb, slot, fwd_off, fwd_bytes, total;
+};
+
+HostLayout host_layout(long long BH, int N, int dk, int dv, int causal, la_dtype dtype, int slices) {
+  HostLayout L{};
+  L.S = (int)(slices < 1 ? 1 : (slices > BH ? BH : slices));
+  if (L.S < 1) L.S = 1;
+  L.base = (int)(BH / L.S);
+  L.extra = (int)(BH % L.S);
+  const long long maxcnt = L.base + (L.extra ? 1 : 0);
+  const size_t elt = dtype == LA_BF16 ? 2 : 4;
+  L.qb = align_up((size_t)maxcnt * N * dk * elt, 256);
+  L.vb = align_up((size_t)maxcnt * N * dv * elt, 256);
+  L.slot = 2 * L.qb + 2 * L.vb;
+  size_t fw = 0;
+  for (int extra = 0; extra <= (L.extra ? 1 : 0); ++extra) {
+    const int cnt = L.base + extra;
+    if (cnt <= 0) continue;
+    const size_t w = la_forward_workspace_size(1, cnt, N, dk, dv, causal, dtype);
+    fw = w > fw ? w : fw;
+  }
+  L.fwd_off = 2 * L.slot;
+  L.fwd_bytes = fw;
+  L.total = L.fwd_off + align_up(fw, 256);
+  return L;
+}
+
 }  // namespace la
 
 using namespace la;
@@ -333,6 +387,90 @@ la_status la_forward(const void* q, const void* k, const void* v, void* out,
   prof_end(LA_SPAN_FWD_OUTPUT, stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward (output)");
   return LA_OK;
+}
+
+size_t la_forward_host_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype,
+                                      int slices) {
+  if (B <= 0 || H <= 0 || N <= 0 || !head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16))
+    return 0;
+  return host_layout((long long)B * H, N, dk, dv, causal, dtype, slices).total;
+}
+
+la_status la_forward_host(const void* q, const void* k, const void* v, void* out, int B, int H, int N, int dk,
+                          int dv, int causal, float eps, la_dtype dtype, int slices, void* workspace,
+                          size_t workspace_bytes, la_stream_t stream_) {
+  bool empty = false;
+  la_status st = check_sizes(B, H, N, dk, dv, dtype, eps, &empty);
+  if (st != LA_OK) return st;
+  if (slices < 1) return fail(LA_ERR_INVALID_ARG, "slices must be >= 1");
+  if (empty) return LA_OK;
+  if (!q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be non-NULL");
+  const long long BH = (long long)B * H;
+  const HostLayout L = host_layout(BH, N, dk, dv, causal, dtype, slices);
+  if (workspace == nullptr || workspace_bytes < L.total)
+    return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", L.total,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(LA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward_host (device)");
+  std::lock_guard<std::mutex> lk(g_pipe.mu);
+  e = host_pipe_ready_locked(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward_host (copy streams)");
+  cudaStream_t s = (cudaStream_t)stream_;
+  const size_t elt = dtype == LA_BF16 ? 2 : 4;
+  char* ws = (char*)workspace;
+  // the copy streams start after the work already on `stream`
+  e = cudaEventRecord(g_pipe.start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(g_pipe.h2d, g_pipe.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(g_pipe.d2h, g_pipe.start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward_host (start)");
+  la_status result = LA_OK;
+  long long seq0 = 0;
+  for (int i = 0; i < L.S; ++i) {
+    const int cnt = L.base + (i < L.extra ? 1 : 0);
+    const int slot = i & 1;
+    char* sq = ws + slot * L.slot;
+    char* sk = sq + L.qb;
+    char* sv = sk + L.qb;
+    char* so = sv + L.vb;
+    const size_t nq = (size_t)cnt * N * dk * elt, nv = (size_t)cnt * N * dv * elt;
+    const size_t oq = (size_t)seq0 * N * dk * elt, ov = (size_t)seq0 * N * dv * elt;
+    // the slot was last read by slice i - 2's compute and output copy
+    if (i >= 2) e = cudaStreamWaitEvent(g_pipe.h2d, g_pipe.freed[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sq, (const char*)q + oq, nq, cudaMemcpyHostToDevice, g_pipe.h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sk, (const char*)k + oq, nq, cudaMemcpyHostToDevice, g_pipe.h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sv, (const char*)v + ov, nv, cudaMemcpyHostToDevice, g_pipe.h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(g_pipe.in[slot], g_pipe.h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, g_pipe.in[slot], 0);
+    if (e != cudaSuccess) {
+      result = cuda_fail(e, "la_forward_host (input copies)");
+      break;
+    }
+    st = la_forward(sq, sk, sv, so, 1, cnt, N, dk, dv, causal, eps, dtype, nullptr, nullptr, ws + L.fwd_off,
+                    L.fwd_bytes, stream_);
+    if (st != LA_OK) {
+      result = st;
+      break;
+    }
+    e = cudaEventRecord(g_pipe.done[slot], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(g_pipe.d2h, g_pipe.done[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((char*)out + ov, so, nv, cudaMemcpyDeviceToHost, g_pipe.d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(g_pipe.freed[slot], g_pipe.d2h);
+    if (e != cudaSuccess) {
+      result = cuda_fail(e, "la_forward_host (output copy)");
+      break;
+    }
+    seq0 += cnt;
+  }
+  // join: `stream` continues after the last output copy (also on an error,
+  // so that nothing enqueued here outlives the caller's view of the stream)
+  e = cudaEventRecord(g_pipe.end, g_pipe.d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, g_pipe.end, 0);
+  if (e == cudaSuccess) e = cudaEventRecord(g_pipe.end, g_pipe.h2d);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, g_pipe.end, 0);
+  if (e != cudaSuccess && result == LA_OK) result = cuda_fail(e, "la_forward_host (join)");
+  return result;
 }
 
 la_status la_profile_enable(int on) {

@@ -115,6 +115,41 @@ LA_API la_status la_forward(const void* q, const void* k, const void* v, void* o
                      la_stream_t stream);
 
 /*
+ * la_forward on inputs and outputs in HOST memory: the call copies q, k, v to
+ * the device, runs the forward and copies out back, overlapping the three.
+ * The B*H sequences are split into `slices` groups of whole sequences
+ * (contiguous in the [B,H,N,d] layout); slice i's host-to-device copies run on
+ * an internal copy stream while slice i-1 is computed on `stream` and slice
+ * i-2's output returns on a second internal copy stream, through two device
+ * staging slots in `workspace`. The outputs equal la_forward's on the same
+ * inputs (each slice is an independent la_forward call over its sequences).
+ *
+ * q, k      [B,H,N,dk] dtype, host memory, in
+ * v         [B,H,N,dv] dtype, host memory, in
+ * out       [B,H,N,dv] dtype, host memory, out (must not alias the inputs)
+ * slices    >= 1; clamped to B*H. 1 runs copy, compute, copy in sequence.
+ * workspace device scratch of at least la_forward_host_workspace_size(...)
+ *           bytes (the two staging slots and one la_forward workspace),
+ *           16-byte aligned.
+ * stream    work is ordered after the work already on `stream`, and the
+ *           call's last copy to `out` is complete when `stream` reaches the
+ *           point after this call (the internal streams join it there).
+ *
+ * Page-locked (pinned) host memory gives the overlap; pageable memory works
+ * but each copy then blocks the calling thread. No final state is returned
+ * (use la_forward for S_final, z_final). Not for CUDA-graph capture. Errors
+ * as la_forward; on an error after the first enqueue, work already enqueued
+ * still completes and `stream` still joins the internal streams.
+ */
+LA_API size_t la_forward_host_workspace_size(int B, int H, int N, int dk, int dv,
+                                              int causal, la_dtype dtype, int slices);
+LA_API la_status la_forward_host(const void* q, const void* k, const void* v, void* out,
+                                 int B, int H, int N, int dk, int dv, int causal,
+                                 float eps, la_dtype dtype, int slices,
+                                 void* workspace, size_t workspace_bytes,
+                                 la_stream_t stream);
+
+/*
  * One recurrent inference step per (batch, head), in place on the state:
  *
  *   S <- S + phi(k) v^T;  z <- z + phi(k);  out = phi(q)^T S / (phi(q)^T z + eps)

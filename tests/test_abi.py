@@ -99,6 +99,34 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(H=0, workspace=None, workspace_bytes=0) == la.LA_OK
 
 
+def test_forward_host_validation(lib):
+    """la_forward_host: staging size and argument checks (no GPU reached)."""
+    f = la.la_forward_host_workspace_size
+    assert f(0, 1, 64, 16, 16, 1, la.LA_F32, 2) == 0
+    assert f(1, 1, 64, 24, 16, 1, la.LA_F32, 2) == 0
+    # two staging slots of [q | k | v | out] for the largest slice, plus one
+    # la_forward workspace for it; more slices, smaller slots
+    B, H, N, d = 4, 8, 4096, 64
+    one = f(B, H, N, d, d, 1, la.LA_BF16, 1)
+    four = f(B, H, N, d, d, 1, la.LA_BF16, 4)
+    assert one >= 2 * 4 * B * H * N * d * 2
+    assert four >= 2 * 4 * (B * H // 4) * N * d * 2 and four < one
+    # slices beyond B*H are clamped: one sequence per slice
+    assert f(1, 2, N, d, d, 1, la.LA_BF16, 64) == f(1, 2, N, d, d, 1, la.LA_BF16, 2)
+    # ragged slices (B*H not a multiple): slots sized for the larger slice
+    assert f(1, 5, N, d, d, 1, la.LA_BF16, 2) >= 2 * 4 * 3 * N * d * 2
+    h = dict(q=16, k=32, v=48, out=64, B=1, H=2, N=64, dk=16, dv=16, causal=1, eps=1e-6,
+             dtype=la.LA_F32, slices=2, workspace=1024, workspace_bytes=1 << 24, stream=None)
+    assert la.la_forward_host(**{**h, "q": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_host(**{**h, "slices": 0}) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_host(**{**h, "workspace_bytes": 64}) == la.LA_ERR_INVALID_ARG
+    assert b"workspace" in lib.la_last_error()
+    assert la.la_forward_host(**{**h, "workspace": 1032}) == la.LA_ERR_INVALID_ARG   # misaligned
+    assert la.la_forward_host(**{**h, "dk": 48}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_forward_host(**{**h, "eps": -1.0}) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_host(**{**h, "N": 0, "q": None}) == la.LA_OK
+
+
 def test_decode_and_backward_reject_bad_arguments(lib):
     d = dict(S=256, z=512, q=16, k=32, v=48, out=64, B=2, H=2, dk=64, dv=64,
              eps=1e-6, dtype=la.LA_BF16, stream=None)
