@@ -21,6 +21,29 @@ STATE_TOL = {"f32": 1e-5, "bf16": 1e-2}
 # Bounded like the state, at 1e-2.
 Z_TOL = {"f32": 1e-5, "bf16": 1e-2}
 
+# Gradient tolerances of the tensor-core backward (bf16 operands, fp32
+# accumulation), per gradient, max abs error relative to that gradient's
+# largest oracle magnitude. dq is ill-conditioned in the phi values: dphi(q_t)
+# = sum_j phi(k_j) ((v_j - o_t) . a_t), whose terms are 10-50 times the sum for
+# random inputs, so the bf16 rounding of phi(k) in the intra-chunk contraction
+# dP' phi(K) (relative 2^-9 per term) and of a and dP' leaves ~2.5 % (median)
+# and up to 5.9 % (worst of 80 seeds and shapes, causal and not, N = 129 ..
+# 4096) of max|dq|; an fp64 emulation of the kernel's roundings reproduces the
+# GPU's figure to three digits. dk and dv stay below 1.3 %. The CUDA-core path
+# (fp32 arithmetic) keeps TOL.
+GRAD_TOL_TC = {"dq": 8e-2, "dk": 2e-2, "dv": 2e-2}
+
+
+def grad_tol(dtype, tensor_core):
+    """Per-gradient tolerances (dq, dk, dv) for a backward path."""
+    if tensor_core and dtype == "bf16":
+        return [GRAD_TOL_TC[n] for n in ("dq", "dk", "dv")]
+    return [TOL[dtype]] * 3
+
+
+def grads_ok(errs, tols):
+    return all(e <= t for e, t in zip(errs, tols))
+
 
 def torch_dtype(name):
     import torch

@@ -14,7 +14,9 @@ import pytest
 import oracle as orc
 import causal_linear_attention_la_gb300 as la
 from causal_linear_attention_la_gb300 import synth
-from helpers import TOL, build_lib, grad_errors, to_dev, to_host
+from helpers import build_lib, grad_errors, grad_tol, grads_ok, to_dev, to_host
+
+TC_TOL = grad_tol("bf16", True)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,7 +67,7 @@ def test_backward_tensor_core(B, H, N):
     assert la.la_launch_count() - n0 in (2, 3)
     assert la.la_device_status(True) == la.LA_OK
     errs = grad_errors(got, want)
-    assert max(errs) <= TOL["bf16"], errs
+    assert grads_ok(errs, TC_TOL), errs
 
 
 @pytest.mark.parametrize("B,H,N", [
@@ -84,7 +86,7 @@ def test_backward_tensor_core_noncausal(B, H, N):
     assert la.la_launch_count() - n0 == 3
     assert la.la_device_status(True) == la.LA_OK
     errs = grad_errors(got, want)
-    assert max(errs) <= TOL["bf16"], errs
+    assert grads_ok(errs, TC_TOL), errs
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -104,7 +106,7 @@ def test_backward_tensor_core_matches_cuda_core(causal):
     finally:
         la.la_set_path(la.LA_PATH_AUTO)
     errs = grad_errors(tc, simt)
-    assert max(errs) <= TOL["bf16"], errs
+    assert grads_ok(errs, TC_TOL), errs
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -113,4 +115,4 @@ def test_backward_tensor_core_eps_zero(causal):
     got, want = _grads(1, 2, 513, seed=4242, eps=0.0, causal=causal)
     assert la.la_device_status(True) == la.LA_OK
     errs = grad_errors(got, want)
-    assert max(errs) <= TOL["bf16"], errs
+    assert grads_ok(errs, TC_TOL), errs

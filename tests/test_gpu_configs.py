@@ -7,7 +7,13 @@ times (default path, one call per pass):
 * decode: fp32 states from a bf16 prefill of N=131072 tokens on B=1 H=16,
   replicated to B=64 x H=32, then one-token steps; every state for the first
   steps, sampled states for more
-* forward + backward B=4 H=8 N=8192 d=64 bf16: every gradient vs the oracle
+* forward + backward B=4 H=8 N=8192 d=64 bf16: every gradient vs the oracle,
+  causal and non-causal
+* decay-gated forward B=4 H=8 N=4096 d=64 bf16 (per-head factors 0.9 ..
+  0.999, as the bench): every output and the final state vs the oracle's
+  decayed recurrence
+* forward through the host-buffer call at B=4 H=8 N=4096 d=64 (the bench's
+  end-to-end line, two sequence groups): every output vs the oracle
 """
 
 import numpy as np
@@ -16,7 +22,7 @@ import pytest
 import oracle as orc
 import causal_linear_attention_la_gb300 as la
 from causal_linear_attention_la_gb300 import synth
-from helpers import STATE_TOL, TOL, Z_TOL, build_lib, grad_errors, rel_err, to_dev, to_host
+from helpers import STATE_TOL, TOL, Z_TOL, build_lib, grad_errors, grad_tol, grads_ok, rel_err, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -115,4 +121,47 @@ def test_forward_backward_b4_h8_n8192_d64():
     assert rel_err(to_host(out), want_o, np.abs(v).max()) <= TOL["bf16"]
     want = orc.backward_recurrent(q, k, v, g, eps=1e-6)
     errs = grad_errors(grads, want)
-    assert max(errs) <= TOL["bf16"], errs
+    assert grads_ok(errs, grad_tol("bf16", True)), errs
+
+
+def test_forward_backward_noncausal_b4_h8_n8192_d64():
+    import torch
+    B, H, N, d = 4, 8, 8192, 64
+    q, k, v = synth.qkv(B, H, N, d, d, seed=5, dtype="bf16")
+    g = synth.upstream_grad(B, H, N, d, seed=5, dtype="bf16")
+    qd, kd, vd, gd = (to_dev(x, "bf16") for x in (q, k, v, g))
+    out = la.forward(qd, kd, vd, causal=False)
+    grads = la.backward(qd, kd, vd, gd, causal=False)
+    torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
+    want_o = orc.forward_recurrent(q, k, v, causal=False, eps=1e-6)
+    assert rel_err(to_host(out), want_o, np.abs(v).max()) <= TOL["bf16"]
+    want = orc.backward_recurrent(q, k, v, g, causal=False, eps=1e-6)
+    errs = grad_errors(grads, want)
+    assert grads_ok(errs, grad_tol("bf16", True)), errs
+
+
+def test_forward_decay_b4_h8_n4096_d64():
+    import torch
+    B, H, N, d = 4, 8, 4096, 64
+    q, k, v = synth.qkv(B, H, N, d, d, seed=2, dtype="bf16")
+    alpha = np.linspace(0.9, 0.999, H).astype(np.float32)
+    out, S, z = la.forward_decay(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
+                                 torch.from_numpy(alpha).cuda(), return_state=True)
+    torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
+    S_w, z_w, o_w = orc.decode_steps_decay(np.zeros((B, H, d, d)), np.zeros((B, H, d)), q, k, v,
+                                           alpha=alpha.astype(np.float64)[None, :])
+    assert rel_err(to_host(out), o_w, np.abs(v).max()) <= TOL["bf16"]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= STATE_TOL["bf16"]
+    assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= Z_TOL["bf16"]
+
+
+def test_forward_host_b4_h8_n4096_d64():
+    import torch
+    q, k, v = synth.qkv(4, 8, 4096, 64, 64, seed=2, dtype="bf16")
+    hq, hk, hv = (to_dev(x, "bf16").cpu().pin_memory() for x in (q, k, v))
+    got = la.forward_host(hq, hk, hv, slices=2)
+    torch.cuda.synchronize()
+    want = orc.forward_recurrent(q, k, v, eps=1e-6)
+    assert rel_err(to_host(got), want, np.abs(v).max()) <= TOL["bf16"]
