@@ -52,7 +52,10 @@ def _digest(paths):
         with open(p, "rb") as f:
             h.update(os.path.relpath(p, PKG).encode())
             h.update(f.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    # flags with the include directories relative to the repository, so that
+    # the digest of a tree does not depend on where it is checked out
+    flags = [os.path.relpath(f, ROOT) if os.path.isabs(f) else f for f in NVCC_FLAGS]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 
