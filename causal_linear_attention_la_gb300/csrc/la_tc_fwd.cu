@@ -982,8 +982,13 @@ template <int D>
 struct NcSmem {
   static constexpr int NB = D / 64;
   static constexpr int TILE = NB * BOX;
-  static constexpr int ST = D == 64 ? 6 : 4;                       // Q tiles in flight
-  static constexpr int SBUF = NB * D * 128;                        // bf16 S_N^T, K-major
+  static constexpr int ST = D == 64 ? 10 : 4;                      // Q tiles in flight (a stage holds its output until stored)
+  // D = 64: z_N rides in the MMA as bf16 hi + lo rows D, D + 1 of the S_N^T
+  // operand (rows D + 2 .. D + 15 zero), so one MMA with N = D + 16 gives
+  // [O | phi(Q) z_hi | phi(Q) z_lo] (about 16 bits of z in the denominator)
+  static constexpr bool ZMMA = D == 64;
+  static constexpr int NO = ZMMA ? D + 16 : D;                     // MMA N and O buffer width
+  static constexpr int SBUF = ZMMA ? NO * 128 : NB * D * 128;      // bf16 [S_N^T ; z rows], K-major
   static constexpr int OFF_SBUF = ST * TILE;
   static constexpr int OFF_Z = OFF_SBUF + SBUF;                    // [D] z_N
   static constexpr int OFF_BAR = OFF_Z + D * 4;
@@ -991,8 +996,8 @@ struct NcSmem {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
-  static constexpr uint32_t COL_O = 0;                             // 2 x D
-  static constexpr uint32_t COL_S = 2 * D;                         // D
+  static constexpr uint32_t COL_O = 0;                             // 2 x NO
+  static constexpr uint32_t COL_S = 2 * NO;                        // D
   static constexpr uint32_t TMEM_COLS = D == 64 ? 256 : 512;
 };
 
@@ -1091,7 +1096,7 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
   } else if (warp == 9) {
     // ---------------- MMA issuer: O = phi(Q) S_N ----------------
     if (lane == 0) {
-      constexpr uint32_t id_qs = make_idesc_bf16(128, D, false, false);
+      constexpr uint32_t id_qs = make_idesc_bf16(128, L::NO, false, false);
       const uint32_t sb = smem_u32(sbuf);
       bool ok = mbar_wait(s_ready, 0, abort_flag, kTimeoutNs);
       for (int c = 0; c < nchunks && ok; ++c) {
@@ -1103,7 +1108,7 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         const uint32_t qa = smem_u32(sm + s * L::TILE);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tmem + L::COL_O + D * ob, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
+          mma_ss(tmem + L::COL_O + L::NO * ob, make_sdesc(qa + (k >> 2) * BOX + (k & 3) * 32, 16, 1024, kSwizzle128B),
                  make_sdesc(sb + (k >> 2) * (D * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qs, k > 0);
         tc_commit(&o_full[ob]);
       }
@@ -1123,7 +1128,16 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       float acc = 0.f;
       for (int p = 0; p < nrec; ++p) acc += recs[p * rstride + D * D + i];
       zn[i] = acc;
+      if constexpr (L::ZMMA) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D, i >> 3) + 2 * (i & 7)) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D + 1, i >> 3) + 2 * (i & 7)) = lo;
+      }
     }
+    if constexpr (L::ZMMA)
+      for (int i = t; i < (L::NO - D - 2) * 8; i += 128)
+        *reinterpret_cast<uint4*>(sbuf + sw128(D + 2 + (i >> 3), i & 7)) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(s_ready);
@@ -1155,6 +1169,12 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       tc_fence_after();
       uint8_t* qt = sm + s * L::TILE;
       float dot = 0.f;
+      if constexpr (L::ZMMA) {
+        uint32_t dz[2];
+        tmem_ld2(lane_addr + L::COL_O + L::NO * ob + D, dz);
+        tmem_ld_wait();
+        dot = __uint_as_float(dz[0]) + __uint_as_float(dz[1]);
+      } else {
 #pragma unroll 1
       for (int b = 0; b < L::NB; ++b)
 #pragma unroll
@@ -1172,12 +1192,13 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
           dot = fmaf(__uint_as_float(pw[3] << 16), z1.z, dot);
           dot = fmaf(__uint_as_float(pw[3] & 0xFFFF0000u), z1.w, dot);
         }
+      }
       const float inv_den = 1.f / (dot + prm.eps);
       // the row of phi(Q) has been read: the Q tile takes the output row
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(lane_addr + L::COL_O + D * ob + c0, v);
+        tmem_ld32(lane_addr + L::COL_O + L::NO * ob + c0, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
