@@ -16,7 +16,9 @@ reported under "sections": the causal forward B=2 H=16 N=32768 d=128, the
 decode step on B=64 x H=32 fp32 states of d=128 (1024 steps in a CUDA graph),
 the same decode with 16 tokens per call (64 calls of la_decode_steps), the
 decay-gated and delta-rule variants in the same shape, forward + backward
-B=4 H=8 N=8192 d=64, and the decay-gated forward in the headline shape.
+B=4 H=8 N=8192 d=64 (causal and not; the backward reuses the forward's
+state records through la_backward_saved), and the decay-gated forward in
+the headline shape.
 
 Timing: W eager warm-up steps, then the K timed steps are captured once in a
 CUDA graph and replayed, bracketed by CUDA events on the launching stream
@@ -297,7 +299,10 @@ def run_forward(w, K, W, barrier, with_bwd=False):
     code = la.LA_BF16
     ws_f = la.la_forward_workspace_size(B, H, N, dk, dv, w["causal"], code)
     ws_b = la.la_backward_workspace_size(B, H, N, dk, dv, w["causal"], code) if with_bwd else 0
-    ws = torch.empty(max(ws_f, ws_b, 1), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(ws_f, 1), dtype=torch.uint8, device=dev)
+    # the backward keeps its own scratch and reads the forward's state
+    # records from `ws` (la_backward_saved: save-for-backward)
+    wsb = torch.empty(max(ws_b, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream()
     alpha = torch.linspace(0.9, 0.999, H, device=dev)       # decay: per-head factors
 
@@ -314,10 +319,10 @@ def run_forward(w, K, W, barrier, with_bwd=False):
                                None, None, ws.data_ptr(), ws.numel(), sp)
         assert st == 0, la.lib().la_last_error()
         if with_bwd:
-            st = la.la_backward(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(),
-                                s["g"].data_ptr(), s["dq"].data_ptr(), s["dk"].data_ptr(),
-                                s["dv"].data_ptr(), B, H, N, dk, dv, w["causal"], EPS, code,
-                                ws.data_ptr(), ws.numel(), sp)
+            st = la.la_backward_saved(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(),
+                                      s["g"].data_ptr(), s["dq"].data_ptr(), s["dk"].data_ptr(),
+                                      s["dv"].data_ptr(), B, H, N, dk, dv, w["causal"], EPS, code,
+                                      ws.data_ptr(), ws.numel(), wsb.data_ptr(), wsb.numel(), sp)
             assert st == 0, la.lib().la_last_error()
 
     with torch.cuda.stream(stream):

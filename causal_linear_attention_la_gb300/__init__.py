@@ -32,6 +32,7 @@ __all__ = [
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "la_forward_host", "la_forward_host_workspace_size", "forward_host",
+    "la_backward_saved", "backward_saved",
     "forward", "decode_step", "decode_steps", "backward",
     "decode_steps_decay", "decode_steps_delta", "state_copy", "forward_decay",
 ]
@@ -52,7 +53,7 @@ exported_symbols = (
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
     "la_device_status", "la_forward_noalloc",
-    "la_forward_host_workspace_size", "la_forward_host",
+    "la_forward_host_workspace_size", "la_forward_host", "la_backward_saved",
 )
 
 
@@ -94,6 +95,9 @@ def lib():
     h.la_forward.restype = _c_int
     h.la_forward.argtypes = ([_c_void] * 4 + [_c_int] * 6 + [_c_float, _c_int]
                              + [_c_void, _c_void, _c_void, _c_size, _c_void])
+    h.la_backward_saved.restype = _c_int
+    h.la_backward_saved.argtypes = ([_c_void] * 7 + [_c_int] * 6 + [_c_float, _c_int]
+                                    + [_c_void, _c_size, _c_void, _c_size, _c_void])
     h.la_forward_host_workspace_size.restype = _c_size
     h.la_forward_host_workspace_size.argtypes = [_c_int] * 8
     h.la_forward_host.restype = _c_int
@@ -161,6 +165,12 @@ def la_forward(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype, S_final,
     return lib().la_forward(q, k, v, out, B, H, N, dk, dv, int(causal), eps,
                             dtype, S_final, z_final, workspace,
                             workspace_bytes, stream)
+
+
+def la_backward_saved(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps, dtype,
+                      saved, saved_bytes, workspace, workspace_bytes, stream):
+    return lib().la_backward_saved(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, int(causal), eps,
+                                   dtype, saved, saved_bytes, workspace, workspace_bytes, stream)
 
 
 def la_forward_host_workspace_size(B, H, N, dk, dv, causal, dtype, slices):
@@ -465,4 +475,27 @@ def backward(q, k, v, dout, causal=True, eps=1e-6, workspace=None):
                        dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(), B, H, N,
                        dk, dv, causal, eps, code, workspace.data_ptr(),
                        workspace.numel(), _stream_ptr(q)))
+    return dq, dkk, dvv
+
+
+def backward_saved(q, k, v, dout, saved, causal=True, eps=1e-6, workspace=None):
+    """backward() reusing ``saved``, the workspace tensor of the matching
+    forward(q, k, v, causal=causal, workspace=saved) call (left unchanged)."""
+    import torch
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, n, q.dtype)
+    _need(saved, "saved")
+    dq = torch.empty_like(q)
+    dkk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    ws_bytes = la_backward_workspace_size(B, H, N, dk, dv, causal, code)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    _check(la_backward_saved(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                             dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(), B, H, N,
+                             dk, dv, causal, eps, code, saved.data_ptr(), saved.numel(),
+                             workspace.data_ptr(), workspace.numel(), _stream_ptr(q)))
     return dq, dkk, dvv

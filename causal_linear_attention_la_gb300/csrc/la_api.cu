@@ -664,11 +664,17 @@ la_status la_state_copy(float* dst_S, float* dst_z, const float* src_S, const fl
   return LA_OK;
 }
 
-la_status la_backward(const void* q, const void* k, const void* v,
-                      const void* dout, void* dq, void* dk_, void* dv_, int B,
-                      int H, int N, int dk, int dv, int causal, float eps,
-                      la_dtype dtype, void* workspace, size_t workspace_bytes,
-                      la_stream_t stream) {
+}  // extern "C"
+
+namespace la {
+namespace {
+
+// la_backward and la_backward_saved: `saved` (nullable) is the workspace a
+// matching la_forward call left its state-pass records in.
+la_status backward_impl(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk_,
+                        void* dv_, int B, int H, int N, int dk, int dv, int causal, float eps, la_dtype dtype,
+                        const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream, const char* name) {
   bool empty = false;
   la_status st = check_sizes(B, H, N, dk, dv, dtype, eps, &empty);
   if (st != LA_OK) return st;
@@ -692,13 +698,50 @@ la_status la_backward(const void* q, const void* k, const void* v,
   a.ws_state = (float*)((char*)workspace + w.state_off);
   a.ws_rev = (float*)((char*)workspace + w.rev_off);
   a.ws_tok = (float*)((char*)workspace + w.tok_off);
-  a.plan = plan; a.stream = (cudaStream_t)stream;
+  a.plan = plan; a.stream = stream;
   const bool use_tc = g_path.load() == LA_PATH_AUTO && tc_backward_supported(dk, dv, dtype, a.causal);
+  if (saved != nullptr) {
+    const SegPlan fplan = forward_plan(BH, N, dk, dv, dtype, a.causal);
+    const size_t need = layout(BH, N, dk, dv, fplan, false).total;
+    if (saved_bytes < need)
+      return fail(LA_ERR_INVALID_ARG, "saved forward workspace of %zu bytes needed, %zu given", need, saved_bytes);
+    if (!aligned16(saved)) return fail(LA_ERR_INVALID_ARG, "saved workspace must be 16-byte aligned");
+    // the tensor-core backward reads the forward's records as they are (the
+    // same segments, F parts each); the CUDA-core path recomputes them
+    if (use_tc && fplan.P == plan.P && fplan.seg_len == plan.seg_len) {
+      a.ws_state = (float*)saved;
+      a.plan.F = fplan.F;
+      a.state_ready = true;
+    }
+  }
   if (use_tc && device_status_ptr() == nullptr)
-    return fail(LA_ERR_CUDA, "la_backward: device status word unavailable");
+    return fail(LA_ERR_CUDA, "%s: device status word unavailable", name);
   cudaError_t e = use_tc ? tc_backward(a) : simt_backward(a);
-  if (e != cudaSuccess) return cuda_fail(e, "la_backward");
+  if (e != cudaSuccess) return cuda_fail(e, name);
   return LA_OK;
+}
+
+}  // namespace
+}  // namespace la
+
+extern "C" {
+
+la_status la_backward(const void* q, const void* k, const void* v,
+                      const void* dout, void* dq, void* dk_, void* dv_, int B,
+                      int H, int N, int dk, int dv, int causal, float eps,
+                      la_dtype dtype, void* workspace, size_t workspace_bytes,
+                      la_stream_t stream) {
+  return backward_impl(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps, dtype, nullptr, 0, workspace,
+                       workspace_bytes, (cudaStream_t)stream, "la_backward");
+}
+
+la_status la_backward_saved(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk_,
+                            void* dv_, int B, int H, int N, int dk, int dv, int causal, float eps, la_dtype dtype,
+                            const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                            la_stream_t stream) {
+  if (saved == nullptr) return fail(LA_ERR_INVALID_ARG, "saved must be the forward's workspace (non-NULL)");
+  return backward_impl(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps, dtype, saved, saved_bytes,
+                       workspace, workspace_bytes, (cudaStream_t)stream, "la_backward_saved");
 }
 
 }  // extern "C"

@@ -79,6 +79,9 @@ struct BwdArgs {
   float* ws_tok;    // [BH][N][2]           D_t and b_t per token
   SegPlan plan;
   cudaStream_t stream;
+  // ws_state already holds the forward's state-pass records (plan.F parts per
+  // segment, as la_forward's tensor-core path leaves them): no state pass
+  bool state_ready = false;
 };
 
 struct DecodeArgs {

@@ -1562,10 +1562,13 @@ cudaError_t launch_backward(const BwdArgs& a) {
   f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = a.causal;
   f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
   f.stream = a.stream;
-  prof_begin(LA_SPAN_BWD_STATE, a.stream);
-  cudaError_t e = tc_segment_state(f);    // sums of S^T, z for segments 0 .. P-2
-  prof_end(LA_SPAN_BWD_STATE, a.stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!a.state_ready) {
+    prof_begin(LA_SPAN_BWD_STATE, a.stream);
+    e = tc_segment_state(f);              // sums of S^T, z for segments 0 .. P-2
+    prof_end(LA_SPAN_BWD_STATE, a.stream);
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap mq, mk, mv, mg;
   e = make_map(&mq, a.q, a.BH, a.N, D);
@@ -1612,10 +1615,13 @@ cudaError_t launch_backward_nc(const BwdArgs& a) {
   f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = 0;
   f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
   f.stream = a.stream;
-  prof_begin(LA_SPAN_BWD_STATE, a.stream);
-  cudaError_t e = tc_segment_state(f);    // sums of S^T, z for every segment
-  prof_end(LA_SPAN_BWD_STATE, a.stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!a.state_ready) {
+    prof_begin(LA_SPAN_BWD_STATE, a.stream);
+    e = tc_segment_state(f);              // sums of S^T, z for every segment
+    prof_end(LA_SPAN_BWD_STATE, a.stream);
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv;
   e = make_map(&mq, a.q, a.BH, a.N, D);

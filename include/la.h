@@ -285,6 +285,30 @@ LA_API la_status la_backward(const void* q, const void* k, const void* v,
                       la_stream_t stream);
 
 /*
+ * la_backward reusing the state records that the matching la_forward call
+ * left in its workspace (save-for-backward): the backward's own pass over k
+ * and v, which rebuilds the per-segment sums of S and z, is skipped.
+ *
+ * saved        the workspace given to la_forward with the same q, k, v, B, H,
+ *              N, dk, dv, causal and dtype, unchanged since, and under the
+ *              same la_set_path setting; saved_bytes at least
+ *              la_forward_workspace_size(...) of those arguments. It is read,
+ *              not written.
+ * workspace    the backward's own scratch, la_backward_workspace_size(...)
+ *              bytes, separate from `saved`.
+ * Other arguments and the results as la_backward. The records are used by
+ * the tensor-core path (bf16, dk = dv = 64); on the CUDA-core path the
+ * backward recomputes them and `saved` is only checked for size. NULL `saved`
+ * is LA_ERR_INVALID_ARG.
+ */
+LA_API la_status la_backward_saved(const void* q, const void* k, const void* v,
+                                   const void* dout, void* dq, void* dk_, void* dv_,
+                                   int B, int H, int N, int dk, int dv, int causal,
+                                   float eps, la_dtype dtype, const void* saved,
+                                   size_t saved_bytes, void* workspace,
+                                   size_t workspace_bytes, la_stream_t stream);
+
+/*
  * Kernel-path selection, for tests and measurements. LA_PATH_AUTO (the
  * default) takes the tensor-core (tcgen05) kernels where they apply (bf16;
  * forward dk = dv in {64, 128}, backward dk = dv = 64, causal or not) and the

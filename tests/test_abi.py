@@ -141,6 +141,14 @@ def test_decode_and_backward_reject_bad_arguments(lib):
     assert la.la_backward(**{**b, "workspace_bytes": 4}) == la.LA_ERR_INVALID_ARG
     assert la.la_backward(**{**b, "dv": 8}) == la.LA_ERR_UNSUPPORTED
     assert la.la_backward(**{**b, "N": 0}) == la.LA_OK
+    # la_backward_saved: the forward's workspace is required and checked for size
+    sv = dict(b, saved=1 << 20, saved_bytes=1 << 20)
+    assert la.la_backward_saved(**{**sv, "saved": None}) == la.LA_ERR_INVALID_ARG
+    assert la.la_backward_saved(**{**sv, "saved_bytes": 16}) == la.LA_ERR_INVALID_ARG
+    assert b"saved" in lib.la_last_error()
+    assert la.la_backward_saved(**{**sv, "saved": (1 << 20) + 8}) == la.LA_ERR_INVALID_ARG   # misaligned
+    assert la.la_backward_saved(**{**sv, "dv": 8}) == la.LA_ERR_UNSUPPORTED
+    assert la.la_backward_saved(**{**sv, "N": 0}) == la.LA_OK
 
 
 def test_decode_steps_validation(lib):

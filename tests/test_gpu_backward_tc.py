@@ -116,3 +116,31 @@ def test_backward_tensor_core_eps_zero(causal):
     assert la.la_device_status(True) == la.LA_OK
     errs = grad_errors(got, want)
     assert grads_ok(errs, TC_TOL), errs
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,H,N", [
+    (1, 1, 100),      # one segment: no records (causal)
+    (2, 3, 1000),     # several segments, ragged tail
+    (1, 1, 16384),    # the forward's state pass splits each segment in two parts
+    (4, 8, 1000),
+])
+def test_backward_saved(B, H, N, causal):
+    """la_backward_saved reads the forward's state records from its workspace
+    (two launches, no state pass) and gives the oracle's gradients."""
+    import torch
+    seed = 2900 + N + B * H
+    q, k, v = synth.qkv(B, H, N, 64, 64, seed=seed, dtype="bf16")
+    g = synth.upstream_grad(B, H, N, 64, seed=seed, dtype="bf16")
+    qd, kd, vd, gd = (to_dev(x, "bf16") for x in (q, k, v, g))
+    ws = torch.empty(max(1, la.la_forward_workspace_size(B, H, N, 64, 64, causal, la.LA_BF16)),
+                     dtype=torch.uint8, device="cuda")
+    la.forward(qd, kd, vd, causal=causal, workspace=ws)
+    n0 = la.la_launch_count()
+    got = la.backward_saved(qd, kd, vd, gd, ws, causal=causal)
+    torch.cuda.synchronize()
+    assert la.la_launch_count() - n0 == 2
+    assert la.la_device_status(True) == la.LA_OK
+    want = orc.backward_recurrent(q, k, v, g, causal=causal, eps=1e-6)
+    errs = grad_errors(got, want)
+    assert grads_ok(errs, TC_TOL), errs
