@@ -258,6 +258,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   // the swizzled operand boxes need 1024-byte alignment of the shared window
+  // a backward launched after this forward (reading its records) may start
+  // filling its pipeline as this grid's CTAs retire; it reads nothing this
+  // kernel writes before its own dependency wait
+  griddep_launch_dependents();
   if ((smem_u32(sm) & 1023u) != 0u) {
     if (threadIdx.x == 0) report_timeout(prm.status);
     return;
@@ -1021,6 +1025,8 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
   uint64_t* mma_fin = o_full + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
+  // as in the causal chunk loop: a following backward may start early
+  griddep_launch_dependents();
   if ((smem_u32(sm) & 1023u) != 0u) {
     if (threadIdx.x == 0) report_timeout(prm.status);
     return;
