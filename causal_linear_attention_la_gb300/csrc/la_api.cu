@@ -224,26 +224,26 @@ SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool c
   return plan;
 }
 
-// la_forward_host: internal copy streams and events, created on first use
-// for the current device and reused under a lock (enqueueing is short).
+// la_forward_host: internal copy streams and events per device, created on
+// first use on that device and reused under its lock (enqueueing is short).
 struct HostPipe {
   std::mutex mu;
-  int device = -1;
+  bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
   cudaEvent_t in[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
 };
-HostPipe g_pipe;
+constexpr int kMaxDevices = 64;
+HostPipe g_pipes[kMaxDevices];
 
-cudaError_t host_pipe_ready_locked(int device) {
-  if (g_pipe.device == device) return cudaSuccess;
-  if (g_pipe.device >= 0) return cudaErrorInvalidDevice;   // one device per process
-  cudaError_t e = cudaStreamCreateWithFlags(&g_pipe.h2d, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_pipe.d2h, cudaStreamNonBlocking);
-  cudaEvent_t* evs[8] = {&g_pipe.start, &g_pipe.end, &g_pipe.in[0], &g_pipe.in[1],
-                         &g_pipe.done[0], &g_pipe.done[1], &g_pipe.freed[0], &g_pipe.freed[1]};
+// With p.mu held and `device` current.
+cudaError_t host_pipe_ready_locked(HostPipe& p) {
+  if (p.ready) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking);
+  cudaEvent_t* evs[8] = {&p.start, &p.end, &p.in[0], &p.in[1], &p.done[0], &p.done[1], &p.freed[0], &p.freed[1]};
   for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
-  if (e == cudaSuccess) g_pipe.device = device;
+  if (e == cudaSuccess) p.ready = true;
   return e;
 }
 
@@ -414,8 +414,10 @@ la_status la_forward_host(const void* q, const void* k, const void* v, void* out
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward_host (device)");
+  if (dev < 0 || dev >= kMaxDevices) return fail(LA_ERR_UNSUPPORTED, "la_forward_host: device %d", dev);
+  HostPipe& g_pipe = g_pipes[dev];
   std::lock_guard<std::mutex> lk(g_pipe.mu);
-  e = host_pipe_ready_locked(dev);
+  e = host_pipe_ready_locked(g_pipe);
   if (e != cudaSuccess) return cuda_fail(e, "la_forward_host (copy streams)");
   cudaStream_t s = (cudaStream_t)stream_;
   const size_t elt = dtype == LA_BF16 ? 2 : 4;
