@@ -289,9 +289,10 @@ LA_API la_status la_backward(const void* q, const void* k, const void* v,
  * left in its workspace (save-for-backward): the backward's own pass over k
  * and v, which rebuilds the per-segment sums of S and z, is skipped.
  *
- * saved        the workspace given to la_forward with the same q, k, v, B, H,
- *              N, dk, dv, causal and dtype, unchanged since, and under the
- *              same la_set_path setting; saved_bytes at least
+ * saved        the workspace given to la_forward (not la_forward_decay, whose
+ *              records are decayed) with the same q, k, v, B, H, N, dk, dv,
+ *              causal and dtype, unchanged since, and under the same
+ *              la_set_path setting; saved_bytes at least
  *              la_forward_workspace_size(...) of those arguments. It is read,
  *              not written.
  * workspace    the backward's own scratch, la_backward_workspace_size(...)
