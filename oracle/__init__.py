@@ -25,6 +25,7 @@ from .la_oracle import (  # noqa: F401
     loss_dot,
 )
 from .variants import (  # noqa: F401
+    backward_decay,
     decode_steps_decay,
     decode_steps_delta,
     impulse_response,

@@ -51,6 +51,54 @@ def decode_steps_decay(S, z, q, k, v, alpha, eps=1e-6, feature="elu1"):
     return S, z, out
 
 
+def backward_decay(q, k, v, g, alpha, eps=1e-6, feature="elu1"):
+    """Gradients (dq, dk, dv) of L = sum(g * out) for the decayed causal
+    attention of decode_steps_decay run from the zero state over the whole
+    sequence (alpha fixed, one factor per head).
+
+    The pages give only the decayed recurrence; its gradient follows by the
+    chain rule through it. With D_t = phi(q_t).z_t + eps, o_t = S_t^T phi(q_t) / D_t:
+
+        a_t = g_t / D_t,  b_t = -(g_t . o_t) / D_t
+        dphi(q_t) = S_t a_t + b_t z_t                       (decayed S_t, z_t)
+        R_j = phi(q_j) a_j^T + alpha R_{j+1},  r_j = b_j phi(q_j) + alpha r_{j+1}
+        dphi(k_j) = R_j v_j + r_j,  dv_j = R_j^T phi(k_j)
+
+    (S_{t+1} = alpha S_t + ..., so the adjoint carried from t+1 to t is
+    scaled by alpha). With alpha = 1 this is oracle.backward_recurrent.
+    Shapes as backward_recurrent; alpha broadcastable to (B, H).
+    """
+    q, k, v, g = _as64(q, k, v, g)
+    phi, dphi = FEATURE_MAPS[feature]
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    a = np.broadcast_to(np.asarray(alpha, dtype=np.float64), (B, H))
+    fq, fk = phi(q), phi(k)
+    S = np.zeros((B, H, dk, dv))
+    z = np.zeros((B, H, dk))
+    at = np.zeros((B, H, N, dv))
+    bt = np.zeros((B, H, N))
+    dfq = np.zeros((B, H, N, dk))
+    for t in range(N):
+        S = a[..., None, None] * S + np.einsum("bhc,bhm->bhcm", fk[:, :, t], v[:, :, t])
+        z = a[..., None] * z + fk[:, :, t]
+        D = np.einsum("bhc,bhc->bh", fq[:, :, t], z) + eps
+        o = np.einsum("bhc,bhcm->bhm", fq[:, :, t], S) / D[..., None]
+        at[:, :, t] = g[:, :, t] / D[..., None]
+        bt[:, :, t] = -np.einsum("bhm,bhm->bh", g[:, :, t], o) / D
+        dfq[:, :, t] = np.einsum("bhcm,bhm->bhc", S, at[:, :, t]) + bt[:, :, t][..., None] * z
+    R = np.zeros((B, H, dk, dv))
+    r = np.zeros((B, H, dk))
+    dfk = np.zeros((B, H, N, dk))
+    dvv = np.zeros((B, H, N, dv))
+    for j in range(N - 1, -1, -1):
+        R = a[..., None, None] * R + np.einsum("bhc,bhm->bhcm", fq[:, :, j], at[:, :, j])
+        r = a[..., None] * r + bt[:, :, j][..., None] * fq[:, :, j]
+        dfk[:, :, j] = np.einsum("bhcm,bhm->bhc", R, v[:, :, j]) + r
+        dvv[:, :, j] = np.einsum("bhcm,bhc->bhm", R, fk[:, :, j])
+    return dfq * dphi(q), dfk * dphi(k), dvv
+
+
 def decode_steps_delta(S, q, k, v, feature="identity"):
     """T delta-rule steps on a given state, one per token: read the state with
     the key, add the key times the difference to the value, read with the query:

@@ -170,3 +170,99 @@ def test_variant_pins_catch_planted_mistakes():
     for t in range(3):
         S = S + kk[t][:, None] * vv[t][None, :]
     assert not np.allclose(S[:, 0], g["S_after"], atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Decay-gated backward: alpha = 1 and finite differences of the decayed forward
+# ---------------------------------------------------------------------------
+
+
+def _decay_loss(q, k, v, g, alpha, eps):
+    B, H, _, dk = q.shape
+    dv = v.shape[-1]
+    out = orc.decode_steps_decay(np.zeros((B, H, dk, dv)), np.zeros((B, H, dk)), q, k, v,
+                                 alpha=alpha, eps=eps)[2]
+    return float(np.sum(g * out))
+
+
+def _fd_decay(q, k, v, g, alpha, eps, h=1e-6):
+    """Central differences of L = sum(g * out) through the decayed forward."""
+    grads = []
+    for x in (q, k, v):
+        gx = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = _decay_loss(q, k, v, g, alpha, eps)
+            x[idx] = old - h
+            lm = _decay_loss(q, k, v, g, alpha, eps)
+            x[idx] = old
+            gx[idx] = (lp - lm) / (2 * h)
+        grads.append(gx)
+    return grads
+
+
+def test_backward_decay_alpha_one_is_plain_backward():
+    q, k, v = _rand(T=23, seed=5)
+    g = np.random.default_rng(6).standard_normal(v.shape)
+    plain = orc.backward_recurrent(q, k, v, g, causal=True)
+    decayed = orc.backward_decay(q, k, v, g, alpha=1.0)
+    for a, b in zip(decayed, plain):
+        assert np.max(np.abs(a - b)) <= 1e-12 * max(1.0, np.max(np.abs(b)))
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.9, [0.6, 0.97]])
+def test_backward_decay_finite_differences(alpha):
+    rng = np.random.default_rng(23)
+    B, H, N, dk, dv = 1, 2, 6, 3, 4
+    q = rng.standard_normal((B, H, N, dk))
+    k = rng.standard_normal((B, H, N, dk))
+    v = rng.standard_normal((B, H, N, dv))
+    g = rng.standard_normal((B, H, N, dv))
+    al = np.asarray(alpha, dtype=np.float64)
+    al_b = al[None, :] if al.ndim else al      # one factor per head
+    eps = 0.05
+    fd = _fd_decay(q, k, v, g, al_b, eps)
+    got = orc.backward_decay(q, k, v, g, alpha=al_b, eps=eps)
+    for a, b in zip(got, fd):
+        err = np.max(np.abs(a - b)) / np.max(np.abs(b))
+        assert err < 1e-6, err
+
+
+def test_backward_decay_pins_catch_planted_mistakes():
+    """Two plausible mistakes in the reverse sweep, each planted in a copy of
+    the oracle's arithmetic, fail the finite-difference pin: the suffix sum
+    decayed after adding the token's term (R_j = alpha (phi(q_j) a_j^T +
+    R_{j+1})), and no decay on the suffix sums at all."""
+    rng = np.random.default_rng(29)
+    B, H, N, dk, dv = 1, 1, 5, 2, 3
+    q = rng.standard_normal((B, H, N, dk))
+    k = rng.standard_normal((B, H, N, dk))
+    v = rng.standard_normal((B, H, N, dv))
+    g = rng.standard_normal((B, H, N, dv))
+    alpha, eps = 0.7, 0.05
+    fd = _fd_decay(q, k, v, g, alpha, eps)
+    phi, dphi = orc.FEATURE_MAPS["elu1"]
+    fq, fk = phi(q[0, 0]), phi(k[0, 0])
+    S = np.zeros((dk, dv)); z = np.zeros(dk)
+    at = np.zeros((N, dv)); bt = np.zeros(N)
+    for t in range(N):
+        S = alpha * S + np.outer(fk[t], v[0, 0, t]); z = alpha * z + fk[t]
+        D = fq[t] @ z + eps
+        o = fq[t] @ S / D
+        at[t] = g[0, 0, t] / D; bt[t] = -(g[0, 0, t] @ o) / D
+
+    def dk_with(decay_after_add, decay):
+        R = np.zeros((dk, dv)); r = np.zeros(dk); out = np.zeros((N, dk))
+        for j in range(N - 1, -1, -1):
+            if decay_after_add:
+                R = alpha * (R + np.outer(fq[j], at[j])); r = alpha * (r + bt[j] * fq[j])
+            else:
+                R = decay * R + np.outer(fq[j], at[j]); r = decay * r + bt[j] * fq[j]
+            out[j] = (R @ v[0, 0, j] + r) * dphi(k[0, 0, j])
+        return out
+
+    right = dk_with(False, alpha)
+    assert np.max(np.abs(right - fd[1][0, 0])) < 1e-6
+    for wrong in (dk_with(True, alpha), dk_with(False, 1.0)):
+        assert np.max(np.abs(wrong - fd[1][0, 0])) > 1e-3
