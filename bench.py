@@ -103,6 +103,32 @@ def dist_env():
     return world, rank, local
 
 
+def dist_helpers(world, device):
+    """barrier() and max_over_ranks(x) over the initialised process group of
+    `world` ranks (plain functions for one rank). `device`: where the
+    all-reduce tensor lives ("cuda" under NCCL, "cpu" under gloo)."""
+    if world <= 1:
+        return (lambda: None), (lambda x: x)
+    import torch
+    import torch.distributed as dist
+
+    def barrier():
+        dist.barrier()
+
+    def max_over_ranks(x):
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_over_ranks
+
+
+def job_throughput(world, units_per_rank, seconds):
+    """Whole-job throughput: the units every rank processed (each rank does
+    the same work: weak scaling) over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
 
@@ -471,7 +497,7 @@ def reference_arm(args, world, rank):
     if rank != 0:
         return 0
     w = WORKLOADS[MAIN]
-    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    budget = args.ref_budget if args.ref_budget else max(1.0, 60.0 / max(1, args.steps + args.warmup))
     vals = []
     desc = ""
     for i in range(args.warmup + args.steps):
@@ -509,6 +535,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="all", help="comma list of extra workloads or 'none'")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=None,
+                    help="reference arm: seconds of oracle work per step (default: 60 s over all steps)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_env()
@@ -530,20 +558,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-        def barrier():
-            dist.barrier()
-
-        def max_over_ranks(x):
-            t = torch.tensor([x], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-    else:
-        def barrier():
-            pass
-
-        def max_over_ranks(x):
-            return x
+    barrier, max_over_ranks = dist_helpers(world, "cuda")
     if rank == 0:
         build()
     if world > 1:
@@ -558,7 +573,7 @@ def main():
     r = run_forward(w, K, W, barrier)
     ms_total = max_over_ranks(r["ms"])
     tokens = w["B"] * w["N"] * K
-    value = world * tokens / (ms_total / 1e3)
+    value = job_throughput(world, tokens, ms_total / 1e3)
     out_span = r["spans"].get("fwd_output", {"avg_ms": float("nan")})
     alg_bytes = fwd_bytes(w)
     achieved = alg_bytes / (out_span["avg_ms"] / 1e3) / 1e9
@@ -580,7 +595,7 @@ def main():
             sp = rr["spans"].get("fwd_output", {"avg_ms": float("nan")})
             ach = fwd_bytes(ws) / (sp["avg_ms"] / 1e3) / 1e9
             sections[name] = {
-                "value": world * ws["B"] * ws["N"] * kk / t, "unit": "tokens/s",
+                "value": job_throughput(world, ws["B"] * ws["N"] * kk, t), "unit": "tokens/s",
                 "ms_per_step": 1e3 * t / kk, "steps": kk,
                 "tflops_algorithmic": fwd_flops(ws) * kk / t / 1e12,
                 "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -600,7 +615,7 @@ def main():
             sections[name] = {
                 "value": gbs, "unit": "GB/s (S/z traffic)", "ms_per_step": 1e3 * per,
                 "steps": rr["steps"], "tokens_per_call": nt,
-                "tokens_per_s": world * ws["B"] * nt / per,
+                "tokens_per_s": job_throughput(world, ws["B"] * nt, per),
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"],
                              "kernel": {"decay": "decay_tokens", "delta": "delta_tokens"}.get(
@@ -618,7 +633,7 @@ def main():
             s2 = rr["spans"].get("bwd_sweep2", {"avg_ms": float("nan")})["avg_ms"]
             ach = bwd_bytes(ws) / ((s1 + s2) / 1e3) / 1e9
             sections[name] = {
-                "value": world * ws["B"] * ws["N"] * kk / t, "unit": "tokens/s (fwd+bwd)",
+                "value": job_throughput(world, ws["B"] * ws["N"] * kk, t), "unit": "tokens/s (fwd+bwd)",
                 "ms_per_step": 1e3 * t / kk, "steps": kk,
                 "tflops_algorithmic": 3 * fwd_flops(ws) * kk / t / 1e12,
                 "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -649,10 +664,10 @@ def main():
             "kernels": r["spans"],
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_threads,
                              "kind": "oracle", "sample": cpu_desc},
-            "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+            "e2e": {"value": job_throughput(world, tokens, e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                     "call": f"la_forward_host, {e2e['slices']} sequence groups",
-                    "unpipelined_value": world * tokens / (e2e_serial_ms / 1e3)},
+                    "unpipelined_value": job_throughput(world, tokens, e2e_serial_ms / 1e3)},
             "gpu_launches": r["launches"],
             "clocks": sampler.summary(),
             "path": {"forward": ["cuda-core", "tensor-core"][la.la_forward_path(w["dk"], w["dv"], la.LA_BF16)],
