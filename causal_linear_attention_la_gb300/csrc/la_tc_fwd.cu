@@ -10,17 +10,19 @@
 //   P    = phi(Q_c) phi(K_c)^T, masked to j <= t            tensor cores
 //   O    = phi(Q_c) S_prev + P V_c                           tensor cores
 //   S   += phi(K_c)^T V_c                                    tensor cores
-//   z   += column sums of phi(K_c)                           CUDA cores, fp32
-//   den  = phi(Q_c) z_prev + P 1 + eps                       CUDA cores, fp32
+//   z   += column sums of phi(K_c)
+//   den  = phi(Q_c) z_prev + P 1 + eps
 //   out  = O / den
 // The state is held transposed (S^T, value index first) in fp32 tensor
 // memory for the whole segment: S^T += V^T phi(K) reads both tiles as they
 // arrive, and its bf16 copy in shared memory is then a K-major operand. At
-// D = 64 that copy sits right after the K tile, so P and phi(Q) S_prev come
-// out of one N = 192 MMA (on GB300 an MMA instruction costs about the same
-// for any N up to 256, so fewer, wider instructions are faster). The
-// normaliser terms stay on the CUDA cores, where the row and column sums fall
-// out of passes they make anyway.
+// D = 64 the normaliser rides in the MMAs too (on GB300 an MMA instruction
+// costs about the same for any N up to 256, so fewer, wider instructions are
+// faster): the copy [S^T ; z rows] sits right after the K tile, so P,
+// phi(Q) S_prev and phi(Q) z_prev come out of one N = 208 MMA; P V runs on
+// [V | 1], so P 1 comes with it; and the held state is [S^T ; z] with a block
+// of ones under V^T, so z is updated by the state MMA. At D = 128 z and den
+// are summed on the CUDA cores, in fp32, in passes they make anyway.
 //
 // Two kernels:
 //   tc_state_kernel   per-segment sums dS^T = V^T phi(K), dz = sum phi(k), for
@@ -33,9 +35,11 @@
 // of the state kernel: it fills its pipeline before waiting for the records.
 //
 // Warp roles in tc_forward_kernel (448 threads):
-//   warps 0-3    group C: phi in place on K with the column sums that update z
+//   warps 0-3    group C: phi in place on K (with the column sums that
+//                update z at D = 128)
 //   warps 4-7    group A: phi in place on Q; state copy S^T -> shared memory
-//   warps 8-11   group B: P mask, bf16 pack and row sums; denominators; epilogue
+//   warps 8-11   group B: P mask and bf16 pack (row sums at D = 128);
+//                denominators; epilogue
 //   warp 12      TMA producer: Q, K, V chunk tiles into a ring of stages
 //   warp 13      TMEM allocator and MMA issuer (one elected lane)
 // (the CUDA-core groups take the lowest warp ids, which the warp schedulers
@@ -976,9 +980,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 // Non-causal output: every query reads the whole sequence's state
 // ([LA-state] fig. 2, [LA-order]: the summary S_N = phi(K)^T V, z_N):
 //   out = phi(Q_c) S_N / (phi(Q_c) z_N + eps)
-// S_N^T and z_N are the sums of all segments' records. Per chunk one MMA group
-// (phi(Q) times the bf16 copy of S_N^T) and the normaliser on the CUDA cores;
-// the output is staged in the chunk's Q tile and stored with TMA.
+// S_N^T and z_N are the sums of all segments' records. Per chunk one MMA group:
+// phi(Q) times the bf16 copy of S_N^T, which at D = 64 also carries z_N as
+// hi + lo rows so that the normaliser comes out of the same MMA (at D = 128 it
+// is summed on the CUDA cores); the output is staged in the chunk's Q tile and
+// stored with TMA.
 // 320 threads: warps 0-3 group A (phi(Q); the state sum and its copy), warps
 // 4-7 group B (den, epilogue), warp 8 TMA producer, warp 9 TMEM and MMA.
 // ---------------------------------------------------------------------------
