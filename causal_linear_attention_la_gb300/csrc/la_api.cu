@@ -66,7 +66,7 @@ struct WsLayout {
 
 WsLayout layout(long long BH, int N, int dk, int dv, const SegPlan& plan, bool backward) {
   WsLayout w{};
-  const size_t rec = sizeof(float) * (size_t)state_words(dk, dv) * (size_t)plan.P * (size_t)BH;
+  const size_t rec = sizeof(float) * (size_t)record_slot_words(dk, dv) * (size_t)plan.P * (size_t)BH;
   w.state_off = 0;
   size_t off = align_up(rec * (size_t)plan.F, 256);
   if (backward) {

@@ -55,8 +55,13 @@ constexpr int kSlots = 152;        // CTAs resident at once: one per SM of a GB3
 // be resident at once.
 SegPlan plan_segments(long long BH, int N, int slots = kSlots);
 
-// Floats per per-segment state record: dk*dv matrix then dk vector.
+// Floats per per-segment state record of the CUDA-core kernels: dk*dv matrix
+// then dk vector.
 inline long long state_words(int dk, int dv) { return (long long)dk * dv + dk; }
+
+// Floats reserved per record in the workspace: the tensor-core kernels' record
+// (dk*dv matrix, dk vector, dv vector) is the larger of the two layouts.
+inline long long record_slot_words(int dk, int dv) { return (long long)dk * dv + dk + dv; }
 
 // ---------------------------------------------------------------------------
 // Launchers (return cudaError_t of the launch; enqueue only)

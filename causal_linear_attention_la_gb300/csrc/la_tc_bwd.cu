@@ -13,14 +13,31 @@
 //   dphi(k_j) = R_j v_j + r_j,  dv_j = R_j^T phi(k_j)
 //   dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k),  phi'(x) = min(phi(x), 1)
 //
-// Sweep 1 (forward through each segment, from the segment's prefix S, z; the
-// state is held transposed, S^T, as in the forward kernel):
-//   P    = phi(Q) phi(K)^T, masked j <= t           MMA (both K-major)
-//   O    = phi(Q) S_prev + P V                      MMA, MMA (P from TMEM)
-//   S^T += V^T phi(K)                               MMA
-//   den  = phi(Q) z_prev + P 1 + eps;  a = g / den;  b = -(g . O) / den^2
-//   dP   = a V^T;  dP' = (dP + b) masked j <= t     MMA, CUDA cores
-//   dQ   = a S_prev^T + dP' phi(K) + b z_prev        MMA, MMA, epilogue
+// dq is ill-conditioned in the feature values: dphi(q_t) = sum_j phi(k_j)
+// ((v_j - o_t) . a_t), and phi(k) = 1 + psi(k) has a common part (the 1)
+// whose terms cancel almost exactly, leaving a sum some 10-50 times smaller
+// than its terms for inputs of unit scale. Rounding phi(k) to bf16 (2^-9 of
+// the 1) would therefore cost percents of dq. Sweep 1 and pass A split phi(k)
+// = 1 + psi(k): the tensor cores see only psi(k) (bf16 rounding relative to
+// psi, which is small), and the parts that carry the 1 are exact fp32
+// scalars per row. With s_t = sum_i phi(q_t)_i, V_t = sum_{j<=t} v_j and n_t =
+// t + 1 (tokens up to t):
+//   D_t = s_t n_t + phi(q_t).z_psi,t + eps
+//   a_t . O_t = s_t a_t . V_t + a_t . O_psi,t,  O_psi,t = S_psi,t^T phi(q_t)
+//   dphi(q_t) = c_t 1 + S_psi,t a_t + b_t z_psi,t,  c_t = a_t . V_t + n_t b_t
+// where S_psi, z_psi sum psi(k) in place of phi(k), and a_t is the bf16 a of
+// the MMAs in every term (b_t = -a_t . O_t / D_t is formed from it too).
+//
+// Sweep 1 (forward through each segment, from the segment's centred prefix
+// S_psi, z_psi and the sum of v before it; the state is held transposed):
+//   P    = phi(Q) psi(K)^T, masked j <= t           MMA (both K-major)
+//   O    = phi(Q) S_psi,prev + P V                  MMA, MMA (P from TMEM)
+//   S_psi^T += V^T psi(K)                           MMA
+//   den  = s n + phi(Q) z_psi,prev + P 1 + eps;  a = g / den (bf16)
+//   dP   = a V^T;  rho = (dP 1) masked j <= t      MMA, CUDA cores
+//   b = -(s (a . V_prev + rho) + a . O) / den;  c = a . V_prev + rho + n b
+//   dP'  = (dP + b) masked j <= t                   CUDA cores
+//   dQ   = a S_psi,prev^T + dP' psi(K) + b z_psi,prev + c    MMA, MMA, epilogue
 //   R   += phi(Q)^T a;  r += phi(Q)^T b             MMA, CUDA cores
 // writing dq, (den, b) per token and the segment's (R, r) sums.
 // Sweep 2 (backward through each segment, from the suffix R, r after it):
@@ -136,6 +153,91 @@ __device__ __forceinline__ float phiq_dot(const uint8_t* qtile, int r, const flo
   return dot;
 }
 
+// As phiq_dot, also returning the row sum of phi(q_r) in *rs.
+template <int D>
+__device__ __forceinline__ float phiq_dot_sum(const uint8_t* qtile, int r, const float* z, float* rs) {
+  float dot = 0.f, sum = 0.f;
+#pragma unroll 2
+  for (int ch = 0; ch < D / 8; ++ch) {
+    const uint4 w = ld_chunk(qtile, r, ch);
+    const uint32_t* pw = reinterpret_cast<const uint32_t*>(&w);
+    const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * ch);
+    const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * ch + 4);
+    const float f[8] = {bf_lo(pw[0]), bf_hi(pw[0]), bf_lo(pw[1]), bf_hi(pw[1]),
+                        bf_lo(pw[2]), bf_hi(pw[2]), bf_lo(pw[3]), bf_hi(pw[3])};
+    const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      dot = fmaf(f[e], zz[e], dot);
+      sum += f[e];
+    }
+  }
+  *rs = sum;
+  return dot;
+}
+
+// Row pass of the centred gradient: with the centred numerator row O_psi
+// (fp32, tensor memory) and the upstream-gradient row g_r (bf16, G tile),
+// overwrite g_r in place with a_r = g_r * inv_den rounded to bf16 (nearest)
+// and return beta1 = a_r . O_psi, with beta0 = a_r . vsum in *beta0. Both
+// dot products take the rounded a_r that the MMAs read, so that every term
+// of the gradient is formed from the same a.
+template <int D>
+__device__ __forceinline__ float grad_row_pass_centred(uint32_t taddr, uint8_t* gtile, int r, float inv_den,
+                                                       const float* vsum, float* beta0) {
+  float b1 = 0.f, b0 = 0.f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c0, v);
+    uint4 gw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) gw[j] = ld_chunk(gtile, r, c0 / 8 + j);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(&gw[j]);
+      const float4 s0 = *reinterpret_cast<const float4*>(vsum + c0 + 8 * j);
+      const float4 s1 = *reinterpret_cast<const float4*>(vsum + c0 + 8 * j + 4);
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      uint4 o;
+      uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        po[h] = pack_bf16x2(bf_lo(pw[h]) * inv_den, bf_hi(pw[h]) * inv_den);
+        const float a0 = bf_lo(po[h]), a1 = bf_hi(po[h]);
+        b1 = fmaf(a0, __uint_as_float(v[8 * j + 2 * h]), b1);
+        b1 = fmaf(a1, __uint_as_float(v[8 * j + 2 * h + 1]), b1);
+        b0 = fmaf(a0, sv[2 * h], b0);
+        b0 = fmaf(a1, sv[2 * h + 1], b0);
+      }
+      st_chunk(gtile, r, c0 / 8 + j, o);
+    }
+  }
+  *beta0 = b0;
+  return b1;
+}
+
+// Sum of the entries j <= r of one 128-column fp32 row in tensor memory (row
+// r = 32 q + lane of the chunk), in fp32.
+__device__ __forceinline__ float masked_rowsum_lower(uint32_t taddr, int q, int lane) {
+  float sum = 0.f;
+#pragma unroll 1
+  for (int p = 0; p <= q; ++p) {
+    uint32_t v[32];
+    tmem_ld32(taddr + 32 * p, v);
+    tmem_ld_wait();
+    if (p < q) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sum += __uint_as_float(v[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sum += j <= lane ? __uint_as_float(v[j]) : 0.f;
+    }
+  }
+  return sum;
+}
+
 // Row pass of sweep 1: with the numerator row O_r (fp32, tensor memory) and
 // the upstream-gradient row g_r (bf16, G tile), return beta = g_r . O_r and
 // overwrite g_r in place with a_r = g_r * inv_den (bf16, nearest).
@@ -168,13 +270,13 @@ __device__ __forceinline__ float grad_row_pass(uint32_t taddr, uint8_t* gtile, i
   return beta;
 }
 
-// Epilogue row of a gradient: x = acc (tensor memory) + add_s * add_v, times
-// phi'(.) = min(phi, 1) read from row r of a phi-transformed tile, written in
-// bf16 to row r of the swizzled output tile `otile` (stored later with TMA).
-// add_v is an fp32 vector of D entries.
+// Epilogue row of a gradient: x = acc (tensor memory) + add_s * add_v +
+// add_c, times phi'(.) = min(phi, 1) read from row r of a phi-transformed
+// tile, written in bf16 to row r of the swizzled output tile `otile` (stored
+// later with TMA). add_v is an fp32 vector of D entries.
 template <int D>
 __device__ __forceinline__ void grad_epilogue(uint32_t taddr, const uint8_t* ftile, int r, float add_s,
-                                              const float* add_v, uint8_t* otile) {
+                                              const float* add_v, uint8_t* otile, float add_c = 0.f) {
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += 32) {
     uint32_t v[32];
@@ -193,9 +295,10 @@ __device__ __forceinline__ void grad_epilogue(uint32_t taddr, const uint8_t* fti
       uint32_t* po = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const float x0 = fmaf(add_s, av[2 * h], __uint_as_float(v[8 * j + 2 * h])) * fminf(bf_lo(pw[h]), 1.f);
+        const float x0 =
+            (fmaf(add_s, av[2 * h], __uint_as_float(v[8 * j + 2 * h])) + add_c) * fminf(bf_lo(pw[h]), 1.f);
         const float x1 =
-            fmaf(add_s, av[2 * h + 1], __uint_as_float(v[8 * j + 2 * h + 1])) * fminf(bf_hi(pw[h]), 1.f);
+            (fmaf(add_s, av[2 * h + 1], __uint_as_float(v[8 * j + 2 * h + 1])) + add_c) * fminf(bf_hi(pw[h]), 1.f);
         po[h] = pack_bf16x2(x0, x1);
       }
       st_chunk(otile, r, c0 / 8 + j, o);
@@ -249,8 +352,10 @@ struct B1 {
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(COL_R + D <= TMEM_COLS, "tensor memory budget");
   // shared memory
-  static constexpr int OFF_ZST = ST * STAGE;              // [ST][D] z before each staged chunk
-  static constexpr int OFF_BARR = OFF_ZST + ST * D * 4;   // [ST][C] b_t of each staged chunk
+  static constexpr int OFF_ZST = ST * STAGE;              // [ST][D] z_psi before each staged chunk
+  static constexpr int OFF_VST = OFF_ZST + ST * D * 4;    // [ST][D] sum of v before each staged chunk
+  static constexpr int OFF_ROW = OFF_VST + ST * D * 4;    // [ST][C] (s_t, a.V_prev, a.O_psi, den) per row
+  static constexpr int OFF_BARR = OFF_ROW + ST * C * 16;  // [ST][C] b_t of each staged chunk
   static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
   static constexpr int NBAR = 3 * ST + 21;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -262,18 +367,19 @@ struct B1 {
 struct Bwd1Params {
   int N, P, seg_len, F;
   float eps;
-  const float* ws_state;   // [BH][P*F][D*D + D] state-pass sums (S^T, z) of segments 0..P-2
-  float* ws_rev;           // [BH][P][D*D + D] segment sums (R, r), all but the first segment
+  const float* ws_state;   // [BH][P*F][rec_words] centred state-pass sums of segments 0..P-2
+  float* ws_rev;           // [BH][P][rec_words] segment sums (R, r), all but the first segment
   float* ws_tok;           // [BH][N][2] (den, b) per token
   __nv_bfloat16* dq;       // [BH][N][D]
   int* status;
 };
 
 // Warp roles (576 threads):
-//   warps 0-3    group C: phi(K) in place (exact fp32, rounded) and z; the r sums
-//   warps 4-7    group A: phi(Q) in place; bf16 copies of S_prev; final R store
-//   warps 8-11   group B: P mask/pack and row sums, den, a and b (row pass)
-//   warps 12-15  group D: dP' mask/pack, dq epilogue
+//   warps 0-3    group C: psi(K) in place (exact fp32, rounded), z_psi and the
+//                sum of v; the r sums
+//   warps 4-7    group A: phi(Q) in place; bf16 copies of S_psi,prev; final R store
+//   warps 8-11   group B: P mask/pack and row sums, den, a (row pass)
+//   warps 12-15  group D: rho, b and c; dP' mask/pack, dq epilogue
 //   warp 16      TMA producer (Q, K, V, G)
 //   warp 17      TMEM allocator and MMA issuer
 template <int D>
@@ -286,6 +392,8 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   float* zst = reinterpret_cast<float*>(sm + G::OFF_ZST);
+  float* vst = reinterpret_cast<float*>(sm + G::OFF_VST);
+  float4* rowinfo = reinterpret_cast<float4*>(sm + G::OFF_ROW);
   float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
   uint64_t* full = bars;                 // [ST]
@@ -317,7 +425,8 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
-  const long long rec = ((long long)bh * prm.P + seg) * (long long)(D * D + D);
+  constexpr long long RW = rec_words<D>();
+  const long long rec = ((long long)bh * prm.P + seg) * RW;
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -476,8 +585,9 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
     griddep_wait();
-    sum_states_to_tmem<D>(prm.ws_state + (long long)bh * prm.P * prm.F * (D * D + D), D * D + D, 0,
-                          seg * prm.F, lane_addr, G::COL_S, row);
+    // the centred prefix S_psi^T (the held state stays centred)
+    sum_states_to_tmem<D>(prm.ws_state + (long long)bh * prm.P * prm.F * RW, RW, 0, seg * prm.F, lane_addr,
+                          G::COL_S, row);
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -505,20 +615,22 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-    float2* tokp = reinterpret_cast<float2*>(prm.ws_tok) + (long long)bh * prm.N;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST, pb = c & 1;
-      // phi(q_r) . z_prev needs only the phi tiles: formed while the MMAs of
-      // the chunk run, before P is ready
+      // phi(q_r) . z_psi,prev and s_r need only the phi tiles: formed while
+      // the MMAs of the chunk run, before P is ready
       ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      const float qz = phiq_dot<D>(sm + s * G::STAGE, r, zst + s * D);
+      float srow;
+      const float qz = phiq_dot_sum<D>(sm + s * G::STAGE, r, zst + s * D, &srow);
       ok = mbar_wait(&p_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
       const float rowsum = mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, 0.f, nullptr);
-      const float den = rowsum + qz + prm.eps;
+      // tokens up to and including this row: the 1 of every phi(k_j) in z_t
+      const float n_t = (float)(tok0 + c * C + r + 1);
+      const float den = fmaf(srow, n_t, rowsum + qz) + prm.eps;
       const float inv_den = 1.f / den;
       tmem_st_wait();
       tc_fence_before();
@@ -526,11 +638,10 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = mbar_wait(&o_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const float beta = grad_row_pass<D>(lane_addr + G::col_oq(pb), sm + s * G::STAGE + G::OFF_G, r, inv_den);
-      const float b = -beta * inv_den * inv_den;
-      barr[s * C + r] = b;
-      const int tok = tok0 + c * C + r;
-      if (tok < tok_end) tokp[tok] = make_float2(den, b);
+      float beta0;
+      const float beta1 = grad_row_pass_centred<D>(lane_addr + G::col_oq(pb), sm + s * G::STAGE + G::OFF_G, r,
+                                                   inv_den, vst + s * D, &beta0);
+      rowinfo[s * C + r] = make_float4(srow, beta0, beta1, den);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&a_ready[pb]);
@@ -540,6 +651,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+    float2* tokp = reinterpret_cast<float2*>(prm.ws_tok) + (long long)bh * prm.N;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST, pb = c & 1;
@@ -548,7 +660,15 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
            mbar_wait(&a_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      const float b = barr[s * C + r];
+      // rho = a . (v_j summed over j <= t in the chunk), from the fp32 dP row
+      const float rho = masked_rowsum_lower(lane_addr + G::col_pd(pb), q, lane);
+      const float4 ri = rowinfo[s * C + r];     // (s_t, a.V_prev, a.O_psi, den)
+      const int tok = tok0 + c * C + r;
+      const float av = ri.y + rho;              // a . V_t
+      const float b = -fmaf(ri.x, av, ri.z) / ri.w;
+      const float cterm = fmaf((float)(tok + 1), b, av);
+      barr[s * C + r] = b;
+      if (tok < tok_end) tokp[tok] = make_float2(ri.w, b);
       mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, b, nullptr);
       tmem_st_wait();
       tc_fence_before();
@@ -556,10 +676,10 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = mbar_wait(&dq_full[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      // dq staged in the chunk's K region (dead once dQ += dP' phiK is done);
+      // dq staged in the chunk's K region (dead once dQ += dP' psiK is done);
       // the TMA producer stores it before refilling the stage
       grad_epilogue<D>(lane_addr + G::col_oq(pb), sm + s * G::STAGE, r, b, zst + s * D,
-                       sm + s * G::STAGE + G::OFF_K);
+                       sm + s * G::STAGE + G::OFF_K, cterm);
       tc_fence_before();
       mbar_arrive(&oq_empty[pb]);
       fence_proxy_async_smem();
@@ -571,10 +691,11 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int t = tid;
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;
-    float zrun[8], racc[8];
+    float zrun[8], vrun[8], racc[8];
     griddep_wait();
-    sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * prm.F * (D * D + D), D * D + D, 0, seg * prm.F,
-                    8 * fc, zrun);
+    // z_psi and the sum of v before the segment, from the centred records
+    sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * prm.F * RW, RW, 0, seg * prm.F, 8 * fc, zrun);
+    sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * prm.F * RW, RW, 0, seg * prm.F, D + 8 * fc, vrun);
 #pragma unroll
     for (int e = 0; e < 8; ++e) racc[e] = 0.f;
     bool ok = true;
@@ -584,22 +705,32 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         const int n_valid = min(C, tok_end - (tok0 + c * C));
         ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
-        float colsum[8];
-        phi_tile_exact<D, 128>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);
+        float colsum[8], vcol[8];
+        phi_tile_exact<D, 128, true, true, false, true>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);
         fence_proxy_async_smem();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vcol[e] = 0.f;
+        colsum_tile<D, 128>(sm + s * G::STAGE + G::OFF_V, t, n_valid, vcol);
+        reduce_row_groups<D, 128>(vcol);
         if (owner) {
           float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
           zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
           zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
+          float4* vd = reinterpret_cast<float4*>(vst + s * D + 8 * fc);
+          vd[0] = make_float4(vrun[0], vrun[1], vrun[2], vrun[3]);
+          vd[1] = make_float4(vrun[4], vrun[5], vrun[6], vrun[7]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
+          for (int e = 0; e < 8; ++e) {
+            zrun[e] += colsum[e];
+            vrun[e] += vcol[e];
+          }
         }
         mbar_arrive(&phi_done[s]);
       }
       if (c >= 1) {
-        // r += sum_t b_t phi(q_t) over the previous chunk
+        // r += sum_t b_t phi(q_t) over the previous chunk (b from group D)
         const int cp = c - 1, sp = cp % ST;
-        ok = mbar_wait(&a_ready[cp & 1], (cp >> 1) & 1, abort_flag, kTimeoutNs);
+        ok = mbar_wait(&dp_ready[cp & 1], (cp >> 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         wcolsum_tile<D, 128>(sm + sp * G::STAGE, barr + sp * C, t, racc);
         mbar_arrive(&empty[sp]);
@@ -658,7 +789,7 @@ struct B2 {
 
 struct Bwd2Params {
   int N, P, seg_len;
-  const float* ws_rev;     // [BH][P][D*D + D] segment sums (R, r), all but the first segment
+  const float* ws_rev;     // [BH][P][rec_words] segment sums (R, r), all but the first segment
   const float* ws_tok;     // [BH][N][2] (den, b)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -864,11 +995,11 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;
     // R_after, r_after of the segment: the sums of the segments after it
-    const float* recs = prm.ws_rev + (long long)bh * prm.P * (D * D + D);
+    const float* recs = prm.ws_rev + (long long)bh * prm.P * rec_words<D>();
     float rrun[8];
     griddep_wait();
-    sum_states_to_tmem<D>(recs, D * D + D, seg + 1, prm.P, lane_addr, G::COL_R, row);
-    sum_vectors8<D>(recs, D * D + D, seg + 1, prm.P, 8 * fc, rrun);
+    sum_states_to_tmem<D>(recs, rec_words<D>(), seg + 1, prm.P, lane_addr, G::COL_R, row);
+    sum_vectors8<D>(recs, rec_words<D>(), seg + 1, prm.P, 8 * fc, rrun);
     bool ok = true;
     for (int i = 0; i < nchunks && ok; ++i) {
       const int s = i % ST;
@@ -1006,13 +1137,16 @@ struct NA {
   static constexpr int ST = 6;
   static constexpr int OFF_G = TILE;
   static constexpr int STAGE = 2 * TILE;
-  // bf16 [S_N^T ; z_hi ; z_lo ; 0] (D + 16 rows): O and den from one MMA
+  // bf16 [S_psi,N^T ; z_hi ; z_lo ; 1 ; 0] (D + 16 rows): O_psi, phi(q).z_psi
+  // and the row sum s_t of phi(q) from one MMA
   static constexpr int NO = D + 16;
   static constexpr uint32_t G_NO = NO;
   static constexpr int OFF_SBUF = ST * STAGE;
-  static constexpr int OFF_ZN = OFF_SBUF + NO * 128;  // [D] z_N (fp32)
-  static constexpr int OFF_BARR = OFF_ZN + D * 4;     // [ST][C] b_t
-  static constexpr int OFF_BAR = OFF_BARR + ST * C * 4;
+  static constexpr int OFF_ZN = OFF_SBUF + NO * 128;  // [D] z_psi,N (fp32)
+  static constexpr int OFF_VN = OFF_ZN + D * 4;       // [D] sum of all v (fp32)
+  static constexpr int OFF_BARR = OFF_VN + D * 4;     // [ST][C] b_t
+  static constexpr int OFF_CARR = OFF_BARR + ST * C * 4;  // [ST][C] c_t
+  static constexpr int OFF_BAR = OFF_CARR + ST * C * 4;
   static constexpr int NBAR = 6 * ST + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
@@ -1031,15 +1165,20 @@ struct NA {
 struct NcBwdParams {
   int N, P, seg_len, F;
   float eps;
-  const float* ws_state;   // [BH][P*F][D*D + D] S^T, z sums of every part (pass A reads)
-  float* ws_rev;           // [BH][P][D*D + D] (R, r) of each segment (A writes, B reads)
+  const float* ws_state;   // [BH][P*F][rec_words] centred sums of every part (pass A reads)
+  float* ws_rev;           // [BH][P][rec_words] (R, r) of each segment (A writes, B reads)
   int* status;
 };
 
-// Pass A (448 threads). Warps 0-3: phi(Q), the S_N / z_N sums and copy, the
-// r sums and the (R, r) record; warps 4-7: the row pass (a, b) from
-// [O | den]; warps 8-11: the dq epilogue; warp 12 TMA (Q, G in; dq out from
-// the dead G tile); warp 13 TMEM and MMA.
+// Pass A (448 threads). Warps 0-3: phi(Q), the centred S_psi,N / z_psi,N sums
+// and copy, the r sums and the (R, r) record; warps 4-7: the row pass (a, b,
+// c) from [O_psi | phi(q).z_psi | s]; warps 8-11: the dq epilogue; warp 12
+// TMA (Q, G in; dq out from the dead G tile); warp 13 TMEM and MMA. In the
+// centred form of sweep 1 with every token before every query (n_t = N,
+// V_t = the sum of all v, no intra-chunk term):
+//   D_t = s_t N + phi(q_t).z_psi,N + eps,  a_t = g_t / D_t (bf16)
+//   b_t = -(s_t a_t . V_N + a_t . O_psi,t) / D_t,  c_t = a_t . V_N + N b_t
+//   dphi(q_t) = S_psi,N a_t + b_t z_psi,N + c_t
 template <int D>
 __global__ void __launch_bounds__(448, 1)
 tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
@@ -1050,7 +1189,9 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
   uint8_t* sm = smem_raw;
   uint8_t* sbuf = sm + G::OFF_SBUF;
   float* zn = reinterpret_cast<float*>(sm + G::OFF_ZN);
+  float* vn = reinterpret_cast<float*>(sm + G::OFF_VN);
   float* barr = reinterpret_cast<float*>(sm + G::OFF_BARR);
+  float* carr = reinterpret_cast<float*>(sm + G::OFF_CARR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::OFF_BAR);
   uint64_t* full = bars;               // [ST]
   uint64_t* phi_done = bars + ST;      // [ST]
@@ -1079,7 +1220,7 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
-  const long long rstride = (long long)(D * D + D);
+  const long long rstride = rec_words<D>();
   const float* recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
   const int nrec = prm.P * prm.F;
   float* rec_out = prm.ws_rev + ((long long)bh * prm.P + seg) * rstride;
@@ -1214,20 +1355,21 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     griddep_wait();
     sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row);
     copy_state_to_smem<D>(lane_addr + G::COL_S, sbuf, row);
-    // z_N: fp32 for the epilogue; as bf16 hi + lo rows D, D + 1 of the MMA
-    // operand (den = phi(q).z_hi + phi(q).z_lo, about 16 bits), rows D + 2 ..
-    // zero
+    // z_psi,N: fp32 for the epilogue; as bf16 hi + lo rows D, D + 1 of the MMA
+    // operand (phi(q).z_psi = phi(q).z_hi + phi(q).z_lo, about 16 bits); row
+    // D + 2 ones (s_t); rows D + 3 .. zero. The sum of all v for the row pass.
     if (t < D) {
-      float acc = 0.f;
-      for (int p = 0; p < nrec; ++p) acc += recs[p * rstride + D * D + t];
+      const float acc = sum_vector_entry<D>(recs, rstride, 0, nrec, t);
       zn[t] = acc;
+      vn[t] = sum_vector_entry<D>(recs, rstride, 0, nrec, D + t);
       const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
       const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
       *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D, t >> 3) + 2 * (t & 7)) = hi;
       *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D + 1, t >> 3) + 2 * (t & 7)) = lo;
+      *reinterpret_cast<__nv_bfloat16*>(sbuf + sw128(D + 2, t >> 3) + 2 * (t & 7)) = __float2bfloat16_rn(1.f);
     }
-    for (int i = t; i < (G::NO - D - 2) * 8; i += 128)
-      *reinterpret_cast<uint4*>(sbuf + sw128(D + 2 + (i >> 3), i & 7)) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = t; i < (G::NO - D - 3) * 8; i += 128)
+      *reinterpret_cast<uint4*>(sbuf + sw128(D + 3 + (i >> 3), i & 7)) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(s_ready);
@@ -1273,12 +1415,19 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
       ok = mbar_wait(&o_full[ob], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      uint32_t dz[2];
+      uint32_t dz[2], sq;
       tmem_ld2(lane_addr + G::col_o(ob) + D, dz);
+      tmem_ld1(lane_addr + G::col_o(ob) + D + 2, sq);
       tmem_ld_wait();
-      const float inv_den = 1.f / (__uint_as_float(dz[0]) + __uint_as_float(dz[1]) + prm.eps);
-      const float beta = grad_row_pass<D>(lane_addr + G::col_o(ob), stg + G::OFF_G, r, inv_den);
-      barr[s * C + r] = -beta * inv_den * inv_den;
+      const float srow = __uint_as_float(sq);
+      const float nt = (float)prm.N;
+      const float den = fmaf(srow, nt, __uint_as_float(dz[0]) + __uint_as_float(dz[1])) + prm.eps;
+      const float inv_den = 1.f / den;
+      float beta0;
+      const float beta1 = grad_row_pass_centred<D>(lane_addr + G::col_o(ob), stg + G::OFF_G, r, inv_den, vn, &beta0);
+      const float b = -fmaf(srow, beta0, beta1) / den;
+      barr[s * C + r] = b;
+      carr[s * C + r] = fmaf(nt, b, beta0);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&a_ready[ob]);
@@ -1302,7 +1451,7 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
       tc_fence_after();
       // dq staged in the dead G tile; the producer stores it before
       // refilling the stage
-      grad_epilogue<D>(lane_addr + G::col_dq(ob), stg, r, barr[s * C + r], zn, stg + G::OFF_G);
+      grad_epilogue<D>(lane_addr + G::col_dq(ob), stg, r, barr[s * C + r], zn, stg + G::OFF_G, carr[s * C + r]);
       tc_fence_before();
       mbar_arrive(&dq_empty[ob]);
       fence_proxy_async_smem();
@@ -1343,7 +1492,7 @@ struct NB {
 
 struct NcBwdBParams {
   int N, P, seg_len;
-  const float* ws_rev;     // [BH][P][D*D + D] (R, r) of every segment
+  const float* ws_rev;     // [BH][P][rec_words] (R, r) of every segment
   int* status;
 };
 
@@ -1383,7 +1532,7 @@ tc_bwd_nc_b_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_const
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
-  const long long rstride = (long long)(D * D + D);
+  const long long rstride = rec_words<D>();
   const float* recs = prm.ws_rev + (long long)bh * prm.P * rstride;
 
   if (tid == 0) {

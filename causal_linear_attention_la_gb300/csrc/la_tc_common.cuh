@@ -19,6 +19,17 @@ constexpr int C = 128;                    // tokens per chunk
 constexpr int BOX = 128 * 128;            // bytes of one [128 rows][64 bf16] SW128 box
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
+// Floats per state record of the tensor-core kernels: [D x D | D | D]. At
+// D = 64 (causal and non-causal, no decay) the state pass writes centred sums
+// over its tokens: S_psi^T = V^T psi(K) and z_psi = sum psi(k) with
+// psi = phi - 1, then the plain sum of the values v; the full state is
+// S^T = S_psi^T + (sum v) 1^T, z = z_psi + n 1 (n the number of tokens). The
+// large common part of phi(k) (its 1) is thus carried exactly in fp32, and
+// only the small part psi goes through bf16 operands. Otherwise the record is
+// [S^T | z | unused].
+template <int D>
+__host__ __device__ constexpr long long rec_words() { return (long long)D * D + 2 * D; }
+
 // Row of the D x D state held by lane `l` of TMEM quadrant `q` (rows live in
 // the quadrant's lanes: all 32 for M = 128, the first 16 for M = 64).
 template <int D>
@@ -66,6 +77,15 @@ __device__ __forceinline__ float phi_f32(float x) {
   return x > 0.f ? x + 1.f : e;
 }
 
+// psi(x) = phi(x) - 1: x for x > 0 (exact), e^x - 1 otherwise (the
+// subtraction is exact in fp32 for e^x in [1/2, 1]; below that the absolute
+// error stays at the exponential's own, ~2^-22).
+__device__ __forceinline__ float psi_f32(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
+  return x > 0.f ? x : e - 1.f;
+}
+
 // phi in place on one [C][D] tile, rounded to nearest, with fp32 column sums
 // over rows < n_valid (rows >= n_valid, past the end of the sequence, become
 // zero). NT threads; warp w owns FCW = D / (NT / 4) consecutive 16-byte
@@ -80,7 +100,7 @@ struct ExactLayout {
   static_assert(FCW >= 1 && FCW <= 8 && (FCW & (FCW - 1)) == 0, "layout");
 };
 
-template <int D, int NT, bool kCheck, bool kSum, bool kScale = false>
+template <int D, int NT, bool kCheck, bool kSum, bool kScale = false, bool kPsi = false>
 __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r0, int n_valid, float (&zacc)[8],
                                                     float log2a = 0.f, int wbase = 0) {
   using X = ExactLayout<D, NT>;
@@ -99,8 +119,10 @@ __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r
       uint32_t* p = reinterpret_cast<uint32_t*>(&wv[i]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        float lo = valid ? phi_f32(__uint_as_float(p[h] << 16)) : 0.f;
-        float hi = valid ? phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)) : 0.f;
+        float lo = valid ? (kPsi ? psi_f32(__uint_as_float(p[h] << 16)) : phi_f32(__uint_as_float(p[h] << 16))) : 0.f;
+        float hi = valid ? (kPsi ? psi_f32(__uint_as_float(p[h] & 0xFFFF0000u))
+                                 : phi_f32(__uint_as_float(p[h] & 0xFFFF0000u)))
+                         : 0.f;
         if (kScale) {
           lo *= w;
           hi *= w;
@@ -122,7 +144,8 @@ __device__ __forceinline__ void phi_tile_exact_rows(uint8_t* base, int ch, int r
 // caller reduces them (reduce_row_groups) when it needs the totals.
 // kSum = false: phi only, zacc untouched. kScale: row r (of the tile) is
 // multiplied by a^(wbase - r), a = 2^log2a (decay weights), before rounding.
-template <int D, int NT, bool kReduce = true, bool kSum = true, bool kScale = false>
+// kPsi: psi = phi - 1 instead of phi (and its column sums).
+template <int D, int NT, bool kReduce = true, bool kSum = true, bool kScale = false, bool kPsi = false>
 __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid, float (&zacc)[8],
                                                float log2a = 0.f, int wbase = 0) {
   using X = ExactLayout<D, NT>;
@@ -137,9 +160,9 @@ __device__ __forceinline__ void phi_tile_exact(uint8_t* tile, int t, int n_valid
   }
   // full tiles skip the per-row validity test
   if (n_valid >= C)
-    phi_tile_exact_rows<D, NT, false, kSum, kScale>(base, ch, r0, n_valid, zacc, log2a, wbase);
+    phi_tile_exact_rows<D, NT, false, kSum, kScale, kPsi>(base, ch, r0, n_valid, zacc, log2a, wbase);
   else
-    phi_tile_exact_rows<D, NT, true, kSum, kScale>(base, ch, r0, n_valid, zacc, log2a, wbase);
+    phi_tile_exact_rows<D, NT, true, kSum, kScale, kPsi>(base, ch, r0, n_valid, zacc, log2a, wbase);
   if (kReduce && kSum) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -180,6 +203,37 @@ __device__ __forceinline__ void wcolsum_tile(const uint8_t* tile, const float* w
       for (int h = 0; h < 4; ++h) {
         acc[2 * h] = fmaf(wr[i], __uint_as_float(p[h] << 16), acc[2 * h]);
         acc[2 * h + 1] = fmaf(wr[i], __uint_as_float(p[h] & 0xFFFF0000u), acc[2 * h + 1]);
+      }
+    }
+  }
+}
+
+// Plain column sums over one [C][D] bf16 tile in the ExactLayout mapping:
+// acc[e] += sum over this thread's rows r < n_valid of tile[r][8 fc + e].
+template <int D, int NT>
+__device__ __forceinline__ void colsum_tile(const uint8_t* tile, int t, int n_valid, float (&acc)[8]) {
+  using X = ExactLayout<D, NT>;
+  constexpr int GR = 4;
+  const int wi = t >> 5, lane = t & 31;
+  const int fc = X::FCW * wi + (lane % X::FCW);
+  const int r0 = lane / X::FCW;
+  const uint8_t* base = tile + (fc >> 3) * BOX;
+  const int ch = fc & 7;
+#pragma unroll 1
+  for (int i0 = 0; i0 < X::RPT; i0 += GR) {
+    uint4 wv[GR];
+#pragma unroll
+    for (int i = 0; i < GR; ++i) {
+      const int r = r0 + X::RG * (i0 + i);
+      wv[i] = r < n_valid ? *reinterpret_cast<const uint4*>(base + sw128(r, ch)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < GR; ++i) {
+      const uint32_t* p = reinterpret_cast<const uint32_t*>(&wv[i]);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        acc[2 * h] += __uint_as_float(p[h] << 16);
+        acc[2 * h + 1] += __uint_as_float(p[h] & 0xFFFF0000u);
       }
     }
   }
@@ -271,16 +325,17 @@ __device__ __forceinline__ void store_state_from_tmem(float* dst, uint32_t lane_
 }
 
 // Sum of the D x D parts of the state records p0 .. p1-1 (`stride` floats
-// apart, row-major) for this thread's state row, into tensor memory at column
-// `col` (rows in the M = D accumulator layout; row < 0: lane unused).
+// apart, row-major) for this thread's state row, plus `add` in every entry,
+// into tensor memory at column `col` (rows in the M = D accumulator layout;
+// row < 0: lane unused).
 template <int D>
 __device__ __forceinline__ void sum_states_to_tmem(const float* recs, long long stride, int p0, int p1,
-                                                   uint32_t lane_addr, uint32_t col, int row) {
+                                                   uint32_t lane_addr, uint32_t col, int row, float add = 0.f) {
 #pragma unroll 1
   for (int h = 0; h < D; h += 64) {
     float4 acc[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 16; ++j) acc[j] = make_float4(add, add, add, add);
     if (row >= 0) {
 #pragma unroll 1
       for (int p = p0; p < p1; ++p) {
@@ -306,6 +361,25 @@ __device__ __forceinline__ void sum_states_to_tmem(const float* recs, long long 
     }
   }
   tmem_st_wait();
+}
+
+// Sum of entry `i` of the vector parts (at D*D) of the state records p0 .. p1-1.
+template <int D>
+__device__ __forceinline__ float sum_vector_entry(const float* recs, long long stride, int p0, int p1, int i) {
+  float acc = 0.f;
+#pragma unroll 1
+  for (int p = p0; p < p1; ++p) acc += recs[p * stride + D * D + i];
+  return acc;
+}
+
+// The value a centred record set adds to row `row` of the held state: the
+// sum of v over the records' tokens (entry D + row of the vector parts) for a
+// row of S^T, `n_tok` (the records' token count) for a row of z (row == D).
+template <int D>
+__device__ __forceinline__ float centred_row_add(const float* recs, long long stride, int p0, int p1, int row,
+                                                 float n_tok) {
+  if (row < 0) return 0.f;
+  return row < D ? sum_vector_entry<D>(recs, stride, p0, p1, D + row) : n_tok;
 }
 
 // Sum of the 8-entry slices [off, off + 8) of the vector parts (at D*D) of the

@@ -89,7 +89,7 @@ struct Cfg {
   // state kernel
   static constexpr int ST_S = D == 128 ? 3 : 6;    // state-pass stages (bytes in flight hide DRAM latency)
   static constexpr int STAGE_S = 2 * TILE;            // K, V
-  static constexpr uint32_t TMEM_COLS_S = D == 128 ? 128 : 64;
+  static constexpr uint32_t TMEM_COLS_S = 128;
 };
 
 template <int D>
@@ -115,7 +115,7 @@ struct FwdSmem {
 struct FwdParams {
   int N, P, seg_len, F;
   float eps;
-  const float* ws_state;   // [BH][P*F][D*D + D] sums of S^T, z over each state-pass part (segments 0..P-2)
+  const float* ws_state;   // [BH][P*F][rec_words] sums over each state-pass part (segments 0..P-2)
   __nv_bfloat16* out;      // [BH][N][D]
   float* S_final;          // [BH][D][D] or null (written by the last segment)
   float* z_final;          // [BH][D] or null
@@ -283,7 +283,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const bool write_final = last_seg && prm.S_final != nullptr;
   // the state update after the last chunk is only needed for the final state
   const int nupdates = write_final ? nchunks : nchunks - 1;
-  const long long rstride = (long long)(D * D + D);
+  const long long rstride = rec_words<D>();
   const float* recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
   const int nrec = seg * prm.F;           // records of the earlier segments
 
@@ -492,6 +492,11 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if constexpr (kDecay)
           sum_states_decayed<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum, log2a, tok0, prm.F,
                                 prm.seg_len, prm.sub_len);
+        else if constexpr (G::MERGE)
+          // centred records: S^T rows add the sum of their value component,
+          // the z rows the token count tok0
+          sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum,
+                                centred_row_add<D>(recs, rstride, 0, nrec, row_sum, (float)tok0));
         else
           sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, G::COL_S, row_sum);
       } else {
@@ -519,8 +524,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (ok) {
         tc_fence_after();
         store_state_transposed<D>(prm.S_final + (long long)bh * D * D, lane_addr, G::COL_S, row);
-        if (G::MERGE && q == 2) {
-          // z from the first z lane
+        if (G::MERGE && kDecay && q == 2) {
+          // z from the first z lane (without decay group C writes the exact sums)
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t v[32];
@@ -717,6 +722,11 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;       // holds the z of features 8 fc .. 8 fc + 7
     float zrun[8];
+    // MERGE without decay, last segment with a final state: per-thread
+    // partial sums of the exact fp32 phi(k) for the exported z
+    float zfin[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) zfin[e] = 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
@@ -729,6 +739,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if constexpr (kDecay)
           phi_tile_exact<D, 128, false, false, true>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum, log2a,
                                                      n_valid - 1);
+        else if (write_final)
+          phi_tile_exact<D, 128, false, true>(sm + s * G::STAGE + G::OFF_K, t, n_valid, zfin);  // K, sums
         else
           phi_tile_exact<D, 128, false, false>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);  // K
         fence_proxy_async_smem();
@@ -751,7 +763,15 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       for (int e = 0; e < 8; ++e) zrun[e] += colsum[e];
       mbar_arrive(&phi_done[s]);
     }
-    if (!G::MERGE && ok && write_final && owner) {
+    if (G::MERGE && !kDecay && ok && write_final) {
+      // z = (sum of the centred records' z_psi) + tok0 + this segment's exact sums
+      reduce_row_groups<D, 128>(zfin);
+      if (nrec > 0) griddep_wait();
+      sum_vectors8<D>(recs, rstride, 0, nrec, 8 * fc, zrun);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) zrun[e] += (float)tok0 + zfin[e];
+    }
+    if ((!G::MERGE || !kDecay) && ok && write_final && owner) {
       float4* zd = reinterpret_cast<float4*>(prm.z_final + (long long)bh * D + 8 * fc);
       zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
       zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
@@ -791,7 +811,7 @@ struct StateSmem {
 struct StateParams {
   int N, P, seg_len, F, sub_len;
   int nseg;         // segments summed: P - 1 (causal) or P (non-causal)
-  float* ws_state;  // [BH][P*F][D*D + D]
+  float* ws_state;  // [BH][P*F][rec_words]
   int* status;
   const float* alpha = nullptr;   // kDecay: [H] per-head factors
   int H = 1;
@@ -799,6 +819,11 @@ struct StateParams {
 
 // kDecay: each record is decayed to its part's last token (row j of a chunk
 // weighted a^(part_end - 1 - token)).
+// D = 64 without decay: centred records (see rec_words). The K tile becomes
+// psi(K) = phi(K) - 1, the MMA is [S_psi^T | sum v ; . | .] = [V^T ; 1]
+// [psi(K) | 1] (N = D + 16, the ones tile as the second 64-wide block of B,
+// so accumulator column D of lane m is the sum of v_m), and z_psi is summed
+// from the exact fp32 psi on the CUDA cores.
 template <int D, bool kDecay = false>
 __global__ void __launch_bounds__(320, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -834,6 +859,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   // a part past the end of a short last segment (non-causal) holds no token
   const int nchunks = max(0, (tok_end - tok0 + C - 1) / C);
   static_assert(!kDecay || StateSmem<D>::ZMMA, "decay gating is laid out for D = 64");
+  constexpr bool kCentre = L::ZMMA && !kDecay;
   const float log2a = kDecay ? log2f(prm.alpha[bh % prm.H]) : 0.f;
 
   if (tid == 0) {
@@ -884,8 +910,9 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      // S^T += V^T phi(K); ZMMA: [S^T ; z] += [V^T ; 1] phi(K)
-      constexpr uint32_t id_vk = make_idesc_bf16(L::ZMMA ? 128 : D, D, true, true);
+      // S^T += V^T phi(K); ZMMA: [S^T ; z] += [V^T ; 1] phi(K); kCentre:
+      // [S_psi^T | sum v ; z_psi | n] += [V^T ; 1] [psi(K) | 1]
+      constexpr uint32_t id_vk = make_idesc_bf16(L::ZMMA ? 128 : D, kCentre ? D + 16 : D, true, true);
       const uint32_t ones_a = smem_u32(sm + L::OFF_ONES);
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
@@ -893,7 +920,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const uint32_t ka = smem_u32(sm + s * G::STAGE_S);
         const uint32_t va = ka + G::TILE;
         const uint64_t dv = make_sdesc(va, L::ZMMA ? ones_a - va : (uint32_t)BOX, 1024, kSwizzle128B);
-        const uint64_t dk = make_sdesc(ka, BOX, 1024, kSwizzle128B);
+        const uint64_t dk = make_sdesc(ka, kCentre ? ones_a - ka : (uint32_t)BOX, 1024, kSwizzle128B);
         ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
@@ -927,6 +954,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       if (kDecay)
         phi_tile_exact<D, 256, false, false, true>(sm + s * G::STAGE_S, t, n_valid, zrun, log2a,
                                                    tok_end - 1 - (tok0 + c * C));
+      else if (kCentre)
+        phi_tile_exact<D, 256, false, true, false, true>(sm + s * G::STAGE_S, t, n_valid, zrun);
       else if (L::ZMMA)
         phi_tile_exact<D, 256, false, false>(sm + s * G::STAGE_S, t, n_valid, zrun);
       else
@@ -935,8 +964,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       mbar_arrive(&phi_done[s]);
     }
     reduce_row_groups<D, 256>(zrun);
-    float* dst = prm.ws_state + ((long long)bh * prm.P * prm.F + j) * (long long)(D * D + D);
-    if (!L::ZMMA && ok && lane < X::FCW) {
+    float* dst = prm.ws_state + ((long long)bh * prm.P * prm.F + j) * rec_words<D>();
+    if ((!L::ZMMA || kCentre) && ok && lane < X::FCW) {
       float4* zd = reinterpret_cast<float4*>(dst + D * D + 8 * fc);
       zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
       zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
@@ -946,7 +975,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       tc_fence_after();
       if (nchunks > 0) {
         store_state_from_tmem<D>(dst, lane_addr, 0, row);
-        if (L::ZMMA && q == 2) {
+        if (kCentre) {
+          // sum v_m from accumulator column D of lane m
+          uint32_t vs;
+          tmem_ld1(lane_addr + D, vs);
+          tmem_ld_wait();
+          if (row >= 0) dst[D * D + D + row] = __uint_as_float(vs);
+        }
+        if (L::ZMMA && !kCentre && q == 2) {
           // dz from the first z lane
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -963,7 +999,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         }
       } else {
         // no MMA wrote the accumulator: the empty part's record is zero
-        for (int i = t; i < (L::ZMMA ? D * D + D : D * D); i += 128) dst[i] = 0.f;
+        // (its z entries were written from zrun = 0 unless ZMMA without kCentre)
+        for (int i = t; i < (L::ZMMA && !kCentre ? D * D + D : D * D); i += 128) dst[i] = 0.f;
+        if (kCentre)
+          for (int i = t; i < D; i += 128) dst[D * D + D + i] = 0.f;
       }
     }
   }
@@ -1044,7 +1083,7 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
   const int tok0 = seg * prm.seg_len;
   const int tok_end = min(prm.N, tok0 + prm.seg_len);
   const int nchunks = (tok_end - tok0 + C - 1) / C;
-  const long long rstride = (long long)(D * D + D);
+  const long long rstride = rec_words<D>();
   const float* recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
   const int nrec = prm.P * prm.F;
 
@@ -1134,10 +1173,13 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
     griddep_wait();
-    sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, L::COL_S, row);
+    // D = 64: centred records (S^T rows add the sum of their value
+    // component, z adds the token count N)
+    sum_states_to_tmem<D>(recs, rstride, 0, nrec, lane_addr, L::COL_S, row,
+                          L::ZMMA ? centred_row_add<D>(recs, rstride, 0, nrec, row, (float)prm.N) : 0.f);
     copy_state_to_smem<D>(lane_addr + L::COL_S, sbuf, row);
     for (int i = t; i < D; i += 128) {
-      float acc = 0.f;
+      float acc = L::ZMMA ? (float)prm.N : 0.f;
       for (int p = 0; p < nrec; ++p) acc += recs[p * rstride + D * D + i];
       zn[i] = acc;
       if constexpr (L::ZMMA) {

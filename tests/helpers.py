@@ -13,31 +13,22 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}
 # bounded here at 1e-2. fp32 inputs keep fp32 phi throughout.
 STATE_TOL = {"f32": 1e-5, "bf16": 1e-2}
 
-# Normaliser tolerance (max abs error relative to max z). With bf16 inputs at
-# d = 64 the tensor cores sum z from the same bf16-rounded phi(k) that feed S
-# (so S and z weight every token alike): each term carries a relative error
-# of at most half a bf16 ulp, 2^-8, which is the bound at N = 1 (2.8e-3
-# observed); over N terms the unbiased rounding errors shrink like 1/sqrt(N).
-# Bounded like the state, at 1e-2.
-Z_TOL = {"f32": 1e-5, "bf16": 1e-2}
+# Normaliser tolerance (max abs error relative to max z). The exported z is
+# summed in fp32 from exact fp32 phi(k) on every path (the tensor-core state
+# records carry the centred sums of psi = phi - 1 exactly, plus the token
+# count), so bf16 inputs meet the fp32 bound.
+Z_TOL = {"f32": 1e-5, "bf16": 1e-5}
 
-# Gradient tolerances of the tensor-core backward (bf16 operands, fp32
-# accumulation), per gradient, max abs error relative to that gradient's
-# largest oracle magnitude. dq is ill-conditioned in the phi values: dphi(q_t)
-# = sum_j phi(k_j) ((v_j - o_t) . a_t), whose terms are 10-50 times the sum for
-# random inputs, so the bf16 rounding of phi(k) in the intra-chunk contraction
-# dP' phi(K) (relative 2^-9 per term) and of a and dP' leaves ~2.5 % (median)
-# and up to 5.9 % (worst of 80 seeds and shapes, causal and not, N = 129 ..
-# 4096) of max|dq|; an fp64 emulation of the kernel's roundings reproduces the
-# GPU's figure to three digits. dk and dv stay below 1.3 %. The CUDA-core path
-# (fp32 arithmetic) keeps TOL.
-GRAD_TOL_TC = {"dq": 8e-2, "dk": 2e-2, "dv": 2e-2}
+# The decay-gated forward sums z on the tensor cores from the decay-weighted
+# phi(k) rounded to bf16 (relative error up to 2^-9 per term, 2.8e-3 observed
+# at one token); bounded like the state.
+Z_TOL_DECAY_BF16 = 1e-2
 
 
 def grad_tol(dtype, tensor_core):
-    """Per-gradient tolerances (dq, dk, dv) for a backward path."""
-    if tensor_core and dtype == "bf16":
-        return [GRAD_TOL_TC[n] for n in ("dq", "dk", "dv")]
+    """Per-gradient tolerances (dq, dk, dv) of a backward path: the output
+    bound of the input dtype for every gradient, on either path."""
+    del tensor_core
     return [TOL[dtype]] * 3
 
 

@@ -90,6 +90,19 @@ def test_backward_tensor_core_noncausal(B, H, N):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("seed", range(20))
+def test_backward_tensor_core_seed_sweep(seed, causal):
+    """Twenty seeds per form across the chunk and segment structure (a chunk
+    and one token, ragged segments, many segments): every gradient within
+    the bf16 bound of 2e-2 of its largest oracle magnitude."""
+    N = (129, 1000, 4096, 8192)[seed % 4]
+    got, want = _grads(1, 2, N, seed=7000 + seed, causal=causal)
+    assert la.la_device_status(True) == la.LA_OK
+    errs = grad_errors(got, want)
+    assert grads_ok(errs, TC_TOL), errs
+
+
+@pytest.mark.parametrize("causal", [True, False])
 def test_backward_tensor_core_matches_cuda_core(causal):
     """Both paths implement the same gradient; on the same bf16 inputs they
     agree to the bf16 tolerance (each is also checked against the oracle)."""
