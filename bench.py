@@ -3,22 +3,23 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints ONE JSON line (rank 0). The headline workload is the causal forward
-B=4 H=8 N=4096 dk=dv=64 bf16 (one step = one la_forward over the batch: the
-per-segment state sums, the segment scan and the chunked output kernel).
-`value` is tokens/s (a token = one position of one sequence, all heads) with
-inputs resident in HBM; `e2e` is the same metric through the host-buffer
-C-ABI call la_forward_host (pinned host q, k, v, out; every step's
-host<->device copies inside the timed region; sequence groups overlap their
-copies with their neighbours' compute, and the unpipelined call is reported
-beside it). The other workloads of the method are measured in the same run and
-reported under "sections": the causal forward B=2 H=16 N=32768 d=128, the
-decode step on B=64 x H=32 fp32 states of d=128 (1024 steps in a CUDA graph),
-the same decode with 16 tokens per call (64 calls of la_decode_steps), the
-decay-gated and delta-rule variants in the same shape, forward + backward
-B=4 H=8 N=8192 d=64 (causal and not; the backward reuses the forward's
-state records through la_backward_saved), and the decay-gated forward in
-the headline shape.
+Prints ONE JSON line (rank 0). The headline workload is the largest
+single-GPU forward: causal, B=2 H=16 N=32768 dk=dv=128 bf16 (one step = one
+la_forward over the batch: the per-segment state sums and the chunked output
+kernel, which adds up the earlier segments' records). `value` is tokens/s (a
+token = one position of one sequence, all heads) with inputs resident in HBM;
+`e2e` is the same metric through the host-buffer C-ABI call la_forward_host
+(pinned host q, k, v, out; every step's host<->device copies inside the timed
+region; sequence groups overlap their copies with their neighbours' compute,
+and the unpipelined call is reported beside it). The other workloads of the
+method are measured in the same run and reported under "sections": the
+causal forward B=4 H=8 N=4096 d=64, the decode step on B=64 x H=32 fp32
+states of d=128 (1024 steps in a CUDA graph), the same decode with 16 tokens
+per call (64 calls of la_decode_steps), the decay-gated and delta-rule
+variants in the same shape, forward + backward B=4 H=8 N=8192 d=64 (causal
+and not; the backward reuses the forward's state records through
+la_backward_saved), and the decay-gated forward in the B=4 H=8 N=4096 d=64
+shape.
 
 Timing: W eager warm-up steps, then the K timed steps are captured once in a
 CUDA graph and replayed, bracketed by CUDA events on the launching stream
@@ -27,8 +28,10 @@ over enough copies that each step reads data not left in the 129 MB L2.
 Kernel spans (for the roofline) come from events the library records around
 its kernels (la_profile_enable), in a second graph of the same K steps.
 
---impl reference times the fp64 CPU oracle on a bounded sample of the same
-workload, on the host cores: the reference implementation of this method.
+cpu_baseline and --impl reference time the fp64 CPU oracle on a bounded
+sample of the same workload (a prefix of every sequence), its sequences
+spread over a process pool on all host cores: the reference implementation
+of this method.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (the
 path has no cross-GPU exchange); value = all ranks' tokens / max rank time.
@@ -76,7 +79,7 @@ WORKLOADS = {
                                  prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16,
                                  variant="delta"),
 }
-MAIN = "fwd_b4_h8_n4096_d64"
+MAIN = "fwd_b2_h16_n32768_d128"
 EPS = 1e-6
 E2E_SLICES = 2          # la_forward_host: sequence groups whose copies overlap compute (best measured)
 
@@ -474,23 +477,61 @@ def run_e2e(w, K, W, slices=E2E_SLICES):
 # ---------------------------------------------------------------------------
 
 
+def _oracle_task(args):
+    """One sequence of the oracle recurrence (runs in a pool worker)."""
+    import oracle as orc
+    q, k, v, causal, eps = args
+    out = orc.forward_recurrent(q, k, v, causal=causal, eps=eps)
+    return float(out[0, 0, -1, 0])
+
+
+_POOL = None
+
+
+def oracle_pool():
+    """A process pool with one worker per host core, started with spawn (the
+    workers import only numpy and the oracle; they never touch CUDA), warmed
+    so that its start-up stays out of the timings. Returns (pool, workers)."""
+    global _POOL
+    if _POOL is None:
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        try:
+            cores = len(os.sched_getaffinity(0))
+        except AttributeError:
+            cores = os.cpu_count() or 1
+        # one BLAS thread per worker: the pool provides the parallelism
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        pool = ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn"))
+        z = np.zeros((1, 1, 2, 4), np.float32)
+        list(pool.map(_oracle_task, [(z, z, z, True, EPS)] * cores))
+        _POOL = (pool, cores)
+    return _POOL
+
+
 def oracle_sample(w, budget_s=10.0):
     """Time the fp64 oracle recurrence on a prefix of every sequence of the
-    workload, growing the prefix until about ``budget_s`` of CPU work.
-    Returns (tokens/s, description, threads)."""
-    import oracle as orc
+    workload (one pool task per sequence, all host cores), growing the prefix
+    until about ``budget_s`` of wall time. Returns (tokens/s, description,
+    workers)."""
     from causal_linear_attention_la_gb300 import synth
+    pool, cores = oracle_pool()
     B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
     n = 32
     while True:
         q, k, v = synth.qkv(B, H, n, dk, dv, seed=w["seed"], dtype="bf16")
+        tasks = [(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], w.get("causal", True), EPS)
+                 for b in range(B) for h in range(H)]
         t0 = time.perf_counter()
-        orc.forward_recurrent(q, k, v, causal=w.get("causal", True), eps=EPS)
+        list(pool.map(_oracle_task, tasks))
         dt = time.perf_counter() - t0
         if dt >= budget_s or n >= N:
             break
         n = min(N, max(n * 2, int(n * budget_s / max(dt, 1e-3) * 0.9)))
-    return B * n / dt, f"oracle recurrence, all {B}x{H} sequences, first {n} of {N} tokens", 1
+    desc = (f"oracle recurrence (fp64 numpy), all {B}x{H} sequences, first {n} of {N} tokens, "
+            f"one sequence per task over {cores} worker processes")
+    return B * n / dt, desc, cores
 
 
 def reference_arm(args, world, rank):
@@ -623,8 +664,15 @@ def main():
                              "traffic": ncu_traffic(("variants_" if ws.get("variant") else "decode_") + name)},
                 "bytes_per_step": call_bytes,
                 "prefill_s_eager": rr["prefill_s"], "gpu_launches": rr["launches"],
-                "l2": f"state {decode_state_bytes(ws) / 2 / 1e6:.0f} MB > L2",
+                "l2": (f"state {decode_state_bytes(ws) / 2 / 1e6:.1f} MB, about the L2 "
+                       f"({L2_BYTES / 1e6:.1f} MB): consecutive steps can meet the previous step's "
+                       "lines in L2, so dram_frac counts measured DRAM bytes"),
             }
+            dram = ncu_traffic(("variants_" if ws.get("variant") else "decode_") + name)
+            if dram is not None:
+                sections[name]["dram_bytes_per_step"] = dram
+                sections[name]["dram_gbs"] = dram / per / 1e9
+                sections[name]["dram_frac"] = dram / per / 1e9 / peaks["hbm_gbs"]
         elif ws["kind"] == "fwdbwd":
             kk = max(3, K // 5)
             rr = run_forward(ws, kk, W, barrier, with_bwd=True)
