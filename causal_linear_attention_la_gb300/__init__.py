@@ -30,7 +30,7 @@ __all__ = [
     "la_forward_workspace_size", "la_backward_workspace_size",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
-    "la_device_status", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
+    "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "la_forward_host", "la_forward_host_workspace_size", "forward_host",
     "la_backward_saved", "backward_saved",
     "forward", "decode_step", "decode_steps", "backward",
@@ -52,7 +52,7 @@ exported_symbols = (
     "la_backward_workspace_size", "la_backward",
     "la_set_path", "la_forward_path", "la_backward_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
-    "la_device_status", "la_forward_noalloc",
+    "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc",
     "la_forward_host_workspace_size", "la_forward_host", "la_backward_saved",
 )
 
@@ -127,6 +127,8 @@ def lib():
     h.la_backward_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
     h.la_device_status.restype = _c_int
     h.la_device_status.argtypes = [_c_int]
+    h.la_test_timeout_next_forward.restype = None
+    h.la_test_timeout_next_forward.argtypes = []
     h.la_forward_noalloc.restype = _c_int
     h.la_forward_noalloc.argtypes = ([_c_void] * 4 + [_c_int] * 6 + [_c_float, _c_int]
                                      + [_c_void, _c_void, _c_void])
@@ -238,6 +240,10 @@ def la_backward_path(dk, dv, dtype, causal=True):
 
 def la_device_status(clear=False):
     return lib().la_device_status(int(clear))
+
+
+def la_test_timeout_next_forward():
+    lib().la_test_timeout_next_forward()
 
 
 def la_profile_enable(on):

@@ -23,6 +23,7 @@ namespace {
 
 thread_local char g_last_error[256] = "";
 std::atomic<int> g_path{LA_PATH_AUTO};
+std::atomic<int> g_timeout_test{0};
 
 la_status fail(la_status s, const char* fmt, ...) {
   va_list ap;
@@ -170,6 +171,8 @@ int* device_status_ptr() {
   }
   return cache[dev];
 }
+
+bool take_timeout_test() { return g_timeout_test.exchange(0) != 0; }
 
 // Pick the number of segments per sequence. Cost model in units of one
 // kSegGranule-token chunk: every CTA pays its chunks plus about one chunk of
@@ -499,6 +502,8 @@ int la_profile_read(int* labels, float* ms, int max) {
 }
 
 long long la_launch_count(void) { return g_launches.load(); }
+
+void la_test_timeout_next_forward(void) { la::g_timeout_test.store(1); }
 
 la_status la_device_status(int clear) {
   int v = 0;

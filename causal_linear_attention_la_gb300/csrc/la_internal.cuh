@@ -17,9 +17,6 @@ namespace la {
 // phi'(x) = 1 for x >= 0 and exp(x) for x < 0, i.e. min(phi(x), 1).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float phi(float x) { return x >= 0.f ? x + 1.f : expf(x); }
-// Same map with the fast exponential (ex2.approx based); used where the
-// result is rounded to bf16 anyway.
-__device__ __forceinline__ float phi_fast(float x) { return x >= 0.f ? x + 1.f : __expf(x); }
 __device__ __forceinline__ float phi_prime_from_phi(float p) { return fminf(p, 1.f); }
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);
@@ -116,6 +113,9 @@ cudaError_t tc_backward(const BwdArgs& a);
 // Device status word of the current device (set to LA_ERR_TIMEOUT by a
 // kernel whose bounded wait gave up); NULL if it cannot be resolved.
 int* device_status_ptr();
+// One-shot test switch (la_test_timeout_next_forward): true once after the
+// switch is set, then false until it is set again.
+bool take_timeout_test();
 
 // Record a one-line reason for `s` as this thread's la_last_error; returns s.
 la_status set_error(la_status s, const char* msg);

@@ -84,6 +84,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait for phase `parity` of `bar` regardless of the CTA's abort flag, giving
+// up only after `timeout_ns`: for draining work already in flight (TMA loads
+// into shared memory, MMAs into tensor memory) before a CTA releases its
+// shared and tensor memory, also on the abort path.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // As mbar_wait, but polling without suspending: for the single thread that
 // issues MMAs, whose wake-up latency is on the critical path.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -274,17 +287,22 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_m
 }
 
 // phi(x) = elu(x) + 1 on a pair of bf16 values, in bf16 arithmetic:
-//   phi(x) = max(x, 0) + min(e^x, 1)
+//   phi(x) = max(x, 0) + min(max(e^x, 2^-62), 1)
 // (x >= 0: e^x >= 1, so the sum is x + 1 with one rounding; x < 0: 0 + e^x).
 // e^x = 2^(x log2 e) with the hardware base-2 exponential on bf16 pairs; the
 // product x log2 e is formed as fma(x, a, x b) with log2 e = a + b, a its bf16
 // head (1.4453125) and b the bf16 of the remainder (-0.00262451171875), so it
-// is rounded once. Exponents below the normal range flush to zero.
+// is rounded once. Values below 2^-62 (x < -43) are raised to 2^-62: phi
+// stays positive for any finite input (the exponential alone flushes below
+// 2^-126 to zero), and the product of two features stays a normal fp32
+// number, so that every normaliser of a query with a nonempty prefix is
+// positive. The change is below 2^-62 per feature.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
   uint32_t u, t, e, m, r;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(u) : "r"(x), "r"(0xBB2CBB2Cu));
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(0x3FB93FB9u), "r"(u));
   asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(e) : "r"(e), "r"(0x20802080u));
   asm("min.bf16x2 %0, %1, %2;" : "=r"(e) : "r"(e), "r"(0x3F803F80u));
   asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(0u));
   asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(e));

@@ -503,7 +503,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
       tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
-        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[c % ST], (c / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 17) {
     // ---------------- MMA issuer ----------------
@@ -576,7 +576,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         tc_commit(&empty[s]);
       }
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- group A: phi(Q), S_prev copies, R ----------------
@@ -745,9 +745,10 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   }
 
   // ---------------- teardown ----------------
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
@@ -918,7 +919,7 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
       tma_store_wait<0>();
       for (int i = max(0, issued - ST); i < issued; ++i)
-        mbar_wait(&full[i % ST], (i / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[i % ST], (i / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
@@ -983,7 +984,7 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         tc_commit(&empty[s]);
       }
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- group A: phi(Q), R_after copies, r_after ----------------
@@ -1107,9 +1108,10 @@ tc_bwd2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   }
 
   // ---------------- teardown ----------------
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
@@ -1288,7 +1290,7 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
       for (int c = max(0, issued - ST); c < issued && ok; ++c) ok = retire(c);
       tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
-        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[c % ST], (c / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
@@ -1339,7 +1341,7 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         tc_commit(&empty[s]);
       }
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp < 4) {
     // ---------------- group A: phi(Q), totals, r, R ----------------
@@ -1460,9 +1462,10 @@ tc_bwd_nc_a_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
   }
 
   // ---------------- teardown ----------------
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
@@ -1594,7 +1597,7 @@ tc_bwd_nc_b_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_const
       for (int c = max(0, issued - ST); c < issued && ok; ++c) ok = retire(c);
       tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
-        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[c % ST], (c / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
@@ -1624,7 +1627,7 @@ tc_bwd_nc_b_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_const
         tc_commit(&empty[s]);
       }
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp < 4) {
     // ---------------- group C: phi(K) ----------------
@@ -1676,9 +1679,10 @@ tc_bwd_nc_b_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_const
   }
 
   // ---------------- teardown ----------------
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);

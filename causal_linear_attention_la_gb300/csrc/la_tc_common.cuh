@@ -69,12 +69,14 @@ __device__ __forceinline__ void phi_tile_bf16(uint8_t* tile, int t) {
 }
 
 // phi(x) in fp32 without branches: x + 1 for x > 0, e^x otherwise, with
-// e^x = 2^(x log2 e) from the hardware base-2 exponential (results below the
-// normal range flush to zero). Rounded to bf16 by the caller.
+// e^x = 2^(x log2 e) from the hardware base-2 exponential. Values below
+// 2^-62 are raised to 2^-62 (as in phi_bf16x2): phi stays positive and the
+// product of two features a normal fp32 number. Rounded to bf16 by the
+// caller.
 __device__ __forceinline__ float phi_f32(float x) {
   float e;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
-  return x > 0.f ? x + 1.f : e;
+  return x > 0.f ? x + 1.f : fmaxf(e, 2.16840434e-19f);
 }
 
 // psi(x) = phi(x) - 1: x for x > 0 (exact), e^x - 1 otherwise (the

@@ -106,7 +106,7 @@ struct FwdSmem {
   static constexpr int OFF_SBUF = OFF_OUT + (G::MERGE ? 2 * G::TILE : 0);  // !MERGE: the S^T copy (1024-aligned)
   static constexpr int OFF_ZST = OFF_SBUF + (G::MERGE ? 0 : G::SBUF);  // !MERGE: [ST][D] fp32 z before each staged chunk
   static constexpr int OFF_BAR = OFF_ZST + (G::MERGE ? 0 : G::ST * D * 4);
-  static constexpr int NBAR = 4 * G::ST + 2 * G::NPB + 2 * G::NOB + 3;
+  static constexpr int NBAR = 4 * G::ST + 2 * G::NPB + 2 * G::NOB + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -124,6 +124,9 @@ struct FwdParams {
   const float* alpha = nullptr;   // [H]
   int H = 1;
   int sub_len = 0;
+  // test of the bounded waits: the MMA issuer first waits on a barrier that
+  // nothing completes (la_test_timeout_next_forward)
+  int timeout_test = 0;
 };
 
 // With decay gating (kDecay, D = 64): S_t = a S_{t-1} + phi(k_t) v_t^T and the
@@ -259,6 +262,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint64_t* s_ready = s_full + 1;
   uint64_t* mma_fin = s_full + 2;
   uint64_t* ost_full = s_full + 3;                // [ST] output tile of the staged chunk written (group B)
+  uint64_t* never = ost_full + ST;                // completed by nobody (timeout test)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
   // the swizzled operand boxes need 1024-byte alignment of the shared window
@@ -305,6 +309,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     mbar_init(s_ready, 128);
     mbar_init(mma_fin, 1);
     for (int i = 0; i < ST; ++i) mbar_init(&ost_full[i], 128);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -369,7 +374,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       // before the CTA's shared memory is released
       tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
-        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[c % ST], (c / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 13) {
     // ---------------- MMA issuer ----------------
@@ -396,7 +401,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_commit(&empty[s]);
         return true;
       };
-      bool ok = true;
+      // timeout test: a wait that can only give up (no MMA is issued)
+      bool ok = prm.timeout_test ? mbar_wait(never, 0, abort_flag, kTimeoutNs) : true;
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST;
         const uint32_t qa = smem_u32(sm + s * G::STAGE);
@@ -461,7 +467,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (G::MERGE && ok && nchunks > 0) ok = issue_pv(nchunks - 1);
       // every MMA issued must have finished before tensor memory is released
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- group A: phi(Q), state copy ----------------
@@ -779,9 +785,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
 
   // ---------------- teardown ----------------
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
@@ -906,7 +913,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         issued = c + 1;
       }
       for (int c = max(0, issued - ST); c < issued; ++c)
-        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[c % ST], (c / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 9) {
     if (lane == 0) {
@@ -931,7 +938,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       }
       tc_commit(s_full);
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else {
     using X = ExactLayout<D, 256>;
@@ -1006,9 +1013,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       }
     }
   }
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS_S);
@@ -1142,7 +1150,7 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       for (int c = stored; c < issued && ok; ++c) ok = store_out(c);
       tma_store_wait<0>();
       for (int c = max(0, issued - ST); c < issued; ++c)
-        mbar_wait(&full[c % ST], (c / ST) & 1, abort_flag, kTimeoutNs);
+        mbar_drain(&full[c % ST], (c / ST) & 1, kTimeoutNs);
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer: O = phi(Q) S_N ----------------
@@ -1164,7 +1172,7 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         tc_commit(&o_full[ob]);
       }
       tc_commit(mma_fin);
-      mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
+      mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp < 4) {
     // ---------------- group A: S_N, z_N; phi(Q) ----------------
@@ -1272,9 +1280,10 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
   }
 
   // ---------------- teardown ----------------
-  if (*abort_flag && tid == 0) report_timeout(prm.status);
   tc_fence_before();
   __syncthreads();
+  // after the barrier: a warp that gave up late is seen too
+  if (*abort_flag && tid == 0) report_timeout(prm.status);
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, L::TMEM_COLS);
@@ -1350,6 +1359,7 @@ cudaError_t launch_forward(const FwdArgs& a, const float* alpha = nullptr, int H
   p.alpha = alpha;
   p.H = H;
   p.sub_len = state_sub_len(a.plan);
+  p.timeout_test = (!kDecay && take_timeout_test()) ? 1 : 0;
   // a dependent of the state kernel (when there is one): it may start before
   // that kernel ends and waits for its records only where it reads them
   cudaLaunchConfig_t cfg{};

@@ -337,16 +337,25 @@ LA_API int la_backward_path(int dk, int dv, la_dtype dtype, int causal);
 LA_API la_status la_device_status(int clear);
 
 /*
+ * Test switch for the bounded waits above. The next causal tensor-core
+ * la_forward launch (bf16, dk = dv in {64, 128}) has its MMA-issuing thread
+ * wait on a barrier that nothing ever completes: the wait gives up after its
+ * limit (2 s), the kernel winds down without issuing any MMA, and
+ * la_device_status reports LA_ERR_TIMEOUT. That call's outputs are
+ * unspecified; later calls run normally. One-shot, process-wide. For tests of
+ * the failure path only; it faults nothing.
+ */
+LA_API void la_test_timeout_next_forward(void);
+
+/*
  * Forward pass for callers that cannot allocate device memory.
  *
  * The pages describe no counterpart to this entry point: it exists for
  * integration. la_forward needs scratch memory, which callers normally
- * allocate once and pass in. Some callers cannot: code that runs while a
- * stream is being captured into a CUDA graph (cudaMalloc is not a stream
- * operation and cannot be captured), plugin or custom-operator hosts that own
- * all device memory and hand an operator only its input and output buffers,
- * and latency-critical serving loops where cudaMalloc's implicit device
- * synchronisation is unacceptable.
+ * allocate once and pass in. Some callers cannot: plugin or custom-operator
+ * hosts that own all device memory and hand an operator only its input and
+ * output buffers, and latency-critical serving loops where cudaMalloc's
+ * implicit device synchronisation is unacceptable.
  *
  * la_forward_noalloc computes exactly what la_forward computes, with the
  * same arguments except the workspace, which here is a file-scope device
@@ -354,8 +363,11 @@ LA_API la_status la_device_status(int clear);
  * the library holds that array until the process exits.
  *
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and caches it for the
+ *    life of the process; make that first call before any stream capture.
+ *    A cudaDeviceReset (or anything else that destroys the device's primary
+ *    context) leaves the cached address stale: calling la_forward_noalloc on
+ *    that device afterwards is not supported.
  *  - Problems whose scratch (la_forward_workspace_size) exceeds
  *    LA_NOALLOC_SCRATCH_BYTES are rejected with LA_ERR_INVALID_ARG before
  *    anything is launched.

@@ -132,6 +132,25 @@ def test_backward_tensor_core_eps_zero(causal):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+def test_backward_tensor_core_extreme_inputs(causal):
+    """bf16 q, k of large magnitude (N(0, 30^2) clipped to +-100, so phi runs
+    from e^-100 to 101) and eps = 0: finite gradients within the bf16 bound."""
+    rng = np.random.default_rng(77 + causal)
+    B, H, N = 1, 2, 700
+    q = synth.round_to_bf16(np.clip(rng.standard_normal((B, H, N, 64)) * 30, -100, 100).astype(np.float32))
+    k = synth.round_to_bf16(np.clip(rng.standard_normal((B, H, N, 64)) * 30, -100, 100).astype(np.float32))
+    v = synth.round_to_bf16((rng.standard_normal((B, H, N, 64)) / 8).astype(np.float32))
+    g = synth.round_to_bf16(rng.standard_normal((B, H, N, 64)).astype(np.float32))
+    got = la.backward(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"), to_dev(g, "bf16"),
+                      causal=causal, eps=0.0)
+    want = orc.backward_recurrent(q, k, v, g, causal=causal, eps=0.0)
+    assert la.la_device_status(True) == la.LA_OK
+    assert all(np.all(np.isfinite(to_host(t))) for t in got)
+    errs = grad_errors(got, want)
+    assert grads_ok(errs, TC_TOL), errs
+
+
+@pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("B,H,N", [
     (1, 1, 100),      # one segment: no records (causal)
     (2, 3, 1000),     # several segments, ragged tail

@@ -2,11 +2,14 @@
 times (default path, one call per pass):
 
 * causal forward B=4 H=8 N=4096 d=64 bf16: every output vs the oracle recurrence
-* causal forward B=2 H=16 N=32768 d=128 bf16: sampled outputs, each computed
-  one by one by the oracle's definition, plus the final state of two heads
+* causal forward B=2 H=16 N=32768 d=128 bf16: two whole heads (every one of
+  their 32768 outputs and the final state) against the oracle recurrence,
+  plus outputs of every head sampled at chunk edges and at random, each
+  computed one by one by the oracle's definition
 * decode: fp32 states from a bf16 prefill of N=131072 tokens on B=1 H=16,
-  replicated to B=64 x H=32, then one-token steps; every state for the first
-  steps, sampled states for more
+  replicated to B=64 x H=32, then 1024 one-token steps; every state's output
+  for the first 8 steps, and 64 sampled states' outputs for all 1024 steps
+  (and their final states)
 * forward + backward B=4 H=8 N=8192 d=64 bf16: every gradient vs the oracle,
   causal and non-causal
 * decay-gated forward B=4 H=8 N=4096 d=64 bf16 (per-head factors 0.9 ..
@@ -45,7 +48,7 @@ def test_forward_b4_h8_n4096_d64():
     assert err <= TOL["bf16"], err
 
 
-def test_forward_b2_h16_n32768_d128_sampled():
+def test_forward_b2_h16_n32768_d128():
     import torch
     B, H, N, d = 2, 16, 32768, 128
     q, k, v = synth.qkv(B, H, N, d, d, seed=3, dtype="bf16")
@@ -53,8 +56,15 @@ def test_forward_b2_h16_n32768_d128_sampled():
                            return_state=True)
     torch.cuda.synchronize()
     out = out.float().cpu().numpy()
-    rng = np.random.default_rng(0)
     vmax = np.abs(v).max()
+    # two whole heads, every output and the final state, element by element
+    for b, h in ((0, 0), (1, H - 1)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        want, S_w, z_w = orc.forward_recurrent(q[sl], k[sl], v[sl], eps=1e-6, return_state=True)
+        assert rel_err(out[sl], want, vmax) <= TOL["bf16"], (b, h)
+        assert rel_err(to_host(S[b, h]), S_w[0, 0], np.abs(S_w).max()) <= STATE_TOL["bf16"]
+        assert rel_err(to_host(z[b, h]), z_w[0, 0], np.abs(z_w).max()) <= Z_TOL["bf16"]
+    rng = np.random.default_rng(0)
     worst = 0.0
     picks = [(b, h, t) for b in range(B) for h in (0, H - 1) for t in (0, 127, 128, N - 1)]
     picks += [(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N)))
@@ -74,6 +84,7 @@ def test_decode_b64_h32_d128_from_prefill_n131072():
     import torch
     d, Hp, Np = 128, 16, 131072
     B, H = 64, 32
+    steps, full_steps = 1024, 8
     qp, kp, vp = synth.qkv(1, Hp, Np, d, d, seed=4, dtype="bf16")
     _, Sp, zp = la.forward(to_dev(qp, "bf16"), to_dev(kp, "bf16"), to_dev(vp, "bf16"),
                            return_state=True)
@@ -83,29 +94,36 @@ def test_decode_b64_h32_d128_from_prefill_n131072():
     z_or = np.stack([orc.phi_elu1(kp[0, h]).sum(0) for h in range(Hp)])
     del qp, kp, vp
     assert rel_err(to_host(Sp[0]), S_or, np.abs(S_or).max()) <= STATE_TOL["bf16"]
+    assert rel_err(to_host(zp[0]), z_or, np.abs(z_or).max()) <= Z_TOL["bf16"]
     # state (b, h) starts from prefill head (b*H + h) mod Hp
     src = (np.arange(B * H) % Hp)
     S = Sp[0][torch.from_numpy(src).cuda()].reshape(B, H, d, d).contiguous()
     z = zp[0][torch.from_numpy(src).cuda()].reshape(B, H, d).contiguous()
     S_ref = S_or[src].reshape(B, H, d, d)
     z_ref = z_or[src].reshape(B, H, d)
-    sample = [(0, 0), (5, 17), (63, 31), (31, 8)]
-    S_s = np.stack([S_ref[b, h] for b, h in sample])
-    z_s = np.stack([z_ref[b, h] for b, h in sample])
-    worst = 0.0
-    for step in range(16):
+    # 64 sampled states followed through all steps
+    pick = np.sort(np.random.default_rng(7).choice(B * H, 64, replace=False))
+    idx = (pick // H, pick % H)
+    S_s, z_s = S_ref[idx].copy(), z_ref[idx].copy()
+    worst_all = worst_s = 0.0
+    for step in range(steps):
         q, k, v = synth.decode_token(B, H, d, d, seed=1000, step=step)
         out = la.decode_step(S, z, to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
         torch.cuda.synchronize()
         got = to_host(out)
         vmax = np.abs(v).max()
-        if step < 2:   # every state
+        if step < full_steps:   # every state
             S_ref, z_ref, o_ref = orc.decode_step(S_ref, z_ref, q, k, v)
-            worst = max(worst, rel_err(got, o_ref, vmax))
-        idx = tuple(np.array(sample).T)
+            worst_all = max(worst_all, rel_err(got, o_ref, vmax))
         S_s, z_s, o_s = orc.decode_step(S_s, z_s, q[idx], k[idx], v[idx])
-        worst = max(worst, rel_err(got[idx], o_s, vmax))
-    assert worst <= TOL["bf16"], worst
+        worst_s = max(worst_s, rel_err(got[idx], o_s, vmax))
+    assert worst_all <= TOL["bf16"], worst_all
+    assert worst_s <= TOL["bf16"], worst_s
+    # the sampled states after all steps (fp32 in-place updates)
+    S_h = to_host(S)[idx]
+    z_h = to_host(z)[idx]
+    assert rel_err(S_h, S_s, np.abs(S_s).max()) <= STATE_TOL["bf16"]
+    assert rel_err(z_h, z_s, np.abs(z_s).max()) <= Z_TOL["bf16"]
 
 
 def test_forward_backward_b4_h8_n8192_d64():

@@ -102,6 +102,56 @@ def test_forward_extreme_inputs():
     assert rel_err(got, want, np.abs(v).max()) <= TOL["f32"]
 
 
+def _extreme_bf16(B, H, N, d, seed):
+    """bf16 q, k of large magnitude (N(0, 30^2), clipped to +-100: phi runs
+    from e^-100 to 101), v of unit scale / 8."""
+    rng = np.random.default_rng(seed)
+    q = synth.round_to_bf16(np.clip(rng.standard_normal((B, H, N, d)) * 30, -100, 100).astype(np.float32))
+    k = synth.round_to_bf16(np.clip(rng.standard_normal((B, H, N, d)) * 30, -100, 100).astype(np.float32))
+    v = synth.round_to_bf16((rng.standard_normal((B, H, N, d)) / 8).astype(np.float32))
+    return q, k, v
+
+
+def _hull_ok(out, v, causal):
+    """Each output coordinate lies between min(0, min_j v_j) and
+    max(0, max_j v_j) over the keys it reads (j <= t causal, all j otherwise):
+    the outputs are nonnegative weightings of v with weights summing to at
+    most 1 ("Linear Attention: KV를 고정 크기 상태에 누적하기", section
+    "점수의 합으로 나누기")."""
+    if causal:
+        lo = np.minimum(np.minimum.accumulate(v, axis=2), 0.0)
+        hi = np.maximum(np.maximum.accumulate(v, axis=2), 0.0)
+    else:
+        lo = np.minimum(v.min(axis=2, keepdims=True), 0.0)
+        hi = np.maximum(v.max(axis=2, keepdims=True), 0.0)
+    slack = 2.0 ** -8 * np.abs(v).max()      # the bf16 rounding of the output
+    return bool(np.all(out >= lo - slack) and np.all(out <= hi + slack))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("eps", [0.0, 1e-6])
+def test_forward_extreme_inputs_tensor_core(d, causal, eps):
+    """bf16 inputs of large magnitude through the tensor-core kernels, eps = 0
+    included. The kernels' exponential flushes results below the normal range
+    to zero; phi is raised to the smallest normal there, so that phi > 0 (the
+    feature map's defining property, "Transformers are RNNs" review,
+    feature-map table) and every normaliser stays positive. Row 5 of every
+    query has all features at -100 (phi(q) = e^-100 in the oracle): the
+    output must still be finite and match."""
+    import torch
+    B, H, N = 1, 2, 700
+    q, k, v = _extreme_bf16(B, H, N, d, seed=d + 3 * causal + int(eps > 0))
+    q[:, :, 5, :] = -100.0
+    want = orc.forward_recurrent(q, k, v, causal=causal, eps=eps)
+    got = to_host(_run(q, k, v, causal, "bf16", eps=eps))
+    assert la.la_forward_path(d, d, la.LA_BF16, causal) == 1
+    assert la.la_device_status(True) == la.LA_OK
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, want, np.abs(v).max()) <= TOL["bf16"]
+    assert _hull_ok(got, v.astype(np.float64), causal)
+
+
 def test_empty_sequence_zeroes_state():
     import torch
     q = torch.zeros((2, 3, 0, 16), device="cuda")

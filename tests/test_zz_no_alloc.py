@@ -1,13 +1,18 @@
 """la_forward_noalloc, the forward entry point for callers that cannot
-allocate device memory (graph-capture regions, operator hosts that own all
-device memory, latency-critical loops): its scratch is a static device array
-inside the library instead of a caller-provided workspace.
+allocate device memory (operator hosts that own all device memory and hand an
+operator only its inputs and outputs, latency-critical loops that cannot
+afford cudaMalloc's implicit synchronisation): its scratch is a static device
+array inside the library instead of a caller-provided workspace.
 
-Through the C ABI, two calls in a row must each match la_forward (with a
-caller-allocated workspace) on the same inputs, within the parity tolerance
-of the other tests; a problem whose scratch exceeds the static array must be
-rejected before anything is launched. Collected last so that a failure here
-never hides the results of the other GPU tests.
+Through the C ABI, calls in a row must each match la_forward (with a
+caller-allocated workspace) on the same inputs: within the parity tolerance
+of the other tests, and in fact bit for bit, since both run the same kernels
+on the same inputs. Between two calls of one shape come calls that change the
+shape, the causality and the dtype, so that every call must rewrite each
+record it reads whatever the previous call left in the shared array. A
+problem whose scratch exceeds the static array must be rejected before
+anything is launched. Collected last so that a failure here never hides the
+results of the other GPU tests.
 """
 
 import numpy as np
@@ -15,7 +20,7 @@ import pytest
 
 import causal_linear_attention_la_gb300 as la
 from causal_linear_attention_la_gb300 import synth
-from helpers import STATE_TOL, TOL, build_lib, rel_err, to_dev, to_host
+from helpers import STATE_TOL, TOL, Z_TOL, build_lib, rel_err, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -42,23 +47,34 @@ def _noalloc(q, k, v, causal, code):
     return out, S, z
 
 
-@pytest.mark.parametrize("dtype,shape", [("bf16", (4, 8, 4096, 64, 64)),
-                                         ("f32", (1, 2, 1000, 32, 64))])
-def test_noalloc_matches_forward_on_two_calls(dtype, shape):
+# (dtype, (B, H, N, dk, dv), causal, seed): the first shape twice, with a
+# different shape, a non-causal call and the CUDA-core (fp32) path between
+CALLS = [
+    ("bf16", (4, 8, 4096, 64, 64), True, 41),
+    ("bf16", (2, 3, 1000, 64, 64), False, 43),
+    ("f32", (1, 2, 1000, 32, 64), True, 44),
+    ("bf16", (1, 2, 5000, 128, 128), True, 45),
+    ("bf16", (4, 8, 4096, 64, 64), True, 42),
+]
+
+
+def test_noalloc_matches_forward_on_calls_in_a_row():
     import torch
-    B, H, N, dk, dv = shape
-    code = la.LA_BF16 if dtype == "bf16" else la.LA_F32
-    assert la.la_forward_workspace_size(B, H, N, dk, dv, 1, code) <= la.LA_NOALLOC_SCRATCH_BYTES
-    for seed in (41, 42):   # two calls in a row reuse the same static scratch
+    for dtype, (B, H, N, dk, dv), causal, seed in CALLS:
+        code = la.LA_BF16 if dtype == "bf16" else la.LA_F32
+        assert la.la_forward_workspace_size(B, H, N, dk, dv, causal, code) <= la.LA_NOALLOC_SCRATCH_BYTES
         q, k, v = synth.qkv(B, H, N, dk, dv, seed=seed, dtype=dtype)
         qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
-        ref, S_ref, z_ref = la.forward(qd, kd, vd, return_state=True)
-        out, S, z = _noalloc(qd, kd, vd, True, code)
+        ref, S_ref, z_ref = la.forward(qd, kd, vd, causal=causal, return_state=True)
+        out, S, z = _noalloc(qd, kd, vd, causal, code)
         torch.cuda.synchronize()
-        assert rel_err(to_host(out), to_host(ref), np.abs(v).max()) <= TOL[dtype]
-        S_ref_h = to_host(S_ref)
-        assert rel_err(to_host(S), S_ref_h, np.abs(S_ref_h).max()) <= STATE_TOL[dtype]
         assert la.la_device_status(True) == la.LA_OK
+        ref_h, S_ref_h, z_ref_h = to_host(ref), to_host(S_ref), to_host(z_ref)
+        assert rel_err(to_host(out), ref_h, np.abs(v).max()) <= TOL[dtype]
+        assert rel_err(to_host(S), S_ref_h, np.abs(S_ref_h).max()) <= STATE_TOL[dtype]
+        assert rel_err(to_host(z), z_ref_h, np.abs(z_ref_h).max()) <= Z_TOL[dtype]
+        assert torch.equal(out, ref), (dtype, B, H, N, causal)
+        assert torch.equal(S, S_ref) and torch.equal(z, z_ref), (dtype, B, H, N, causal)
 
 
 def test_noalloc_rejects_oversized_problem():
