@@ -218,24 +218,21 @@ __device__ __forceinline__ float grad_row_pass_centred(uint32_t taddr, uint8_t* 
   return b1;
 }
 
-// Sum of the entries j <= r of one 128-column fp32 row in tensor memory (row
-// r = 32 q + lane of the chunk), in fp32.
-__device__ __forceinline__ float masked_rowsum_lower(uint32_t taddr, int q, int lane) {
-  float sum = 0.f;
-#pragma unroll 1
-  for (int p = 0; p <= q; ++p) {
-    uint32_t v[32];
-    tmem_ld32(taddr + 32 * p, v);
-    tmem_ld_wait();
-    if (p < q) {
+// The masked constant row [x for j <= r, 0 for j > r] (r = 32 q + lane) as
+// 64 packed bf16 columns at tensor-memory address `taddr`.
+__device__ __forceinline__ void store_lower_block(uint32_t taddr, int q, int lane, float x) {
+  const uint32_t xx = pack_bf16x2(x, x), x0 = pack_bf16x2(x, 0.f);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) sum += __uint_as_float(v[j]);
-    } else {
+  for (int p = 0; p < 4; ++p) {
+    uint32_t w[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) sum += j <= lane ? __uint_as_float(v[j]) : 0.f;
+    for (int j = 0; j < 16; ++j) {
+      // columns 2j, 2j + 1 of piece p
+      const int c0 = 2 * j;
+      w[j] = p < q ? xx : p > q ? 0u : (c0 + 1 <= lane ? xx : c0 <= lane ? x0 : 0u);
     }
+    tmem_st16(taddr + 16 * p, w);
   }
-  return sum;
 }
 
 // Row pass of sweep 1: with the numerator row O_r (fp32, tensor memory) and
@@ -376,8 +373,9 @@ struct Bwd1Params {
 
 // Warp roles (576 threads):
 //   warps 0-3    group C: psi(K) in place (exact fp32, rounded), z_psi and the
-//                sum of v; the r sums
-//   warps 4-7    group A: phi(Q) in place; bf16 copies of S_psi,prev; final R store
+//                sum of v
+//   warps 4-7    group A: phi(Q) in place; bf16 copies of S_psi,prev; the r
+//                sums; final (R, r) store
 //   warps 8-11   group B: P mask/pack and row sums, den, a (row pass)
 //   warps 12-15  group D: rho, b and c; dP' mask/pack, dq epilogue
 //   warp 16      TMA producer (Q, K, V, G)
@@ -512,23 +510,23 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       constexpr uint32_t id_qs = make_idesc_bf16(128, 128 + D, false, false);  // [P | O] = phiQ [phiK ; S_prev^T]^T
       constexpr uint32_t id_as = make_idesc_bf16(128, D, false, true);     // dQ = a S_prev^T (S^T copy MN-major)
       constexpr uint32_t id_tt = make_idesc_bf16(D, D, true, true);        // S^T += V^T phiK, R += phiQ^T a
-      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V, dQ += dP' phiK
-      bool ok = true;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int s = c % ST, pb = c & 1;
-        const uint32_t qa = smem_u32(sm + s * G::STAGE);
-        const uint32_t ka = qa + G::OFF_K, va = qa + G::OFF_V, ga = qa + G::OFF_G, sb = qa + G::OFF_SC;
+      constexpr uint32_t id_pv = make_idesc_bf16(128, D, false, true);     // O += P V, dQ += [dP | b] [psiK ; psiK]
+      // The four MMA groups of a chunk wait on different CUDA-core passes;
+      // the issuer polls them and issues whichever is ready, the oldest
+      // chunk first, so that the front MMAs of chunk c + 1 and its P V run
+      // while chunk c's passes are still busy. Per chunk, in order:
+      //   F  [P | O] = phiQ [psiK ; S_psi^T]^T and the state update   (phi/psi, S copy, buffers of c - 2 free)
+      //   PV O += P V                                                (P packed)
+      //   G  dP = a V^T, dQ = a S_psi^T, R += phiQ^T a               (a written)
+      //   Q2 dQ += [dP | b] [psiK ; psiK]                            (dP and b packed)
+      // F of chunk c needs Q2 of c - 2 issued (its P/dP buffer is then read
+      // before F overwrites it: MMAs run in issue order).
+      auto stage_addr = [&](int c) { return smem_u32(sm + (c % ST) * G::STAGE); };
+      auto issue_f = [&](int c) {
+        const int pb = c & 1;
+        const uint32_t qa = stage_addr(c), ka = qa + G::OFF_K, va = qa + G::OFF_V;
         const uint32_t pd = tmem + G::col_pd(pb);
-        const uint32_t oq = tmem + G::col_oq(pb);
-        ok = mbar_wait(&phi_done[s], (c / ST) & 1, abort_flag, kTimeoutNs);
-        // the P/dP and O/dQ buffers of chunk c - 2 are free once its last MMA
-        // is done and its dq epilogue has read them
-        if (ok && c >= 2) ok = mbar_wait(&dq_full[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
-        if (ok) ok = mbar_wait(s_ready, c & 1, abort_flag, kTimeoutNs);
-        if (ok && c >= 2) ok = mbar_wait(&oq_empty[pb], ((c >> 1) - 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        // P and O = phiQ S_prev share A = phiQ: one MMA over [phiK ; S_prev^T]
+        // P and O = phiQ S_psi,prev share A = phiQ: one MMA over [psiK ; S_psi^T]
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
@@ -541,16 +539,20 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
           mma_ss(tmem + G::COL_S, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B),
                  make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_tt, 1);
         tc_commit(s_full);
-        ok = mbar_wait(&p_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
+      };
+      auto issue_pv = [&](int c) {
+        const int pb = c & 1;
+        const uint32_t va = stage_addr(c) + G::OFF_V;
+        const uint32_t pd = tmem + G::col_pd(pb), oq = tmem + G::col_oq(pb);
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           mma_ts(oq, pd + k * 8, make_sdesc(va + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
         tc_commit(&o_full[pb]);
-        ok = mbar_wait(&a_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
+      };
+      auto issue_g = [&](int c) {
+        const int pb = c & 1;
+        const uint32_t qa = stage_addr(c), va = qa + G::OFF_V, ga = qa + G::OFF_G, sb = qa + G::OFF_SC;
+        const uint32_t pd = tmem + G::col_pd(pb), oq = tmem + G::col_oq(pb);
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
           const uint32_t off = (k >> 2) * BOX + (k & 3) * 32;
@@ -566,43 +568,104 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         for (int k = 0; k < C / 16; ++k)
           mma_ss(tmem + G::COL_R, make_sdesc(qa + k * 2048, BOX, 1024, kSwizzle128B),
                  make_sdesc(ga + k * 2048, BOX, 1024, kSwizzle128B), id_tt, (c > 0 || k > 0) ? 1u : 0u);
-        ok = mbar_wait(&dp_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
+      };
+      auto issue_q2 = [&](int c) {
+        const int pb = c & 1;
+        const uint32_t ka = stage_addr(c) + G::OFF_K;
+        const uint32_t pd = tmem + G::col_pd(pb), oq = tmem + G::col_oq(pb);
+        // K = 256: the packed dP (columns 0..63) and the b block (64..127),
+        // both against psiK
 #pragma unroll
-        for (int k = 0; k < C / 16; ++k)
-          mma_ts(oq, pd + k * 8, make_sdesc(ka + k * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
+        for (int k = 0; k < 2 * C / 16; ++k)
+          mma_ts(oq, pd + k * 8, make_sdesc(ka + (k & 7) * 2048, BOX, 1024, kSwizzle128B), id_pv, 1);
         tc_commit(&dq_full[pb]);
-        tc_commit(&empty[s]);
+        tc_commit(&empty[c % ST]);
+      };
+      int nf = 0, npv = 0, ng = 0, nq = 0;   // next chunk of each MMA group
+      bool ok = true;
+      uint64_t t_last = globaltimer_ns();
+      while (nq < nchunks) {
+        bool issued = false;
+        if (nq < ng && mbar_try_wait(&dp_ready[nq & 1], (nq >> 1) & 1)) {
+          tc_fence_after();
+          issue_q2(nq++);
+          issued = true;
+        } else if (ng < npv && mbar_try_wait(&a_ready[ng & 1], (ng >> 1) & 1)) {
+          tc_fence_after();
+          issue_g(ng++);
+          issued = true;
+        } else if (npv < nf && mbar_try_wait(&p_ready[npv & 1], (npv >> 1) & 1)) {
+          tc_fence_after();
+          issue_pv(npv++);
+          issued = true;
+        } else if (nf < nchunks && nf <= nq + 1 && mbar_try_wait(&phi_done[nf % ST], (nf / ST) & 1) &&
+                   mbar_try_wait(s_ready, nf & 1) &&
+                   (nf < 2 || (mbar_try_wait(&dq_full[nf & 1], ((nf >> 1) - 1) & 1) &&
+                               mbar_try_wait(&oq_empty[nf & 1], ((nf >> 1) - 1) & 1)))) {
+          tc_fence_after();
+          issue_f(nf++);
+          issued = true;
+        }
+        if (issued) {
+          t_last = globaltimer_ns();
+        } else if (*abort_flag || globaltimer_ns() - t_last > kTimeoutNs) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
       }
+      (void)ok;
       tc_commit(mma_fin);
       mbar_drain(mma_fin, 0, kTimeoutNs);
     }
   } else if (warp >= 4 && warp < 8) {
-    // ---------------- group A: phi(Q), S_prev copies, R ----------------
+    // ---------------- group A: phi(Q), S_prev copies, the r sums, R ----------------
+    using X = ExactLayout<D, 128>;
     const int t = tid - 128;
     const int q = warp & 3;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
     const int row = state_row<D>(q, lane);
+    const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
+    float racc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) racc[e] = 0.f;
     griddep_wait();
     // the centred prefix S_psi^T (the held state stays centred)
     sum_states_to_tmem<D>(prm.ws_state + (long long)bh * prm.P * prm.F * RW, RW, 0, seg * prm.F, lane_addr,
                           G::COL_S, row);
     bool ok = true;
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int s = c % ST;
-      ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
-      if (!ok) break;
-      phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);
-      fence_proxy_async_smem();
-      mbar_arrive(&phi_done[s]);
-      if (c > 0) ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
-      if (!ok) break;
-      tc_fence_after();
-      copy_state_to_smem<D>(lane_addr + G::COL_S, sm + s * G::STAGE + G::OFF_SC, row);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(s_ready);
+    for (int c = 0; c <= nchunks && ok; ++c) {
+      if (c < nchunks) {
+        const int s = c % ST;
+        ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        phi_tile_bf16<D, 128>(sm + s * G::STAGE, t);
+        fence_proxy_async_smem();
+        mbar_arrive(&phi_done[s]);
+        if (c > 0) ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        copy_state_to_smem<D>(lane_addr + G::COL_S, sm + s * G::STAGE + G::OFF_SC, row);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(s_ready);
+      }
+      if (c >= 1) {
+        // r += sum_t b_t phi(q_t) over the previous chunk (b from group D);
+        // here rather than in group C, so that the psi(K) passes never wait
+        // for a chunk's dP pack
+        const int cp = c - 1, sp = cp % ST;
+        ok = mbar_wait(&dp_ready[cp & 1], (cp >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        wcolsum_tile<D, 128>(sm + sp * G::STAGE, barr + sp * C, t, racc);
+        mbar_arrive(&empty[sp]);
+      }
+    }
+    reduce_row_groups<D, 128>(racc);
+    if (ok && lane < X::FCW && seg > 0) {
+      float4* rd = reinterpret_cast<float4*>(prm.ws_rev + rec + D * D + 8 * fc);
+      rd[0] = make_float4(racc[0], racc[1], racc[2], racc[3]);
+      rd[1] = make_float4(racc[4], racc[5], racc[6], racc[7]);
     }
     // the first segment's (R, r) sums are never read
     if (ok && seg > 0) ok = mbar_wait(mma_fin, 0, abort_flag, kTimeoutNs);
@@ -660,8 +723,13 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
            mbar_wait(&a_ready[pb], (c >> 1) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
-      // rho = a . (v_j summed over j <= t in the chunk), from the fp32 dP row
-      const float rho = masked_rowsum_lower(lane_addr + G::col_pd(pb), q, lane);
+      // the masked dP row packed to bf16 (columns 0..63) with its fp32 sum
+      // rho = a . (v_j summed over j <= t in the chunk); then b, c and the
+      // masked b block (columns 64..127): dP' = dP + b enters dQ as
+      // [dP | b] [psiK ; psiK]. c and b depend on rho only through small
+      // terms (c = (Y a.V_t - n a.O_psi) / den with Y = den - s n), so the
+      // two roundings cost no accuracy.
+      const float rho = mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, 0.f, nullptr);
       const float4 ri = rowinfo[s * C + r];     // (s_t, a.V_prev, a.O_psi, den)
       const int tok = tok0 + c * C + r;
       const float av = ri.y + rho;              // a . V_t
@@ -669,7 +737,7 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       const float cterm = fmaf((float)(tok + 1), b, av);
       barr[s * C + r] = b;
       if (tok < tok_end) tokp[tok] = make_float2(ri.w, b);
-      mask_pack_row<true, false>(lane_addr + G::col_pd(pb), q, lane, b, nullptr);
+      store_lower_block(lane_addr + G::col_pd(pb) + 64, q, lane, b);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&dp_ready[pb]);
@@ -686,61 +754,43 @@ tc_bwd1_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       mbar_arrive(&empty[s]);
     }
   } else {
-    // ---------------- group C: phi(K), z, r ----------------
+    // ---------------- group C: psi(K), z_psi and the sum of v ----------------
     using X = ExactLayout<D, 128>;
     const int t = tid;
     const int fc = X::FCW * (t >> 5) + (lane % X::FCW);
     const bool owner = lane < X::FCW;
-    float zrun[8], vrun[8], racc[8];
+    float zrun[8], vrun[8];
     griddep_wait();
     // z_psi and the sum of v before the segment, from the centred records
     sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * prm.F * RW, RW, 0, seg * prm.F, 8 * fc, zrun);
     sum_vectors8<D>(prm.ws_state + (long long)bh * prm.P * prm.F * RW, RW, 0, seg * prm.F, D + 8 * fc, vrun);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) racc[e] = 0.f;
     bool ok = true;
-    for (int c = 0; c <= nchunks && ok; ++c) {
-      if (c < nchunks) {
-        const int s = c % ST;
-        const int n_valid = min(C, tok_end - (tok0 + c * C));
-        ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        float colsum[8], vcol[8];
-        phi_tile_exact<D, 128, true, true, false, true>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);
-        fence_proxy_async_smem();
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % ST;
+      const int n_valid = min(C, tok_end - (tok0 + c * C));
+      ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      float colsum[8], vcol[8];
+      phi_tile_exact<D, 128, true, true, false, true>(sm + s * G::STAGE + G::OFF_K, t, n_valid, colsum);
+      fence_proxy_async_smem();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vcol[e] = 0.f;
-        colsum_tile<D, 128>(sm + s * G::STAGE + G::OFF_V, t, n_valid, vcol);
-        reduce_row_groups<D, 128>(vcol);
-        if (owner) {
-          float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
-          zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
-          zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
-          float4* vd = reinterpret_cast<float4*>(vst + s * D + 8 * fc);
-          vd[0] = make_float4(vrun[0], vrun[1], vrun[2], vrun[3]);
-          vd[1] = make_float4(vrun[4], vrun[5], vrun[6], vrun[7]);
+      for (int e = 0; e < 8; ++e) vcol[e] = 0.f;
+      colsum_tile<D, 128>(sm + s * G::STAGE + G::OFF_V, t, n_valid, vcol);
+      reduce_row_groups<D, 128>(vcol);
+      if (owner) {
+        float4* zd = reinterpret_cast<float4*>(zst + s * D + 8 * fc);
+        zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
+        zd[1] = make_float4(zrun[4], zrun[5], zrun[6], zrun[7]);
+        float4* vd = reinterpret_cast<float4*>(vst + s * D + 8 * fc);
+        vd[0] = make_float4(vrun[0], vrun[1], vrun[2], vrun[3]);
+        vd[1] = make_float4(vrun[4], vrun[5], vrun[6], vrun[7]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            zrun[e] += colsum[e];
-            vrun[e] += vcol[e];
-          }
+        for (int e = 0; e < 8; ++e) {
+          zrun[e] += colsum[e];
+          vrun[e] += vcol[e];
         }
-        mbar_arrive(&phi_done[s]);
       }
-      if (c >= 1) {
-        // r += sum_t b_t phi(q_t) over the previous chunk (b from group D)
-        const int cp = c - 1, sp = cp % ST;
-        ok = mbar_wait(&dp_ready[cp & 1], (cp >> 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        wcolsum_tile<D, 128>(sm + sp * G::STAGE, barr + sp * C, t, racc);
-        mbar_arrive(&empty[sp]);
-      }
-    }
-    reduce_row_groups<D, 128>(racc);
-    if (ok && owner && seg > 0) {
-      float4* rd = reinterpret_cast<float4*>(prm.ws_rev + rec + D * D + 8 * fc);
-      rd[0] = make_float4(racc[0], racc[1], racc[2], racc[3]);
-      rd[1] = make_float4(racc[4], racc[5], racc[6], racc[7]);
+      mbar_arrive(&phi_done[s]);
     }
   }
 

@@ -15,7 +15,8 @@ in two forms:
   place of phi(k), the state and z are carried as their psi sums, and the
   parts that hold the 1 (the row sum s_t of phi(q_t), the value sums V_t and
   the token count) are exact scalars per row; b_t is formed from the rounded
-  a_t that the MMAs read.
+  a_t that the MMAs read, and the intra-chunk dP' = dP + b enters as the
+  separately rounded pair [dP | b].
 
 It checks that both models reproduce the oracle exactly without rounding,
 that the plain form's rounding costs percents of max|dq| for random inputs,
@@ -72,7 +73,8 @@ def _dq_model(q, k, v, g, centred, rounded=True, eps=1e-6):
                     av = a @ vsum + np.tril(dP).sum(1)          # a_t . V_t
                     bb = -(s * av + (a * O).sum(1)) / den
                     cc = av + nt * bb
-                    dPp = rd(np.tril(dP + bb[:, None]))
+                    # dP and b packed separately: [dP | b] [psiK ; psiK]
+                    dPp = rd(np.tril(dP)) + rd(bb)[:, None] * np.tril(np.ones((m, m)))
                     dQ = a @ Sb.T + dPp @ kin[sl] + bb[:, None] * z[None, :] + cc[:, None]
                 else:
                     den = P.sum(1) + pq[sl] @ z + eps
