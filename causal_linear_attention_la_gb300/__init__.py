@@ -28,7 +28,7 @@ __all__ = [
     "la_forward", "la_decode_step", "la_decode_steps", "la_backward",
     "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy", "la_forward_decay",
     "la_forward_workspace_size", "la_backward_workspace_size",
-    "la_set_path", "la_forward_path", "la_backward_path",
+    "la_set_path", "la_forward_path", "la_backward_path", "la_decode_path",
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "la_forward_host", "la_forward_host_workspace_size", "forward_host",
@@ -50,7 +50,7 @@ exported_symbols = (
     "la_forward_workspace_size", "la_forward", "la_decode_step", "la_decode_steps",
     "la_decode_steps_decay", "la_decode_steps_delta", "la_state_copy", "la_forward_decay",
     "la_backward_workspace_size", "la_backward",
-    "la_set_path", "la_forward_path", "la_backward_path",
+    "la_set_path", "la_forward_path", "la_backward_path", "la_decode_path",
     "la_profile_enable", "la_profile_read", "la_launch_count",
     "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc",
     "la_forward_host_workspace_size", "la_forward_host", "la_backward_saved",
@@ -125,6 +125,8 @@ def lib():
     h.la_forward_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
     h.la_backward_path.restype = _c_int
     h.la_backward_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
+    h.la_decode_path.restype = _c_int
+    h.la_decode_path.argtypes = [_c_int, _c_int, _c_int, _c_int]
     h.la_device_status.restype = _c_int
     h.la_device_status.argtypes = [_c_int]
     h.la_test_timeout_next_forward.restype = None
@@ -236,6 +238,10 @@ def la_forward_path(dk, dv, dtype, causal=True):
 
 def la_backward_path(dk, dv, dtype, causal=True):
     return lib().la_backward_path(dk, dv, dtype, int(causal))
+
+
+def la_decode_path(dk, dv, dtype, T):
+    return lib().la_decode_path(dk, dv, dtype, int(T))
 
 
 def la_device_status(clear=False):

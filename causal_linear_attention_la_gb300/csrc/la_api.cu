@@ -312,6 +312,11 @@ int la_forward_path(int dk, int dv, la_dtype dtype, int causal) {
   return (g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, causal != 0)) ? 1 : 0;
 }
 
+int la_decode_path(int dk, int dv, la_dtype dtype, int T) {
+  if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16) || T < 0) return -1;
+  return (g_path.load() == LA_PATH_AUTO && tc_decode_supported(dk, dv, dtype, T)) ? 1 : 0;
+}
+
 int la_backward_path(int dk, int dv, la_dtype dtype, int causal) {
   if (!head_ok(dk) || !head_ok(dv) || (dtype != LA_F32 && dtype != LA_BF16)) return -1;
   return (g_path.load() == LA_PATH_AUTO && tc_backward_supported(dk, dv, dtype, causal != 0)) ? 1 : 0;
@@ -559,8 +564,11 @@ la_status la_decode_steps(float* S, float* z, const void* q, const void* k,
   a.BH = B * H; a.dk = dk; a.dv = dv; a.eps = eps; a.dtype = dtype;
   a.stream = (cudaStream_t)stream;
   a.ntok = T;
+  const bool use_tc = g_path.load() == LA_PATH_AUTO && tc_decode_supported(dk, dv, dtype, T);
+  if (use_tc && device_status_ptr() == nullptr)
+    return fail(LA_ERR_CUDA, "la_decode_steps: device status word unavailable");
   prof_begin(LA_SPAN_DECODE, a.stream);
-  cudaError_t e = la::decode_step(a);
+  cudaError_t e = use_tc ? la::tc_decode_steps(a) : la::decode_step(a);
   prof_end(LA_SPAN_DECODE, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps");
   return LA_OK;

@@ -101,6 +101,9 @@ cudaError_t segment_scan(float* ws, int BH, int P, long long words,
 cudaError_t simt_forward_output(const FwdArgs& a);
 cudaError_t simt_backward(const BwdArgs& a);
 cudaError_t decode_step(const DecodeArgs& a);
+// tensor-core multi-token decode (bf16, dk = dv = 128, two tokens or more)
+bool tc_decode_supported(int dk, int dv, la_dtype dtype, int ntok);
+cudaError_t tc_decode_steps(const DecodeArgs& a);
 
 // Tensor-core kernels (bf16, dk = dv in {64, 128}; causal and non-causal)
 bool tc_forward_supported(int dk, int dv, la_dtype dtype, int causal);

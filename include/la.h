@@ -324,6 +324,9 @@ LA_API int la_set_path(int path);
  * current setting: 0 = CUDA-core, 1 = tensor-core; -1 if unsupported. */
 LA_API int la_forward_path(int dk, int dv, la_dtype dtype, int causal);
 LA_API int la_backward_path(int dk, int dv, la_dtype dtype, int causal);
+/* Which kernel la_decode_steps takes for T tokens per call: 1 = tensor-core
+ * (bf16, dk = dv = 128, T >= 2), 0 = CUDA-core; -1 if unsupported. */
+LA_API int la_decode_path(int dk, int dv, la_dtype dtype, int T);
 
 /*
  * Device-side status. The tensor-core kernels bound every wait on another

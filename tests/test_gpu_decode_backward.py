@@ -67,8 +67,66 @@ def test_decode_tokens(B, H, T, dk, dv, dtype):
     assert la.la_device_status(True) == la.LA_OK
     err = rel_err(to_host(out), o_w, np.abs(v).max())
     assert err <= TOL[dtype], err
-    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-6
+    # the tensor-core kernel (bf16, d = 128) updates the state through MMAs
+    # whose psi(k) operand is split into two bf16 parts (about 16 bits):
+    # 1e-5 of max|S|; the CUDA-core kernels update in fp32 FMAs
+    s_tol = 1e-5 if la.la_decode_path(dk, dv, la.LA_BF16 if dtype == "bf16" else la.LA_F32, T) == 1 else 1e-6
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= s_tol
     assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= 1e-6
+
+
+@pytest.mark.parametrize("B,H,T", [(1, 1, 2), (2, 3, 15), (1, 2, 16), (2, 1, 17), (3, 2, 40),
+                                   (64, 32, 16), (1, 1, 200)])
+def test_decode_tokens_tensor_core(B, H, T):
+    """The tensor-core multi-token decode (bf16, d = 128) against the oracle's
+    T single steps and against the CUDA-core kernel on the same inputs:
+    groups of 16 tokens, partial last groups, one and many groups."""
+    import torch
+    d = 128
+    assert la.la_decode_path(d, d, la.LA_BF16, T) == 1
+    q0, k0, v0 = synth.qkv(B, H, 40, d, d, seed=T + 7, dtype="bf16")
+    _, S_ref, z_ref = orc.forward_recurrent(q0, k0, v0, return_state=True)
+    S_ref, z_ref = S_ref.astype(np.float32), z_ref.astype(np.float32)
+    q, k, v = synth.qkv(B, H, T, d, d, seed=500 + T, dtype="bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    S, z = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+    out = la.decode_steps(S, z, qd, kd, vd)
+    la.la_set_path(la.LA_PATH_SIMT)
+    try:
+        assert la.la_decode_path(d, d, la.LA_BF16, T) == 0
+        S2, z2 = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+        out2 = la.decode_steps(S2, z2, qd, kd, vd)
+        torch.cuda.synchronize()
+    finally:
+        la.la_set_path(la.LA_PATH_AUTO)
+    assert la.la_device_status(True) == la.LA_OK
+    S_w, z_w, o_w = orc.decode_steps(S_ref, z_ref, q, k, v)
+    vmax = np.abs(v).max()
+    assert rel_err(to_host(out), o_w, vmax) <= TOL["bf16"]
+    assert rel_err(to_host(out), to_host(out2), vmax) <= TOL["bf16"]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+    assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= 1e-6
+
+
+def test_decode_tokens_tensor_core_extreme_inputs():
+    """bf16 q, k of large magnitude (|x| up to 100) and eps = 0 through the
+    tensor-core decode: finite outputs within the bf16 bound."""
+    import torch
+    rng = np.random.default_rng(91)
+    B, H, T, d = 2, 2, 20, 128
+    mk = lambda s: synth.round_to_bf16(np.clip(rng.standard_normal((B, H, T, d)) * s, -100, 100).astype(np.float32))
+    q, k = mk(30.0), mk(30.0)
+    v = synth.round_to_bf16((rng.standard_normal((B, H, T, d)) / 8).astype(np.float32))
+    S0 = np.zeros((B, H, d, d), np.float32)
+    z0 = np.zeros((B, H, d), np.float32)
+    S, z = torch.from_numpy(S0).cuda(), torch.from_numpy(z0).cuda()
+    out = la.decode_steps(S, z, to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"), eps=0.0)
+    torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
+    _, _, o_w = orc.decode_steps(S0, z0, q, k, v, eps=0.0)
+    got = to_host(out)
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, o_w, np.abs(v).max()) <= TOL["bf16"]
 
 
 def test_decode_tokens_edge_cases():
