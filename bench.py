@@ -197,6 +197,7 @@ KERNEL_SOURCES = {
     "fwd_output": ["la_tc_fwd.cu"] + _COMMON_TC,
     "bwd": ["la_tc_bwd.cu"] + _COMMON_TC,
     "decode": ["la_decode.cu", "la_internal.cuh"],
+    "decodetc": ["la_decode_tc.cu"] + _COMMON_TC,
     "variants": ["la_variants.cu", "la_variants.cuh", "la_internal.cuh"],
 }
 
@@ -650,6 +651,8 @@ def main():
             t = max_over_ranks(rr["ms"]) / 1e3
             per = t / rr["steps"]
             nt = ws.get("tokens", 1)
+            tc_decode = not ws.get("variant") and la.la_decode_path(ws["dk"], ws["dv"], la.LA_BF16, nt) == 1
+            traffic_key = ("variants_" if ws.get("variant") else "decodetc_" if tc_decode else "decode_") + name
             # bytes of one call: the state once, q, k, v, out once per token
             call_bytes = decode_state_bytes(ws) + nt * decode_io_bytes(ws)
             gbs = decode_state_bytes(ws) / per / 1e9
@@ -660,15 +663,15 @@ def main():
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"],
                              "kernel": {"decay": "decay_tokens", "delta": "delta_tokens"}.get(
-                                 ws.get("variant"), "decode"),
-                             "traffic": ncu_traffic(("variants_" if ws.get("variant") else "decode_") + name)},
+                                 ws.get("variant"), "decode_tc" if tc_decode else "decode"),
+                             "traffic": ncu_traffic(traffic_key)},
                 "bytes_per_step": call_bytes,
                 "prefill_s_eager": rr["prefill_s"], "gpu_launches": rr["launches"],
                 "l2": (f"state {decode_state_bytes(ws) / 2 / 1e6:.1f} MB, about the L2 "
                        f"({L2_BYTES / 1e6:.1f} MB): consecutive steps can meet the previous step's "
                        "lines in L2, so dram_frac counts measured DRAM bytes"),
             }
-            dram = ncu_traffic(("variants_" if ws.get("variant") else "decode_") + name)
+            dram = ncu_traffic(traffic_key)
             if dram is not None:
                 sections[name]["dram_bytes_per_step"] = dram
                 sections[name]["dram_gbs"] = dram / per / 1e9
