@@ -32,7 +32,7 @@ __all__ = [
     "la_profile_enable", "la_profile_read", "la_launch_count", "SPAN_NAMES",
     "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc", "LA_NOALLOC_SCRATCH_BYTES",
     "la_forward_host", "la_forward_host_workspace_size", "forward_host",
-    "la_backward_saved", "backward_saved",
+    "la_backward_saved", "backward_saved", "la_backward_decay", "backward_decay",
     "forward", "decode_step", "decode_steps", "backward",
     "decode_steps_decay", "decode_steps_delta", "state_copy", "forward_decay",
 ]
@@ -54,6 +54,7 @@ exported_symbols = (
     "la_profile_enable", "la_profile_read", "la_launch_count",
     "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc",
     "la_forward_host_workspace_size", "la_forward_host", "la_backward_saved",
+    "la_backward_decay",
 )
 
 
@@ -98,6 +99,9 @@ def lib():
     h.la_backward_saved.restype = _c_int
     h.la_backward_saved.argtypes = ([_c_void] * 7 + [_c_int] * 6 + [_c_float, _c_int]
                                     + [_c_void, _c_size, _c_void, _c_size, _c_void])
+    h.la_backward_decay.restype = _c_int
+    h.la_backward_decay.argtypes = ([_c_void] * 7 + [_c_int] * 5 + [_c_void, _c_float, _c_int]
+                                    + [_c_void, _c_size, _c_void])
     h.la_forward_host_workspace_size.restype = _c_size
     h.la_forward_host_workspace_size.argtypes = [_c_int] * 8
     h.la_forward_host.restype = _c_int
@@ -169,6 +173,12 @@ def la_forward(q, k, v, out, B, H, N, dk, dv, causal, eps, dtype, S_final,
     return lib().la_forward(q, k, v, out, B, H, N, dk, dv, int(causal), eps,
                             dtype, S_final, z_final, workspace,
                             workspace_bytes, stream)
+
+
+def la_backward_decay(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, alpha, eps, dtype,
+                      workspace, workspace_bytes, stream):
+    return lib().la_backward_decay(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, alpha, eps, dtype,
+                                   workspace, workspace_bytes, stream)
 
 
 def la_backward_saved(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps, dtype,
@@ -487,6 +497,30 @@ def backward(q, k, v, dout, causal=True, eps=1e-6, workspace=None):
                        dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(), B, H, N,
                        dk, dv, causal, eps, code, workspace.data_ptr(),
                        workspace.numel(), _stream_ptr(q)))
+    return dq, dkk, dvv
+
+
+def backward_decay(q, k, v, dout, alpha, eps=1e-6, workspace=None):
+    """Gradients (dq, dk, dv) of the decay-gated causal attention
+    (la_backward_decay); alpha: fp32 CUDA tensor [H], one factor per head."""
+    import torch
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, n, q.dtype)
+    if alpha.dtype != torch.float32 or not alpha.is_cuda or alpha.numel() != H:
+        raise ValueError("alpha must be an fp32 CUDA tensor of H factors")
+    dq = torch.empty_like(q)
+    dkk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    ws_bytes = la_backward_workspace_size(B, H, N, dk, dv, True, code)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    _check(la_backward_decay(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                             dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(), B, H, N,
+                             dk, dv, alpha.contiguous().data_ptr(), eps, code, workspace.data_ptr(),
+                             workspace.numel(), _stream_ptr(q)))
     return dq, dkk, dvv
 
 

@@ -689,7 +689,7 @@ namespace {
 la_status backward_impl(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk_,
                         void* dv_, int B, int H, int N, int dk, int dv, int causal, float eps, la_dtype dtype,
                         const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream, const char* name) {
+                        cudaStream_t stream, const char* name, const float* alpha = nullptr) {
   bool empty = false;
   la_status st = check_sizes(B, H, N, dk, dv, dtype, eps, &empty);
   if (st != LA_OK) return st;
@@ -714,7 +714,10 @@ la_status backward_impl(const void* q, const void* k, const void* v, const void*
   a.ws_rev = (float*)((char*)workspace + w.rev_off);
   a.ws_tok = (float*)((char*)workspace + w.tok_off);
   a.plan = plan; a.stream = stream;
-  const bool use_tc = g_path.load() == LA_PATH_AUTO && tc_backward_supported(dk, dv, dtype, a.causal);
+  a.alpha = alpha; a.H = H;
+  // decay gating runs on the CUDA-core kernels
+  const bool use_tc = alpha == nullptr && g_path.load() == LA_PATH_AUTO &&
+                      tc_backward_supported(dk, dv, dtype, a.causal);
   if (saved != nullptr) {
     const SegPlan fplan = forward_plan(BH, N, dk, dv, dtype, a.causal);
     const size_t need = layout(BH, N, dk, dv, fplan, false).total;
@@ -757,6 +760,14 @@ la_status la_backward_saved(const void* q, const void* k, const void* v, const v
   if (saved == nullptr) return fail(LA_ERR_INVALID_ARG, "saved must be the forward's workspace (non-NULL)");
   return backward_impl(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, causal, eps, dtype, saved, saved_bytes,
                        workspace, workspace_bytes, (cudaStream_t)stream, "la_backward_saved");
+}
+
+la_status la_backward_decay(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk_,
+                            void* dv_, int B, int H, int N, int dk, int dv, const float* alpha, float eps,
+                            la_dtype dtype, void* workspace, size_t workspace_bytes, la_stream_t stream) {
+  if (alpha == nullptr && (long long)B * H * N > 0) return fail(LA_ERR_INVALID_ARG, "alpha must be non-NULL");
+  return backward_impl(q, k, v, dout, dq, dk_, dv_, B, H, N, dk, dv, 1, eps, dtype, nullptr, 0, workspace,
+                       workspace_bytes, (cudaStream_t)stream, "la_backward_decay", alpha);
 }
 
 }  // extern "C"

@@ -70,6 +70,9 @@ struct FwdArgs {
   float* ws_state;  // [BH][P][dk*dv + dk]
   SegPlan plan;
   cudaStream_t stream;
+  // decay gating on the CUDA-core state pass: per-head factors [H] or null
+  const float* alpha = nullptr;
+  int H = 1;
 };
 
 struct BwdArgs {
@@ -84,6 +87,9 @@ struct BwdArgs {
   // ws_state already holds the forward's state-pass records (plan.F parts per
   // segment, as la_forward's tensor-core path leaves them): no state pass
   bool state_ready = false;
+  // decay gating (CUDA-core path, causal): per-head factors [H] or null
+  const float* alpha = nullptr;
+  int H = 1;
 };
 
 struct DecodeArgs {
@@ -97,7 +103,9 @@ struct DecodeArgs {
 cudaError_t simt_segment_state(const FwdArgs& a);                 // per-segment (dS, dz)
 cudaError_t segment_scan(float* ws, int BH, int P, long long words,
                          int mode, float* S_final, float* z_final,
-                         int dk, int dv, cudaStream_t stream);     // prefix / suffix / total
+                         int dk, int dv, cudaStream_t stream,
+                         const float* alpha = nullptr, int H = 1,
+                         int seg_len = 0, int N = 0);               // prefix / suffix / total
 cudaError_t simt_forward_output(const FwdArgs& a);
 cudaError_t simt_backward(const BwdArgs& a);
 cudaError_t decode_step(const DecodeArgs& a);

@@ -18,6 +18,14 @@
 // Sweep 1 runs forward, writes dq, the per-token scalars D_t, b_t and the
 // per-segment reverse sums (dR, dr); after a reverse segment scan, sweep 2
 // runs backward through each segment and writes dk, dv.
+// Decay gating (alpha: per-head factors, else null; causal): S_t = alpha
+// S_{t-1} + phi(k_t) v_t^T and z likewise ("Linear Attention, 곱의 순서를
+// 바꾸면 생기는 일", paragraph on 감쇠 게이팅), and the reverse sums decay the
+// same way, R_j = phi(q_j) a_j^T + alpha R_{j+1}. In a tile the pair (t, j)
+// carries alpha^(t-j), the tile's starting state alpha^(t+1) at row t, the
+// suffix after the tile alpha^(n-j) at key j; records are decayed to their
+// segment's last token (forward) or first token (reverse) and the segment
+// scan decays across segments.
 #include "la_internal.cuh"
 
 #ifndef LA_DK
@@ -47,7 +55,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
                 const T* __restrict__ v, const T* __restrict__ g,
                 T* __restrict__ dq, int N, int P, int seg_len, int causal,
                 float eps, const float* __restrict__ ws_state,
-                float* __restrict__ ws_rev, float* __restrict__ ws_tok) {
+                float* __restrict__ ws_rev, float* __restrict__ ws_tok,
+                const float* __restrict__ alpha, int H) {
   constexpr int LDK = DK + 1, LDV = DV + 1;
   constexpr int LST = (DK > DV ? DK : DV) + 1;
   constexpr int RG = NT / DV;     // (c, m) layout: m = tid % DV
@@ -89,6 +98,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll
   for (int e = 0; e < E; ++e) racc[e] = 0.f;
   float rz = 0.f;
+  const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
+  auto dec = [&](int e) { return exp2f((float)e * log2a); };   // alpha^e (1 without decay)
   __syncthreads();
 
   for (int s = t0; s < t1; s += TT) {
@@ -110,8 +121,10 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       for (int idx = tid; idx < TT * TT; idx += NT) {
         const int t = idx / TT, j = idx % TT;
         float a = 0.f;
-        if (j <= t && t < n)
+        if (j <= t && t < n) {
           for (int c = 0; c < DK; ++c) a = fmaf(fq[t * LDK + c], fk[j * LDK + c], a);
+          a *= dec(t - j);
+        }
         W[t * (TT + 1) + j] = a;
       }
       __syncthreads();
@@ -120,6 +133,7 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       const int t = tid;
       float d = 0.f;
       for (int c = 0; c < DK; ++c) d = fmaf(fq[t * LDK + c], z[c], d);
+      d *= dec(t + 1);
       if (causal)
         for (int j = 0; j <= t; ++j) d += W[t * (TT + 1) + j];
       den[t] = t < n ? d + eps : 1.f;  // padding rows stay finite when eps = 0
@@ -129,6 +143,7 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       const int t = tid / DV + r * RG;
       float a = 0.f;
       for (int c = 0; c < DK; ++c) a = fmaf(fq[t * LDK + c], S[c * DV + m], a);
+      a *= dec(t + 1);
       if (causal)
         for (int j = 0; j <= t; ++j) a = fmaf(W[t * (TT + 1) + j], vv[j * LDV + m], a);
       num[r] = a;
@@ -159,7 +174,7 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
         float a = 0.f;
         if (j <= t && t < n) {
           for (int mm = 0; mm < DV; ++mm) a = fmaf(aa[t * LDV + mm], vv[j * LDV + mm], a);
-          a += bsc[t];
+          a = (a + bsc[t]) * dec(t - j);
         }
         dW[t * (TT + 1) + j] = a;
       }
@@ -172,6 +187,7 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
         const int c = tid / TT + e * CG;
         float a = bsc[t] * z[c];
         for (int mm = 0; mm < DV; ++mm) a = fmaf(aa[t * LDV + mm], S[c * DV + mm], a);
+        a *= dec(t + 1);
         if (causal)
           for (int j = 0; j <= t; ++j) a = fmaf(dW[t * (TT + 1) + j], fk[j * LDK + c], a);
         stg[t * LST + c] = a * phi_prime_from_phi(fq[t * LDK + c]);
@@ -183,26 +199,28 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       if (t < n) dqb[(long long)(s + t) * DK + c] = from_f32<T>(stg[t * LST + c]);
     }
     // segment reverse sums dR += phi(q)^T a, dr += sum_t b_t phi(q_t)
+    // (decayed to the segment's first token)
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = c0 + e * RG;
       float a = racc[e];
-      for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c], aa[t * LDV + m], a);
+      for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(s + t - t0), aa[t * LDV + m], a);
       racc[e] = a;
     }
     if (tid < DK)
-      for (int t = 0; t < n; ++t) rz = fmaf(bsc[t], fq[t * LDK + tid], rz);
+      for (int t = 0; t < n; ++t) rz = fmaf(bsc[t] * dec(s + t - t0), fq[t * LDK + tid], rz);
     if (causal) {
+      // the state after the tile: alpha^n S + sum_j alpha^(n-1-j) phi(k_j) v_j^T
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int c = c0 + e * RG;
-        float a = S[c * DV + m];
-        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + c], vv[t * LDV + m], a);
+        float a = S[c * DV + m] * dec(n);
+        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + c] * dec(n - 1 - t), vv[t * LDV + m], a);
         S[c * DV + m] = a;
       }
       if (tid < DK) {
-        float a = z[tid];
-        for (int t = 0; t < n; ++t) a += fk[t * LDK + tid];
+        float a = z[tid] * dec(n);
+        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + tid], dec(n - 1 - t), a);
         z[tid] = a;
       }
     }
@@ -227,7 +245,7 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
                 const T* __restrict__ v, const T* __restrict__ g,
                 T* __restrict__ dk_, T* __restrict__ dv_, int N, int P,
                 int seg_len, int causal, const float* __restrict__ ws_rev,
-                const float* __restrict__ ws_tok) {
+                const float* __restrict__ ws_tok, const float* __restrict__ alpha, int H) {
   constexpr int LDK = DK + 1, LDV = DV + 1;
   constexpr int RG = NT / DV;
   constexpr int E = DK / RG;
@@ -264,6 +282,8 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
   const float* st = ws_rev + (bh * P + p) * (long long)(DK * DV + DK);
   for (int i = tid; i < DK * DV + DK; i += NT) R[i] = st[i];
   const int m = tid % DV, c0 = tid / DV;
+  const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
+  auto dec = [&](int e) { return exp2f((float)e * log2a); };   // alpha^e (1 without decay)
   __syncthreads();
 
   const int ntiles = (t1 - t0 + TT - 1) / TT;
@@ -295,7 +315,9 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
         if (j <= t && t < n) {
           for (int c = 0; c < DK; ++c) w = fmaf(fq[t * LDK + c], fk[j * LDK + c], w);
           for (int mm = 0; mm < DV; ++mm) dw = fmaf(aa[t * LDV + mm], vv[j * LDV + mm], dw);
-          dw += bsc[t];
+          const float f = dec(t - j);
+          w *= f;
+          dw = (dw + bsc[t]) * f;
         }
         W[t * (TT + 1) + j] = w;
         dW[t * (TT + 1) + j] = dw;
@@ -308,6 +330,7 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
         const int c = tid / TT + e * CG;
         float a = r[c];
         for (int mm = 0; mm < DV; ++mm) a = fmaf(R[c * DV + mm], vv[j * LDV + mm], a);
+        a *= dec(n - j);    // the suffix after the tile, seen from key j
         if (causal)
           for (int t = j; t < TT; ++t) a = fmaf(dW[t * (TT + 1) + j], fq[t * LDK + c], a);
         sdk[j * LDK + c] = a * phi_prime_from_phi(fk[j * LDK + c]);
@@ -316,6 +339,7 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
         const int mm = tid / TT + e * CG;
         float a = 0.f;
         for (int c = 0; c < DK; ++c) a = fmaf(R[c * DV + mm], fk[j * LDK + c], a);
+        a *= dec(n - j);
         if (causal)
           for (int t = j; t < TT; ++t) a = fmaf(W[t * (TT + 1) + j], aa[t * LDV + mm], a);
         sdv[j * LDV + mm] = a;
@@ -332,15 +356,16 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
     }
     if (causal) {
 #pragma unroll
+      // the suffix at the tile's first token: alpha^n R + sum_t alpha^t phi(q_t) a_t^T
       for (int e = 0; e < E; ++e) {
         const int c = c0 + e * RG;
-        float a = R[c * DV + m];
-        for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c], aa[t * LDV + m], a);
+        float a = R[c * DV + m] * dec(n);
+        for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(t), aa[t * LDV + m], a);
         R[c * DV + m] = a;
       }
       if (tid < DK) {
-        float a = r[tid];
-        for (int t = 0; t < n; ++t) a = fmaf(bsc[t], fq[t * LDK + tid], a);
+        float a = r[tid] * dec(n);
+        for (int t = 0; t < n; ++t) a = fmaf(bsc[t] * dec(t), fq[t * LDK + tid], a);
         r[tid] = a;
       }
     }
@@ -355,13 +380,14 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = a.causal;
   f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
   f.stream = a.stream;
+  f.alpha = a.alpha; f.H = a.H;
   const long long words = state_words(DK, DV);
   prof_begin(LA_SPAN_BWD_STATE, a.stream);
   cudaError_t err = simt_segment_state(f);
   if (err == cudaSuccess)
     err = segment_scan(a.ws_state, a.BH, a.plan.P, words,
                        a.causal ? SCAN_EXCLUSIVE_FWD : SCAN_TOTAL, nullptr,
-                       nullptr, DK, DV, a.stream);
+                       nullptr, DK, DV, a.stream, a.alpha, a.H, a.plan.seg_len, a.N);
   prof_end(LA_SPAN_BWD_STATE, a.stream);
   if (err != cudaSuccess) return err;
 
@@ -374,7 +400,7 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   k1<<<grid, NT, smem1, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v,
                                     (const T*)a.dout, (T*)a.dq, a.N, a.plan.P,
                                     a.plan.seg_len, a.causal, a.eps, a.ws_state,
-                                    a.ws_rev, a.ws_tok);
+                                    a.ws_rev, a.ws_tok, a.alpha, a.H);
   prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -382,7 +408,7 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   prof_begin(LA_SPAN_BWD_SCAN, a.stream);
   err = segment_scan(a.ws_rev, a.BH, a.plan.P, words,
                      a.causal ? SCAN_EXCLUSIVE_REV : SCAN_TOTAL, nullptr,
-                     nullptr, DK, DV, a.stream);
+                     nullptr, DK, DV, a.stream, a.alpha, a.H, a.plan.seg_len, a.N);
   prof_end(LA_SPAN_BWD_SCAN, a.stream);
   if (err != cudaSuccess) return err;
   constexpr size_t smem2 = sizeof(float) * sweep2_smem_floats<DK, DV>();
@@ -393,7 +419,7 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   k2<<<grid, NT, smem2, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v,
                                     (const T*)a.dout, (T*)a.dk_, (T*)a.dv_, a.N,
                                     a.plan.P, a.plan.seg_len, a.causal,
-                                    a.ws_rev, a.ws_tok);
+                                    a.ws_rev, a.ws_tok, a.alpha, a.H);
   prof_end(LA_SPAN_BWD_SWEEP2, a.stream);
   err = cudaGetLastError();
   if (err == cudaSuccess) note_launch();

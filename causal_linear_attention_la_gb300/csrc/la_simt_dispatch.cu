@@ -24,9 +24,15 @@ namespace {
 // 4 consecutive words (records are 16-byte multiples) and issues its loads in
 // batches of 8 records before using them, so the dependent-latency chain is
 // P / 8 loads long rather than P.
+// With decay gating (alpha: per-head factors, else null; exclusive modes) the
+// running sum decays by alpha^L_p across segment p of L_p tokens: forward
+// records hold a segment's sums decayed to its last token, reverse records
+// decayed to its first, so that slot p receives the state at segment p's
+// start (forward) or the adjoint at the token after its end (reverse).
 __global__ void scan_kernel(float* __restrict__ ws, int P, long long words,
                             int mode, float* __restrict__ S_final,
-                            float* __restrict__ z_final, int dkdv, int dk) {
+                            float* __restrict__ z_final, int dkdv, int dk,
+                            const float* __restrict__ alpha, int H, int seg_len, int N) {
   const long long e = 4 * ((long long)blockIdx.y * blockDim.x + threadIdx.x);
   if (e >= words) return;
   const long long bh = blockIdx.x;
@@ -46,6 +52,7 @@ __global__ void scan_kernel(float* __restrict__ ws, int P, long long words,
     for (int p = 0; p < P; ++p) base[p * stride] = run;
   } else {
     const bool rev = mode == SCAN_EXCLUSIVE_REV;
+    const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
     for (int p0 = 0; p0 < P; p0 += BATCH) {
       float4 x[BATCH];
 #pragma unroll
@@ -56,7 +63,14 @@ __global__ void scan_kernel(float* __restrict__ ws, int P, long long words,
 #pragma unroll
       for (int i = 0; i < BATCH; ++i) {
         const int p = rev ? P - 1 - (p0 + i) : p0 + i;
-        if (p0 + i < P) base[p * stride] = run;
+        if (p0 + i < P) {
+          base[p * stride] = run;
+          if (alpha != nullptr) {
+            // segment p's tokens decay what the running sum carries past it
+            const float f = exp2f((float)min(seg_len, N - p * seg_len) * log2a);
+            run.x *= f; run.y *= f; run.z *= f; run.w *= f;
+          }
+        }
         add(run, x[i]);
       }
     }
@@ -106,11 +120,11 @@ cudaError_t simt_backward(const BwdArgs& a) {
 
 cudaError_t segment_scan(float* ws, int BH, int P, long long words, int mode,
                          float* S_final, float* z_final, int dk, int dv,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const float* alpha, int H, int seg_len, int N) {
   // records of dk*dv + dk floats: always a multiple of 4 (dk >= 16)
   dim3 grid(BH, (unsigned)((words / 4 + 255) / 256));
   scan_kernel<<<grid, 256, 0, stream>>>(ws, P, words, mode, S_final, z_final,
-                                        dk * dv, dk);
+                                        dk * dv, dk, alpha, H, seg_len, N);
   const cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess) note_launch();
   return err;

@@ -27,11 +27,14 @@ constexpr int TT = 32;   // tokens per tile
 template <typename T>
 __device__ __forceinline__ float ld(const T* p) { return to_f32<T>(*p); }
 
-// Per-segment sums dS = sum phi(k) v^T, dz = sum phi(k) -> ws[bh][p].
+// Per-segment sums dS = sum phi(k) v^T, dz = sum phi(k) -> ws[bh][p]. With
+// decay gating (alpha: per-head factors, else null) each token's term is
+// weighted alpha^(last - token), the segment's sums decayed to its last token.
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(NT)
 simt_state_kernel(const T* __restrict__ k, const T* __restrict__ v, int N,
-                  int P, int seg_len, float* __restrict__ ws) {
+                  int P, int seg_len, float* __restrict__ ws,
+                  const float* __restrict__ alpha, int H) {
   constexpr int RG = NT / DV;  // row groups
   constexpr int E = DK / RG;   // S rows per thread
   static_assert(E >= 1, "head size too small for this thread layout");
@@ -50,11 +53,12 @@ simt_state_kernel(const T* __restrict__ k, const T* __restrict__ v, int N,
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float zacc = 0.f;
+  const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
   for (int s = t0; s < t1; s += TT) {
     const int n = min(TT, t1 - s);
     for (int idx = tid; idx < TT * DK; idx += NT) {
       const int t = idx / DK, c = idx % DK;
-      fk[t][c] = t < n ? phi(ld(kb + (long long)(s + t) * DK + c)) : 0.f;
+      fk[t][c] = t < n ? phi(ld(kb + (long long)(s + t) * DK + c)) * exp2f((float)(t1 - 1 - s - t) * log2a) : 0.f;
     }
     for (int idx = tid; idx < TT * DV; idx += NT) {
       const int t = idx / DV, c = idx % DV;
@@ -191,7 +195,7 @@ template <int DK, int DV, typename T>
 cudaError_t launch_state(const FwdArgs& a) {
   dim3 grid(a.BH, a.plan.P);
   simt_state_kernel<DK, DV, T><<<grid, NT, 0, a.stream>>>(
-      (const T*)a.k, (const T*)a.v, a.N, a.plan.P, a.plan.seg_len, a.ws_state);
+      (const T*)a.k, (const T*)a.v, a.N, a.plan.P, a.plan.seg_len, a.ws_state, a.alpha, a.H);
   const cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess) note_launch();
   return err;

@@ -225,6 +225,28 @@ LA_API la_status la_forward_decay(const void* q, const void* k, const void* v, v
                            void* workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * Gradients of the decay-gated causal attention (la_decode_steps_decay run
+ * over the whole sequence from the zero state; la_forward_decay's outputs):
+ * dq, dk, dv of L = sum(dout * out) by the same forward and reverse
+ * cumulative sums as la_backward, with the reverse sums decaying like the
+ * state, R_j = phi(q_j) a_j^T + alpha R_{j+1}, r_j = b_j phi(q_j) + alpha
+ * r_{j+1} (the chain rule through S_t = alpha S_{t-1} + phi(k_t) v_t^T).
+ *
+ * Arguments as la_backward with causal = 1, plus alpha [H] fp32 device
+ * memory, one factor per head in (0, 1] (not checked). Runs on the CUDA-core
+ * kernels (f32 or bf16, every supported head size), segments of each
+ * sequence in parallel: the segment sums are decayed to their ends and
+ * combined by a decaying scan. Workspace: la_backward_workspace_size(B, H,
+ * N, dk, dv, 1, dtype) bytes. NULL alpha is LA_ERR_INVALID_ARG.
+ */
+LA_API la_status la_backward_decay(const void* q, const void* k, const void* v,
+                                   const void* dout, void* dq, void* dk_, void* dv_,
+                                   int B, int H, int N, int dk, int dv,
+                                   const float* alpha, float eps, la_dtype dtype,
+                                   void* workspace, size_t workspace_bytes,
+                                   la_stream_t stream);
+
+/*
  * Delta-rule decode: T steps per (batch, head) in one call; each step reads
  * the state with the key and adds only the difference to the value (the
  * paragraph on 델타 규칙 of the same page):

@@ -184,3 +184,47 @@ def test_forward_decay_one_is_forward():
     # decayed records, so the outputs agree to within one bf16 step of
     # max|v| (2^-8), not bit for bit
     assert rel_err(to_host(o1), to_host(o2), float(v.abs().max())) <= 2.0 ** -8
+
+
+# ---------------------------------------------------------------------------
+# Decay-gated backward (CUDA-core sweeps with decayed segment records) vs the
+# oracle's chain-rule gradient of the decayed recurrence
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 1, 1, 64),       # one token
+    (1, 2, 100, 64),     # one partial tile per sequence
+    (2, 3, 1000, 64),    # several segments, ragged tail
+    (1, 1, 4096, 16),    # many segments: long decayed scans
+    (2, 2, 777, 128),
+    (4, 8, 3000, 64),
+])
+def test_backward_decay(B, H, N, d, dtype):
+    import torch
+    from helpers import grad_errors, grad_tol, grads_ok
+    q, k, v = synth.qkv(B, H, N, d, d, seed=70 + N + d, dtype=dtype)
+    g = synth.upstream_grad(B, H, N, d, seed=70 + N + d, dtype=dtype)
+    alpha_h = np.random.default_rng(N + H).uniform(0.5, 1.0, H).astype(np.float32)
+    got = la.backward_decay(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype), to_dev(g, dtype),
+                            torch.from_numpy(alpha_h).cuda())
+    torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
+    want = orc.backward_decay(q, k, v, g, alpha=alpha_h.astype(np.float64)[None, :])
+    errs = grad_errors(got, want)
+    assert grads_ok(errs, grad_tol(dtype, False)), errs
+
+
+def test_backward_decay_one_is_backward():
+    """alpha = 1 is the plain gradient: the same CUDA-core sweeps without decay."""
+    import torch
+    B, H, N, d = 2, 3, 1500, 64
+    q, k, v = synth.qkv(B, H, N, d, d, seed=81, dtype="f32")
+    g = synth.upstream_grad(B, H, N, d, seed=81, dtype="f32")
+    args = [to_dev(x, "f32") for x in (q, k, v, g)]
+    got = la.backward_decay(*args, torch.ones(H, device="cuda"))
+    plain = la.backward(*args)
+    torch.cuda.synchronize()
+    for a, b in zip(got, plain):
+        assert rel_err(to_host(a), to_host(b), float(b.abs().max())) <= 1e-6
