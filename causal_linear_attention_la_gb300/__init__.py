@@ -35,6 +35,7 @@ __all__ = [
     "la_backward_saved", "backward_saved", "la_backward_decay", "backward_decay",
     "forward", "decode_step", "decode_steps", "backward",
     "decode_steps_decay", "decode_steps_delta", "state_copy", "forward_decay",
+    "la_forward_delta", "forward_delta",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
@@ -54,7 +55,7 @@ exported_symbols = (
     "la_profile_enable", "la_profile_read", "la_launch_count",
     "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc",
     "la_forward_host_workspace_size", "la_forward_host", "la_backward_saved",
-    "la_backward_decay",
+    "la_backward_decay", "la_forward_delta",
 )
 
 
@@ -115,6 +116,8 @@ def lib():
     h.la_decode_steps_decay.argtypes = [_c_void] * 6 + [_c_int] * 5 + [_c_void, _c_float, _c_int, _c_void]
     h.la_decode_steps_delta.restype = _c_int
     h.la_decode_steps_delta.argtypes = [_c_void] * 5 + [_c_int] * 6 + [_c_void]
+    h.la_forward_delta.restype = _c_int
+    h.la_forward_delta.argtypes = [_c_void] * 5 + [_c_int] * 6 + [_c_void]
     h.la_forward_decay.restype = _c_int
     h.la_forward_decay.argtypes = [_c_void] * 4 + [_c_int] * 5 + [_c_void, _c_float, _c_int] + \
         [_c_void] * 3 + [ctypes.c_size_t, _c_void]
@@ -219,6 +222,10 @@ def la_decode_steps_decay(S, z, q, k, v, out, B, H, T, dk, dv, alpha, eps, dtype
 
 def la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream):
     return lib().la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream)
+
+
+def la_forward_delta(S, q, k, v, out, B, H, N, dk, dv, dtype, stream):
+    return lib().la_forward_delta(S, q, k, v, out, B, H, N, dk, dv, dtype, stream)
 
 
 def la_forward_decay(q, k, v, out, B, H, N, dk, dv, alpha, eps, dtype, S_final, z_final,
@@ -464,6 +471,23 @@ def decode_steps_delta(S, q, k, v, out=None):
         out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
     _check(la_decode_steps_delta(S.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                  out.data_ptr(), B, H, T, dk, dv, code, _stream_ptr(q)))
+    return out
+
+
+def forward_delta(S, q, k, v, out=None):
+    """Delta rule over N tokens per (batch, head), chunk by chunk, from and
+    into the fp32 state S [B,H,d,d] (in place); returns out [B,H,N,d]."""
+    import torch
+    B, H, dk, dv = S.shape
+    N = q.shape[2]
+    code = _dtype_code(q)
+    _need(S, "S", torch.float32)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=q.dtype, device=q.device)
+    _check(la_forward_delta(S.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                            out.data_ptr(), B, H, N, dk, dv, code, _stream_ptr(q)))
     return out
 
 

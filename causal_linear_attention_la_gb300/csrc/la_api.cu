@@ -661,6 +661,27 @@ la_status la_decode_steps_delta(float* S, const void* q, const void* k, const vo
   return LA_OK;
 }
 
+la_status la_forward_delta(float* S, const void* q, const void* k, const void* v, void* out,
+                           int B, int H, int N, int dk, int dv, la_dtype dtype,
+                           la_stream_t stream) {
+  if (N < 0) return fail(LA_ERR_INVALID_ARG, "N must be >= 0");
+  bool empty = false;
+  la_status st = check_sizes(B, H, N, dk, dv, dtype, 0.f, &empty);
+  if (st != LA_OK) return st;
+  if (dk != dv) return fail(LA_ERR_UNSUPPORTED, "la_forward_delta needs dk == dv");
+  if (empty) return LA_OK;
+  if (!S || !q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "S, q, k, v, out must be non-NULL");
+  if (!aligned16(S) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  VariantArgs a{};
+  a.S = S; a.q = q; a.k = k; a.v = v; a.out = out;
+  a.H = H; a.BH = B * H; a.ntok = N; a.dk = dk; a.dv = dv; a.dtype = dtype;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = la::forward_delta_chunked(a);
+  if (e != cudaSuccess) return cuda_fail(e, "la_forward_delta");
+  return LA_OK;
+}
+
 la_status la_state_copy(float* dst_S, float* dst_z, const float* src_S, const float* src_z,
                         int B, int H, int dk, int dv, la_stream_t stream) {
   bool empty = false;

@@ -18,6 +18,9 @@ struct VariantArgs {
 
 cudaError_t decode_steps_decay(const VariantArgs& a);
 cudaError_t decode_steps_delta(const VariantArgs& a);
+// Delta rule over whole sequences in 32-token chunks (la_delta_fwd.cu):
+// ntok = N tokens per (batch, head), dk = dv in {16, 32, 64, 128}.
+cudaError_t forward_delta_chunked(const VariantArgs& a);
 // Decay-gated causal forward on the tensor cores (bf16, dk = dv = 64): the
 // state pass and the chunk loop with per-head factors alpha [H]; FwdArgs as
 // for la_forward (its segment plan and workspace).

@@ -2,7 +2,8 @@
 
     python -m causal_linear_attention_la_gb300.run_once --workload fwd --B 4 --H 8 --N 4096 --d 64 --calls 2
 
-Workloads: fwd (la_forward; la_forward_decay with --decay), bwd (la_forward
+Workloads: fwd (la_forward; la_forward_decay with --decay; la_forward_delta,
+the chunked delta rule on unit-norm keys, with --delta), bwd (la_forward
 then la_backward), decode (la_decode_step on zero-initialised states, or
 la_decode_steps with --tokens T; --variant decay|delta for the gated and
 delta-rule updates). Inputs are seeded normal values scaled by 1/sqrt(d),
@@ -28,6 +29,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=1, help="decode: tokens per call (la_decode_steps when > 1)")
     ap.add_argument("--noncausal", action="store_true")
     ap.add_argument("--decay", action="store_true", help="fwd: decay-gated forward")
+    ap.add_argument("--delta", action="store_true", help="fwd: chunked delta rule")
     ap.add_argument("--variant", choices=["plain", "decay", "delta"], default="plain",
                     help="decode: state update variant")
     ap.add_argument("--f32", action="store_true")
@@ -67,8 +69,13 @@ def main(argv=None):
     else:
         q, k, v = rnd(B, H, N, d), rnd(B, H, N, d), rnd(B, H, N, d)
         gout = rnd(B, H, N, d, scale=1.0)
+        if args.delta:
+            k = (k.float() / k.float().norm(dim=-1, keepdim=True)).to(dt)
+            S = torch.zeros((B, H, d, d), device="cuda")
         for _ in range(args.calls):
-            if args.decay:
+            if args.delta:
+                la.forward_delta(S, q, k, v)
+            elif args.decay:
                 la.forward_decay(q, k, v, alpha)
             else:
                 la.forward(q, k, v, causal=causal)

@@ -263,6 +263,25 @@ LA_API la_status la_decode_steps_delta(float* S, const void* q, const void* k, c
                                 la_dtype dtype, la_stream_t stream);
 
 /*
+ * Delta rule over whole sequences: the same recurrence as
+ * la_decode_steps_delta, N tokens per (batch, head), computed chunk by chunk
+ * (32 tokens). Within a chunk the increments u'_t = v_t - S_{t-1}^T k_t solve
+ * a unit lower-triangular system (I + A) U' = V - K S_0, A the chunk's key
+ * products k_t . k_j below the diagonal; then out = Q S_0 + (Q K^T, j <= t) U'
+ * and S <- S_0 + K^T U'. Exact up to rounding against the token-by-token
+ * update; the work per chunk is dense products instead of N dependent steps.
+ *
+ * S [B,H,dk,dv] fp32 in/out (the state before the first token; after the
+ * call, the state after the last one); q, k [B,H,N,dk], v [B,H,N,dv] in,
+ * out [B,H,N,dv] out, dtype; fp32 arithmetic. dk == dv in {16, 32, 64, 128}
+ * (otherwise LA_ERR_UNSUPPORTED); N = 0 or B*H = 0 is a no-op. Pointers
+ * 16-byte aligned device memory, not overlapping. Errors as la_decode_steps.
+ */
+LA_API la_status la_forward_delta(float* S, const void* q, const void* k, const void* v,
+                                  void* out, int B, int H, int N, int dk, int dv,
+                                  la_dtype dtype, la_stream_t stream);
+
+/*
  * State snapshot / restore: dst_S <- src_S ([B,H,dk,dv] fp32) and, if both
  * are given, dst_z <- src_z ([B,H,dk] fp32), on `stream`. The same call saves
  * a state (prefix caching) and puts it back; a later step from the restored

@@ -1,5 +1,5 @@
-"""Decay-gated and delta-rule decode, and the state copy: CUDA path (through the
-C ABI) vs the fp64 oracle."""
+"""Decay-gated and delta-rule decode, the chunked delta rule, and the state
+copy: CUDA path (through the C ABI) vs the fp64 oracle."""
 
 import json
 import os
@@ -115,6 +115,106 @@ def test_delta_tokens(B, H, T, dk, dv, dtype):
     scale = max(np.abs(o_w).max(), np.abs(v).max())
     assert rel_err(to_host(out), o_w, scale) <= TOL[dtype]
     assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+
+
+def _unit_qkv(B, H, N, d, dtype, seed):
+    """Unit-norm queries and keys rounded to the input dtype, and the values
+    the kernel sees (host copies read back from the device tensors)."""
+    q, k, v = synth.qkv(B, H, N, d, d, seed=seed, dtype=dtype)
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    q = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    qd, kd, vd = to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype)
+    return (qd, kd, vd), (to_host(qd), to_host(kd), to_host(vd))
+
+
+# N spans one partial chunk, exact multiples of the 32-token chunk, ragged
+# tails and many chunks; d covers every supported head size
+DELTA_SHAPES = [(1, 1, 1, 16), (2, 3, 31, 32), (2, 2, 32, 64), (2, 2, 33, 64),
+                (1, 2, 100, 128), (3, 1, 257, 16), (2, 4, 1000, 128), (4, 2, 513, 32)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,N,d", DELTA_SHAPES)
+def test_forward_delta_chunked(B, H, N, d, dtype):
+    """Chunked delta rule (triangular solve per chunk) against the oracle's
+    token-by-token recurrence from a random state."""
+    import torch
+    S0 = np.random.default_rng(N * 3 + d).standard_normal((B, H, d, d)).astype(np.float32)
+    (qd, kd, vd), (q, k, v) = _unit_qkv(B, H, N, d, dtype, seed=900 + N)
+    S = torch.from_numpy(S0).cuda()
+    out = la.forward_delta(S, qd, kd, vd)
+    torch.cuda.synchronize()
+    S_w, o_w = orc.decode_steps_delta(S0, q, k, v)
+    scale = max(np.abs(o_w).max(), np.abs(v).max())
+    assert rel_err(to_host(out), o_w, scale) <= TOL[dtype]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+
+
+def test_forward_delta_whole_heads_d128():
+    """Thirty-two heads of 2048 tokens at d = 128 (fp32), every output
+    against the oracle; the final states too."""
+    import torch
+    B, H, N, d = 2, 16, 2048, 128
+    S0 = np.zeros((B, H, d, d), np.float32)
+    (qd, kd, vd), (q, k, v) = _unit_qkv(B, H, N, d, "f32", seed=77)
+    S = torch.from_numpy(S0).cuda()
+    out = la.forward_delta(S, qd, kd, vd)
+    torch.cuda.synchronize()
+    S_w, o_w = orc.decode_steps_delta(S0, q, k, v)
+    assert rel_err(to_host(out), o_w, np.abs(o_w).max()) <= TOL["f32"]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+
+
+def test_forward_delta_matches_token_steps():
+    """The chunked form and the token-by-token kernel compute the same
+    recurrence; they differ only in rounding order."""
+    import torch
+    B, H, N, d = 2, 3, 200, 64
+    S0 = torch.randn(B, H, d, d, generator=torch.Generator().manual_seed(3)).cuda()
+    (qd, kd, vd), _ = _unit_qkv(B, H, N, d, "f32", seed=5)
+    S1, S2 = S0.clone(), S0.clone()
+    o1 = la.forward_delta(S1, qd, kd, vd)
+    o2 = la.decode_steps_delta(S2, qd, kd, vd)
+    torch.cuda.synchronize()
+    assert rel_err(to_host(o1), to_host(o2), float(o2.abs().max())) <= 1e-5
+    assert rel_err(to_host(S1), to_host(S2), float(S2.abs().max())) <= 1e-5
+
+
+def test_forward_delta_page_example():
+    """The worked example of the delta rule as one sequence of three tokens
+    (two writes, then the write under key (0.6, 0.8)), embedded in d = 16."""
+    import torch
+    with open(os.path.join(GOLDEN, "la_order_delta_rule.json")) as f:
+        g = json.load(f)
+    keys = g["k"] + [g["write"]["k"]]
+    vals = [x[0] for x in g["v"]] + [g["write"]["v"][0]]
+    S = torch.zeros(1, 1, 16, 16, device="cuda")
+    q = torch.zeros(1, 1, 3, 16, device="cuda")
+    k = torch.zeros(1, 1, 3, 16, device="cuda")
+    v = torch.zeros(1, 1, 3, 16, device="cuda")
+    for t in range(3):
+        k[0, 0, t, :2] = torch.tensor(keys[t])
+        v[0, 0, t, 0] = vals[t]
+        q[0, 0, t, :2] = torch.tensor(g["reads_after"]["queries"][0])
+    out = la.forward_delta(S, q, k, v)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to_host(S)[0, 0, :2, 0], g["S_after"], rtol=0, atol=1e-5)
+    assert abs(float(out[0, 0, 2, 0]) - g["reads_after"]["values"][0]) <= 1e-5
+
+
+def test_forward_delta_edges():
+    """N = 0 leaves the state alone; dk != dv is refused."""
+    import torch
+    S = torch.randn(1, 2, 32, 32, device="cuda")
+    S_before = S.clone()
+    e = torch.empty(1, 2, 0, 32, device="cuda")
+    la.forward_delta(S, e, e, e)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S_before)
+    S2 = torch.zeros(1, 1, 32, 64, device="cuda")
+    q = torch.zeros(1, 1, 4, 32, device="cuda")
+    with pytest.raises(la.LaError):
+        la.forward_delta(S2, q, q, torch.zeros(1, 1, 4, 64, device="cuda"))
 
 
 def test_state_snapshot_restore_round_trip():
