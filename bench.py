@@ -18,8 +18,9 @@ states of d=128 (1024 steps in a CUDA graph), the same decode with 16 tokens
 per call (64 calls of la_decode_steps), the decay-gated and delta-rule
 variants in the same shape, forward + backward B=4 H=8 N=8192 d=64 (causal
 and not; the backward reuses the forward's state records through
-la_backward_saved), and the decay-gated forward in the B=4 H=8 N=4096 d=64
-shape.
+la_backward_saved), the decay-gated forward in the B=4 H=8 N=4096 d=64
+shape, and the chunked delta rule over B=2 H=16 N=8192 d=128 (CUDA cores,
+against the fp32 FMA rate at the sampled SM clock).
 
 Timing: W eager warm-up steps, then the K timed steps are captured once in a
 CUDA graph and replayed, bracketed by CUDA events on the launching stream
@@ -75,6 +76,8 @@ WORKLOADS = {
     "decay16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                  prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16,
                                  variant="decay"),
+    # the delta rule over whole sequences, chunk by chunk (la_forward_delta)
+    "deltafwd_b2_h16_n8192_d128": dict(kind="delta_fwd", B=2, H=16, N=8192, dk=128, dv=128, seed=6),
     "delta16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                  prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16,
                                  variant="delta"),
@@ -245,6 +248,18 @@ def decode_state_bytes(w):
     """S and z read and written once per step (call), fp32; the delta rule keeps no z."""
     zwords = 0 if w.get("variant") == "delta" else w["dk"]
     return w["B"] * w["H"] * (w["dk"] * w["dv"] + zwords) * 4 * 2
+
+
+def delta_flops(w):
+    """Algorithmic flops of the delta rule token by token: the read with the
+    key, the rank-one write and the read with the query, 3 * 2 * dk * dv per
+    token-head."""
+    return 6.0 * w["dk"] * w["dv"] * w["B"] * w["H"] * w["N"]
+
+
+def fp32_peak_tflops(sm_mhz):
+    """CUDA-core fp32 rate: 152 SMs x 128 FMA lanes x 2 flops at the SM clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 def decode_io_bytes(w, elt=2):
@@ -434,6 +449,40 @@ def run_decode(w, K, W, barrier):
     torch.cuda.synchronize()
     ms, launches, _ = _graph_time(step, T, stream, barrier)
     return dict(ms=ms, launches=launches, steps=T, prefill_s=prefill_s)
+
+
+def run_delta_fwd(w, K, W, barrier):
+    """K calls of la_forward_delta on one fp32 state, inputs rotating past L2
+    (unit-norm keys: each write replaces what its key held)."""
+    import torch
+    import causal_linear_attention_la_gb300 as la
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w["seed"])
+    B, H, N, d = w["B"], w["H"], w["N"], w["dk"]
+    R = _rotations(fwd_bytes(w))
+    sets = []
+    for _ in range(R):
+        q = (torch.randn((B, H, N, d), generator=gen, device=dev) * d ** -0.5).to(torch.bfloat16)
+        k = torch.randn((B, H, N, d), generator=gen, device=dev)
+        k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+        v = (torch.randn((B, H, N, d), generator=gen, device=dev) * d ** -0.5).to(torch.bfloat16)
+        sets.append((q, k, v, torch.empty_like(v)))
+    S = torch.zeros((B, H, d, d), device=dev)
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        q, k, v, o = sets[i % R]
+        st = la.la_forward_delta(S.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 B, H, N, d, d, la.LA_BF16, torch.cuda.current_stream().cuda_stream)
+        assert st == 0, la.lib().la_last_error()
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    torch.cuda.synchronize()
+    ms, launches, _ = _graph_time(step, K, stream, barrier)
+    return dict(ms=ms, launches=launches, rotations=R, bytes_per_set=fwd_bytes(w))
 
 
 def run_e2e(w, K, W, slices=E2E_SLICES):
@@ -676,6 +725,22 @@ def main():
                 sections[name]["dram_bytes_per_step"] = dram
                 sections[name]["dram_gbs"] = dram / per / 1e9
                 sections[name]["dram_frac"] = dram / per / 1e9 / peaks["hbm_gbs"]
+        elif ws["kind"] == "delta_fwd":
+            kk = max(3, K // 10)
+            rr = run_delta_fwd(ws, kk, W, barrier)
+            t = max_over_ranks(rr["ms"]) / 1e3
+            mhz = sampler.summary()["sm_mhz"] or 2070.0
+            ach = delta_flops(ws) * kk / t / 1e12
+            sections[name] = {
+                "value": job_throughput(world, ws["B"] * ws["N"] * kk, t), "unit": "tokens/s",
+                "ms_per_step": 1e3 * t / kk, "steps": kk,
+                "roofline": {"bound": "alu", "achieved": ach, "peak": fp32_peak_tflops(mhz),
+                             "unit": "TFLOP/s", "frac": ach / fp32_peak_tflops(mhz),
+                             "kernel": "delta_chunk",
+                             "peak_source": f"152 SMs x 128 fp32 FMA lanes x 2 at {mhz:.0f} MHz"},
+                "gpu_launches": rr["launches"],
+                "l2": f"{rr['rotations']} input set(s) of {rr['bytes_per_set'] / 1e6:.0f} MB",
+            }
         elif ws["kind"] == "fwdbwd":
             kk = max(3, K // 5)
             rr = run_forward(ws, kk, W, barrier, with_bwd=True)
