@@ -239,6 +239,30 @@ def fwd_flops(w):
     return 4.0 * w["dk"] * w["dv"] * w["B"] * w["H"] * w["N"]
 
 
+def fwd_mma_flops(w, C=128):
+    """Flops the tensor cores execute in the causal chunk loop, per launch:
+    per 128-token chunk and head, d = 64: [P | O | dz] (M128 N208 K64),
+    [S^T ; z] += [V^T ; 1] phi(K) (M128 N64 K128), [O | den] += P [V | 1]
+    (M128 N80 K128); d = 128: P, O, the state update and P V, each M128
+    N128 K128."""
+    chunks = w["B"] * w["H"] * -(-w["N"] // C)
+    if w["dk"] == 64:
+        per = 2 * 128 * (208 * 64 + 64 * 128 + 80 * 128)
+    else:
+        per = 4 * 2 * 128 * 128 * w["dk"]
+    return float(chunks * per)
+
+
+def tensor_line(w, span_ms, peaks):
+    """Tensor-pipe use of the chunk loop: executed MMA flops / its live span,
+    against the measured bf16 dense peak (burst: the kernel is timed alone)."""
+    ach = fwd_mma_flops(w) / (span_ms / 1e3) / 1e12
+    return {"achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "kernel": "fwd_output",
+            "flops_per_launch": fwd_mma_flops(w),
+            "flops": "MMA flops executed by the chunk loop (not the recurrence's 4 dk dv per token-head)"}
+
+
 def bwd_bytes(w, elt=2):
     """Minimum HBM bytes of one backward: read q, k, v, dout; write dq, dk, dv."""
     return w["B"] * w["H"] * w["N"] * (4 * w["dk"] + 3 * w["dv"]) * elt
@@ -692,6 +716,7 @@ def main():
                 "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": ach / peaks["hbm_gbs"], "kernel": "fwd_output",
                              "traffic": ncu_traffic("fwd_output_" + name)},
+                "tensor": tensor_line(ws, sp["avg_ms"], peaks),
                 "kernels": rr["spans"], "gpu_launches": rr["launches"],
                 "l2": f"{rr['rotations']} input set(s) of {rr['bytes_per_set'] / 1e6:.0f} MB",
             }
@@ -777,6 +802,7 @@ def main():
                          "traffic": ncu_traffic("fwd_output_" + MAIN), "kernel": "fwd_output",
                          "peak_source": f"{peak_src} hbm_gbs",
                          "algorithmic_bytes_per_launch": alg_bytes},
+            "tensor": tensor_line(w, out_span["avg_ms"], peaks),
             "kernels": r["spans"],
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_threads,
                              "kind": "oracle", "sample": cpu_desc},
