@@ -35,7 +35,7 @@ __all__ = [
     "la_backward_saved", "backward_saved", "la_backward_decay", "backward_decay",
     "forward", "decode_step", "decode_steps", "backward",
     "decode_steps_decay", "decode_steps_delta", "state_copy", "forward_decay",
-    "la_forward_delta", "forward_delta",
+    "la_forward_delta", "forward_delta", "la_forward_plan", "forward_plan",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
@@ -55,7 +55,7 @@ exported_symbols = (
     "la_profile_enable", "la_profile_read", "la_launch_count",
     "la_device_status", "la_test_timeout_next_forward", "la_forward_noalloc",
     "la_forward_host_workspace_size", "la_forward_host", "la_backward_saved",
-    "la_backward_decay", "la_forward_delta",
+    "la_backward_decay", "la_forward_delta", "la_forward_plan",
 )
 
 
@@ -117,6 +117,8 @@ def lib():
     h.la_decode_steps_delta.restype = _c_int
     h.la_decode_steps_delta.argtypes = [_c_void] * 5 + [_c_int] * 6 + [_c_void]
     h.la_forward_delta.restype = _c_int
+    h.la_forward_plan.restype = _c_int
+    h.la_forward_plan.argtypes = [_c_int] * 8 + [_c_void]
     h.la_forward_delta.argtypes = [_c_void] * 5 + [_c_int] * 6 + [_c_void]
     h.la_forward_decay.restype = _c_int
     h.la_forward_decay.argtypes = [_c_void] * 4 + [_c_int] * 5 + [_c_void, _c_float, _c_int] + \
@@ -222,6 +224,18 @@ def la_decode_steps_decay(S, z, q, k, v, out, B, H, T, dk, dv, alpha, eps, dtype
 
 def la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream):
     return lib().la_decode_steps_delta(S, q, k, v, out, B, H, T, dk, dv, dtype, stream)
+
+
+def la_forward_plan(B, H, N, dk, dv, causal, dtype, final_state, out):
+    return lib().la_forward_plan(B, H, N, dk, dv, causal, dtype, final_state, out)
+
+
+def forward_plan(B, H, N, dk, dv, causal=True, dtype=LA_BF16, final_state=False):
+    """The split la_forward uses for these sizes: dict with P, seg_len, F,
+    pieces (0: by segments) and piece_len (chunks of 128 tokens)."""
+    buf = (ctypes.c_int * 5)()
+    _check(la_forward_plan(B, H, N, dk, dv, int(causal), dtype, int(final_state), ctypes.cast(buf, ctypes.c_void_p)))
+    return dict(P=buf[0], seg_len=buf[1], F=buf[2], pieces=buf[3], piece_len=buf[4])
 
 
 def la_forward_delta(S, q, k, v, out, B, H, N, dk, dv, dtype, stream):

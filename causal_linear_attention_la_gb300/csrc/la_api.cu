@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -68,8 +69,11 @@ struct WsLayout {
 WsLayout layout(long long BH, int N, int dk, int dv, const SegPlan& plan, bool backward) {
   WsLayout w{};
   const size_t rec = sizeof(float) * (size_t)record_slot_words(dk, dv) * (size_t)plan.P * (size_t)BH;
+  // forward records: one per piece, or F per segment
+  const size_t frec = plan.NP > 0 ? sizeof(float) * (size_t)record_slot_words(dk, dv) * (size_t)plan.NP
+                                  : rec * (size_t)plan.F;
   w.state_off = 0;
-  size_t off = align_up(rec * (size_t)plan.F, 256);
+  size_t off = align_up(frec, 256);
   if (backward) {
     w.rev_off = off;
     off += align_up(rec, 256);
@@ -205,9 +209,29 @@ SegPlan plan_segments(long long BH, int N, int slots) {
 // kernel's CTAs, which need a whole SM, start on the SMs the state pass
 // leaves free (measured: a state pass spread over every SM delays them more
 // than its shorter CTAs save).
-SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool causal) {
+// The causal tensor-core forward at d = 128 without a final state takes
+// balanced pieces instead (SegPlan) when they cost less: with B*H heads the
+// segments give B*H*P CTAs of whole segments, which leaves SMs idle whenever
+// B*H does not divide the SM count (32 heads: 128 CTAs on 152 SMs), while
+// pieces give every SM the same number of chunks.
+SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool causal, bool final_state) {
   SegPlan plan = plan_segments(BH, N, kSlots);
   const bool tc = g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, causal);
+  if (tc && causal && dk == 128 && dv == 128 && !final_state) {
+    const long long nch = (N + kSegGranule - 1) / kSegGranule;
+    const long long total = BH * nch;
+    const long long np0 = std::min<long long>(kSlots, total);
+    const long long len = (total + np0 - 1) / np0;          // chunks per piece
+    const long long np = (total + len - 1) / len;
+    const long long L = (plan.seg_len + kSegGranule - 1) / kSegGranule;
+    const long long waves = (BH * plan.P + kSlots - 1) / kSlots;
+    // a piece spans at most two heads (len <= chunks per head)
+    if (len <= nch && len + 1 < waves * (L + 1)) {
+      plan.NP = (int)np;
+      plan.piece_len = (int)len;
+      return plan;
+    }
+  }
   // segments the state pass sums: the earlier ones (causal) or all of them
   const int nseg = causal ? plan.P - 1 : plan.P;
   if (!tc || nseg < 1) return plan;
@@ -325,7 +349,25 @@ int la_backward_path(int dk, int dv, la_dtype dtype, int causal) {
 size_t la_forward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
   if (B <= 0 || H <= 0 || N <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
   const long long BH = (long long)B * H;
-  return layout(BH, N, dk, dv, forward_plan(BH, N, dk, dv, dtype, causal != 0), false).total;
+  // with or without a final state (the plan may differ): the larger
+  const size_t a = layout(BH, N, dk, dv, forward_plan(BH, N, dk, dv, dtype, causal != 0, false), false).total;
+  const size_t b = layout(BH, N, dk, dv, forward_plan(BH, N, dk, dv, dtype, causal != 0, true), false).total;
+  return std::max(a, b);
+}
+
+la_status la_forward_plan(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype, int final_state,
+                          int* out) {
+  if (out == nullptr) return fail(LA_ERR_INVALID_ARG, "out must be non-NULL");
+  if (B <= 0 || H <= 0 || N <= 0) return fail(LA_ERR_INVALID_ARG, "B, H, N must be positive");
+  if (!head_ok(dk) || !head_ok(dv)) return fail(LA_ERR_INVALID_ARG, "head sizes dk=%d dv=%d", dk, dv);
+  if (dtype != LA_F32 && dtype != LA_BF16) return fail(LA_ERR_INVALID_ARG, "dtype %d", (int)dtype);
+  const SegPlan p = forward_plan((long long)B * H, N, dk, dv, dtype, causal != 0, final_state != 0);
+  out[0] = p.P;
+  out[1] = p.seg_len;
+  out[2] = p.F;
+  out[3] = p.NP;
+  out[4] = p.piece_len;
+  return LA_OK;
 }
 
 size_t la_backward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
@@ -359,7 +401,7 @@ la_status la_forward(const void* q, const void* k, const void* v, void* out,
   if (!q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be non-NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
-  const SegPlan plan = forward_plan(BH, N, dk, dv, dtype, causal != 0);
+  const SegPlan plan = forward_plan(BH, N, dk, dv, dtype, causal != 0, S_final != nullptr);
   const WsLayout w = layout(BH, N, dk, dv, plan, false);
   if (workspace == nullptr || workspace_bytes < w.total)
     return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
@@ -600,7 +642,7 @@ la_status la_forward_decay(const void* q, const void* k, const void* v, void* ou
   if (!q || !k || !v || !out || !alpha) return fail(LA_ERR_INVALID_ARG, "q, k, v, out, alpha must be non-NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LA_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
-  const SegPlan plan = forward_plan(BH, N, dk, dv, dtype, true);
+  const SegPlan plan = forward_plan(BH, N, dk, dv, dtype, true, true);
   const WsLayout w = layout(BH, N, dk, dv, plan, false);
   if (workspace == nullptr || workspace_bytes < w.total)
     return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
@@ -740,7 +782,7 @@ la_status backward_impl(const void* q, const void* k, const void* v, const void*
   const bool use_tc = alpha == nullptr && g_path.load() == LA_PATH_AUTO &&
                       tc_backward_supported(dk, dv, dtype, a.causal);
   if (saved != nullptr) {
-    const SegPlan fplan = forward_plan(BH, N, dk, dv, dtype, a.causal);
+    const SegPlan fplan = forward_plan(BH, N, dk, dv, dtype, a.causal, true);
     const size_t need = layout(BH, N, dk, dv, fplan, false).total;
     if (saved_bytes < need)
       return fail(LA_ERR_INVALID_ARG, "saved forward workspace of %zu bytes needed, %zu given", need, saved_bytes);

@@ -37,6 +37,14 @@ struct SegPlan {
   int P;        // segments per sequence (>= 1)
   int seg_len;  // tokens per segment, multiple of kSegGranule (except when N is smaller)
   int F = 1;    // tensor-core state pass: CTAs (and sum records) per segment
+  // Balanced pieces (NP > 0; the causal tensor-core forward at d = 128 without
+  // a final state): the heads' chunks laid end to end, head after head, and
+  // cut into NP pieces of piece_len chunks (the last one shorter), one CTA
+  // each; a piece may end one head and start the next. Record i is the sum
+  // over the part of piece i in its last head, when that head goes on after
+  // the piece. P and seg_len still describe the segment plan.
+  int NP = 0;
+  int piece_len = 0;
 };
 
 // Tokens summed by one state-pass CTA: ceil(chunks per segment / F) chunks.

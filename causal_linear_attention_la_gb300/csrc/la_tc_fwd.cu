@@ -127,6 +127,26 @@ struct FwdParams {
   // test of the bounded waits: the MMA issuer first waits on a barrier that
   // nothing completes (la_test_timeout_next_forward)
   int timeout_test = 0;
+  // balanced pieces (SegPlan, d = 128 causal without a final state): CTA i
+  // runs chunks i * piece_len .. of the heads laid end to end
+  int NP = 0, piece_len = 0, nch = 0, BH = 0;
+};
+
+// The chunks one CTA of the chunk loop runs. By segments: chunks of head bh
+// from token tok0. By pieces: global chunks g0, g0 + 1, ... of the heads
+// laid end to end (nch chunks each), so a piece may end one head and start
+// the next; chunk c then belongs to head (g0 + c) / nch.
+struct ChunkMap {
+  long long g0;
+  int nch, bh, tok0, N;
+  bool pieces;
+  __device__ __forceinline__ int bh_of(int c) const { return pieces ? (int)((g0 + c) / nch) : bh; }
+  __device__ __forceinline__ int y_of(int c) const {
+    return pieces ? (int)((g0 + c) % nch) * C : tok0 + c * C;
+  }
+  // chunk c > 0 starts a head: the state goes back to zero
+  __device__ __forceinline__ bool head_start(int c) const { return pieces && c > 0 && (g0 + c) % nch == 0; }
+  __device__ __forceinline__ int n_valid(int c) const { return min(C, N - y_of(c)); }
 };
 
 // With decay gating (kDecay, D = 64): S_t = a S_{t-1} + phi(k_t) v_t^T and the
@@ -276,20 +296,42 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // segment-major order: the first segments (which wait for no records) come first
-  const int BH = gridDim.x / prm.P;
-  const int bh = blockIdx.x % BH, seg = blockIdx.x / BH;
-  const int tok0 = seg * prm.seg_len;
-  const int tok_end = min(prm.N, tok0 + prm.seg_len);
-  const int nchunks = (tok_end - tok0 + C - 1) / C;
+  const long long rstride = rec_words<D>();
+  int bh, tok0, tok_end, nchunks, nrec;
+  bool last_seg;
+  const float* recs;
+  ChunkMap cmap;
+  if (!kDecay && prm.NP > 0) {
+    // piece blockIdx.x; its first head starts from the records of the
+    // pieces before it in that head (one each), a later head from zero
+    const long long g0 = (long long)blockIdx.x * prm.piece_len;
+    const long long g1 = min((long long)prm.BH * prm.nch, g0 + prm.piece_len);
+    bh = (int)(g0 / prm.nch);
+    tok0 = (int)(g0 % prm.nch) * C;
+    tok_end = prm.N;
+    nchunks = (int)(g1 - g0);
+    const long long first = (long long)bh * prm.nch / prm.piece_len;   // piece holding the head's start
+    recs = prm.ws_state + first * rstride;
+    nrec = (int)(blockIdx.x - first);
+    last_seg = false;
+    cmap = ChunkMap{g0, prm.nch, bh, tok0, prm.N, true};
+  } else {
+    // segment-major order: the first segments (which wait for no records) come first
+    const int BH = gridDim.x / prm.P;
+    bh = blockIdx.x % BH;
+    const int seg = blockIdx.x / BH;
+    tok0 = seg * prm.seg_len;
+    tok_end = min(prm.N, tok0 + prm.seg_len);
+    nchunks = (tok_end - tok0 + C - 1) / C;
+    recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
+    nrec = seg * prm.F;                   // records of the earlier segments
+    last_seg = seg == prm.P - 1;
+    cmap = ChunkMap{0, 0, bh, tok0, prm.N, false};
+  }
   const float log2a = kDecay ? log2f(prm.alpha[bh % prm.H]) : 0.f;
-  const bool last_seg = seg == prm.P - 1;
   const bool write_final = last_seg && prm.S_final != nullptr;
   // the state update after the last chunk is only needed for the final state
   const int nupdates = write_final ? nchunks : nchunks - 1;
-  const long long rstride = rec_words<D>();
-  const float* recs = prm.ws_state + (long long)bh * prm.P * prm.F * rstride;
-  const int nrec = seg * prm.F;           // records of the earlier segments
 
   if (tid == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -342,7 +384,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!mbar_wait(&ost_full[s], (c / ST) & 1, abort_flag, kTimeoutNs)) return false;
         uint8_t* stg = sm + s * G::STAGE;
 #pragma unroll
-        for (int b = 0; b < G::NB; ++b) tma_store_3d(&map_o, stg + b * BOX, 64 * b, tok0 + c * C, bh);
+        for (int b = 0; b < G::NB; ++b) tma_store_3d(&map_o, stg + b * BOX, 64 * b, cmap.y_of(c), cmap.bh_of(c));
         tma_store_commit();
         tma_store_wait_read<0>();
         return true;
@@ -357,13 +399,13 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           stored = c - ST + 1;
         }
         uint8_t* stg = sm + s * G::STAGE;
-        const int y = tok0 + c * C;
+        const int y = cmap.y_of(c), cbh = cmap.bh_of(c);
         mbar_arrive_expect_tx(&full[s], 3 * G::TILE);
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
-          tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + G::OFF_K + b * BOX, &map_k, &full[s], 64 * b, y, bh);
-          tma_load_3d(stg + G::OFF_V + b * BOX, &map_v, &full[s], 64 * b, y, bh);
+          tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, cbh);
+          tma_load_3d(stg + G::OFF_K + b * BOX, &map_k, &full[s], 64 * b, y, cbh);
+          tma_load_3d(stg + G::OFF_V + b * BOX, &map_v, &full[s], 64 * b, y, cbh);
         }
         issued = c + 1;
       }
@@ -510,6 +552,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         ok = mbar_wait(s_full, (c - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        // a piece's next head starts from zero (a sum of no records)
+        if (!kDecay && !G::MERGE && cmap.head_start(c))
+          sum_states_to_tmem<D>(recs, rstride, 0, 0, lane_addr, G::COL_S, row_sum);
       }
       if constexpr (kDecay) {
         // the copy of S_prev, and the held state decayed by a^n before this
@@ -736,7 +781,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % ST;
-      const int n_valid = min(C, tok_end - (tok0 + c * C));
+      const int n_valid = kDecay ? min(C, tok_end - (tok0 + c * C)) : cmap.n_valid(c);
       ok = mbar_wait(&full[s], (c / ST) & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
       float colsum[8];
@@ -758,6 +803,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (c == 0) {
         if (nrec > 0) griddep_wait();
         sum_vectors8<D>(recs, rstride, 0, nrec, 8 * fc, zrun);
+      } else if (cmap.head_start(c)) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zrun[e] = 0.f;
       }
       if (owner) {
         // z before this chunk, for group B's denominators
@@ -822,6 +870,9 @@ struct StateParams {
   int* status;
   const float* alpha = nullptr;   // kDecay: [H] per-head factors
   int H = 1;
+  // balanced pieces (SegPlan): CTA i sums the part of piece i in its last
+  // head into record i, if that head goes on after the piece
+  int NP = 0, piece_len = 0, nch = 0, BH = 0;
 };
 
 // kDecay: each record is decayed to its part's last token (row j of a chunk
@@ -856,13 +907,29 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // part j of segment j / F covers sub_len tokens from j % F * sub_len
-  const int nparts = prm.nseg * prm.F;
-  const int bh = blockIdx.x / nparts, j = blockIdx.x % nparts;
-  const int seg = j / prm.F, part = j % prm.F;
-  const int seg_end = min(prm.N, (seg + 1) * prm.seg_len);
-  const int tok0 = seg * prm.seg_len + part * prm.sub_len;
-  const int tok_end = min(seg_end, tok0 + prm.sub_len);
+  int bh, tok0, tok_end;
+  long long rec_index;
+  if (prm.NP > 0) {
+    const long long g0 = (long long)blockIdx.x * prm.piece_len;
+    const long long g1 = min((long long)prm.BH * prm.nch, g0 + prm.piece_len);
+    const long long h = (g1 - 1) / prm.nch;
+    if (g1 == (h + 1) * prm.nch) return;   // the piece ends its head: no record
+    const long long s0 = max(g0, h * prm.nch);
+    bh = (int)h;
+    tok0 = (int)(s0 - h * prm.nch) * C;
+    tok_end = min(prm.N, (int)(g1 - h * prm.nch) * C);
+    rec_index = blockIdx.x;
+  } else {
+    // part j of segment j / F covers sub_len tokens from j % F * sub_len
+    const int nparts = prm.nseg * prm.F;
+    const int j = blockIdx.x % nparts;
+    bh = blockIdx.x / nparts;
+    const int seg = j / prm.F, part = j % prm.F;
+    const int seg_end = min(prm.N, (seg + 1) * prm.seg_len);
+    tok0 = seg * prm.seg_len + part * prm.sub_len;
+    tok_end = min(seg_end, tok0 + prm.sub_len);
+    rec_index = (long long)bh * prm.P * prm.F + j;
+  }
   // a part past the end of a short last segment (non-causal) holds no token
   const int nchunks = max(0, (tok_end - tok0 + C - 1) / C);
   static_assert(!kDecay || StateSmem<D>::ZMMA, "decay gating is laid out for D = 64");
@@ -971,7 +1038,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       mbar_arrive(&phi_done[s]);
     }
     reduce_row_groups<D, 256>(zrun);
-    float* dst = prm.ws_state + ((long long)bh * prm.P * prm.F + j) * rec_words<D>();
+    float* dst = prm.ws_state + rec_index * rec_words<D>();
     if ((!L::ZMMA || kCentre) && ok && lane < X::FCW) {
       float4* zd = reinterpret_cast<float4*>(dst + D * D + 8 * fc);
       zd[0] = make_float4(zrun[0], zrun[1], zrun[2], zrun[3]);
@@ -1292,9 +1359,11 @@ tc_noncausal_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 
 template <int D, bool kDecay = false>
 cudaError_t launch_state(const FwdArgs& a, const float* alpha = nullptr, int H = 1) {
-  // causal: the segments before the last (none with one segment); non-causal: all
+  // causal: the segments before the last (none with one segment); non-causal:
+  // all; with pieces, one CTA per piece (those that end their head exit)
   const int nseg = a.causal ? a.plan.P - 1 : a.plan.P;
-  if (nseg < 1) return cudaSuccess;
+  const bool pieces = !kDecay && a.plan.NP > 0;
+  if (!pieces && nseg < 1) return cudaSuccess;
   CUtensorMap mk, mv;
   cudaError_t e = make_map(&mk, a.k, a.BH, a.N, D);
   if (e == cudaSuccess) e = make_map(&mv, a.v, a.BH, a.N, D);
@@ -1306,7 +1375,14 @@ cudaError_t launch_state(const FwdArgs& a, const float* alpha = nullptr, int H =
                 device_status_ptr()};
   p.alpha = alpha;
   p.H = H;
-  tc_state_kernel<D, kDecay><<<a.BH * nseg * a.plan.F, 320, smem, a.stream>>>(mk, mv, p);
+  if (pieces) {
+    p.NP = a.plan.NP;
+    p.piece_len = a.plan.piece_len;
+    p.nch = (a.N + C - 1) / C;
+    p.BH = a.BH;
+  }
+  const unsigned grid = pieces ? (unsigned)a.plan.NP : (unsigned)(a.BH * nseg * a.plan.F);
+  tc_state_kernel<D, kDecay><<<grid, 320, smem, a.stream>>>(mk, mv, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -1360,10 +1436,17 @@ cudaError_t launch_forward(const FwdArgs& a, const float* alpha = nullptr, int H
   p.H = H;
   p.sub_len = state_sub_len(a.plan);
   p.timeout_test = (!kDecay && take_timeout_test()) ? 1 : 0;
+  const bool pieces = !kDecay && a.plan.NP > 0;
+  if (pieces) {
+    p.NP = a.plan.NP;
+    p.piece_len = a.plan.piece_len;
+    p.nch = (a.N + C - 1) / C;
+    p.BH = a.BH;
+  }
   // a dependent of the state kernel (when there is one): it may start before
   // that kernel ends and waits for its records only where it reads them
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(a.BH * a.plan.P);
+  cfg.gridDim = dim3(pieces ? a.plan.NP : a.BH * a.plan.P);
   cfg.blockDim = dim3(448);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;

@@ -263,6 +263,20 @@ LA_API la_status la_decode_steps_delta(float* S, const void* q, const void* k, c
                                 la_dtype dtype, la_stream_t stream);
 
 /*
+ * How la_forward splits a call of these sizes (with a final state requested
+ * or not: the split may differ), for tests and tuning. out[5] receives: the
+ * segments per sequence P, the tokens per segment, the state-pass CTAs per
+ * segment F, the number of balanced pieces (0 when the call runs by
+ * segments) and the 128-token chunks per piece. With pieces, the heads'
+ * chunks are laid end to end and cut into equal pieces, one CTA each, so
+ * that every SM gets the same work even when B*H does not divide the SM
+ * count (causal tensor-core forward at d = 128 without a final state).
+ * LA_ERR_INVALID_ARG for sizes outside la_forward's range or a NULL out.
+ */
+LA_API la_status la_forward_plan(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype,
+                                 int final_state, int* out);
+
+/*
  * Delta rule over whole sequences: the same recurrence as
  * la_decode_steps_delta, N tokens per (batch, head), computed chunk by chunk
  * (32 tokens). Within a chunk the increments u'_t = v_t - S_{t-1}^T k_t solve

@@ -212,3 +212,22 @@ def test_path_selection(lib):
     la.la_set_path(prev)
     assert la.la_forward_path(48, 64, la.LA_BF16) == -1
     assert la.la_forward_path(16, 16, la.LA_F32) == 0
+
+
+def test_forward_plan_pieces():
+    """The causal bf16 forward at d = 128 without a final state takes balanced
+    pieces when B*H*P segments would leave SMs idle; with a final state, at
+    d = 64, non-causal or fp32 it runs by segments."""
+    import causal_linear_attention_la_gb300 as la
+    p = la.forward_plan(2, 16, 32768, 128, 128)
+    assert (p["pieces"], p["piece_len"]) == (152, 54)
+    assert p["pieces"] * p["piece_len"] >= 2 * 16 * 256
+    assert la.forward_plan(2, 16, 32768, 128, 128, final_state=True)["pieces"] == 0
+    assert la.forward_plan(2, 16, 32768, 128, 128, causal=False)["pieces"] == 0
+    assert la.forward_plan(2, 16, 32768, 128, 128, dtype=la.LA_F32)["pieces"] == 0
+    assert la.forward_plan(4, 8, 4096, 64, 64)["pieces"] == 0
+    # 38 heads of 4 segments already fill the SMs: no pieces
+    assert la.forward_plan(2, 19, 27648, 128, 128)["pieces"] == 0
+    # the workspace query covers both plans
+    ws = la.la_forward_workspace_size(2, 16, 32768, 128, 128, 1, la.LA_BF16)
+    assert ws >= 152 * (128 * 128 + 2 * 128) * 4

@@ -2,10 +2,11 @@
 times (default path, one call per pass):
 
 * causal forward B=4 H=8 N=4096 d=64 bf16: every output vs the oracle recurrence
-* causal forward B=2 H=16 N=32768 d=128 bf16: two whole heads (every one of
-  their 32768 outputs and the final state) against the oracle recurrence,
-  plus outputs of every head sampled at chunk edges and at random, each
-  computed one by one by the oracle's definition
+* causal forward B=2 H=16 N=32768 d=128 bf16, as the bench runs it
+  (balanced pieces) and with the final state (segments): three whole heads
+  (every one of their 32768 outputs, and the final state) against the
+  oracle recurrence, plus outputs sampled at every piece's first and last
+  chunk and at random, each computed one by one by the oracle's definition
 * decode: fp32 states from a bf16 prefill of N=131072 tokens on B=1 H=16,
   replicated to B=64 x H=32, then 1024 one-token steps; every state's output
   for the first 8 steps, and 64 sampled states' outputs for all 1024 steps
@@ -52,26 +53,39 @@ def test_forward_b2_h16_n32768_d128():
     import torch
     B, H, N, d = 2, 16, 32768, 128
     q, k, v = synth.qkv(B, H, N, d, d, seed=3, dtype="bf16")
-    out, S, z = la.forward(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
-                           return_state=True)
+    qd, kd, vd = to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16")
+    # as the bench runs it (no final state): 152 balanced pieces of 54 chunks
+    plan = la.forward_plan(B, H, N, d, d)
+    assert (plan["pieces"], plan["piece_len"]) == (152, 54), plan
+    out_p = la.forward(qd, kd, vd).float().cpu().numpy()
+    # with the final state: by segments
+    out, S, z = la.forward(qd, kd, vd, return_state=True)
     torch.cuda.synchronize()
     out = out.float().cpu().numpy()
     vmax = np.abs(v).max()
-    # two whole heads, every output and the final state, element by element
-    for b, h in ((0, 0), (1, H - 1)):
+    # three whole heads, every output of both calls and the final state,
+    # element by element (head (0, 7) holds piece boundaries at chunks 10,
+    # 64, 118, 172 and 226 of its 256)
+    for b, h in ((0, 0), (0, 7), (1, H - 1)):
         sl = (slice(b, b + 1), slice(h, h + 1))
         want, S_w, z_w = orc.forward_recurrent(q[sl], k[sl], v[sl], eps=1e-6, return_state=True)
+        assert rel_err(out_p[sl], want, vmax) <= TOL["bf16"], (b, h)
         assert rel_err(out[sl], want, vmax) <= TOL["bf16"], (b, h)
         assert rel_err(to_host(S[b, h]), S_w[0, 0], np.abs(S_w).max()) <= STATE_TOL["bf16"]
         assert rel_err(to_host(z[b, h]), z_w[0, 0], np.abs(z_w).max()) <= Z_TOL["bf16"]
     rng = np.random.default_rng(0)
     worst = 0.0
     picks = [(b, h, t) for b in range(B) for h in (0, H - 1) for t in (0, 127, 128, N - 1)]
+    # the first and last token of every piece
+    for i in range(plan["pieces"]):
+        for g in (i * 54, min(B * H * 256, i * 54 + 54) - 1):
+            bh, c = divmod(g, 256)
+            picks += [(bh // H, bh % H, 128 * c), (bh // H, bh % H, 128 * c + 127)]
     picks += [(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N)))
               for _ in range(48)]
     for b, h, t in picks:
         want = orc.output_at(q[b, h], k[b, h], v[b, h], t, eps=1e-6)
-        worst = max(worst, rel_err(out[b, h, t], want, vmax))
+        worst = max(worst, rel_err(out[b, h, t], want, vmax), rel_err(out_p[b, h, t], want, vmax))
     assert worst <= TOL["bf16"], worst
     for b, h in ((0, 0), (1, H - 1)):
         fk = orc.phi_elu1(k[b, h])

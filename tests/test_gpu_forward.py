@@ -222,3 +222,37 @@ def test_state_pass_split_over_ctas():
         assert rel_err(out[b:b + 1, h:h + 1], want, np.abs(v).max()) <= TOL["bf16"]
         assert rel_err(S[b, h], S_w[0, 0], np.abs(S_w).max()) <= STATE_TOL["bf16"]
         assert rel_err(z[b, h], z_w[0, 0], np.abs(z_w).max()) <= Z_TOL["bf16"]
+
+
+# Balanced pieces (causal, d = 128, bf16, no final state): the heads' chunks
+# laid end to end and cut into equal pieces, one CTA each. Shapes: pieces of
+# two chunks over heads of 5 and 7 chunks with ragged last chunks (most
+# pieces end one head and start the next), heads of 33 chunks, and the
+# bench's B=2 H=16 N=8192 split (14-chunk pieces, piece 32 starting exactly
+# at head 7, a short last piece).
+@pytest.mark.parametrize("B,H,N,heads", [
+    (3, 17, 544, None),
+    (1, 39, 803, None),
+    (1, 9, 4224, None),
+    (2, 16, 8192, [0, 6, 7, 8, 15, 16, 31]),
+])
+def test_forward_balanced_pieces(B, H, N, heads):
+    import torch
+    d = 128
+    plan = la.forward_plan(B, H, N, d, d)
+    assert plan["pieces"] > 0, plan
+    assert la.forward_plan(B, H, N, d, d, final_state=True)["pieces"] == 0
+    q, k, v = synth.qkv(B, H, N, d, d, seed=840 + N, dtype="bf16")
+    n0 = la.la_launch_count()
+    got = to_host(_run(q, k, v, True, "bf16"))
+    assert la.la_launch_count() - n0 == 2
+    assert la.la_device_status(True) == la.LA_OK
+    flat = lambda x: x.reshape(B * H, N, -1)
+    sel = list(range(B * H)) if heads is None else heads
+    want = orc.forward_recurrent(flat(q)[None, sel], flat(k)[None, sel], flat(v)[None, sel], eps=1e-6)
+    err = rel_err(flat(got)[sel], want[0], np.abs(v).max())
+    assert err <= TOL["bf16"], err
+    # with a final state the same call runs by segments: same outputs
+    got2, S, z = _run(q, k, v, True, "bf16", state=True)
+    err2 = rel_err(flat(to_host(got2))[sel], want[0], np.abs(v).max())
+    assert err2 <= TOL["bf16"], err2
