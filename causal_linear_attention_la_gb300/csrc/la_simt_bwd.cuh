@@ -42,6 +42,21 @@ constexpr int TT = 32;
 template <typename T>
 __device__ __forceinline__ float ld(const T* p) { return to_f32<T>(*p); }
 
+// init + sum_{i < n} x[i sx] y[i sy] with four independent partial sums, so
+// that a thread's FMAs do not wait on each other
+__device__ __forceinline__ float dot4(const float* x, int sx, const float* y, int sy, int n, float init = 0.f) {
+  float a0 = init, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int i = 0;
+  for (; i + 4 <= n; i += 4) {
+    a0 = fmaf(x[i * sx], y[i * sy], a0);
+    a1 = fmaf(x[(i + 1) * sx], y[(i + 1) * sy], a1);
+    a2 = fmaf(x[(i + 2) * sx], y[(i + 2) * sy], a2);
+    a3 = fmaf(x[(i + 3) * sx], y[(i + 3) * sy], a3);
+  }
+  for (; i < n; ++i) a0 = fmaf(x[i * sx], y[i * sy], a0);
+  return (a0 + a1) + (a2 + a3);
+}
+
 template <int DK, int DV>
 constexpr size_t sweep1_smem_floats() {
   // S, z, fq, fk, vv, gg, aa, oo(stage), W, dW, den, bsc
@@ -99,7 +114,9 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
   for (int e = 0; e < E; ++e) racc[e] = 0.f;
   float rz = 0.f;
   const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
-  auto dec = [&](int e) { return exp2f((float)e * log2a); };   // alpha^e (1 without decay)
+  const bool decay = alpha != nullptr;
+  // alpha^e (1 without decay: no exponential in the inner loops)
+  auto dec = [&](int e) { return decay ? exp2f((float)e * log2a) : 1.f; };
   __syncthreads();
 
   for (int s = t0; s < t1; s += TT) {
@@ -121,19 +138,14 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       for (int idx = tid; idx < TT * TT; idx += NT) {
         const int t = idx / TT, j = idx % TT;
         float a = 0.f;
-        if (j <= t && t < n) {
-          for (int c = 0; c < DK; ++c) a = fmaf(fq[t * LDK + c], fk[j * LDK + c], a);
-          a *= dec(t - j);
-        }
+        if (j <= t && t < n) a = dot4(fq + t * LDK, 1, fk + j * LDK, 1, DK) * dec(t - j);
         W[t * (TT + 1) + j] = a;
       }
       __syncthreads();
     }
     if (tid < TT) {
       const int t = tid;
-      float d = 0.f;
-      for (int c = 0; c < DK; ++c) d = fmaf(fq[t * LDK + c], z[c], d);
-      d *= dec(t + 1);
+      float d = dot4(fq + t * LDK, 1, z, 1, DK) * dec(t + 1);
       if (causal)
         for (int j = 0; j <= t; ++j) d += W[t * (TT + 1) + j];
       den[t] = t < n ? d + eps : 1.f;  // padding rows stay finite when eps = 0
@@ -141,11 +153,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
     float num[TR];
     for (int r = 0; r < TR; ++r) {
       const int t = tid / DV + r * RG;
-      float a = 0.f;
-      for (int c = 0; c < DK; ++c) a = fmaf(fq[t * LDK + c], S[c * DV + m], a);
-      a *= dec(t + 1);
-      if (causal)
-        for (int j = 0; j <= t; ++j) a = fmaf(W[t * (TT + 1) + j], vv[j * LDV + m], a);
+      float a = dot4(fq + t * LDK, 1, S + m, DV, DK) * dec(t + 1);
+      if (causal) a = dot4(W + t * (TT + 1), 1, vv + m, LDV, t + 1, a);
       num[r] = a;
     }
     __syncthreads();
@@ -158,8 +167,7 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
     __syncthreads();
     if (tid < TT) {
       const int t = tid;
-      float beta = 0.f;
-      for (int mm = 0; mm < DV; ++mm) beta = fmaf(gg[t * LDV + mm], stg[t * LST + mm], beta);
+      const float beta = dot4(gg + t * LDV, 1, stg + t * LST, 1, DV);
       const float b = -beta / den[t];
       bsc[t] = t < n ? b : 0.f;
       if (t < n) {
@@ -172,10 +180,7 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       for (int idx = tid; idx < TT * TT; idx += NT) {
         const int t = idx / TT, j = idx % TT;
         float a = 0.f;
-        if (j <= t && t < n) {
-          for (int mm = 0; mm < DV; ++mm) a = fmaf(aa[t * LDV + mm], vv[j * LDV + mm], a);
-          a = (a + bsc[t]) * dec(t - j);
-        }
+        if (j <= t && t < n) a = (dot4(aa + t * LDV, 1, vv + j * LDV, 1, DV) + bsc[t]) * dec(t - j);
         dW[t * (TT + 1) + j] = a;
       }
       __syncthreads();
@@ -185,11 +190,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       const int t = tid % TT;
       for (int e = 0; e < EC; ++e) {
         const int c = tid / TT + e * CG;
-        float a = bsc[t] * z[c];
-        for (int mm = 0; mm < DV; ++mm) a = fmaf(aa[t * LDV + mm], S[c * DV + mm], a);
-        a *= dec(t + 1);
-        if (causal)
-          for (int j = 0; j <= t; ++j) a = fmaf(dW[t * (TT + 1) + j], fk[j * LDK + c], a);
+        float a = dot4(aa + t * LDV, 1, S + c * DV, 1, DV, bsc[t] * z[c]) * dec(t + 1);
+        if (causal) a = dot4(dW + t * (TT + 1), 1, fk + c, LDK, t + 1, a);
         stg[t * LST + c] = a * phi_prime_from_phi(fq[t * LDK + c]);
       }
     }
@@ -204,18 +206,28 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
     for (int e = 0; e < E; ++e) {
       const int c = c0 + e * RG;
       float a = racc[e];
-      for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(s + t - t0), aa[t * LDV + m], a);
+      if (decay)
+        for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(s + t - t0), aa[t * LDV + m], a);
+      else
+        a = dot4(fq + c, LDK, aa + m, LDV, n, a);
       racc[e] = a;
     }
-    if (tid < DK)
-      for (int t = 0; t < n; ++t) rz = fmaf(bsc[t] * dec(s + t - t0), fq[t * LDK + tid], rz);
+    if (tid < DK) {
+      if (decay)
+        for (int t = 0; t < n; ++t) rz = fmaf(bsc[t] * dec(s + t - t0), fq[t * LDK + tid], rz);
+      else
+        rz = dot4(bsc, 1, fq + tid, LDK, n, rz);
+    }
     if (causal) {
       // the state after the tile: alpha^n S + sum_j alpha^(n-1-j) phi(k_j) v_j^T
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int c = c0 + e * RG;
         float a = S[c * DV + m] * dec(n);
-        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + c] * dec(n - 1 - t), vv[t * LDV + m], a);
+        if (decay)
+          for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + c] * dec(n - 1 - t), vv[t * LDV + m], a);
+        else
+          a = dot4(fk + c, LDK, vv + m, LDV, n, a);
         S[c * DV + m] = a;
       }
       if (tid < DK) {
@@ -283,7 +295,9 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
   for (int i = tid; i < DK * DV + DK; i += NT) R[i] = st[i];
   const int m = tid % DV, c0 = tid / DV;
   const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
-  auto dec = [&](int e) { return exp2f((float)e * log2a); };   // alpha^e (1 without decay)
+  const bool decay = alpha != nullptr;
+  // alpha^e (1 without decay: no exponential in the inner loops)
+  auto dec = [&](int e) { return decay ? exp2f((float)e * log2a) : 1.f; };
   __syncthreads();
 
   const int ntiles = (t1 - t0 + TT - 1) / TT;
@@ -313,8 +327,8 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
         const int t = idx / TT, j = idx % TT;
         float w = 0.f, dw = 0.f;
         if (j <= t && t < n) {
-          for (int c = 0; c < DK; ++c) w = fmaf(fq[t * LDK + c], fk[j * LDK + c], w);
-          for (int mm = 0; mm < DV; ++mm) dw = fmaf(aa[t * LDV + mm], vv[j * LDV + mm], dw);
+          w = dot4(fq + t * LDK, 1, fk + j * LDK, 1, DK);
+          dw = dot4(aa + t * LDV, 1, vv + j * LDV, 1, DV);
           const float f = dec(t - j);
           w *= f;
           dw = (dw + bsc[t]) * f;
@@ -328,20 +342,15 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
       const int j = tid % TT;
       for (int e = 0; e < EC; ++e) {
         const int c = tid / TT + e * CG;
-        float a = r[c];
-        for (int mm = 0; mm < DV; ++mm) a = fmaf(R[c * DV + mm], vv[j * LDV + mm], a);
+        float a = dot4(R + c * DV, 1, vv + j * LDV, 1, DV, r[c]);
         a *= dec(n - j);    // the suffix after the tile, seen from key j
-        if (causal)
-          for (int t = j; t < TT; ++t) a = fmaf(dW[t * (TT + 1) + j], fq[t * LDK + c], a);
+        if (causal) a = dot4(dW + j * (TT + 1) + j, TT + 1, fq + j * LDK + c, LDK, TT - j, a);
         sdk[j * LDK + c] = a * phi_prime_from_phi(fk[j * LDK + c]);
       }
       for (int e = 0; e < EM; ++e) {
         const int mm = tid / TT + e * CG;
-        float a = 0.f;
-        for (int c = 0; c < DK; ++c) a = fmaf(R[c * DV + mm], fk[j * LDK + c], a);
-        a *= dec(n - j);
-        if (causal)
-          for (int t = j; t < TT; ++t) a = fmaf(W[t * (TT + 1) + j], aa[t * LDV + mm], a);
+        float a = dot4(R + mm, DV, fk + j * LDK, 1, DK) * dec(n - j);
+        if (causal) a = dot4(W + j * (TT + 1) + j, TT + 1, aa + j * LDV + mm, LDV, TT - j, a);
         sdv[j * LDV + mm] = a;
       }
     }
@@ -360,12 +369,18 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
       for (int e = 0; e < E; ++e) {
         const int c = c0 + e * RG;
         float a = R[c * DV + m] * dec(n);
-        for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(t), aa[t * LDV + m], a);
+        if (decay)
+          for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(t), aa[t * LDV + m], a);
+        else
+          a = dot4(fq + c, LDK, aa + m, LDV, n, a);
         R[c * DV + m] = a;
       }
       if (tid < DK) {
         float a = r[tid] * dec(n);
-        for (int t = 0; t < n; ++t) a = fmaf(bsc[t] * dec(t), fq[t * LDK + tid], a);
+        if (decay)
+          for (int t = 0; t < n; ++t) a = fmaf(bsc[t] * dec(t), fq[t * LDK + tid], a);
+        else
+          a = dot4(bsc, 1, fq + tid, LDK, n, a);
         r[tid] = a;
       }
     }
