@@ -200,7 +200,7 @@ KERNEL_SOURCES = {
     "fwd_output": ["la_tc_fwd.cu"] + _COMMON_TC,
     "bwd": ["la_tc_bwd.cu"] + _COMMON_TC,
     "decode": ["la_decode.cu", "la_internal.cuh"],
-    "decodetc": ["la_decode_tc.cu"] + _COMMON_TC,
+    "decodetc": ["la_decode_tc.cu", "la_variants.cuh"] + _COMMON_TC,
     "variants": ["la_variants.cu", "la_variants.cuh", "la_internal.cuh"],
 }
 
@@ -725,8 +725,9 @@ def main():
             t = max_over_ranks(rr["ms"]) / 1e3
             per = t / rr["steps"]
             nt = ws.get("tokens", 1)
-            tc_decode = not ws.get("variant") and la.la_decode_path(ws["dk"], ws["dv"], la.LA_BF16, nt) == 1
-            traffic_key = ("variants_" if ws.get("variant") else "decodetc_" if tc_decode else "decode_") + name
+            # the plain and the decay-gated multi-token decode take the tensor cores
+            tc_decode = ws.get("variant") in (None, "decay") and la.la_decode_path(ws["dk"], ws["dv"], la.LA_BF16, nt) == 1
+            traffic_key = ("decodetc_" if tc_decode else "variants_" if ws.get("variant") else "decode_") + name
             # bytes of one call: the state once, q, k, v, out once per token
             call_bytes = decode_state_bytes(ws) + nt * decode_io_bytes(ws)
             gbs = decode_state_bytes(ws) / per / 1e9
@@ -736,8 +737,9 @@ def main():
                 "tokens_per_s": job_throughput(world, ws["B"] * nt, per),
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"],
-                             "kernel": {"decay": "decay_tokens", "delta": "delta_tokens"}.get(
-                                 ws.get("variant"), "decode_tc" if tc_decode else "decode"),
+                             "kernel": "decode_tc" if tc_decode else {"decay": "decay_tokens",
+                                                                      "delta": "delta_tokens"}.get(
+                                 ws.get("variant"), "decode"),
                              "traffic": ncu_traffic(traffic_key)},
                 "bytes_per_step": call_bytes,
                 "prefill_s_eager": rr["prefill_s"], "gpu_launches": rr["launches"],

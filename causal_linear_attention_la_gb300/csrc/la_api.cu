@@ -674,6 +674,19 @@ la_status la_decode_steps_decay(float* S, float* z, const void* q, const void* k
   if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
       !aligned16(v) || !aligned16(out))
     return fail(LA_ERR_INVALID_ARG, "S, z, q, k, v, out must be 16-byte aligned");
+  if (g_path.load() == LA_PATH_AUTO && tc_decode_supported(dk, dv, dtype, T)) {
+    // the tensor-core multi-token decode with the decay weights
+    if (device_status_ptr() == nullptr)
+      return fail(LA_ERR_CUDA, "la_decode_steps_decay: device status word unavailable");
+    DecodeArgs d{};
+    d.S = S; d.z = z; d.q = q; d.k = k; d.v = v; d.out = out;
+    d.BH = B * H; d.dk = dk; d.dv = dv; d.eps = eps; d.dtype = dtype;
+    d.stream = (cudaStream_t)stream;
+    d.ntok = T;
+    cudaError_t e = la::tc_decode_steps_decay(d, alpha, H);
+    if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps_decay");
+    return LA_OK;
+  }
   VariantArgs a{};
   a.S = S; a.z = z; a.q = q; a.k = k; a.v = v; a.out = out; a.alpha = alpha;
   a.H = H; a.BH = B * H; a.ntok = T; a.dk = dk; a.dv = dv; a.eps = eps; a.dtype = dtype;

@@ -25,6 +25,19 @@
 // rounds the state and phi(q) to bf16, as the chunked forward does. z is
 // updated in fp32 from 1 + psi_hi + psi_lo.
 //
+// Decay gating ("Linear Attention, 곱의 순서를 바꾸면 생기는 일", paragraph on
+// 감쇠 게이팅; per-head factor a): S_t = a S_{t-1} + phi(k_t) v_t^T and z
+// likewise, so over a group
+//   num_t = a^(t+1) S_0^T phi(q_t) + sum_{j <= t} a^(t-j) (phi(q_t) . phi(k_j)) v_j
+//   den_t = a^(t+1) phi(q_t) . z_0 + sum_{j <= t} a^(t-j) phi(q_t) . phi(k_j) + eps
+//   S    <- a^n S_0 + sum_j a^(n-1-j) phi(k_j) v_j^T
+// The read takes a second phi(Q) tile with row t weighted a^(t+1); the P
+// round keeps the unweighted one and the CUDA cores weight P_tj by a^(t-j)
+// (and phi(q_t) . z_0 by a^(t+1)); the update's B tiles carry w_j =
+// a^(n-1-j) as bf16 hi + lo rows (for the 1 of phi(k)) and w_j psi(k_j) as
+// hi + lo, so the state keeps the accuracy of the undecayed update; the held
+// state is multiplied by a^n in the pass that makes its bf16 copy.
+//
 // A persistent CTA per SM (a kernel that allocates tensor memory runs one
 // CTA per SM) with two teams of 128 threads, each working through its own
 // states with its own shared memory, half of tensor memory and its own
@@ -40,6 +53,7 @@
 #include <algorithm>
 
 #include "la_tc_common.cuh"
+#include "la_variants.cuh"
 
 namespace la {
 
@@ -55,7 +69,8 @@ constexpr int TTILE = 2 * TBOX;         // a [16][128] bf16 tile (two boxes)
 constexpr int KROWS = 32;                // rows of the psi tiles (16 keys, then z_hi, z_lo, ones)
 constexpr int KBOX = KROWS * 128;       // bytes of one [32 rows][64 bf16] SW128 box
 
-struct DecTc {
+template <bool kDecay>
+struct DecTcT {
   static constexpr int OFF_SST = 0;                         // fp32 [128][128] state (bulk load)
   static constexpr int OFF_Q = OFF_SST + DT * DT * 4;       // phi(Q) bf16, K-major [t][i] (16 rows)
   static constexpr int OFF_KH = OFF_Q + TTILE;              // [psi_hi ; z_hi ; z_lo ; 1 ; 0] [32][128]
@@ -63,7 +78,12 @@ struct DecTc {
   static constexpr int OFF_V = OFF_KL + 2 * KBOX;           // V bf16 [t][c] (16 rows)
   static constexpr int OFF_ONES = OFF_V + TTILE;            // ones [16][128]
   static constexpr int OFF_P = OFF_ONES + TTILE;            // P bf16, K-major [t][j] (j < 16 used)
-  static constexpr int OFF_Z = OFF_P + TBOX;                // fp32 z [128]
+  // decay: phi(Q) rows weighted a^(t+1) (the read), and the update's B tiles
+  // [w_lo], [w psi]_hi, [w psi]_lo, each [16][128] ([w_hi] takes the place
+  // of the ones tile, which the decayed update does not use)
+  static constexpr int OFF_QS = OFF_P + TBOX;
+  static constexpr int OFF_UW = OFF_QS + (kDecay ? TTILE : 0);
+  static constexpr int OFF_Z = OFF_UW + (kDecay ? 3 * TTILE : 0);   // fp32 z [128]
   static constexpr int OFF_DEN = OFF_Z + DT * 4;            // fp32 1 / den [16]
   static constexpr int OFF_BAR = OFF_DEN + TG * 4;          // 3 mbarriers
   // one team's region, 1024-aligned; the CTA holds two, then the tensor-
@@ -71,7 +91,7 @@ struct DecTc {
   static constexpr int TEAM_BYTES = (OFF_BAR + 24 + 1023) / 1024 * 1024;
   static constexpr int BYTES = 2 * TEAM_BYTES + 16;
   static_assert(OFF_Q % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_KL % 1024 == 0 && OFF_V % 1024 == 0 &&
-                    OFF_ONES % 1024 == 0 && OFF_P % 1024 == 0,
+                    OFF_ONES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_QS % 1024 == 0 && OFF_UW % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   // the P round reads 128 rows of phi(Q) (rows 16.. are whatever follows in
   // shared memory; their results are never read): inside the team's region
@@ -85,6 +105,7 @@ struct DecTc {
   static constexpr uint32_t TMEM_COLS = 256;                // per team
   static_assert(BYTES <= 232448, "shared memory budget");
 };
+using DecTc = DecTcT<false>;   // tensor-memory columns (the same for both)
 
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -141,7 +162,10 @@ __device__ __forceinline__ void load_group_rows(const __nv_bfloat16* qb, const _
 
 // The bf16 copy of this thread's lane of S^T (fp32 columns COL_S..+127) into
 // columns COL_SB..+63, two values per column (lower key index in the low half).
-__device__ __forceinline__ void refresh_bf16_copy(uint32_t lane_addr) {
+// kScale: the fp32 lane is then multiplied by `scale` in place (decay: the
+// held state becomes a^n S before the next group's update adds to it).
+template <bool kScale>
+__device__ __forceinline__ void refresh_bf16_copy(uint32_t lane_addr, float scale = 1.f) {
 #pragma unroll 1
   for (int i0 = 0; i0 < DT; i0 += 32) {
     uint32_t v[32];
@@ -151,6 +175,11 @@ __device__ __forceinline__ void refresh_bf16_copy(uint32_t lane_addr) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
     tmem_st16(lane_addr + DecTc::COL_SB + i0 / 2, pk);
+    if constexpr (kScale) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * scale);
+      tmem_st32(lane_addr + DecTc::COL_S + i0, v);
+    }
   }
   tmem_st_wait();
 }
@@ -163,11 +192,13 @@ __device__ __forceinline__ void team_sync(int team) {
 
 // Two independent teams of 128 threads per CTA, each taking states
 // bh = 2 * cta + team, + 2 * gridDim.x, ...
+template <bool kDecay>
 __global__ void __launch_bounds__(256, 1)
 decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat16* __restrict__ q,
                  const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                 __nv_bfloat16* __restrict__ out, int BH, int ntok, float eps, int* status) {
-  using L = DecTc;
+                 __nv_bfloat16* __restrict__ out, int BH, int ntok, float eps, int* status,
+                 const float* __restrict__ alpha, int H) {
+  using L = DecTcT<kDecay>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 2 * L::TEAM_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 2 * L::TEAM_BYTES + 4);
@@ -226,6 +257,7 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
   const uint32_t qa = smem_u32(sm + L::OFF_Q), kha = smem_u32(sm + L::OFF_KH), kla = smem_u32(sm + L::OFF_KL);
   const uint32_t va = smem_u32(sm + L::OFF_V);
   const uint32_t onea = smem_u32(sm + L::OFF_ONES), pa = smem_u32(sm + L::OFF_P);
+  const uint32_t qsa = smem_u32(sm + L::OFF_QS), uwa = smem_u32(sm + L::OFF_UW);
   const int ngroups = (ntok + TG - 1) / TG;
   uint32_t ph_s = 0, ph_p = 0, ph_mma = 0;   // phases waited for on each barrier
   uint32_t loads = 0;                        // state loads issued (thread 0 of the team)
@@ -254,6 +286,7 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
     __nv_bfloat16* ob = out + bh * (long long)ntok * DT;
     float zr = z[bh * DT + tid];          // z of key index tid
     zs[tid] = zr;
+    const float la = kDecay ? log2f(alpha[(int)(bh % H)]) : 0.f;   // log2 a
     team_sync(team);
     for (int g = 0; g < ngroups; ++g) {
       const int t0 = g * TG;
@@ -266,14 +299,21 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
       {
         const int t = tid >> 3, ch = tid & 7;
         const bool valid = t < n;
+        // decay: the read's weight a^(t+1) of query row t and the update's
+        // weight w_t = a^(n-1-t) of key row t (0 past the last token)
+        const float qsc = kDecay ? exp2f((float)(t + 1) * la) : 1.f;
+        const float wt = kDecay && valid ? exp2f((float)(n - 1 - t) * la) : 0.f;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const uint32_t* pq = reinterpret_cast<const uint32_t*>(&rows[b]);
           const uint32_t* pk = reinterpret_cast<const uint32_t*>(&rows[2 + b]);
-          uint4 oq, ok4, ol4;
+          uint4 oq, ok4, ol4, oqs, owh, owl;
           uint32_t* poq = reinterpret_cast<uint32_t*>(&oq);
           uint32_t* pok = reinterpret_cast<uint32_t*>(&ok4);
           uint32_t* pol = reinterpret_cast<uint32_t*>(&ol4);
+          uint32_t* pqs = reinterpret_cast<uint32_t*>(&oqs);
+          uint32_t* pwh = reinterpret_cast<uint32_t*>(&owh);
+          uint32_t* pwl = reinterpret_cast<uint32_t*>(&owl);
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             float ph0, ps0, ph1, ps1;
@@ -285,8 +325,25 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
             poq[h] = pack_bf16x2(fq0, fq1);
             pok[h] = pack_bf16x2(ps0, ps1);
             pol[h] = pack_bf16x2(ps0 - __uint_as_float(pok[h] << 16), ps1 - __uint_as_float(pok[h] & 0xFFFF0000u));
+            if constexpr (kDecay) {
+              pqs[h] = pack_bf16x2(fq0 * qsc, fq1 * qsc);
+              const float x0 = wt * ps0, x1 = wt * ps1;
+              pwh[h] = pack_bf16x2(x0, x1);
+              pwl[h] = pack_bf16x2(x0 - __uint_as_float(pwh[h] << 16), x1 - __uint_as_float(pwh[h] & 0xFFFF0000u));
+            }
           }
           *reinterpret_cast<uint4*>(sm + L::OFF_Q + b * TBOX + sw128(t, ch)) = oq;
+          if constexpr (kDecay) {
+            // [w_hi], [w_lo] (constant along the row), [w psi]_hi, [w psi]_lo
+            const uint32_t whi = pack_bf16x2(wt, wt);
+            const float wlo = wt - __uint_as_float(whi << 16);
+            const uint32_t wlo2 = pack_bf16x2(wlo, wlo);
+            *reinterpret_cast<uint4*>(sm + L::OFF_QS + b * TBOX + sw128(t, ch)) = oqs;
+            *reinterpret_cast<uint4*>(sm + L::OFF_ONES + b * TBOX + sw128(t, ch)) = make_uint4(whi, whi, whi, whi);
+            *reinterpret_cast<uint4*>(sm + L::OFF_UW + b * TBOX + sw128(t, ch)) = make_uint4(wlo2, wlo2, wlo2, wlo2);
+            *reinterpret_cast<uint4*>(sm + L::OFF_UW + TTILE + b * TBOX + sw128(t, ch)) = owh;
+            *reinterpret_cast<uint4*>(sm + L::OFF_UW + 2 * TTILE + b * TBOX + sw128(t, ch)) = owl;
+          }
           *reinterpret_cast<uint4*>(sm + L::OFF_KH + b * KBOX + sw128(t, ch)) = ok4;
           *reinterpret_cast<uint4*>(sm + L::OFF_KL + b * KBOX + sw128(t, ch)) = ol4;
           *reinterpret_cast<uint4*>(sm + L::OFF_V + b * TBOX + sw128(t, ch)) = rows[4 + b];
@@ -315,16 +372,22 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
         ok = mbar_wait(bar_s, ph_s & 1, abort_flag, kTimeoutNs);
         ++ph_s;
         if (!ok) break;
+        // (decay: the fp32 state a^n S_0, the copy S_0)
+        const float sc0 = kDecay ? exp2f((float)n * la) : 1.f;
 #pragma unroll 1
         for (int i0 = 0; i0 < DT; i0 += 32) {
           uint32_t w[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(sst[(i0 + j) * DT + tid]);
-          tmem_st32(lane_addr + L::COL_S + i0, w);
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1]));
           tmem_st16(lane_addr + L::COL_SB + i0 / 2, pk);
+          if constexpr (kDecay) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(w[j]) * sc0);
+          }
+          tmem_st32(lane_addr + L::COL_S + i0, w);
         }
         tmem_st_wait();
       }
@@ -354,10 +417,12 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
         tc_commit(bar_p);
         // read: D[c][t] = sum_i S^T[c][i] phi(q_t)[i]; A = the bf16 copy in
         // tensor memory (8 columns per K-step of 16), B = phi(Q) K-major
+        // (decay: the rows weighted a^(t+1))
+        const uint32_t qra = kDecay ? qsa : qa;
 #pragma unroll
         for (int kk = 0; kk < DT / 16; ++kk)
           mma_ts(tmem + L::COL_O, tmem + L::COL_SB + kk * 8,
-                 make_sdesc(qa + (kk >> 2) * TBOX + (kk & 3) * 32, 16, 1024, kSwizzle128B), id_read, kk > 0);
+                 make_sdesc(qra + (kk >> 2) * TBOX + (kk & 3) * 32, 16, 1024, kSwizzle128B), id_read, kk > 0);
       }
       ok = mbar_wait(bar_p, ph_p & 1, abort_flag, kTimeoutNs);
       ++ph_p;
@@ -376,6 +441,7 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             pr[j] = (j <= t && t < n) ? __uint_as_float(d[j]) + st : 0.f;
+            if (kDecay) pr[j] *= exp2f((float)(t - j) * la);    // a^(t-j)
             sum += pr[j];
           }
 #pragma unroll
@@ -387,7 +453,8 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
             w.w = pack_bf16x2(pr[8 * c2 + 6], pr[8 * c2 + 7]);
             *reinterpret_cast<uint4*>(sm + L::OFF_P + sw128(t, c2)) = w;
           }
-          rden[t] = 1.f / (__uint_as_float(d[16]) + __uint_as_float(d[17]) + sum + eps);
+          const float zq = __uint_as_float(d[16]) + __uint_as_float(d[17]);   // phi(q_t) . z_0
+          rden[t] = 1.f / ((kDecay ? exp2f((float)(t + 1) * la) * zq : zq) + sum + eps);
         }
       }
       fence_proxy_async_smem();
@@ -402,12 +469,20 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
                id_intra, 1);
         // update: S^T += V^T 1 + V^T psi_hi + V^T psi_lo (the psi tiles read
         // as MN-major with K = 16: rows 0..15)
-        mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B), make_sdesc(kha, KBOX, 1024, kSwizzle128B),
-               id_upd, 1);
-        mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B), make_sdesc(kla, KBOX, 1024, kSwizzle128B),
-               id_upd, 1);
-        mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B), make_sdesc(onea, TBOX, 1024, kSwizzle128B),
-               id_upd, 1);
+        if constexpr (kDecay) {
+          // S^T += V^T (w_hi + w_lo + [w psi]_hi + [w psi]_lo), on a^n S_0
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B),
+                   make_sdesc(u == 0 ? onea : uwa + (u - 1) * TTILE, TBOX, 1024, kSwizzle128B), id_upd, 1);
+        } else {
+          mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B), make_sdesc(kha, KBOX, 1024, kSwizzle128B),
+                 id_upd, 1);
+          mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B), make_sdesc(kla, KBOX, 1024, kSwizzle128B),
+                 id_upd, 1);
+          mma_ss(tmem + L::COL_S, make_sdesc(va, TBOX, 1024, kSwizzle128B),
+                 make_sdesc(onea, TBOX, 1024, kSwizzle128B), id_upd, 1);
+        }
         tc_commit(bar_mma);
       }
       ok = mbar_wait(bar_mma, ph_mma & 1, abort_flag, kTimeoutNs);
@@ -428,17 +503,26 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
         const uint8_t* hb = sm + L::OFF_KH + (tid >> 6) * KBOX;
         const uint8_t* lb = sm + L::OFF_KL + (tid >> 6) * KBOX;
         const int ch = (tid & 63) >> 3, pos = tid & 7;
-        float acc = (float)n;
+        float acc = kDecay ? 0.f : (float)n;
 #pragma unroll
         for (int t = 0; t < TG; ++t) {
           const uint32_t off = sw128(t, ch) + 2 * pos;
-          acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hb + off)) +
-                 __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(lb + off));
+          const float ps = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hb + off)) +
+                           __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(lb + off));
+          if (kDecay)
+            acc += t < n ? exp2f((float)(n - 1 - t) * la) * (1.f + ps) : 0.f;   // w_t phi(k_t)
+          else
+            acc += ps;
         }
-        zr += acc;
+        zr = kDecay ? exp2f((float)n * la) * zr + acc : zr + acc;
       }
       // the next group reads the updated state through its bf16 copy
-      if (g + 1 < ngroups) refresh_bf16_copy(lane_addr);
+      if (g + 1 < ngroups) {
+        if constexpr (kDecay)
+          refresh_bf16_copy<true>(lane_addr, exp2f((float)min(TG, ntok - t0 - TG) * la));   // a^(next n)
+        else
+          refresh_bf16_copy<false>(lane_addr);
+      }
       tc_fence_before();
       team_sync(team);    // tiles, rden and zs are rewritten next
       zs[tid] = zr;
@@ -487,9 +571,10 @@ bool tc_decode_supported(int dk, int dv, la_dtype dtype, int ntok) {
   return dtype == LA_BF16 && dk == DT && dv == DT && ntok >= 2;
 }
 
-cudaError_t tc_decode_steps(const DecodeArgs& a) {
-  constexpr int smem = DecTc::BYTES;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <bool kDecay>
+cudaError_t launch_decode_tc(const DecodeArgs& a, const float* alpha = nullptr, int H = 1) {
+  constexpr int smem = DecTcT<kDecay>::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kDecay>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
@@ -497,12 +582,18 @@ cudaError_t tc_decode_steps(const DecodeArgs& a) {
   if (e != cudaSuccess) return e;
   // two states at a time per CTA (one per team), one CTA per SM
   const int ctas = (int)std::min<long long>((a.BH + 1) / 2, (long long)sms);
-  decode_tc_kernel<<<ctas, 256, smem, a.stream>>>(a.S, a.z, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k,
-                                                  (const __nv_bfloat16*)a.v, (__nv_bfloat16*)a.out, a.BH, a.ntok,
-                                                  a.eps, device_status_ptr());
+  decode_tc_kernel<kDecay><<<ctas, 256, smem, a.stream>>>(
+      a.S, a.z, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+      (__nv_bfloat16*)a.out, a.BH, a.ntok, a.eps, device_status_ptr(), alpha, H);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
+}
+
+cudaError_t tc_decode_steps(const DecodeArgs& a) { return launch_decode_tc<false>(a); }
+
+cudaError_t tc_decode_steps_decay(const DecodeArgs& a, const float* alpha, int H) {
+  return launch_decode_tc<true>(a, alpha, H);
 }
 
 }  // namespace la

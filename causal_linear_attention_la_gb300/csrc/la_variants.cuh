@@ -26,6 +26,10 @@ cudaError_t forward_delta_chunked(const VariantArgs& a);
 // for la_forward (its segment plan and workspace).
 struct FwdArgs;
 cudaError_t tc_forward_decay(const FwdArgs& a, const float* alpha, int H);
+// The tensor-core multi-token decode with decay gating (la_decode_tc.cu;
+// where tc_decode_supported holds): per-head factors alpha [H] (device).
+struct DecodeArgs;
+cudaError_t tc_decode_steps_decay(const DecodeArgs& a, const float* alpha, int H);
 // dst <- src for n floats (16-byte aligned pointers)
 cudaError_t copy_floats(float* dst, const float* src, long long n, cudaStream_t stream);
 

@@ -51,8 +51,51 @@ def test_decay_tokens(B, H, T, dk, dv, dtype):
     S_w, z_w, o_w = orc.decode_steps_decay(S_ref, z_ref, q, k, v,
                                            alpha=alpha_h.astype(np.float64)[None, :])
     assert rel_err(to_host(out), o_w, np.abs(v).max()) <= TOL[dtype]
-    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-6
+    # the tensor-core decode carries psi(k) and the decay weights as bf16
+    # hi + lo pairs (about 16 bits): 1e-5 of max|S|, as the undecayed one
+    tc = la.la_decode_path(dk, dv, la.LA_BF16 if dtype == "bf16" else la.LA_F32, T) == 1
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= (1e-5 if tc else 1e-6)
     assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= 1e-6
+
+
+@pytest.mark.parametrize("B,H,T,lo,hi", [(1, 1, 2, 0.9, 0.9), (2, 3, 15, 0.5, 1.0), (2, 1, 17, 0.5, 0.99),
+                                         (3, 2, 40, 0.05, 0.3), (64, 32, 16, 0.9, 0.999),
+                                         (1, 2, 200, 1.0, 1.0)])
+def test_decay_tokens_tensor_core(B, H, T, lo, hi):
+    """The tensor-core multi-token decode with decay (bf16, d = 128): against
+    the oracle's decayed steps and against the CUDA-core kernel on the same
+    inputs; partial and many groups, strong decay (a down to 0.05) and a = 1."""
+    import torch
+    d = 128
+    assert la.la_decode_path(d, d, la.LA_BF16, T) == 1
+    S_ref, z_ref = _prefill_state(B, H, d, d, "bf16", seed=T + 3)
+    alpha_h = np.linspace(lo, hi, H).astype(np.float32)
+    q, k, v = synth.qkv(B, H, T, d, d, seed=900 + T, dtype="bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    al = torch.from_numpy(alpha_h).cuda()
+    S, z = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+    out = la.decode_steps_decay(S, z, qd, kd, vd, al)
+    la.la_set_path(la.LA_PATH_SIMT)
+    try:
+        S2, z2 = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+        out2 = la.decode_steps_decay(S2, z2, qd, kd, vd, al)
+        torch.cuda.synchronize()
+    finally:
+        la.la_set_path(la.LA_PATH_AUTO)
+    assert la.la_device_status(True) == la.LA_OK
+    S_w, z_w, o_w = orc.decode_steps_decay(S_ref, z_ref, q, k, v, alpha=alpha_h.astype(np.float64)[None, :])
+    vmax = np.abs(v).max()
+    assert rel_err(to_host(out), o_w, vmax) <= TOL["bf16"]
+    assert rel_err(to_host(out), to_host(out2), vmax) <= TOL["bf16"]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+    assert rel_err(to_host(z), z_w, np.abs(z_w).max()) <= 1e-6
+    if lo == hi == 1.0:
+        # a = 1 is the undecayed tensor-core decode
+        S3, z3 = torch.from_numpy(S_ref).cuda(), torch.from_numpy(z_ref).cuda()
+        out3 = la.decode_steps(S3, z3, qd, kd, vd)
+        torch.cuda.synchronize()
+        assert rel_err(to_host(out), to_host(out3), vmax) <= 1e-2
+        assert rel_err(to_host(S), to_host(S3), float(S3.abs().max())) <= 1e-5
 
 
 def test_decay_one_matches_plain_decode():
