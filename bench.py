@@ -725,8 +725,8 @@ def main():
             t = max_over_ranks(rr["ms"]) / 1e3
             per = t / rr["steps"]
             nt = ws.get("tokens", 1)
-            # the plain and the decay-gated multi-token decode take the tensor cores
-            tc_decode = ws.get("variant") in (None, "decay") and la.la_decode_path(ws["dk"], ws["dv"], la.LA_BF16, nt) == 1
+            # the plain, decay-gated and delta-rule multi-token decodes take the tensor cores
+            tc_decode = la.la_decode_path(ws["dk"], ws["dv"], la.LA_BF16, nt) == 1
             traffic_key = ("decodetc_" if tc_decode else "variants_" if ws.get("variant") else "decode_") + name
             # bytes of one call: the state once, q, k, v, out once per token
             call_bytes = decode_state_bytes(ws) + nt * decode_io_bytes(ws)

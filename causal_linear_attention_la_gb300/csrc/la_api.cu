@@ -707,6 +707,20 @@ la_status la_decode_steps_delta(float* S, const void* q, const void* k, const vo
   if (!S || !q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "S, q, k, v, out must be non-NULL");
   if (!aligned16(S) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  if (g_path.load() == LA_PATH_AUTO && tc_decode_supported(dk, dv, dtype, T)) {
+    // on the tensor cores: pair products, the state read (hi + lo) and the
+    // update as MMAs, the triangular solve per value index
+    if (device_status_ptr() == nullptr)
+      return fail(LA_ERR_CUDA, "la_decode_steps_delta: device status word unavailable");
+    DecodeArgs d{};
+    d.S = S; d.q = q; d.k = k; d.v = v; d.out = out;
+    d.BH = B * H; d.dk = dk; d.dv = dv; d.dtype = dtype;
+    d.stream = (cudaStream_t)stream;
+    d.ntok = T;
+    cudaError_t e = la::tc_decode_steps_delta(d);
+    if (e != cudaSuccess) return cuda_fail(e, "la_decode_steps_delta");
+    return LA_OK;
+  }
   VariantArgs a{};
   a.S = S; a.q = q; a.k = k; a.v = v; a.out = out;
   a.H = H; a.BH = B * H; a.ntok = T; a.dk = dk; a.dv = dv; a.dtype = dtype;

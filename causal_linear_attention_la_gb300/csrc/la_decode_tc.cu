@@ -565,6 +565,299 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
   }
 }
 
+// ---------------------------------------------------------------------------
+// Delta rule ("Linear Attention, 곱의 순서를 바꾸면 생기는 일", paragraph on 델타
+// 규칙): u_t = S_{t-1}^T k_t, S_t = S_{t-1} + k_t (v_t - u_t)^T, out_t = S_t^T q_t,
+// keys and queries as given. Over a group of n tokens from S_0 the increments
+// u'_t = v_t - S_{t-1}^T k_t solve the unit lower-triangular system
+//   u'_t = v_t - S_0^T k_t - sum_{j < t} (k_t . k_j) u'_j,
+// and out_t = S_0^T q_t + sum_{j <= t} (q_t . k_j) u'_j, S_n = S_0 + sum_t k_t u'_t^T.
+// Per group:
+//   MMA      D_P[r][j] = [K ; Q]_r . k_j        (pair products, exact in fp32)
+//   MMA x 2  D[c][r] = S^T [K ; Q]^T            (the state as bf16 hi, then lo:
+//                                               about 16 bits, since the
+//                                               correction v - S^T k needs them)
+//   lane c   the 16-step forward substitution for u'[c][.] and the outputs
+//   MMA x 2  S^T += U'^T K                      (U' as bf16 hi + lo in tensor memory)
+// Two teams per CTA as the kernel above; no z.
+// ---------------------------------------------------------------------------
+constexpr int DROWS = 32;                // rows of the [K ; Q] tile
+constexpr int DBOX = DROWS * 128;        // bytes of one [32 rows][64 bf16] SW128 box
+
+struct DecDelta {
+  static constexpr int OFF_SST = 0;                         // fp32 [128][128] state (bulk load)
+  static constexpr int OFF_KQ = OFF_SST + DT * DT * 4;      // [K ; Q] bf16, K-major, two boxes
+  static constexpr int OFF_A = OFF_KQ + 2 * DBOX;           // fp32 [16][16] k_t . k_j
+  static constexpr int OFF_QK = OFF_A + TG * TG * 4;        // fp32 [16][16] q_t . k_j
+  static constexpr int OFF_BAR = OFF_QK + TG * TG * 4;      // 4 mbarriers
+  // the pair-product MMA reads [K ; Q] as 128 rows (rows 32.. are whatever
+  // follows; their results are not read): inside the team's region
+  static constexpr int TEAM_BYTES =
+      ((OFF_BAR + 32 > OFF_KQ + DBOX + 16 * 1024 ? OFF_BAR + 32 : OFF_KQ + DBOX + 16 * 1024) + 1023) / 1024 * 1024;
+  static constexpr int BYTES = 2 * TEAM_BYTES + 16;
+  static_assert(OFF_KQ % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+  static_assert(BYTES <= 232448, "shared memory budget");
+  // tensor memory columns (per team)
+  static constexpr uint32_t COL_S = 0;                      // S^T fp32, 128 columns
+  static constexpr uint32_t COL_SB = 128;                   // S^T bf16 (hi, then lo), 64 columns
+  static constexpr uint32_t COL_KQ = 192;                   // S^T [K ; Q]^T, 32 columns
+  static constexpr uint32_t COL_P = 224;                    // pair products, 16 columns
+  static constexpr uint32_t COL_U = 240;                    // U' bf16 hi (8) and lo (8)
+  static constexpr uint32_t TMEM_COLS = 256;
+};
+
+// The remainder S - bf16(S) of this thread's lane of S^T, as bf16, into the
+// copy columns (the high part's read has finished).
+__device__ __forceinline__ void lo_copy(uint32_t lane_addr) {
+#pragma unroll 1
+  for (int i0 = 0; i0 < DT; i0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(lane_addr + DecDelta::COL_S + i0, v);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float a = __uint_as_float(v[2 * j]), b = __uint_as_float(v[2 * j + 1]);
+      const uint32_t hi = pack_bf16x2(a, b);
+      pk[j] = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+    }
+    tmem_st16(lane_addr + DecDelta::COL_SB + i0 / 2, pk);
+  }
+  tmem_st_wait();
+}
+
+__global__ void __launch_bounds__(256, 1)
+decode_tc_delta_kernel(float* __restrict__ S, const __nv_bfloat16* __restrict__ q,
+                       const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                       __nv_bfloat16* __restrict__ out, int BH, int ntok, int* status) {
+  using L = DecDelta;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 2 * L::TEAM_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 2 * L::TEAM_BYTES + 4);
+  if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    if (threadIdx.x == 0) report_timeout(status);
+    return;
+  }
+  const int team = threadIdx.x >> 7;
+  const int tid = threadIdx.x & 127;              // thread of the team: lane / value index
+  const int warp = tid >> 5;
+  uint8_t* sm = smem_raw + team * L::TEAM_BYTES;
+  float* sst = reinterpret_cast<float*>(sm + L::OFF_SST);
+  float* sA = reinterpret_cast<float*>(sm + L::OFF_A);
+  float* sQK = reinterpret_cast<float*>(sm + L::OFF_QK);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+  uint64_t* bar_r = bar_s + 1;
+  uint64_t* bar_mma = bar_s + 2;
+
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_r, 1);
+    mbar_init(bar_mma, 1);
+    if (team == 0) *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) {
+    tmem_alloc(tmem_slot, 2 * L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot + team * L::TMEM_COLS;
+  const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);   // lane = tid
+
+  constexpr uint32_t id_pair = make_idesc_bf16(128, TG, false, false);     // A, B K-major (smem)
+  constexpr uint32_t id_read = make_idesc_bf16(128, DROWS, false, false);  // A tensor memory, B K-major
+  constexpr uint32_t id_upd = make_idesc_bf16(128, DT, false, true);       // A tensor memory, B MN-major
+  const uint32_t kqa = smem_u32(sm + L::OFF_KQ);
+  const int ngroups = (ntok + TG - 1) / TG;
+  uint32_t ph_s = 0, ph_r = 0, ph_mma = 0;
+  uint32_t loads = 0;
+  bool ok = true;
+
+  if (team == 1) __nanosleep(3000);
+  const long long bh0 = 2LL * blockIdx.x + team, bh_step = 2LL * gridDim.x;
+  if (tid == 0 && bh0 < BH) {
+    mbar_arrive_expect_tx(bar_s, DT * DT * 4);
+    bulk_load(sst, S + bh0 * (long long)(DT * DT), DT * DT * 4, bar_s);
+    ++loads;
+  }
+  for (long long bh = bh0; bh < BH && ok; bh += bh_step) {
+    float* Sg = S + bh * (long long)(DT * DT);
+    const __nv_bfloat16* qb = q + bh * (long long)ntok * DT;
+    const __nv_bfloat16* kb = k + bh * (long long)ntok * DT;
+    const __nv_bfloat16* vb = v + bh * (long long)ntok * DT;
+    __nv_bfloat16* ob = out + bh * (long long)ntok * DT;
+    for (int g = 0; g < ngroups; ++g) {
+      const int t0 = g * TG;
+      const int n = min(TG, ntok - t0);
+      // ---- [K ; Q] tile: thread tid fills row t = tid / 8 (k_t) and row
+      // 16 + t (q_t), 16-byte chunk tid % 8 of both boxes; zeros past n.
+      // Lane tid's values v_t[tid] for the substitution.
+      {
+        const int t = tid >> 3, ch = tid & 7;
+        const bool valid = t < n;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const long long off = (long long)(t0 + t) * DT + 64 * b + 8 * ch;
+          const uint4 kk = valid ? *reinterpret_cast<const uint4*>(kb + off) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 qq = valid ? *reinterpret_cast<const uint4*>(qb + off) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(sm + L::OFF_KQ + b * DBOX + sw128(t, ch)) = kk;
+          *reinterpret_cast<uint4*>(sm + L::OFF_KQ + b * DBOX + sw128(16 + t, ch)) = qq;
+        }
+      }
+      float vr[TG];
+#pragma unroll
+      for (int t = 0; t < TG; ++t)
+        vr[t] = t < n ? __bfloat162float(vb[(long long)(t0 + t) * DT + tid]) : 0.f;
+      if (g == 0) {
+        // the state: column tid of S -> lane tid of S^T, fp32 and the bf16 high part
+        ok = mbar_wait(bar_s, ph_s & 1, abort_flag, kTimeoutNs);
+        ++ph_s;
+        if (!ok) break;
+#pragma unroll 1
+        for (int i0 = 0; i0 < DT; i0 += 32) {
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(sst[(i0 + j) * DT + tid]);
+          tmem_st32(lane_addr + L::COL_S + i0, w);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1]));
+          tmem_st16(lane_addr + L::COL_SB + i0 / 2, pk);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      team_sync(team);
+      // ---- pair products and the read with the high part
+      if (tid == 0) {
+        if (g == 0 && bh + bh_step < BH) {
+          mbar_arrive_expect_tx(bar_s, DT * DT * 4);
+          bulk_load(sst, S + (bh + bh_step) * (long long)(DT * DT), DT * DT * 4, bar_s);
+          ++loads;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < DT / 16; ++kk) {
+          const uint64_t d = make_sdesc(kqa + (kk >> 2) * DBOX + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          mma_ss(tmem + L::COL_P, d, d, id_pair, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DT / 16; ++kk)
+          mma_ts(tmem + L::COL_KQ, tmem + L::COL_SB + kk * 8,
+                 make_sdesc(kqa + (kk >> 2) * DBOX + (kk & 3) * 32, 16, 1024, kSwizzle128B), id_read, kk > 0);
+        tc_commit(bar_r);
+      }
+      ok = mbar_wait(bar_r, ph_r & 1, abort_flag, kTimeoutNs);
+      ++ph_r;
+      if (!ok) break;
+      tc_fence_after();
+      // ---- the low part of the state into the copy; warp 0 moves the pair
+      // products to shared memory (row r < 16: k_r . k_j; row 16 + t: q_t . k_j)
+      lo_copy(lane_addr);
+      if (warp == 0) {
+        uint32_t d[16];
+        tmem_ld16(lane_addr + L::COL_P, d);
+        tmem_ld_wait();
+        float* dst = tid < TG ? sA + tid * TG : sQK + (tid - TG) * TG;
+#pragma unroll
+        for (int j = 0; j < TG; ++j) dst[j] = __uint_as_float(d[j]);
+      }
+      tc_fence_before();
+      team_sync(team);
+      if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < DT / 16; ++kk)
+          mma_ts(tmem + L::COL_KQ, tmem + L::COL_SB + kk * 8,
+                 make_sdesc(kqa + (kk >> 2) * DBOX + (kk & 3) * 32, 16, 1024, kSwizzle128B), id_read, 1);
+        tc_commit(bar_r);
+      }
+      ok = mbar_wait(bar_r, ph_r & 1, abort_flag, kTimeoutNs);
+      ++ph_r;
+      if (!ok) break;
+      tc_fence_after();
+      // ---- lane tid: u'_t = v_t - (S^T k_t) - sum_{j<t} (k_t . k_j) u'_j,
+      // out_t = (S^T q_t) + sum_{j<=t} (q_t . k_j) u'_j
+      {
+        uint32_t d[32];
+        tmem_ld32(lane_addr + L::COL_KQ, d);
+        tmem_ld_wait();
+        float u[TG];
+#pragma unroll
+        for (int t = 0; t < TG; ++t) {
+          float x = vr[t] - __uint_as_float(d[t]);
+#pragma unroll
+          for (int j = 0; j < t; ++j) x = fmaf(-sA[t * TG + j], u[j], x);
+          u[t] = t < n ? x : 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < TG; ++t) {
+          float o = __uint_as_float(d[TG + t]);
+#pragma unroll
+          for (int j = 0; j <= t; ++j) o = fmaf(sQK[t * TG + j], u[j], o);
+          if (t < n) ob[(long long)(t0 + t) * DT + tid] = __float2bfloat16_rn(o);
+        }
+        // U' as bf16 hi (columns COL_U..+7) and lo (COL_U+8..+15), token
+        // pairs per column (lower token in the low half)
+        uint32_t pu[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          pu[j] = pack_bf16x2(u[2 * j], u[2 * j + 1]);
+          pu[8 + j] = pack_bf16x2(u[2 * j] - __uint_as_float(pu[j] << 16),
+                                  u[2 * j + 1] - __uint_as_float(pu[j] & 0xFFFF0000u));
+        }
+        tmem_st16(lane_addr + L::COL_U, pu);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      team_sync(team);
+      // ---- update: S^T += U'_hi K + U'_lo K (K = 16 tokens, B = the K rows
+      // of the tile read MN-major)
+      if (tid == 0) {
+        tc_fence_after();
+        mma_ts(tmem + L::COL_S, tmem + L::COL_U, make_sdesc(kqa, DBOX, 1024, kSwizzle128B), id_upd, 1);
+        mma_ts(tmem + L::COL_S, tmem + L::COL_U + 8, make_sdesc(kqa, DBOX, 1024, kSwizzle128B), id_upd, 1);
+        tc_commit(bar_mma);
+      }
+      ok = mbar_wait(bar_mma, ph_mma & 1, abort_flag, kTimeoutNs);
+      ++ph_mma;
+      if (!ok) break;
+      tc_fence_after();
+      if (g + 1 < ngroups) refresh_bf16_copy<false>(lane_addr);
+      tc_fence_before();
+      team_sync(team);    // the tile and the pair products are rewritten next
+    }
+    if (!ok) break;
+#pragma unroll 1
+    for (int i0 = 0; i0 < DT; i0 += 32) {
+      uint32_t w[32];
+      tmem_ld32(lane_addr + L::COL_S + i0, w);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) Sg[(i0 + j) * DT + tid] = __uint_as_float(w[j]);
+    }
+    tc_fence_before();
+    team_sync(team);
+  }
+  // ---------------- teardown ----------------
+  if (tid == 0) {
+    if (loads > ph_s) mbar_drain(bar_s, ph_s & 1, kTimeoutNs);
+    if (ph_r > 0) mbar_drain(bar_r, (ph_r - 1) & 1, kTimeoutNs);
+    if (ph_mma > 0) mbar_drain(bar_mma, (ph_mma - 1) & 1, kTimeoutNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) report_timeout(status);
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(*tmem_slot, 2 * L::TMEM_COLS);
+  }
+}
+
 }  // namespace
 
 bool tc_decode_supported(int dk, int dv, la_dtype dtype, int ntok) {
@@ -594,6 +887,23 @@ cudaError_t tc_decode_steps(const DecodeArgs& a) { return launch_decode_tc<false
 
 cudaError_t tc_decode_steps_decay(const DecodeArgs& a, const float* alpha, int H) {
   return launch_decode_tc<true>(a, alpha, H);
+}
+
+cudaError_t tc_decode_steps_delta(const DecodeArgs& a) {
+  constexpr int smem = DecDelta::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int ctas = (int)std::min<long long>((a.BH + 1) / 2, (long long)sms);
+  decode_tc_delta_kernel<<<ctas, 256, smem, a.stream>>>(
+      a.S, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v, (__nv_bfloat16*)a.out,
+      a.BH, a.ntok, device_status_ptr());
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 }  // namespace la

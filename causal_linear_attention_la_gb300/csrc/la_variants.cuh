@@ -30,6 +30,8 @@ cudaError_t tc_forward_decay(const FwdArgs& a, const float* alpha, int H);
 // where tc_decode_supported holds): per-head factors alpha [H] (device).
 struct DecodeArgs;
 cudaError_t tc_decode_steps_decay(const DecodeArgs& a, const float* alpha, int H);
+// ... and the delta rule (S only; no z)
+cudaError_t tc_decode_steps_delta(const DecodeArgs& a);
 // dst <- src for n floats (16-byte aligned pointers)
 cudaError_t copy_floats(float* dst, const float* src, long long n, cudaStream_t stream);
 

@@ -160,6 +160,39 @@ def test_delta_tokens(B, H, T, dk, dv, dtype):
     assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
 
 
+@pytest.mark.parametrize("B,H,T", [(1, 1, 2), (2, 3, 15), (2, 1, 17), (3, 2, 40), (64, 32, 16), (1, 2, 200)])
+def test_delta_tokens_tensor_core(B, H, T):
+    """The tensor-core delta-rule decode (bf16, d = 128): against the oracle's
+    token steps and against the CUDA-core kernel on the same inputs; partial
+    and many groups of 16, unit-norm keys on a random state."""
+    import torch
+    d = 128
+    assert la.la_decode_path(d, d, la.LA_BF16, T) == 1
+    rng = np.random.default_rng(T + 31)
+    S0 = rng.standard_normal((B, H, d, d)).astype(np.float32)
+    q, k, v = synth.qkv(B, H, T, d, d, seed=1300 + T, dtype="bf16")
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    q = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    qd, kd, vd = to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16")
+    q, k = to_host(qd), to_host(kd)
+    S = torch.from_numpy(S0).cuda()
+    out = la.decode_steps_delta(S, qd, kd, vd)
+    la.la_set_path(la.LA_PATH_SIMT)
+    try:
+        S2 = torch.from_numpy(S0).cuda()
+        out2 = la.decode_steps_delta(S2, qd, kd, vd)
+        torch.cuda.synchronize()
+    finally:
+        la.la_set_path(la.LA_PATH_AUTO)
+    assert la.la_device_status(True) == la.LA_OK
+    S_w, o_w = orc.decode_steps_delta(S0, q, k, v)
+    scale = max(np.abs(o_w).max(), np.abs(v).max())
+    assert rel_err(to_host(out), o_w, scale) <= TOL["bf16"]
+    assert rel_err(to_host(out), to_host(out2), scale) <= TOL["bf16"]
+    # the state read carries S as bf16 hi + lo and U' likewise (about 16 bits)
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+
+
 def _unit_qkv(B, H, N, d, dtype, seed):
     """Unit-norm queries and keys rounded to the input dtype, and the values
     the kernel sees (host copies read back from the device tensors)."""
