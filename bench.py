@@ -78,6 +78,8 @@ WORKLOADS = {
                                  variant="decay"),
     # the delta rule over whole sequences, chunk by chunk (la_forward_delta)
     "deltafwd_b2_h16_n8192_d128": dict(kind="delta_fwd", B=2, H=16, N=8192, dk=128, dv=128, seed=6),
+    # 256 heads: the tensor-core group kernel
+    "deltafwd_b8_h32_n2048_d128": dict(kind="delta_fwd", B=8, H=32, N=2048, dk=128, dv=128, seed=6),
     "delta16_b64_h32_d128": dict(kind="decode", B=64, H=32, dk=128, dv=128, seed=4,
                                  prefill=dict(B=1, H=16, N=131072), steps=64, tokens=16,
                                  variant="delta"),
@@ -758,13 +760,18 @@ def main():
             t = max_over_ranks(rr["ms"]) / 1e3
             mhz = sampler.summary()["sm_mhz"] or 2070.0
             ach = delta_flops(ws) * kk / t / 1e12
+            # bf16 d = 128 with >= 64 heads runs the tensor-core group kernel
+            tc = ws["dk"] == 128 and ws["B"] * ws["H"] >= 64
+            peak = peaks["bf16_tflops"] if tc else fp32_peak_tflops(mhz)
             sections[name] = {
                 "value": job_throughput(world, ws["B"] * ws["N"] * kk, t), "unit": "tokens/s",
                 "ms_per_step": 1e3 * t / kk, "steps": kk,
-                "roofline": {"bound": "alu", "achieved": ach, "peak": fp32_peak_tflops(mhz),
-                             "unit": "TFLOP/s", "frac": ach / fp32_peak_tflops(mhz),
-                             "kernel": "delta_chunk",
-                             "peak_source": f"152 SMs x 128 fp32 FMA lanes x 2 at {mhz:.0f} MHz"},
+                "roofline": {"bound": "tensor" if tc else "alu", "achieved": ach, "peak": peak,
+                             "unit": "TFLOP/s", "frac": ach / peak,
+                             "kernel": "decode_tc_delta" if tc else "delta_chunk",
+                             "peak_source": (f"{peak_src} bf16_tflops" if tc else
+                                             f"152 SMs x 128 fp32 FMA lanes x 2 at {mhz:.0f} MHz"),
+                             "flops": "the token recurrence's 6 dk dv per token-head"},
                 "gpu_launches": rr["launches"],
                 "l2": f"{rr['rotations']} input set(s) of {rr['bytes_per_set'] / 1e6:.0f} MB",
             }

@@ -742,6 +742,22 @@ la_status la_forward_delta(float* S, const void* q, const void* k, const void* v
   if (!S || !q || !k || !v || !out) return fail(LA_ERR_INVALID_ARG, "S, q, k, v, out must be non-NULL");
   if (!aligned16(S) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  // with at least 64 heads the tensor-core group kernel (one head per team
+  // of a persistent CTA, 16 tokens per group) fills the GPU and is faster
+  // than the column-split CUDA-core kernel (measured: 32 heads level, 128
+  // heads 3.2x at d = 128)
+  if (g_path.load() == LA_PATH_AUTO && tc_decode_supported(dk, dv, dtype, N) && (long long)B * H >= 64) {
+    if (device_status_ptr() == nullptr)
+      return fail(LA_ERR_CUDA, "la_forward_delta: device status word unavailable");
+    DecodeArgs d{};
+    d.S = S; d.q = q; d.k = k; d.v = v; d.out = out;
+    d.BH = B * H; d.dk = dk; d.dv = dv; d.dtype = dtype;
+    d.stream = (cudaStream_t)stream;
+    d.ntok = N;
+    cudaError_t e = la::tc_decode_steps_delta(d);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward_delta");
+    return LA_OK;
+  }
   VariantArgs a{};
   a.S = S; a.q = q; a.k = k; a.v = v; a.out = out;
   a.H = H; a.BH = B * H; a.ntok = N; a.dk = dk; a.dv = dv; a.dtype = dtype;

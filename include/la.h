@@ -290,6 +290,11 @@ LA_API la_status la_forward_plan(int B, int H, int N, int dk, int dv, int causal
  * out [B,H,N,dv] out, dtype; fp32 arithmetic. dk == dv in {16, 32, 64, 128}
  * (otherwise LA_ERR_UNSUPPORTED); N = 0 or B*H = 0 is a no-op. Pointers
  * 16-byte aligned device memory, not overlapping. Errors as la_decode_steps.
+ * bf16 at d = 128 with B*H >= 64 runs the tensor-core kernel of
+ * la_decode_steps_delta (groups of 16 tokens; the state read and the update
+ * as MMAs with the fp32 state split into bf16 hi + lo, the triangular solve
+ * per value index), which is faster there; otherwise 32-token chunks on the
+ * CUDA cores, the state split into 32-column blocks.
  */
 LA_API la_status la_forward_delta(float* S, const void* q, const void* k, const void* v,
                                   void* out, int B, int H, int N, int dk, int dv,

@@ -226,6 +226,24 @@ def test_forward_delta_chunked(B, H, N, d, dtype):
     assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
 
 
+def test_forward_delta_many_heads_tensor_core():
+    """bf16, d = 128 and at least 64 heads: la_forward_delta takes the
+    tensor-core group kernel; every output and the final states against the
+    oracle's token recurrence (ragged last group)."""
+    import torch
+    B, H, N, d = 4, 16, 300, 128
+    S0 = np.random.default_rng(5).standard_normal((B, H, d, d)).astype(np.float32)
+    (qd, kd, vd), (q, k, v) = _unit_qkv(B, H, N, d, "bf16", seed=55)
+    S = torch.from_numpy(S0).cuda()
+    out = la.forward_delta(S, qd, kd, vd)
+    torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
+    S_w, o_w = orc.decode_steps_delta(S0, q, k, v)
+    scale = max(np.abs(o_w).max(), np.abs(v).max())
+    assert rel_err(to_host(out), o_w, scale) <= TOL["bf16"]
+    assert rel_err(to_host(S), S_w, np.abs(S_w).max()) <= 1e-5
+
+
 def test_forward_delta_whole_heads_d128():
     """Thirty-two heads of 2048 tokens at d = 128 (fp32), every output
     against the oracle; the final states too."""
