@@ -86,7 +86,7 @@ WORKLOADS = {
 }
 MAIN = "fwd_b2_h16_n32768_d128"
 EPS = 1e-6
-E2E_SLICES = 2          # la_forward_host: sequence groups whose copies overlap compute (best measured)
+E2E_SLICES = 8          # la_forward_host: sequence groups whose copies overlap compute (best measured on the headline shape)
 
 
 # ---------------------------------------------------------------------------

@@ -12,13 +12,13 @@
 // with phi(k) = 1 + psi(k) and psi = psi_hi + psi_lo (two bf16 parts, about
 // 16 bits). The state is held transposed in tensor memory, S^T (lane = value
 // index c, column = key index i), in fp32, with a bf16 copy of it beside.
-// Per group two rounds of MMAs (M = 128):
-//   round 1  D_P[t][.] = phi(q_t) [psi_hi ; z_hi ; z_lo ; 1]^T + phi(q_t) psi_lo^T
+// Per group two passes of MMAs (M = 128):
+//   pass 1   D_P[t][.] = phi(q_t) [psi_hi ; z_hi ; z_lo ; 1]^T + phi(q_t) psi_lo^T
 //            (N = 32: the scores against the group's keys without their 1,
 //            phi(q_t) . z_0 and s_t = sum_i phi(q_t)_i; rows t >= 16 unused)
 //            D[c][t] = S^T (bf16 copy) x phi(Q)^T                  (the read)
 //   CUDA cores: P_tj = D_P[t][j] + s_t masked to j <= t < n, den_t
-//   round 2  D[c][t] += V^T P^T                                    (intra-group)
+//   pass 2   D[c][t] += V^T P^T                                    (intra-group)
 //            S^T += V^T 1 + V^T psi_hi + V^T psi_lo               (update)
 // The update carries the common 1 of phi(k) exactly (V^T times a tile of
 // ones) and psi to about 16 bits, so the state keeps fp32 accuracy; the read
@@ -32,7 +32,7 @@
 //   den_t = a^(t+1) phi(q_t) . z_0 + sum_{j <= t} a^(t-j) phi(q_t) . phi(k_j) + eps
 //   S    <- a^n S_0 + sum_j a^(n-1-j) phi(k_j) v_j^T
 // The read takes a second phi(Q) tile with row t weighted a^(t+1); the P
-// round keeps the unweighted one and the CUDA cores weight P_tj by a^(t-j)
+// pass keeps the unweighted one and the CUDA cores weight P_tj by a^(t-j)
 // (and phi(q_t) . z_0 by a^(t+1)); the update's B tiles carry w_j =
 // a^(n-1-j) as bf16 hi + lo rows (for the 1 of phi(k)) and w_j psi(k_j) as
 // hi + lo, so the state keeps the accuracy of the undecayed update; the held
@@ -93,7 +93,7 @@ struct DecTcT {
   static_assert(OFF_Q % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_KL % 1024 == 0 && OFF_V % 1024 == 0 &&
                     OFF_ONES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_QS % 1024 == 0 && OFF_UW % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
-  // the P round reads 128 rows of phi(Q) (rows 16.. are whatever follows in
+  // the P pass reads 128 rows of phi(Q) (rows 16.. are whatever follows in
   // shared memory; their results are never read): inside the team's region
   static_assert(OFF_Q + TBOX + 16 * 1024 <= TEAM_BYTES, "phi(Q) read as M = 128 stays in the region");
   static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
@@ -101,7 +101,7 @@ struct DecTcT {
   static constexpr uint32_t COL_S = 0;                      // S^T fp32, 128 columns
   static constexpr uint32_t COL_SB = 128;                   // S^T bf16 pairs, 64 columns
   static constexpr uint32_t COL_O = 192;                    // read + intra output, 16 columns
-  static constexpr uint32_t COL_P = 208;                    // P round, 32 columns
+  static constexpr uint32_t COL_P = 208;                    // P pass, 32 columns
   static constexpr uint32_t TMEM_COLS = 256;                // per team
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -394,7 +394,7 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
       fence_proxy_async_smem();
       tc_fence_before();
       team_sync(team);
-      // ---- round 1: the P round and the read (after the first group's
+      // ---- pass 1: the P pass and the read (after the first group's
       // barrier the staging buffer has been read: the next state's load goes
       // into it)
       if (tid == 0) {
@@ -460,7 +460,7 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
       fence_proxy_async_smem();
       tc_fence_before();
       team_sync(team);
-      // ---- round 2: intra-group and the update
+      // ---- pass 2: intra-group and the update
       if (tid == 0) {
         tc_fence_after();
         // intra: D[c][t] += sum_j v_j[c] P[t][j]; A = V MN-major (second
@@ -551,7 +551,7 @@ decode_tc_kernel(float* __restrict__ S, float* __restrict__ z, const __nv_bfloat
   // ---------------- teardown ----------------
   if (tid == 0) {
     // nothing in flight once shared and tensor memory are released: a state
-    // load issued but not waited for (abort path), the last MMA rounds
+    // load issued but not waited for (abort path), the last MMA passes
     if (loads > ph_s) mbar_drain(bar_s, ph_s & 1, kTimeoutNs);
     if (ph_p > 0) mbar_drain(bar_p, (ph_p - 1) & 1, kTimeoutNs);
     if (ph_mma > 0) mbar_drain(bar_mma, (ph_mma - 1) & 1, kTimeoutNs);
