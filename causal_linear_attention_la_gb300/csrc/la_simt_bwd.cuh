@@ -26,6 +26,8 @@
 // suffix after the tile alpha^(n-j) at key j; records are decayed to their
 // segment's last token (forward) or first token (reverse) and the segment
 // scan decays across segments.
+#include <type_traits>
+
 #include "la_internal.cuh"
 
 #ifndef LA_DK
@@ -388,6 +390,515 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
   }
 }
 
+// ---------------------------------------------------------------------------
+// dk = dv = 128 without decay: the same two sweeps with register tiles.
+// Every product against the 128 x 128 state (or suffix sums) runs as 4 x 4
+// outputs per thread with 16-byte shared loads of the state rows; the
+// thread's rows of the state are lane, lane + 32, ... so that a warp's
+// 16-byte loads of one column block hit distinct banks (rows are 132 floats
+// apart). The reverse sums (sweep 1) and the state / suffix updates are 8 x 8
+// tiles per thread. Same inputs, outputs and order of summation by tile as
+// the kernels above.
+// ---------------------------------------------------------------------------
+namespace t128 {
+constexpr int D = 128, LD = 132, LW = TT + 1;
+constexpr size_t smem_floats() { return (size_t)D * LD + D + 4 * TT * LD + 2 * TT * LW + 2 * TT; }
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float dot4f(float4 a, float4 b, float c) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, c))));
+}
+// x . y over 128 floats (16-byte aligned rows)
+__device__ __forceinline__ float dot128(const float* x, const float* y) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < D; c += 8) {
+    a0 = dot4f(ld4(x + c), ld4(y + c), a0);
+    a1 = dot4f(ld4(x + c + 4), ld4(y + c + 4), a1);
+  }
+  return a0 + a1;
+}
+
+// rows [TT][LD] of phi(x) (or x) from global, zeros past n
+template <typename T, bool kPhi>
+__device__ __forceinline__ void load_rows(float* dst, const T* src, int n, int tid, float scale_unused = 1.f) {
+  for (int idx = tid; idx < TT * D; idx += NT) {
+    const int t = idx / D, c = idx % D;
+    const float x = t < n ? ld(src + (long long)t * D + c) : 0.f;
+    dst[t * LD + c] = t < n ? (kPhi ? phi(x) : x) : 0.f;
+  }
+}
+}  // namespace t128
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 1)
+simt_bwd128_sweep1(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   const T* __restrict__ g, T* __restrict__ dq, int N, int P, int seg_len, int causal, float eps,
+                   const float* __restrict__ ws_state, long long state_words, int state_transposed,
+                   float* __restrict__ ws_rev, float* __restrict__ ws_tok) {
+  using namespace t128;
+  extern __shared__ __align__(16) float sm[];
+  float* S = sm;                  // [D][LD] state before the tile (row = key)
+  float* z = S + D * LD;          // [D]
+  float* fq = z + D;              // [TT][LD]
+  float* fk = fq + TT * LD;
+  float* vv = fk + TT * LD;
+  float* aa = vv + TT * LD;       // g, then a = g / den
+  float* W = aa + TT * LD;        // [TT][LW]
+  float* dW = W + TT * LW;
+  float* den = dW + TT * LW;      // [TT]
+  float* bsc = den + TT;          // [TT]
+
+  const long long bh = blockIdx.x;
+  const int p = blockIdx.y;
+  const int t0 = p * seg_len, t1 = min(N, t0 + seg_len);
+  const int tid = threadIdx.x, lane = tid & 31, tg = tid >> 5;
+  const int ir = tid >> 4, mr = tid & 15;           // 8 x 8 tiles: rows ir + 16 e, columns 4 mr + {0..3, 64..67}
+  const T* qb = q + bh * (long long)N * D;
+  const T* kb = k + bh * (long long)N * D;
+  const T* vb = v + bh * (long long)N * D;
+  const T* gb = g + bh * (long long)N * D;
+  T* dqb = dq + bh * (long long)N * D;
+  float* tok = ws_tok + bh * (long long)N * 2;
+  // the state before the segment: [S | z] records, or [S^T | z | .] from the
+  // tensor-core state pass
+  const float* st = ws_state + (bh * P + p) * state_words;
+  if (state_transposed)
+    for (int i = tid; i < D * D; i += NT) S[(i % D) * LD + i / D] = st[i];
+  else
+    for (int i = tid; i < D * D; i += NT) S[(i / D) * LD + i % D] = st[i];
+  if (tid < D) z[tid] = st[D * D + tid];
+  float racc[8][8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int f = 0; f < 8; ++f) racc[e][f] = 0.f;
+  float rz = 0.f;
+  __syncthreads();
+
+  for (int s = t0; s < t1; s += TT) {
+    const int n = min(TT, t1 - s);
+    load_rows<T, true>(fq, qb + (long long)s * D, n, tid);
+    load_rows<T, true>(fk, kb + (long long)s * D, n, tid);
+    load_rows<T, false>(vv, vb + (long long)s * D, n, tid);
+    load_rows<T, false>(aa, gb + (long long)s * D, n, tid);
+    __syncthreads();
+    if (causal) {
+      // W_tj = phi(q_t) . phi(k_j), j <= t (a warp per row t, lane j)
+      for (int idx = tid; idx < TT * TT; idx += NT) {
+        const int t = idx / TT, j = idx % TT;
+        W[t * LW + j] = (j <= t && t < n) ? dot128(fq + t * LD, fk + j * LD) : 0.f;
+      }
+      __syncthreads();
+    }
+    // den_t = phi(q_t) . z_prev + sum_{j <= t} W_tj + eps
+    if (tid < TT) {
+      const int t = tid;
+      float d = dot128(fq + t * LD, z);
+      if (causal)
+        for (int j = 0; j <= t; ++j) d += W[t * LW + j];
+      den[t] = t < n ? d + eps : 1.f;   // padding rows stay finite when eps = 0
+    }
+    // num[t][m] = sum_i phi(q_t)_i S[i][m] + sum_{j <= t} W_tj v_j[m]: rows 4 tg + e, columns 4 lane + f
+    float num[4][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int f = 0; f < 4; ++f) num[e][f] = 0.f;
+    {
+      const float* q0 = fq + (4 * tg) * LD;
+#pragma unroll 4
+      for (int i = 0; i < D; ++i) {
+        const float4 s4 = ld4(S + i * LD + 4 * lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x = q0[e * LD + i];
+          num[e][0] = fmaf(x, s4.x, num[e][0]);
+          num[e][1] = fmaf(x, s4.y, num[e][1]);
+          num[e][2] = fmaf(x, s4.z, num[e][2]);
+          num[e][3] = fmaf(x, s4.w, num[e][3]);
+        }
+      }
+      if (causal) {
+        for (int j = 0; j <= 4 * tg + 3; ++j) {
+          const float4 v4 = ld4(vv + j * LD + 4 * lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float w = j <= 4 * tg + e ? W[(4 * tg + e) * LW + j] : 0.f;
+            num[e][0] = fmaf(w, v4.x, num[e][0]);
+            num[e][1] = fmaf(w, v4.y, num[e][1]);
+            num[e][2] = fmaf(w, v4.z, num[e][2]);
+            num[e][3] = fmaf(w, v4.w, num[e][3]);
+          }
+        }
+      }
+    }
+    __syncthreads();   // den
+    // a = g / den in place; b_t = -(a_t . num_t) / den_t (a warp holds rows 4 tg .. 4 tg + 3)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * tg + e;
+      const float inv = 1.f / den[t];
+      float4 g4 = ld4(aa + t * LD + 4 * lane);
+      g4.x *= inv; g4.y *= inv; g4.z *= inv; g4.w *= inv;
+      *reinterpret_cast<float4*>(aa + t * LD + 4 * lane) = g4;
+      float part = g4.x * num[e][0] + g4.y * num[e][1] + g4.z * num[e][2] + g4.w * num[e][3];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == 0) {
+        const float b = -part * inv;
+        bsc[t] = t < n ? b : 0.f;
+        if (t < n) {
+          tok[(long long)(s + t) * 2 + 0] = den[t];
+          tok[(long long)(s + t) * 2 + 1] = b;
+        }
+      }
+    }
+    __syncthreads();
+    if (causal) {
+      // dW_tj = a_t . v_j + b_t, j <= t
+      for (int idx = tid; idx < TT * TT; idx += NT) {
+        const int t = idx / TT, j = idx % TT;
+        dW[t * LW + j] = (j <= t && t < n) ? dot128(aa + t * LD, vv + j * LD) + bsc[t] : 0.f;
+      }
+      __syncthreads();
+    }
+    // dphi(q_t)[i] = b_t z_i + sum_m a_t[m] S[i][m] + sum_{j <= t} dW_tj phi(k_j)_i:
+    // rows 4 tg + e, columns lane + 32 f
+    {
+      float acc[4][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) acc[e][f] = bsc[4 * tg + e] * z[lane + 32 * f];
+#pragma unroll 2
+      for (int m = 0; m < D; m += 4) {
+        float4 a4[4], s4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a4[e] = ld4(aa + (4 * tg + e) * LD + m);
+#pragma unroll
+        for (int f = 0; f < 4; ++f) s4[f] = ld4(S + (lane + 32 * f) * LD + m);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int f = 0; f < 4; ++f) acc[e][f] = dot4f(a4[e], s4[f], acc[e][f]);
+      }
+      if (causal) {
+        for (int j = 0; j <= 4 * tg + 3; ++j) {
+          float kf[4];
+#pragma unroll
+          for (int f = 0; f < 4; ++f) kf[f] = fk[j * LD + lane + 32 * f];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float w = j <= 4 * tg + e ? dW[(4 * tg + e) * LW + j] : 0.f;
+#pragma unroll
+            for (int f = 0; f < 4; ++f) acc[e][f] = fmaf(w, kf[f], acc[e][f]);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = 4 * tg + e;
+        if (t < n)
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const int i = lane + 32 * f;
+            dqb[(long long)(s + t) * D + i] = from_f32<T>(acc[e][f] * phi_prime_from_phi(fq[t * LD + i]));
+          }
+      }
+    }
+    // reverse sums over the segment: R += phi(Q)^T a, r += sum_t b_t phi(q_t)
+    for (int t = 0; t < n; ++t) {
+      const float4 a0 = ld4(aa + t * LD + 4 * mr), a1 = ld4(aa + t * LD + 64 + 4 * mr);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = fq[t * LD + ir + 16 * e];
+        racc[e][0] = fmaf(x, a0.x, racc[e][0]); racc[e][1] = fmaf(x, a0.y, racc[e][1]);
+        racc[e][2] = fmaf(x, a0.z, racc[e][2]); racc[e][3] = fmaf(x, a0.w, racc[e][3]);
+        racc[e][4] = fmaf(x, a1.x, racc[e][4]); racc[e][5] = fmaf(x, a1.y, racc[e][5]);
+        racc[e][6] = fmaf(x, a1.z, racc[e][6]); racc[e][7] = fmaf(x, a1.w, racc[e][7]);
+      }
+    }
+    if (tid < D)
+      for (int t = 0; t < n; ++t) rz = fmaf(bsc[t], fq[t * LD + tid], rz);
+    if (causal) {
+      __syncthreads();   // every read of S and z for this tile is done
+      // S += phi(K)^T V, z += sum phi(k)
+      float sacc[8][8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 s0 = ld4(S + (ir + 16 * e) * LD + 4 * mr), s1 = ld4(S + (ir + 16 * e) * LD + 64 + 4 * mr);
+        sacc[e][0] = s0.x; sacc[e][1] = s0.y; sacc[e][2] = s0.z; sacc[e][3] = s0.w;
+        sacc[e][4] = s1.x; sacc[e][5] = s1.y; sacc[e][6] = s1.z; sacc[e][7] = s1.w;
+      }
+      for (int t = 0; t < n; ++t) {
+        const float4 v0 = ld4(vv + t * LD + 4 * mr), v1 = ld4(vv + t * LD + 64 + 4 * mr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = fk[t * LD + ir + 16 * e];
+          sacc[e][0] = fmaf(x, v0.x, sacc[e][0]); sacc[e][1] = fmaf(x, v0.y, sacc[e][1]);
+          sacc[e][2] = fmaf(x, v0.z, sacc[e][2]); sacc[e][3] = fmaf(x, v0.w, sacc[e][3]);
+          sacc[e][4] = fmaf(x, v1.x, sacc[e][4]); sacc[e][5] = fmaf(x, v1.y, sacc[e][5]);
+          sacc[e][6] = fmaf(x, v1.z, sacc[e][6]); sacc[e][7] = fmaf(x, v1.w, sacc[e][7]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        *reinterpret_cast<float4*>(S + (ir + 16 * e) * LD + 4 * mr) =
+            make_float4(sacc[e][0], sacc[e][1], sacc[e][2], sacc[e][3]);
+        *reinterpret_cast<float4*>(S + (ir + 16 * e) * LD + 64 + 4 * mr) =
+            make_float4(sacc[e][4], sacc[e][5], sacc[e][6], sacc[e][7]);
+      }
+      if (tid < D) {
+        float a = z[tid];
+        for (int t = 0; t < n; ++t) a += fk[t * LD + tid];
+        z[tid] = a;
+      }
+    }
+    __syncthreads();
+  }
+  float* o = ws_rev + (bh * P + p) * (long long)(D * D + D);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    *reinterpret_cast<float4*>(o + (ir + 16 * e) * D + 4 * mr) = make_float4(racc[e][0], racc[e][1], racc[e][2], racc[e][3]);
+    *reinterpret_cast<float4*>(o + (ir + 16 * e) * D + 64 + 4 * mr) =
+        make_float4(racc[e][4], racc[e][5], racc[e][6], racc[e][7]);
+  }
+  if (tid < D) o[D * D + tid] = rz;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 1)
+simt_bwd128_sweep2(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   const T* __restrict__ g, T* __restrict__ dk_, T* __restrict__ dv_, int N, int P, int seg_len,
+                   int causal, const float* __restrict__ ws_rev, const float* __restrict__ ws_tok) {
+  using namespace t128;
+  extern __shared__ __align__(16) float sm[];
+  float* R = sm;                  // [D][LD] suffix sums after the tile (row = key)
+  float* r = R + D * LD;          // [D]
+  float* fq = r + D;
+  float* fk = fq + TT * LD;
+  float* vv = fk + TT * LD;
+  float* aa = vv + TT * LD;       // a = g / den
+  float* W = aa + TT * LD;
+  float* dW = W + TT * LW;
+  float* den = dW + TT * LW;
+  float* bsc = den + TT;
+
+  const long long bh = blockIdx.x;
+  const int p = blockIdx.y;
+  const int t0 = p * seg_len, t1 = min(N, t0 + seg_len);
+  const int tid = threadIdx.x, lane = tid & 31, tg = tid >> 5;
+  const int ir = tid >> 4, mr = tid & 15;
+  const T* qb = q + bh * (long long)N * D;
+  const T* kb = k + bh * (long long)N * D;
+  const T* vb = v + bh * (long long)N * D;
+  const T* gb = g + bh * (long long)N * D;
+  T* dkb = dk_ + bh * (long long)N * D;
+  T* dvb = dv_ + bh * (long long)N * D;
+  const float* tok = ws_tok + bh * (long long)N * 2;
+  const float* st = ws_rev + (bh * P + p) * (long long)(D * D + D);
+  for (int i = tid; i < D * D; i += NT) R[(i / D) * LD + i % D] = st[i];
+  if (tid < D) r[tid] = st[D * D + tid];
+  __syncthreads();
+
+  const int ntiles = (t1 - t0 + TT - 1) / TT;
+  for (int it = ntiles - 1; it >= 0; --it) {
+    const int s = t0 + it * TT;
+    const int n = min(TT, t1 - s);
+    if (tid < TT) {
+      den[tid] = tid < n ? tok[(long long)(s + tid) * 2 + 0] : 1.f;
+      bsc[tid] = tid < n ? tok[(long long)(s + tid) * 2 + 1] : 0.f;
+    }
+    load_rows<T, true>(fq, qb + (long long)s * D, n, tid);
+    load_rows<T, true>(fk, kb + (long long)s * D, n, tid);
+    load_rows<T, false>(vv, vb + (long long)s * D, n, tid);
+    load_rows<T, false>(aa, gb + (long long)s * D, n, tid);
+    __syncthreads();   // den visible
+    for (int idx = tid; idx < TT * D; idx += NT) {
+      const int t = idx / D, c = idx % D;
+      aa[t * LD + c] /= den[t];
+    }
+    __syncthreads();
+    if (causal) {
+      for (int idx = tid; idx < TT * TT; idx += NT) {
+        const int t = idx / TT, j = idx % TT;
+        const bool keep = j <= t && t < n;
+        W[t * LW + j] = keep ? dot128(fq + t * LD, fk + j * LD) : 0.f;
+        dW[t * LW + j] = keep ? dot128(aa + t * LD, vv + j * LD) + bsc[t] : 0.f;
+      }
+      __syncthreads();
+    }
+    // dphi(k_j)[i] = r_i + sum_m R[i][m] v_j[m] + sum_{t >= j} dW_tj phi(q_t)_i:
+    // rows j = 4 tg + e, columns i = lane + 32 f
+    {
+      float acc[4][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) acc[e][f] = r[lane + 32 * f];
+#pragma unroll 2
+      for (int m = 0; m < D; m += 4) {
+        float4 v4[4], r4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v4[e] = ld4(vv + (4 * tg + e) * LD + m);
+#pragma unroll
+        for (int f = 0; f < 4; ++f) r4[f] = ld4(R + (lane + 32 * f) * LD + m);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int f = 0; f < 4; ++f) acc[e][f] = dot4f(v4[e], r4[f], acc[e][f]);
+      }
+      if (causal) {
+        for (int t = 4 * tg; t < TT; ++t) {
+          float qf[4];
+#pragma unroll
+          for (int f = 0; f < 4; ++f) qf[f] = fq[t * LD + lane + 32 * f];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * tg + e;
+            const float w = t >= j ? dW[t * LW + j] : 0.f;
+#pragma unroll
+            for (int f = 0; f < 4; ++f) acc[e][f] = fmaf(w, qf[f], acc[e][f]);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * tg + e;
+        if (j < n)
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const int i = lane + 32 * f;
+            dkb[(long long)(s + j) * D + i] = from_f32<T>(acc[e][f] * phi_prime_from_phi(fk[j * LD + i]));
+          }
+      }
+    }
+    // dv_j[m] = sum_i R[i][m] phi(k_j)_i + sum_{t >= j} W_tj a_t[m]: rows j = 4 tg + e, columns 4 lane + f
+    {
+      float acc[4][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) acc[e][f] = 0.f;
+      const float* k0 = fk + (4 * tg) * LD;
+#pragma unroll 4
+      for (int i = 0; i < D; ++i) {
+        const float4 r4 = ld4(R + i * LD + 4 * lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x = k0[e * LD + i];
+          acc[e][0] = fmaf(x, r4.x, acc[e][0]);
+          acc[e][1] = fmaf(x, r4.y, acc[e][1]);
+          acc[e][2] = fmaf(x, r4.z, acc[e][2]);
+          acc[e][3] = fmaf(x, r4.w, acc[e][3]);
+        }
+      }
+      if (causal) {
+        for (int t = 4 * tg; t < TT; ++t) {
+          const float4 a4 = ld4(aa + t * LD + 4 * lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * tg + e;
+            const float w = t >= j ? W[t * LW + j] : 0.f;
+            acc[e][0] = fmaf(w, a4.x, acc[e][0]);
+            acc[e][1] = fmaf(w, a4.y, acc[e][1]);
+            acc[e][2] = fmaf(w, a4.z, acc[e][2]);
+            acc[e][3] = fmaf(w, a4.w, acc[e][3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * tg + e;
+        if (j < n)
+#pragma unroll
+          for (int f = 0; f < 4; ++f) dvb[(long long)(s + j) * D + 4 * lane + f] = from_f32<T>(acc[e][f]);
+      }
+    }
+    if (causal) {
+      __syncthreads();   // every read of R and r for this tile is done
+      // R += phi(Q)^T a, r += sum_t b_t phi(q_t): the suffix at the tile's first token
+      float racc[8][8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 s0 = ld4(R + (ir + 16 * e) * LD + 4 * mr), s1 = ld4(R + (ir + 16 * e) * LD + 64 + 4 * mr);
+        racc[e][0] = s0.x; racc[e][1] = s0.y; racc[e][2] = s0.z; racc[e][3] = s0.w;
+        racc[e][4] = s1.x; racc[e][5] = s1.y; racc[e][6] = s1.z; racc[e][7] = s1.w;
+      }
+      for (int t = 0; t < n; ++t) {
+        const float4 a0 = ld4(aa + t * LD + 4 * mr), a1 = ld4(aa + t * LD + 64 + 4 * mr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = fq[t * LD + ir + 16 * e];
+          racc[e][0] = fmaf(x, a0.x, racc[e][0]); racc[e][1] = fmaf(x, a0.y, racc[e][1]);
+          racc[e][2] = fmaf(x, a0.z, racc[e][2]); racc[e][3] = fmaf(x, a0.w, racc[e][3]);
+          racc[e][4] = fmaf(x, a1.x, racc[e][4]); racc[e][5] = fmaf(x, a1.y, racc[e][5]);
+          racc[e][6] = fmaf(x, a1.z, racc[e][6]); racc[e][7] = fmaf(x, a1.w, racc[e][7]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        *reinterpret_cast<float4*>(R + (ir + 16 * e) * LD + 4 * mr) =
+            make_float4(racc[e][0], racc[e][1], racc[e][2], racc[e][3]);
+        *reinterpret_cast<float4*>(R + (ir + 16 * e) * LD + 64 + 4 * mr) =
+            make_float4(racc[e][4], racc[e][5], racc[e][6], racc[e][7]);
+      }
+      if (tid < D) {
+        float a = r[tid];
+        for (int t = 0; t < n; ++t) a = fmaf(bsc[t], fq[t * LD + tid], a);
+        r[tid] = a;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// dk = dv = 128 without decay: the state pass (on the tensor cores for bf16
+// inputs: the forward's state kernel, records [S^T | z | .]), the scans and
+// the register-tiled sweeps
+template <typename T>
+cudaError_t launch_bwd128(const BwdArgs& a, const FwdArgs& f) {
+  constexpr int D = 128;
+  const long long words = state_words(D, D);
+  const bool tc_state = std::is_same<T, __nv_bfloat16>::value && a.plan.F == 1 && device_status_ptr() != nullptr;
+  const long long swords = tc_state ? (long long)D * D + 2 * D : words;
+  prof_begin(LA_SPAN_BWD_STATE, a.stream);
+  cudaError_t err = tc_state ? tc_segment_state(f) : simt_segment_state(f);
+  if (err == cudaSuccess)
+    err = segment_scan(a.ws_state, a.BH, a.plan.P, swords, a.causal ? SCAN_EXCLUSIVE_FWD : SCAN_TOTAL, nullptr,
+                       nullptr, D, D, a.stream, nullptr, 1, a.plan.seg_len, a.N);
+  prof_end(LA_SPAN_BWD_STATE, a.stream);
+  if (err != cudaSuccess) return err;
+  dim3 grid(a.BH, a.plan.P);
+  constexpr size_t smem = sizeof(float) * t128::smem_floats();
+  auto s1 = simt_bwd128_sweep1<T>;
+  auto s2 = simt_bwd128_sweep2<T>;
+  err = cudaFuncSetAttribute(s1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err == cudaSuccess) err = cudaFuncSetAttribute(s2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  prof_begin(LA_SPAN_BWD_SWEEP1, a.stream);
+  s1<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.dout, (T*)a.dq, a.N,
+                                   a.plan.P, a.plan.seg_len, a.causal, a.eps, a.ws_state, swords, tc_state ? 1 : 0,
+                                   a.ws_rev, a.ws_tok);
+  prof_end(LA_SPAN_BWD_SWEEP1, a.stream);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  note_launch();
+  prof_begin(LA_SPAN_BWD_SCAN, a.stream);
+  err = segment_scan(a.ws_rev, a.BH, a.plan.P, words, a.causal ? SCAN_EXCLUSIVE_REV : SCAN_TOTAL, nullptr, nullptr,
+                     D, D, a.stream, nullptr, 1, a.plan.seg_len, a.N);
+  prof_end(LA_SPAN_BWD_SCAN, a.stream);
+  if (err != cudaSuccess) return err;
+  prof_begin(LA_SPAN_BWD_SWEEP2, a.stream);
+  s2<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.dout, (T*)a.dk_,
+                                   (T*)a.dv_, a.N, a.plan.P, a.plan.seg_len, a.causal, a.ws_rev, a.ws_tok);
+  prof_end(LA_SPAN_BWD_SWEEP2, a.stream);
+  err = cudaGetLastError();
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
+
 template <int DK, int DV, typename T>
 cudaError_t launch_bwd(const BwdArgs& a) {
   FwdArgs f{};
@@ -396,6 +907,9 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
   f.stream = a.stream;
   f.alpha = a.alpha; f.H = a.H;
+  if constexpr (DK == 128 && DV == 128) {
+    if (a.alpha == nullptr) return launch_bwd128<T>(a, f);
+  }
   const long long words = state_words(DK, DV);
   prof_begin(LA_SPAN_BWD_STATE, a.stream);
   cudaError_t err = simt_segment_state(f);

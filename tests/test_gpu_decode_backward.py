@@ -177,6 +177,8 @@ PATHS = [la.LA_PATH_AUTO, la.LA_PATH_SIMT]
     (2, 1, 129, 64, 64),
     (1, 2, 700, 32, 128),
     (1, 1, 1500, 128, 128),
+    (2, 3, 333, 128, 128),
+    (1, 2, 2049, 128, 128),
     (1, 3, 333, 128, 16),
 ])
 def test_backward_shapes(B, H, N, dk, dv, causal, dtype, path):
