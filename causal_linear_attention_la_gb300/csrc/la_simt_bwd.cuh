@@ -419,14 +419,57 @@ __device__ __forceinline__ float dot128(const float* x, const float* y) {
   return a0 + a1;
 }
 
-// rows [TT][LD] of phi(x) (or x) from global, zeros past n
-template <typename T, bool kPhi>
-__device__ __forceinline__ void load_rows(float* dst, const T* src, int n, int tid, float scale_unused = 1.f) {
-  for (int idx = tid; idx < TT * D; idx += NT) {
-    const int t = idx / D, c = idx % D;
-    const float x = t < n ? ld(src + (long long)t * D + c) : 0.f;
-    dst[t * LD + c] = t < n ? (kPhi ? phi(x) : x) : 0.f;
-  }
+// A tile's q, k, v and dout rows as 16-byte pieces in registers: piece
+// idx = tid + i NT is row idx / (D / VPT), elements VPT (idx % (D / VPT)) ..
+template <typename T>
+struct TileRegs {
+  static constexpr int VPT = 16 / (int)sizeof(T);      // elements per 16 bytes
+  static constexpr int PER = TT * D / VPT / NT;         // pieces per thread and tensor
+  uint4 r[4][PER];
+};
+template <typename T>
+__device__ __forceinline__ void load_tile(TileRegs<T>& R, const T* q, const T* k, const T* v, const T* g, int n,
+                                          int tid) {
+  using TR = TileRegs<T>;
+  const T* src[4] = {q, k, v, g};
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int i = 0; i < TR::PER; ++i) {
+      const int idx = tid + i * NT, t = idx / (D / TR::VPT), cv = idx % (D / TR::VPT);
+      R.r[x][i] = t < n ? *reinterpret_cast<const uint4*>(src[x] + (long long)t * D + cv * TR::VPT)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+// rows [TT][LD]: phi of q and k, v and dout as they are; zero rows past n
+template <typename T>
+__device__ __forceinline__ void store_tile(const TileRegs<T>& R, float* fq, float* fk, float* vv, float* gg, int n,
+                                           int tid) {
+  using TR = TileRegs<T>;
+  float* dst[4] = {fq, fk, vv, gg};
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int i = 0; i < TR::PER; ++i) {
+      const int idx = tid + i * NT, t = idx / (D / TR::VPT), cv = idx % (D / TR::VPT);
+      float f[TR::VPT];
+      if constexpr (sizeof(T) == 4) {
+        f[0] = __uint_as_float(R.r[x][i].x); f[1] = __uint_as_float(R.r[x][i].y);
+        f[2] = __uint_as_float(R.r[x][i].z); f[3] = __uint_as_float(R.r[x][i].w);
+      } else {
+        const uint32_t w[4] = {R.r[x][i].x, R.r[x][i].y, R.r[x][i].z, R.r[x][i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f[2 * j] = __uint_as_float(w[j] << 16);
+          f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < TR::VPT; ++j) f[j] = t < n ? (x < 2 ? phi(f[j]) : f[j]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < TR::VPT; j += 4)
+        *reinterpret_cast<float4*>(dst[x] + t * LD + cv * TR::VPT + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+    }
 }
 }  // namespace t128
 
@@ -474,14 +517,26 @@ simt_bwd128_sweep1(const T* __restrict__ q, const T* __restrict__ k, const T* __
 #pragma unroll
     for (int f = 0; f < 8; ++f) racc[e][f] = 0.f;
   float rz = 0.f;
+  // bf16: the next tile's inputs are loaded while a tile computes
+  constexpr bool kPrefetch = sizeof(T) == 2;
+  TileRegs<T> nxt;
+  if (kPrefetch && t0 < t1) {
+    const long long o = (long long)t0 * D;
+    load_tile<T>(nxt, qb + o, kb + o, vb + o, gb + o, min(TT, t1 - t0), tid);
+  }
   __syncthreads();
 
   for (int s = t0; s < t1; s += TT) {
     const int n = min(TT, t1 - s);
-    load_rows<T, true>(fq, qb + (long long)s * D, n, tid);
-    load_rows<T, true>(fk, kb + (long long)s * D, n, tid);
-    load_rows<T, false>(vv, vb + (long long)s * D, n, tid);
-    load_rows<T, false>(aa, gb + (long long)s * D, n, tid);
+    if (!kPrefetch) {
+      const long long o = (long long)s * D;
+      load_tile<T>(nxt, qb + o, kb + o, vb + o, gb + o, n, tid);
+    }
+    store_tile<T>(nxt, fq, fk, vv, aa, n, tid);
+    if (kPrefetch && s + TT < t1) {
+      const long long o = (long long)(s + TT) * D;
+      load_tile<T>(nxt, qb + o, kb + o, vb + o, gb + o, min(TT, t1 - s - TT), tid);
+    }
     __syncthreads();
     if (causal) {
       // W_tj = phi(q_t) . phi(k_j), j <= t (a warp per row t, lane j)
@@ -703,6 +758,13 @@ simt_bwd128_sweep2(const T* __restrict__ q, const T* __restrict__ k, const T* __
   __syncthreads();
 
   const int ntiles = (t1 - t0 + TT - 1) / TT;
+  constexpr bool kPrefetch = sizeof(T) == 2;
+  TileRegs<T> nxt;
+  if (kPrefetch && ntiles > 0) {
+    const int s = t0 + (ntiles - 1) * TT;
+    const long long o = (long long)s * D;
+    load_tile<T>(nxt, qb + o, kb + o, vb + o, gb + o, min(TT, t1 - s), tid);
+  }
   for (int it = ntiles - 1; it >= 0; --it) {
     const int s = t0 + it * TT;
     const int n = min(TT, t1 - s);
@@ -710,10 +772,16 @@ simt_bwd128_sweep2(const T* __restrict__ q, const T* __restrict__ k, const T* __
       den[tid] = tid < n ? tok[(long long)(s + tid) * 2 + 0] : 1.f;
       bsc[tid] = tid < n ? tok[(long long)(s + tid) * 2 + 1] : 0.f;
     }
-    load_rows<T, true>(fq, qb + (long long)s * D, n, tid);
-    load_rows<T, true>(fk, kb + (long long)s * D, n, tid);
-    load_rows<T, false>(vv, vb + (long long)s * D, n, tid);
-    load_rows<T, false>(aa, gb + (long long)s * D, n, tid);
+    if (!kPrefetch) {
+      const long long o = (long long)s * D;
+      load_tile<T>(nxt, qb + o, kb + o, vb + o, gb + o, n, tid);
+    }
+    store_tile<T>(nxt, fq, fk, vv, aa, n, tid);
+    if (kPrefetch && it > 0) {
+      // the tile before this one (the sweep runs backwards): always whole
+      const long long o = (long long)(s - TT) * D;
+      load_tile<T>(nxt, qb + o, kb + o, vb + o, gb + o, TT, tid);
+    }
     __syncthreads();   // den visible
     for (int idx = tid; idx < TT * D; idx += NT) {
       const int t = idx / D, c = idx % D;
