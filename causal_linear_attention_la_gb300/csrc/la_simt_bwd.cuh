@@ -419,6 +419,23 @@ __device__ __forceinline__ float dot128(const float* x, const float* y) {
   return a0 + a1;
 }
 
+// The 2 x 2 block x_t . y_j, t = 2 tr + {0, 1}, j = 2 jr + {0, 1}, of rows of
+// 128 floats (four 16-byte loads per 16 FMAs)
+__device__ __forceinline__ void pair_dots(const float* x, const float* y, int tr, int jr, float (&o)[2][2]) {
+  o[0][0] = o[0][1] = o[1][0] = o[1][1] = 0.f;
+  const float* x0 = x + (2 * tr) * LD;
+  const float* y0 = y + (2 * jr) * LD;
+#pragma unroll 8
+  for (int c = 0; c < D; c += 4) {
+    const float4 a0 = ld4(x0 + c), a1 = ld4(x0 + LD + c);
+    const float4 b0 = ld4(y0 + c), b1 = ld4(y0 + LD + c);
+    o[0][0] = dot4f(a0, b0, o[0][0]);
+    o[0][1] = dot4f(a0, b1, o[0][1]);
+    o[1][0] = dot4f(a1, b0, o[1][0]);
+    o[1][1] = dot4f(a1, b1, o[1][1]);
+  }
+}
+
 // A tile's q, k, v and dout rows as 16-byte pieces in registers: piece
 // idx = tid + i NT is row idx / (D / VPT), elements VPT (idx % (D / VPT)) ..
 template <typename T>
@@ -539,11 +556,16 @@ simt_bwd128_sweep1(const T* __restrict__ q, const T* __restrict__ k, const T* __
     }
     __syncthreads();
     if (causal) {
-      // W_tj = phi(q_t) . phi(k_j), j <= t (a warp per row t, lane j)
-      for (int idx = tid; idx < TT * TT; idx += NT) {
-        const int t = idx / TT, j = idx % TT;
-        W[t * LW + j] = (j <= t && t < n) ? dot128(fq + t * LD, fk + j * LD) : 0.f;
-      }
+      // W_tj = phi(q_t) . phi(k_j), j <= t: 2 x 2 blocks, t = 2 (tid / 16) + .., j = 2 (tid % 16) + ..
+      float o[2][2];
+      pair_dots(fq, fk, tid >> 4, tid & 15, o);
+#pragma unroll
+      for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+        for (int b2 = 0; b2 < 2; ++b2) {
+          const int t = 2 * (tid >> 4) + a2, j = 2 * (tid & 15) + b2;
+          W[t * LW + j] = (j <= t && t < n) ? o[a2][b2] : 0.f;
+        }
       __syncthreads();
     }
     // den_t = phi(q_t) . z_prev + sum_{j <= t} W_tj + eps
@@ -612,10 +634,15 @@ simt_bwd128_sweep1(const T* __restrict__ q, const T* __restrict__ k, const T* __
     __syncthreads();
     if (causal) {
       // dW_tj = a_t . v_j + b_t, j <= t
-      for (int idx = tid; idx < TT * TT; idx += NT) {
-        const int t = idx / TT, j = idx % TT;
-        dW[t * LW + j] = (j <= t && t < n) ? dot128(aa + t * LD, vv + j * LD) + bsc[t] : 0.f;
-      }
+      float o[2][2];
+      pair_dots(aa, vv, tid >> 4, tid & 15, o);
+#pragma unroll
+      for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+        for (int b2 = 0; b2 < 2; ++b2) {
+          const int t = 2 * (tid >> 4) + a2, j = 2 * (tid & 15) + b2;
+          dW[t * LW + j] = (j <= t && t < n) ? o[a2][b2] + bsc[t] : 0.f;
+        }
       __syncthreads();
     }
     // dphi(q_t)[i] = b_t z_i + sum_m a_t[m] S[i][m] + sum_{j <= t} dW_tj phi(k_j)_i:
@@ -789,12 +816,18 @@ simt_bwd128_sweep2(const T* __restrict__ q, const T* __restrict__ k, const T* __
     }
     __syncthreads();
     if (causal) {
-      for (int idx = tid; idx < TT * TT; idx += NT) {
-        const int t = idx / TT, j = idx % TT;
-        const bool keep = j <= t && t < n;
-        W[t * LW + j] = keep ? dot128(fq + t * LD, fk + j * LD) : 0.f;
-        dW[t * LW + j] = keep ? dot128(aa + t * LD, vv + j * LD) + bsc[t] : 0.f;
-      }
+      float o[2][2], od[2][2];
+      pair_dots(fq, fk, tid >> 4, tid & 15, o);
+      pair_dots(aa, vv, tid >> 4, tid & 15, od);
+#pragma unroll
+      for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+        for (int b2 = 0; b2 < 2; ++b2) {
+          const int t = 2 * (tid >> 4) + a2, j = 2 * (tid & 15) + b2;
+          const bool keep = j <= t && t < n;
+          W[t * LW + j] = keep ? o[a2][b2] : 0.f;
+          dW[t * LW + j] = keep ? od[a2][b2] + bsc[t] : 0.f;
+        }
       __syncthreads();
     }
     // dphi(k_j)[i] = r_i + sum_m R[i][m] v_j[m] + sum_{t >= j} dW_tj phi(q_t)_i:
