@@ -33,38 +33,51 @@ def _lib():
     la.lib()
 
 
-def _noalloc(q, k, v, causal, code):
+def _noalloc(q, k, v, causal, code, state=True):
     import torch
     B, H, N, dk = q.shape
     dv = v.shape[-1]
     out = torch.empty((B, H, N, dv), dtype=q.dtype, device=q.device)
-    S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    z = torch.empty((B, H, dk), dtype=torch.float32, device=q.device)
+    S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if state else None
+    z = torch.empty((B, H, dk), dtype=torch.float32, device=q.device) if state else None
     st = la.la_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                               B, H, N, dk, dv, causal, 1e-6, code, S.data_ptr(),
-                               z.data_ptr(), torch.cuda.current_stream().cuda_stream)
+                               B, H, N, dk, dv, causal, 1e-6, code,
+                               S.data_ptr() if state else None, z.data_ptr() if state else None,
+                               torch.cuda.current_stream().cuda_stream)
     assert st == la.LA_OK, la.lib().la_last_error()
     return out, S, z
 
 
-# (dtype, (B, H, N, dk, dv), causal, seed): the first shape twice, with a
-# different shape, a non-causal call and the CUDA-core (fp32) path between
+# (dtype, (B, H, N, dk, dv), causal, seed, final state): the first shape
+# twice, with a different shape, a non-causal call, the CUDA-core (fp32) path
+# and a d = 128 call without a final state (balanced pieces: the records are
+# laid out per piece) between
 CALLS = [
-    ("bf16", (4, 8, 4096, 64, 64), True, 41),
-    ("bf16", (2, 3, 1000, 64, 64), False, 43),
-    ("f32", (1, 2, 1000, 32, 64), True, 44),
-    ("bf16", (1, 2, 5000, 128, 128), True, 45),
-    ("bf16", (4, 8, 4096, 64, 64), True, 42),
+    ("bf16", (4, 8, 4096, 64, 64), True, 41, True),
+    ("bf16", (2, 3, 1000, 64, 64), False, 43, True),
+    ("f32", (1, 2, 1000, 32, 64), True, 44, True),
+    ("bf16", (3, 17, 640, 128, 128), True, 46, False),
+    ("bf16", (1, 2, 5000, 128, 128), True, 45, True),
+    ("bf16", (4, 8, 4096, 64, 64), True, 42, True),
 ]
 
 
 def test_noalloc_matches_forward_on_calls_in_a_row():
     import torch
-    for dtype, (B, H, N, dk, dv), causal, seed in CALLS:
+    for dtype, (B, H, N, dk, dv), causal, seed, state in CALLS:
         code = la.LA_BF16 if dtype == "bf16" else la.LA_F32
         assert la.la_forward_workspace_size(B, H, N, dk, dv, causal, code) <= la.LA_NOALLOC_SCRATCH_BYTES
         q, k, v = synth.qkv(B, H, N, dk, dv, seed=seed, dtype=dtype)
         qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
+        if not state:
+            assert la.forward_plan(B, H, N, dk, dv, causal=causal, dtype=code)["pieces"] > 0
+            ref = la.forward(qd, kd, vd, causal=causal)
+            out, _, _ = _noalloc(qd, kd, vd, causal, code, state=False)
+            torch.cuda.synchronize()
+            assert la.la_device_status(True) == la.LA_OK
+            assert rel_err(to_host(out), to_host(ref), np.abs(v).max()) <= TOL[dtype]
+            assert torch.equal(out, ref), (dtype, B, H, N, causal)
+            continue
         ref, S_ref, z_ref = la.forward(qd, kd, vd, causal=causal, return_state=True)
         out, S, z = _noalloc(qd, kd, vd, causal, code)
         torch.cuda.synchronize()
