@@ -36,6 +36,10 @@
 
 namespace la {
 
+// dk = dv = 128 without decay: the register-tiled sweeps (their own
+// translation unit, la_simt_bwd_t128.cu)
+cudaError_t simt_backward_tiled128(const BwdArgs& a);
+
 namespace {
 
 constexpr int NT = 256;
@@ -44,26 +48,12 @@ constexpr int TT = 32;
 template <typename T>
 __device__ __forceinline__ float ld(const T* p) { return to_f32<T>(*p); }
 
-// init + sum_{i < n} x[i sx] y[i sy] with four independent partial sums, so
-// that a thread's FMAs do not wait on each other
-__device__ __forceinline__ float dot4(const float* x, int sx, const float* y, int sy, int n, float init = 0.f) {
-  float a0 = init, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  int i = 0;
-  for (; i + 4 <= n; i += 4) {
-    a0 = fmaf(x[i * sx], y[i * sy], a0);
-    a1 = fmaf(x[(i + 1) * sx], y[(i + 1) * sy], a1);
-    a2 = fmaf(x[(i + 2) * sx], y[(i + 2) * sy], a2);
-    a3 = fmaf(x[(i + 3) * sx], y[(i + 3) * sy], a3);
-  }
-  for (; i < n; ++i) a0 = fmaf(x[i * sx], y[i * sy], a0);
-  return (a0 + a1) + (a2 + a3);
-}
-
+#ifndef LA_TILED128_ONLY
 template <int DK, int DV>
 constexpr size_t sweep1_smem_floats() {
-  // S, z, fq, fk, vv, gg, aa, oo(stage), W, dW, den, bsc
+  // S, z, fq, fk, vv, gg, aa, oo(stage), W, dW, den, bsc, the tile's decay weights
   return (size_t)DK * DV + DK + 2 * TT * (DK + 1) + 3 * TT * (DV + 1) +
-         (size_t)TT * ((DK > DV ? DK : DV) + 1) + 2 * TT * (TT + 1) + 2 * TT;
+         (size_t)TT * ((DK > DV ? DK : DV) + 1) + 2 * TT * (TT + 1) + 2 * TT + 2 * TT;
 }
 
 template <int DK, int DV, typename T>
@@ -94,6 +84,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
   float* dW = W + TT * (TT + 1);
   float* den = dW + TT * (TT + 1);
   float* bsc = den + TT;
+  float* wr = bsc + TT;           // alpha^(token - segment start) of the tile's tokens
+  float* wk = wr + TT;            // alpha^(n - 1 - t)
 
   const long long bh = blockIdx.x;
   const int p = blockIdx.y;
@@ -116,9 +108,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
   for (int e = 0; e < E; ++e) racc[e] = 0.f;
   float rz = 0.f;
   const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
-  const bool decay = alpha != nullptr;
-  // alpha^e (1 without decay: no exponential in the inner loops)
-  auto dec = [&](int e) { return decay ? exp2f((float)e * log2a) : 1.f; };
+  // alpha^e (1 without decay); the innermost loops read per-tile tables instead
+  auto dec = [&](int e) { return exp2f((float)e * log2a); };
   __syncthreads();
 
   for (int s = t0; s < t1; s += TT) {
@@ -135,19 +126,28 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       vv[t * LDV + c] = in ? ld(vb + (long long)(s + t) * DV + c) : 0.f;
       gg[t * LDV + c] = in ? ld(gb + (long long)(s + t) * DV + c) : 0.f;
     }
+    if (tid < TT) {
+      wr[tid] = dec(s + tid - t0);
+      wk[tid] = dec(n - 1 - tid);
+    }
     __syncthreads();
     if (causal) {
       for (int idx = tid; idx < TT * TT; idx += NT) {
         const int t = idx / TT, j = idx % TT;
         float a = 0.f;
-        if (j <= t && t < n) a = dot4(fq + t * LDK, 1, fk + j * LDK, 1, DK) * dec(t - j);
+        if (j <= t && t < n) {
+          for (int c = 0; c < DK; ++c) a = fmaf(fq[t * LDK + c], fk[j * LDK + c], a);
+          a *= dec(t - j);
+        }
         W[t * (TT + 1) + j] = a;
       }
       __syncthreads();
     }
     if (tid < TT) {
       const int t = tid;
-      float d = dot4(fq + t * LDK, 1, z, 1, DK) * dec(t + 1);
+      float d = 0.f;
+      for (int c = 0; c < DK; ++c) d = fmaf(fq[t * LDK + c], z[c], d);
+      d *= dec(t + 1);
       if (causal)
         for (int j = 0; j <= t; ++j) d += W[t * (TT + 1) + j];
       den[t] = t < n ? d + eps : 1.f;  // padding rows stay finite when eps = 0
@@ -155,8 +155,11 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
     float num[TR];
     for (int r = 0; r < TR; ++r) {
       const int t = tid / DV + r * RG;
-      float a = dot4(fq + t * LDK, 1, S + m, DV, DK) * dec(t + 1);
-      if (causal) a = dot4(W + t * (TT + 1), 1, vv + m, LDV, t + 1, a);
+      float a = 0.f;
+      for (int c = 0; c < DK; ++c) a = fmaf(fq[t * LDK + c], S[c * DV + m], a);
+      a *= dec(t + 1);
+      if (causal)
+        for (int j = 0; j <= t; ++j) a = fmaf(W[t * (TT + 1) + j], vv[j * LDV + m], a);
       num[r] = a;
     }
     __syncthreads();
@@ -169,7 +172,8 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
     __syncthreads();
     if (tid < TT) {
       const int t = tid;
-      const float beta = dot4(gg + t * LDV, 1, stg + t * LST, 1, DV);
+      float beta = 0.f;
+      for (int mm = 0; mm < DV; ++mm) beta = fmaf(gg[t * LDV + mm], stg[t * LST + mm], beta);
       const float b = -beta / den[t];
       bsc[t] = t < n ? b : 0.f;
       if (t < n) {
@@ -182,7 +186,10 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       for (int idx = tid; idx < TT * TT; idx += NT) {
         const int t = idx / TT, j = idx % TT;
         float a = 0.f;
-        if (j <= t && t < n) a = (dot4(aa + t * LDV, 1, vv + j * LDV, 1, DV) + bsc[t]) * dec(t - j);
+        if (j <= t && t < n) {
+          for (int mm = 0; mm < DV; ++mm) a = fmaf(aa[t * LDV + mm], vv[j * LDV + mm], a);
+          a = (a + bsc[t]) * dec(t - j);
+        }
         dW[t * (TT + 1) + j] = a;
       }
       __syncthreads();
@@ -192,8 +199,11 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
       const int t = tid % TT;
       for (int e = 0; e < EC; ++e) {
         const int c = tid / TT + e * CG;
-        float a = dot4(aa + t * LDV, 1, S + c * DV, 1, DV, bsc[t] * z[c]) * dec(t + 1);
-        if (causal) a = dot4(dW + t * (TT + 1), 1, fk + c, LDK, t + 1, a);
+        float a = bsc[t] * z[c];
+        for (int mm = 0; mm < DV; ++mm) a = fmaf(aa[t * LDV + mm], S[c * DV + mm], a);
+        a *= dec(t + 1);
+        if (causal)
+          for (int j = 0; j <= t; ++j) a = fmaf(dW[t * (TT + 1) + j], fk[j * LDK + c], a);
         stg[t * LST + c] = a * phi_prime_from_phi(fq[t * LDK + c]);
       }
     }
@@ -208,33 +218,23 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
     for (int e = 0; e < E; ++e) {
       const int c = c0 + e * RG;
       float a = racc[e];
-      if (decay)
-        for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(s + t - t0), aa[t * LDV + m], a);
-      else
-        a = dot4(fq + c, LDK, aa + m, LDV, n, a);
+      for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * wr[t], aa[t * LDV + m], a);
       racc[e] = a;
     }
-    if (tid < DK) {
-      if (decay)
-        for (int t = 0; t < n; ++t) rz = fmaf(bsc[t] * dec(s + t - t0), fq[t * LDK + tid], rz);
-      else
-        rz = dot4(bsc, 1, fq + tid, LDK, n, rz);
-    }
+    if (tid < DK)
+      for (int t = 0; t < n; ++t) rz = fmaf(bsc[t] * wr[t], fq[t * LDK + tid], rz);
     if (causal) {
       // the state after the tile: alpha^n S + sum_j alpha^(n-1-j) phi(k_j) v_j^T
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int c = c0 + e * RG;
         float a = S[c * DV + m] * dec(n);
-        if (decay)
-          for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + c] * dec(n - 1 - t), vv[t * LDV + m], a);
-        else
-          a = dot4(fk + c, LDK, vv + m, LDV, n, a);
+        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + c] * wk[t], vv[t * LDV + m], a);
         S[c * DV + m] = a;
       }
       if (tid < DK) {
         float a = z[tid] * dec(n);
-        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + tid], dec(n - 1 - t), a);
+        for (int t = 0; t < n; ++t) a = fmaf(fk[t * LDK + tid], wk[t], a);
         z[tid] = a;
       }
     }
@@ -248,9 +248,9 @@ simt_bwd_sweep1(const T* __restrict__ q, const T* __restrict__ k,
 
 template <int DK, int DV>
 constexpr size_t sweep2_smem_floats() {
-  // R, r, fq, fk, vv, aa, W, dW, bsc, den, dk stage, dv stage
+  // R, r, fq, fk, vv, aa, W, dW, bsc, den, dk stage, dv stage, the tile's decay weights
   return (size_t)DK * DV + DK + 2 * TT * (DK + 1) + 2 * TT * (DV + 1) +
-         2 * TT * (TT + 1) + 2 * TT + TT * (DK + 1) + TT * (DV + 1);
+         2 * TT * (TT + 1) + 2 * TT + TT * (DK + 1) + TT * (DV + 1) + TT;
 }
 
 template <int DK, int DV, typename T>
@@ -279,6 +279,7 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
   float* den = bsc + TT;
   float* sdk = den + TT;
   float* sdv = sdk + TT * LDK;
+  float* wt = sdv + TT * LDV;     // alpha^t of the tile's tokens
 
   const long long bh = blockIdx.x;
   const int p = blockIdx.y;
@@ -297,9 +298,8 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
   for (int i = tid; i < DK * DV + DK; i += NT) R[i] = st[i];
   const int m = tid % DV, c0 = tid / DV;
   const float log2a = alpha != nullptr ? log2f(alpha[bh % H]) : 0.f;
-  const bool decay = alpha != nullptr;
-  // alpha^e (1 without decay: no exponential in the inner loops)
-  auto dec = [&](int e) { return decay ? exp2f((float)e * log2a) : 1.f; };
+  // alpha^e (1 without decay); the innermost loops read per-tile tables instead
+  auto dec = [&](int e) { return exp2f((float)e * log2a); };
   __syncthreads();
 
   const int ntiles = (t1 - t0 + TT - 1) / TT;
@@ -309,6 +309,7 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
     if (tid < TT) {
       den[tid] = tid < n ? tok[(long long)(s + tid) * 2 + 0] : 1.f;
       bsc[tid] = tid < n ? tok[(long long)(s + tid) * 2 + 1] : 0.f;
+      wt[tid] = dec(tid);
     }
     for (int idx = tid; idx < TT * DK; idx += NT) {
       const int t = idx / DK, c = idx % DK;
@@ -329,8 +330,8 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
         const int t = idx / TT, j = idx % TT;
         float w = 0.f, dw = 0.f;
         if (j <= t && t < n) {
-          w = dot4(fq + t * LDK, 1, fk + j * LDK, 1, DK);
-          dw = dot4(aa + t * LDV, 1, vv + j * LDV, 1, DV);
+          for (int c = 0; c < DK; ++c) w = fmaf(fq[t * LDK + c], fk[j * LDK + c], w);
+          for (int mm = 0; mm < DV; ++mm) dw = fmaf(aa[t * LDV + mm], vv[j * LDV + mm], dw);
           const float f = dec(t - j);
           w *= f;
           dw = (dw + bsc[t]) * f;
@@ -344,15 +345,20 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
       const int j = tid % TT;
       for (int e = 0; e < EC; ++e) {
         const int c = tid / TT + e * CG;
-        float a = dot4(R + c * DV, 1, vv + j * LDV, 1, DV, r[c]);
+        float a = r[c];
+        for (int mm = 0; mm < DV; ++mm) a = fmaf(R[c * DV + mm], vv[j * LDV + mm], a);
         a *= dec(n - j);    // the suffix after the tile, seen from key j
-        if (causal) a = dot4(dW + j * (TT + 1) + j, TT + 1, fq + j * LDK + c, LDK, TT - j, a);
+        if (causal)
+          for (int t = j; t < TT; ++t) a = fmaf(dW[t * (TT + 1) + j], fq[t * LDK + c], a);
         sdk[j * LDK + c] = a * phi_prime_from_phi(fk[j * LDK + c]);
       }
       for (int e = 0; e < EM; ++e) {
         const int mm = tid / TT + e * CG;
-        float a = dot4(R + mm, DV, fk + j * LDK, 1, DK) * dec(n - j);
-        if (causal) a = dot4(W + j * (TT + 1) + j, TT + 1, aa + j * LDV + mm, LDV, TT - j, a);
+        float a = 0.f;
+        for (int c = 0; c < DK; ++c) a = fmaf(R[c * DV + mm], fk[j * LDK + c], a);
+        a *= dec(n - j);
+        if (causal)
+          for (int t = j; t < TT; ++t) a = fmaf(W[t * (TT + 1) + j], aa[t * LDV + mm], a);
         sdv[j * LDV + mm] = a;
       }
     }
@@ -371,18 +377,12 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
       for (int e = 0; e < E; ++e) {
         const int c = c0 + e * RG;
         float a = R[c * DV + m] * dec(n);
-        if (decay)
-          for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * dec(t), aa[t * LDV + m], a);
-        else
-          a = dot4(fq + c, LDK, aa + m, LDV, n, a);
+        for (int t = 0; t < n; ++t) a = fmaf(fq[t * LDK + c] * wt[t], aa[t * LDV + m], a);
         R[c * DV + m] = a;
       }
       if (tid < DK) {
         float a = r[tid] * dec(n);
-        if (decay)
-          for (int t = 0; t < n; ++t) a = fmaf(bsc[t] * dec(t), fq[t * LDK + tid], a);
-        else
-          a = dot4(bsc, 1, fq + tid, LDK, n, a);
+        for (int t = 0; t < n; ++t) a = fmaf(bsc[t] * wt[t], fq[t * LDK + tid], a);
         r[tid] = a;
       }
     }
@@ -390,6 +390,9 @@ simt_bwd_sweep2(const T* __restrict__ q, const T* __restrict__ k,
   }
 }
 
+#endif  // !LA_TILED128_ONLY
+
+#ifdef LA_TILED128_ONLY
 // ---------------------------------------------------------------------------
 // dk = dv = 128 without decay: the same two sweeps with register tiles.
 // Every product against the 128 x 128 state (or suffix sums) runs as 4 x 4
@@ -1000,6 +1003,9 @@ cudaError_t launch_bwd128(const BwdArgs& a, const FwdArgs& f) {
   return err;
 }
 
+#endif  // LA_TILED128_ONLY
+
+#ifndef LA_TILED128_ONLY
 template <int DK, int DV, typename T>
 cudaError_t launch_bwd(const BwdArgs& a) {
   FwdArgs f{};
@@ -1009,7 +1015,7 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   f.stream = a.stream;
   f.alpha = a.alpha; f.H = a.H;
   if constexpr (DK == 128 && DV == 128) {
-    if (a.alpha == nullptr) return launch_bwd128<T>(a, f);
+    if (a.alpha == nullptr) return simt_backward_tiled128(a);
   }
   const long long words = state_words(DK, DV);
   prof_begin(LA_SPAN_BWD_STATE, a.stream);
@@ -1056,8 +1062,20 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   return err;
 }
 
+#endif  // !LA_TILED128_ONLY
+
 }  // namespace
 
+#ifdef LA_TILED128_ONLY
+cudaError_t simt_backward_tiled128(const BwdArgs& a) {
+  FwdArgs f{};
+  f.q = a.q; f.k = a.k; f.v = a.v; f.out = nullptr;
+  f.BH = a.BH; f.N = a.N; f.dk = a.dk; f.dv = a.dv; f.causal = a.causal;
+  f.eps = a.eps; f.dtype = a.dtype; f.ws_state = a.ws_state; f.plan = a.plan;
+  f.stream = a.stream;
+  return a.dtype == LA_BF16 ? launch_bwd128<__nv_bfloat16>(a, f) : launch_bwd128<float>(a, f);
+}
+#else
 #define LA_PASTE2(a, b) a##b
 #define LA_PASTE(a, b) LA_PASTE2(a, b)
 
@@ -1071,5 +1089,7 @@ cudaError_t LA_PASTE(simt_backward_dk, LA_DK)(const BwdArgs& a) {
     default: return cudaErrorInvalidValue;
   }
 }
+
+#endif  // LA_TILED128_ONLY
 
 }  // namespace la
