@@ -12,7 +12,8 @@ times (default path, one call per pass):
   for the first 8 steps, and 64 sampled states' outputs for all 1024 steps
   (and their final states)
 * forward + backward B=4 H=8 N=8192 d=64 bf16: every gradient vs the oracle,
-  causal and non-causal
+  causal and non-causal, with the backward recomputing the state records and
+  reusing the forward's (la_backward_saved, as the bench runs it)
 * decay-gated forward B=4 H=8 N=4096 d=64 bf16 (per-head factors 0.9 ..
   0.999, as the bench): every output and the final state vs the oracle's
   decayed recurrence
@@ -148,11 +149,18 @@ def test_forward_backward_b4_h8_n8192_d64():
     qd, kd, vd, gd = (to_dev(x, "bf16") for x in (q, k, v, g))
     out = la.forward(qd, kd, vd)
     grads = la.backward(qd, kd, vd, gd)
+    # as the bench runs it: the backward reusing the forward's state records
+    ws = torch.empty(la.la_forward_workspace_size(B, H, N, d, d, 1, la.LA_BF16), dtype=torch.uint8, device="cuda")
+    la.forward(qd, kd, vd, workspace=ws)
+    grads_saved = la.backward_saved(qd, kd, vd, gd, ws)
     torch.cuda.synchronize()
+    assert la.la_device_status(True) == la.LA_OK
     want_o = orc.forward_recurrent(q, k, v, eps=1e-6)
     assert rel_err(to_host(out), want_o, np.abs(v).max()) <= TOL["bf16"]
     want = orc.backward_recurrent(q, k, v, g, eps=1e-6)
     errs = grad_errors(grads, want)
+    assert grads_ok(errs, grad_tol("bf16", True)), errs
+    errs = grad_errors(grads_saved, want)
     assert grads_ok(errs, grad_tol("bf16", True)), errs
 
 
@@ -164,12 +172,17 @@ def test_forward_backward_noncausal_b4_h8_n8192_d64():
     qd, kd, vd, gd = (to_dev(x, "bf16") for x in (q, k, v, g))
     out = la.forward(qd, kd, vd, causal=False)
     grads = la.backward(qd, kd, vd, gd, causal=False)
+    ws = torch.empty(la.la_forward_workspace_size(B, H, N, d, d, 0, la.LA_BF16), dtype=torch.uint8, device="cuda")
+    la.forward(qd, kd, vd, causal=False, workspace=ws)
+    grads_saved = la.backward_saved(qd, kd, vd, gd, ws, causal=False)
     torch.cuda.synchronize()
     assert la.la_device_status(True) == la.LA_OK
     want_o = orc.forward_recurrent(q, k, v, causal=False, eps=1e-6)
     assert rel_err(to_host(out), want_o, np.abs(v).max()) <= TOL["bf16"]
     want = orc.backward_recurrent(q, k, v, g, causal=False, eps=1e-6)
     errs = grad_errors(grads, want)
+    assert grads_ok(errs, grad_tol("bf16", True)), errs
+    errs = grad_errors(grads_saved, want)
     assert grads_ok(errs, grad_tol("bf16", True)), errs
 
 
