@@ -199,7 +199,10 @@ LA_API la_status la_decode_steps(float* S, float* z, const void* q, const void* 
  *
  * alpha [H] fp32 device memory, one factor per head (alpha = 1 gives
  * la_decode_steps; values above 1 make the state grow without bound and are
- * not checked). Other arguments and errors as la_decode_steps.
+ * not checked). Other arguments and errors as la_decode_steps. Where
+ * la_decode_path(dk, dv, dtype, T) is 1 the call runs on the tensor cores
+ * (the decay weights as bf16 hi + lo rows of the update, the state within
+ * 1e-5 of its largest entry against the fp32 recurrence).
  */
 LA_API la_status la_decode_steps_decay(float* S, float* z, const void* q, const void* k,
                                 const void* v, void* out, int B, int H, int T, int dk,
@@ -256,7 +259,12 @@ LA_API la_status la_backward_decay(const void* q, const void* k, const void* v,
  * q and k are used as given (no feature map) and the read is not normalised,
  * as in the page's example; with unit-norm keys a write replaces what the key
  * held. S [B,H,dk,dv] fp32 in/out; q, k [B,H,T,dk], v [B,H,T,dv] in, out
- * [B,H,T,dv] out, dtype. Errors as la_decode_steps.
+ * [B,H,T,dv] out, dtype. Errors as la_decode_steps. Where
+ * la_decode_path(dk, dv, dtype, T) is 1 the call runs on the tensor cores in
+ * groups of 16 tokens: the increments of a group solve a unit lower-
+ * triangular system (the chunked form of the same recurrence), the state is
+ * read with its bf16 high and low parts, and the state stays within 1e-5 of
+ * its largest entry against the fp32 token recurrence.
  */
 LA_API la_status la_decode_steps_delta(float* S, const void* q, const void* k, const void* v,
                                 void* out, int B, int H, int T, int dk, int dv,
@@ -384,8 +392,9 @@ LA_API int la_set_path(int path);
  * current setting: 0 = CUDA-core, 1 = tensor-core; -1 if unsupported. */
 LA_API int la_forward_path(int dk, int dv, la_dtype dtype, int causal);
 LA_API int la_backward_path(int dk, int dv, la_dtype dtype, int causal);
-/* Which kernel la_decode_steps takes for T tokens per call: 1 = tensor-core
- * (bf16, dk = dv = 128, T >= 2), 0 = CUDA-core; -1 if unsupported. */
+/* Which kernel la_decode_steps (and la_decode_steps_decay,
+ * la_decode_steps_delta) takes for T tokens per call: 1 = tensor-core (bf16,
+ * dk = dv = 128, T >= 2), 0 = CUDA-core; -1 if unsupported. */
 LA_API int la_decode_path(int dk, int dv, la_dtype dtype, int T);
 
 /*
