@@ -394,19 +394,31 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % ST;
         if (c >= ST) {
-          ok = mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs) && (G::MERGE || store_out(c - ST));
+          ok = mbar_wait(&empty[s], ((c / ST) - 1) & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
-          stored = c - ST + 1;
         }
         uint8_t* stg = sm + s * G::STAGE;
         const int y = cmap.y_of(c), cbh = cmap.bh_of(c);
         mbar_arrive_expect_tx(&full[s], 3 * G::TILE);
+        // K and V regions are free once the stage's MMAs are done; !MERGE:
+        // the Q region holds the previous chunk's output until its store has
+        // read it, so its load goes last
 #pragma unroll
         for (int b = 0; b < G::NB; ++b) {
-          tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, cbh);
           tma_load_3d(stg + G::OFF_K + b * BOX, &map_k, &full[s], 64 * b, y, cbh);
           tma_load_3d(stg + G::OFF_V + b * BOX, &map_v, &full[s], 64 * b, y, cbh);
         }
+        if (c >= ST && !G::MERGE) {
+          ok = store_out(c - ST);
+          if (!ok) {
+            // the K and V loads of this stage are in flight: let them land
+            issued = c + 1;
+            break;
+          }
+          stored = c - ST + 1;
+        }
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b) tma_load_3d(stg + b * BOX, &map_q, &full[s], 64 * b, y, cbh);
         issued = c + 1;
       }
       // the chunks still in the ring: their outputs
