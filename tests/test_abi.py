@@ -231,3 +231,31 @@ def test_forward_plan_pieces():
     # the workspace query covers both plans
     ws = la.la_forward_workspace_size(2, 16, 32768, 128, 128, 1, la.LA_BF16)
     assert ws >= 152 * (128 * 128 + 2 * 128) * 4
+
+
+def test_forward_plan_pieces_invariants():
+    """Over many shapes: pieces never exceed one per SM (152), cover every
+    chunk of every head, span at most two heads (piece_len <= chunks per head),
+    and are taken only where they cost less than the segment plan; invalid
+    sizes are refused."""
+    import causal_linear_attention_la_gb300 as la
+    seen = 0
+    for BH in (1, 3, 16, 32, 38, 51, 64, 100, 152, 300):
+        for N in (100, 640, 1000, 4096, 8192, 32768):
+            p = la.forward_plan(1, BH, N, 128, 128)
+            nch = -(-N // 128)
+            if p["pieces"] == 0:
+                continue
+            seen += 1
+            assert p["pieces"] <= 152
+            assert p["pieces"] * p["piece_len"] >= BH * nch > (p["pieces"] - 1) * p["piece_len"]
+            assert p["piece_len"] <= nch
+            L = -(-p["seg_len"] // 128)
+            waves = -(-(BH * p["P"]) // 152)
+            assert p["piece_len"] + 1 < waves * (L + 1)
+    assert seen > 5
+    import ctypes
+    buf = (ctypes.c_int * 5)()
+    assert la.la_forward_plan(0, 1, 100, 128, 128, 1, la.LA_BF16, 0, ctypes.cast(buf, ctypes.c_void_p)) != la.LA_OK
+    assert la.la_forward_plan(1, 1, 100, 48, 128, 1, la.LA_BF16, 0, ctypes.cast(buf, ctypes.c_void_p)) != la.LA_OK
+    assert la.la_forward_plan(1, 1, 100, 128, 128, 1, la.LA_BF16, 0, None) != la.LA_OK
