@@ -436,7 +436,7 @@ LA_API void la_test_timeout_next_forward(void);
  *
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it for the
- *    life of the process; make that first call before any stream capture.
+ *    life of the process.
  *    A cudaDeviceReset (or anything else that destroys the device's primary
  *    context) leaves the cached address stale: calling la_forward_noalloc on
  *    that device afterwards is not supported.
