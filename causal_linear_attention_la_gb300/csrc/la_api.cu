@@ -180,10 +180,12 @@ bool take_timeout_test() { return g_timeout_test.exchange(0) != 0; }
 
 // Pick the number of segments per sequence. Cost model in units of one
 // kSegGranule-token chunk: every CTA pays its chunks plus about one chunk of
-// prologue (loading its starting state); CTAs run in waves of kSlots; the
-// segment scan adds a little per segment. Pure function of the sizes, so the
-// workspace query and the call agree.
-SegPlan plan_segments(long long BH, int N, int slots) {
+// prologue (loading its starting state); CTAs run in waves of `slots`; the
+// segment scan adds a little per segment, and `record_cost` per state record
+// the costliest segment sums before its first chunk (P - 1 records causal,
+// P non-causal). Pure function of the sizes, so the workspace query and the
+// call agree.
+static SegPlan plan_segments_cost(long long BH, int N, int slots, double record_cost, bool causal) {
   SegPlan best{1, N > 0 ? N : 1};
   if (BH <= 0 || N <= 0) return best;
   const int nch = (N + kSegGranule - 1) / kSegGranule;
@@ -193,7 +195,7 @@ SegPlan plan_segments(long long BH, int N, int slots) {
     if ((nch + L - 1) / L != P) continue;      // P not reachable with equal segments
     const long long ctas = BH * P;
     const long long waves = (ctas + slots - 1) / slots;
-    const double cost = (double)waves * (L + 1) + 0.02 * P;
+    const double cost = (double)waves * (L + 1) + 0.02 * P + record_cost * (causal ? P - 1 : P);
     if (cost < best_cost) {
       best_cost = cost;
       best.P = P;
@@ -201,6 +203,21 @@ SegPlan plan_segments(long long BH, int N, int slots) {
     }
   }
   return best;
+}
+
+SegPlan plan_segments(long long BH, int N, int slots) { return plan_segments_cost(BH, N, slots, 0.0, true); }
+
+// A state record summed at the start of a tensor-core chunk loop or backward
+// sweep costs about half a chunk: one thread per state row reads it from L2
+// with 16 loads in flight, ~2.1 us per 128 x 128 record against ~3.9 us per
+// chunk with every SM streaming (measured at d = 128; a d = 64 record and
+// chunk are both about half). With few heads the record sums decide the
+// plan: one head of 32768 tokens in 128 segments of 2 chunks took 278 us in
+// its chunk loop, 127 records for the last segment.
+constexpr double kRecordCost = 0.5;
+
+static SegPlan plan_segments_tc(long long BH, int N, bool causal) {
+  return plan_segments_cost(BH, N, kSlots, kRecordCost, causal);
 }
 
 // The forward's segment plan (one CTA per SM for the output kernels). On the
@@ -215,8 +232,8 @@ SegPlan plan_segments(long long BH, int N, int slots) {
 // B*H does not divide the SM count (32 heads: 128 CTAs on 152 SMs), while
 // pieces give every SM the same number of chunks.
 SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool causal, bool final_state) {
-  SegPlan plan = plan_segments(BH, N, kSlots);
   const bool tc = g_path.load() == LA_PATH_AUTO && tc_forward_supported(dk, dv, dtype, causal);
+  SegPlan plan = tc ? plan_segments_tc(BH, N, causal) : plan_segments(BH, N, kSlots);
   if (tc && causal && dk == 128 && dv == 128 && !final_state) {
     const long long nch = (N + kSegGranule - 1) / kSegGranule;
     const long long total = BH * nch;
@@ -225,8 +242,12 @@ SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool c
     const long long np = (total + len - 1) / len;
     const long long L = (plan.seg_len + kSegGranule - 1) / kSegGranule;
     const long long waves = (BH * plan.P + kSlots - 1) / kSlots;
+    // a piece sums the records of the pieces before it in its head (at most
+    // ceil(nch / len)), a segment those of the segments before it
+    const double piece_cost = (double)(len + 1) + kRecordCost * (double)((nch + len - 1) / len);
+    const double seg_cost = (double)(waves * (L + 1)) + kRecordCost * (plan.P - 1);
     // a piece spans at most two heads (len <= chunks per head)
-    if (len <= nch && len + 1 < waves * (L + 1)) {
+    if (len <= nch && piece_cost <= seg_cost) {
       plan.NP = (int)np;
       plan.piece_len = (int)len;
       return plan;
@@ -242,7 +263,9 @@ SegPlan forward_plan(long long BH, int N, int dk, int dv, la_dtype dtype, bool c
     if ((F - 1) * sub >= L) continue;          // every part must hold a chunk
     const long long ctas = BH * nseg * F;
     if (F > 1 && ctas > kSlots) break;
-    const double cost = (double)((ctas + kSlots - 1) / kSlots) * (sub + 1);
+    // every part is a record the costliest chunk-loop CTA sums
+    const double cost = (double)((ctas + kSlots - 1) / kSlots) * (sub + 1) +
+                        kRecordCost * (causal ? plan.P - 1 : plan.P) * F;
     if (cost < best) {
       best = cost;
       plan.F = F;
@@ -371,10 +394,13 @@ la_status la_forward_plan(int B, int H, int N, int dk, int dv, int causal, la_dt
 }
 
 size_t la_backward_workspace_size(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype) {
-  (void)causal; (void)dtype;
+  (void)dtype;
   if (B <= 0 || H <= 0 || N <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
   const long long BH = (long long)B * H;
-  return layout(BH, N, dk, dv, plan_segments(BH, N), true).total;
+  // the CUDA-core and the tensor-core plans (the path is chosen at the call): the larger
+  const size_t a = layout(BH, N, dk, dv, plan_segments(BH, N), true).total;
+  const size_t b = layout(BH, N, dk, dv, plan_segments_tc(BH, N, causal != 0), true).total;
+  return std::max(a, b);
 }
 
 la_status la_forward(const void* q, const void* k, const void* v, void* out,
@@ -806,7 +832,11 @@ la_status backward_impl(const void* q, const void* k, const void* v, const void*
       !aligned16(dq) || !aligned16(dk_) || !aligned16(dv_))
     return fail(LA_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
   const long long BH = (long long)B * H;
-  const SegPlan plan = plan_segments(BH, N);
+  // decay gating runs on the CUDA-core kernels
+  const bool use_tc = alpha == nullptr && g_path.load() == LA_PATH_AUTO &&
+                      tc_backward_supported(dk, dv, dtype, causal != 0);
+  // the tensor-core sweeps take the forward's record-aware segments
+  const SegPlan plan = use_tc ? plan_segments_tc(BH, N, causal != 0) : plan_segments(BH, N);
   const WsLayout w = layout(BH, N, dk, dv, plan, true);
   if (workspace == nullptr || workspace_bytes < w.total)
     return fail(LA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", w.total,
@@ -821,9 +851,6 @@ la_status backward_impl(const void* q, const void* k, const void* v, const void*
   a.ws_tok = (float*)((char*)workspace + w.tok_off);
   a.plan = plan; a.stream = stream;
   a.alpha = alpha; a.H = H;
-  // decay gating runs on the CUDA-core kernels
-  const bool use_tc = alpha == nullptr && g_path.load() == LA_PATH_AUTO &&
-                      tc_backward_supported(dk, dv, dtype, a.causal);
   if (saved != nullptr) {
     const SegPlan fplan = forward_plan(BH, N, dk, dv, dtype, a.causal, true);
     const size_t need = layout(BH, N, dk, dv, fplan, false).total;

@@ -236,8 +236,9 @@ def test_forward_plan_pieces():
 def test_forward_plan_pieces_invariants():
     """Over many shapes: pieces never exceed one per SM (152), cover every
     chunk of every head, span at most two heads (piece_len <= chunks per head),
-    and are taken only where they cost less than the segment plan; invalid
-    sizes are refused."""
+    and are taken only where they cost no more than the segment plan, counting
+    the records a piece or segment sums (half a chunk each); invalid sizes are
+    refused."""
     import causal_linear_attention_la_gb300 as la
     seen = 0
     for BH in (1, 3, 16, 32, 38, 51, 64, 100, 152, 300):
@@ -252,10 +253,35 @@ def test_forward_plan_pieces_invariants():
             assert p["piece_len"] <= nch
             L = -(-p["seg_len"] // 128)
             waves = -(-(BH * p["P"]) // 152)
-            assert p["piece_len"] + 1 < waves * (L + 1)
+            ln = p["piece_len"]
+            assert (ln + 1) + 0.5 * -(-nch // ln) <= waves * (L + 1) + 0.5 * (p["P"] - 1)
     assert seen > 5
     import ctypes
     buf = (ctypes.c_int * 5)()
     assert la.la_forward_plan(0, 1, 100, 128, 128, 1, la.LA_BF16, 0, ctypes.cast(buf, ctypes.c_void_p)) != la.LA_OK
     assert la.la_forward_plan(1, 1, 100, 48, 128, 1, la.LA_BF16, 0, ctypes.cast(buf, ctypes.c_void_p)) != la.LA_OK
     assert la.la_forward_plan(1, 1, 100, 128, 128, 1, la.LA_BF16, 0, None) != la.LA_OK
+
+
+def test_forward_plan_few_heads():
+    """With few heads the tensor-core plans take fewer, longer segments than
+    the CUDA-core plan, since every segment first sums the records of the
+    segments before it: one head of 32768 tokens runs in at most 32 segments
+    (the CUDA-core plan, which pays no record sums, takes 128), and the chosen
+    plan has the lowest modelled cost among all equal-length splits."""
+    import causal_linear_attention_la_gb300 as la
+    def cost(BH, N, P, L, causal):
+        waves = -(-(BH * P) // 152)
+        return waves * (L + 1) + 0.02 * P + 0.5 * ((P - 1) if causal else P)
+    for BH, N in [(1, 32768), (2, 32768), (4, 32768), (1, 131072), (6, 1000)]:
+        for causal in (True, False):
+            tc = la.forward_plan(1, BH, N, 128, 128, causal=causal, final_state=True)
+            f32 = la.forward_plan(1, BH, N, 128, 128, causal=causal, dtype=la.LA_F32, final_state=True)
+            assert tc["P"] <= f32["P"]
+            nch = -(-N // 128)
+            L = tc["seg_len"] // 128
+            best = min(cost(BH, N, P, -(-nch // P), causal) for P in range(1, nch + 1)
+                       if -(-nch // -(-nch // P)) == P)
+            assert abs(cost(BH, N, tc["P"], L, causal) - best) < 1e-9
+    assert la.forward_plan(1, 1, 32768, 128, 128, final_state=True)["P"] <= 32
+    assert la.forward_plan(1, 1, 32768, 128, 128, dtype=la.LA_F32, final_state=True)["P"] == 128

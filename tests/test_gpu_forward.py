@@ -227,13 +227,14 @@ def test_state_pass_split_over_ctas():
 # Balanced pieces (causal, d = 128, bf16, no final state): the heads' chunks
 # laid end to end and cut into equal pieces, one CTA each. Shapes: pieces of
 # two chunks over heads of 5 and 7 chunks with ragged last chunks (most
-# pieces end one head and start the next), heads of 33 chunks, and the
+# pieces end one head and start the next), heads of 33 chunks (pieces of 5,
+# up to 7 records summed per piece), and the
 # bench's B=2 H=16 N=8192 split (14-chunk pieces, piece 32 starting exactly
 # at head 7, a short last piece).
 @pytest.mark.parametrize("B,H,N,heads", [
     (3, 17, 544, None),
     (1, 39, 803, None),
-    (1, 9, 4224, None),
+    (1, 22, 4224, None),
     (2, 16, 8192, [0, 6, 7, 8, 15, 16, 31]),
 ])
 def test_forward_balanced_pieces(B, H, N, heads):
