@@ -279,6 +279,9 @@ LA_API la_status la_decode_steps_delta(float* S, const void* q, const void* k, c
  * chunks are laid end to end and cut into equal pieces, one CTA each, so
  * that every SM gets the same work even when B*H does not divide the SM
  * count (causal tensor-core forward at d = 128 without a final state).
+ * On the tensor-core paths the split also weighs the state records each
+ * segment or piece sums before its first chunk, so calls with few heads get
+ * fewer, longer segments than the CUDA-core path.
  * LA_ERR_INVALID_ARG for sizes outside la_forward's range or a NULL out.
  */
 LA_API la_status la_forward_plan(int B, int H, int N, int dk, int dv, int causal, la_dtype dtype,
@@ -323,7 +326,9 @@ LA_API la_status la_state_copy(float* dst_S, float* dst_z, const float* src_S,
  * Bytes of scratch memory la_backward needs (0 if none): one fp32 state and
  * one fp32 reverse accumulator (dk*dv + dk each) per (batch, head, segment)
  * plus two fp32 scalars per token (the denominator and the normaliser's
- * gradient coefficient), no per-token states.
+ * gradient coefficient), no per-token states. The tensor-core and CUDA-core
+ * paths may split the sequences into different segments: the size covers
+ * both.
  */
 LA_API size_t la_backward_workspace_size(int B, int H, int N, int dk, int dv,
                                   int causal, la_dtype dtype);
