@@ -285,3 +285,20 @@ def test_forward_plan_few_heads():
             assert abs(cost(BH, N, tc["P"], L, causal) - best) < 1e-9
     assert la.forward_plan(1, 1, 32768, 128, 128, final_state=True)["P"] <= 32
     assert la.forward_plan(1, 1, 32768, 128, 128, dtype=la.LA_F32, final_state=True)["P"] == 128
+
+
+def test_backward_workspace_covers_both_plans():
+    """The backward's workspace query covers the tensor-core plan (fewer,
+    longer segments with few heads) and the CUDA-core plan (more segments):
+    two records per (head, segment) of each plus two floats per token."""
+    import causal_linear_attention_la_gb300 as la
+    rec = (64 * 64 + 64) * 4
+    for BH, N in [(1, 32768), (2, 16384), (6, 1000), (32, 8192)]:
+        for causal in (1, 0):
+            ws = la.la_backward_workspace_size(1, BH, N, 64, 64, causal, la.LA_BF16)
+            p_tc = la.forward_plan(1, BH, N, 64, 64, causal=bool(causal), final_state=True)["P"]
+            p_cc = la.forward_plan(1, BH, N, 64, 64, causal=bool(causal), dtype=la.LA_F32,
+                                   final_state=True)["P"]
+            for P in (p_tc, p_cc):
+                assert ws >= 2 * BH * P * rec + 8 * BH * N
+            assert ws == la.la_backward_workspace_size(1, BH, N, 64, 64, causal, la.LA_F32)
